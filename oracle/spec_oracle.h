@@ -1,0 +1,105 @@
+/*
+ * Oracle for the batched speculative-decoding verifier: plain, slow, float64, host only.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * may load this code. It shares no source, header or helper with the CUDA library: the
+ * structs below are this file's own, and nothing here includes the library's header.
+ *
+ * What it computes follows the pages:
+ *   - "SOTA-227: Decode with a draft model and an accept-reject rule", section "What to do",
+ *     steps 3 and 4: walk the draft left to right, accept x_i when r_i <= p_i(x)/q_i(x),
+ *     at the first rejection resample from the normalised positive part of p - q and stop;
+ *     if nothing was rejected, draw the extra token from p at position gamma + 1.
+ *   - "Speculative Decoding Coordination Protocol (SDCP)", section "Acceptance Rules",
+ *     Rule 2 (speculative sampling): the same rule, q(x) must be checked non-zero before any
+ *     random draw; the accept draw and the extra-token draw are separate values.
+ *   - SDCP, section "Session Model": p is the target's distribution after temperature.
+ *   - "M7.8 - Speculative Serving", section 0x03C (ragged acceptance) and 0x09 (draft,
+ *     target and frontier cache transitions): L_out = P + A + 1, L_kv = P + A.
+ *   - SOTA-227, section "Why it is free rather than a trade": alpha = E[min(p, q)] and the
+ *     expected wall-time improvement (1 - alpha^(gamma+1)) / ((1 - alpha)(gamma*c + 1)).
+ *
+ * Parity status: every function here is pinned by CPU tests against values the pages print
+ * (ledgers), closed forms, brute-force enumeration of the exact law on tiny vocabularies and a
+ * chi-square test of the exactness theorem.
+ */
+#ifndef SPEC_ORACLE_H
+#define SPEC_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* request status bits (a request with any bit set emits nothing) */
+#define ORACLE_REQ_BAD_PROPOSAL 1 /* draft token outside [0,V) or q(x) == 0 (draft logit -inf) */
+#define ORACLE_REQ_BAD_LOGITS   2 /* a row holds NaN or +inf, or has no finite logit          */
+#define ORACLE_REQ_BAD_SHAPE    4 /* K_i < 0 or K_i > K_max                                  */
+#define ORACLE_REQ_BAD_PARAM    8 /* temperature not finite or < 0                           */
+#define ORACLE_REQ_BAD_BLOCKS  16 /* compaction: a committed position has no page            */
+
+typedef struct {
+    int32_t B, V, K_max;
+    int32_t dtype;              /* 0: float32 logits, 1: bfloat16 logits given as raw uint16 */
+    const void *target;         /* [T][V], T = row_off[B]; request i owns rows row_off[i]..  */
+    const void *draft;          /* [T-B][V]; request i owns rows row_off[i]-i ..             */
+    const int32_t *row_off;     /* [B+1], K_i = row_off[i+1]-row_off[i]-1                    */
+    const int32_t *draft_tokens;/* [T-B]                                                     */
+    const double *uniforms;     /* [T]: slot j<K_i accept draw of draft j, slot K_i the draw
+                                   of the extra token                                        */
+    const float *temperature;   /* [B]; 0 selects the greedy rule                             */
+    const int32_t *stop_token;  /* [B] or NULL: token that ends generation (-1: none)         */
+    const int32_t *max_new;     /* [B] or NULL: output tokens still allowed (budget)          */
+} oracle_batch;
+
+typedef struct {
+    int32_t *accept_len;        /* [B] A_i: accepted drafts actually emitted                  */
+    int32_t *out_tokens;        /* [T] slot j of request i; -1 where nothing was emitted       */
+    int32_t *n_emitted;         /* [B] tokens emitted this round (A_i + frontier flag)        */
+    int32_t *req_status;        /* [B] status bits                                            */
+    double *alpha;              /* [T-B] sum_v min(p_j(v), q_j(v)), every draft position      */
+    double *rho;                /* [T-B] p_j(x_j) / q_j(x_j)                                  */
+    double *resid_mass;         /* [T-B] sum_v max(p_j(v) - q_j(v), 0)                        */
+    double *accept_margin;      /* [T-B] u_j - rho_j                                          */
+    double *sample_margin;      /* [B] distance of u*Z to the nearer end of the chosen token's
+                                   CDF interval, divided by Z (NaN when no draw was made)     */
+    double *sample_prob;        /* [B] probability of the frontier token under the law it was
+                                   drawn from                                                  */
+    int32_t *fallback;          /* [B] 1 when the residual had zero mass and p was used        */
+} oracle_result;
+
+int oracle_verify(const oracle_batch *in, oracle_result *out);
+
+typedef struct {
+    int32_t B, page_size, max_blocks;
+    const int32_t *row_off;      /* [B+1] as for oracle_verify                                 */
+    const int32_t *accept_len;   /* [B]                                                        */
+    const int32_t *n_emitted;    /* [B]                                                        */
+    const int32_t *out_tokens;   /* [T]                                                        */
+    const int32_t *req_status;   /* [B]                                                        */
+    const int32_t *prefix_len;   /* [B] P_i, committed target KV length before the round       */
+    const int32_t *cand_kv_rows; /* [T-B] physical row holding draft j's candidate target KV   */
+    const int32_t *block_table;  /* [B][max_blocks] page ids                                  */
+    int32_t *out_off;            /* [B+1]                                                      */
+    int32_t *packed_tokens;      /* [sum emitted]                                              */
+    int32_t *packed_pos;         /* [sum emitted]                                              */
+    int32_t *kv_off;             /* [B+1]                                                      */
+    int32_t *kv_src;             /* [sum A]                                                    */
+    int32_t *kv_dst;             /* [sum A]                                                    */
+    int32_t *new_seq_len;        /* [B] L_out                                                  */
+    int32_t *new_kv_len;         /* [B] L_target                                               */
+    int32_t *new_draft_len;      /* [B] L_draft                                                */
+    int32_t *compact_status;     /* [B] req_status | ORACLE_REQ_BAD_BLOCKS                     */
+} oracle_compact_args;
+
+int oracle_compact(const oracle_compact_args *a);
+
+double oracle_gamma_objective(double alpha, double c, int32_t gamma);
+int32_t oracle_choose_gamma(double alpha_sum, int32_t alpha_count, double alpha_prev, double c,
+                            int32_t gamma_min, int32_t gamma_max, double *alpha_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
