@@ -1,0 +1,184 @@
+/*
+ * spec_verify.h - C ABI of the batched speculative-decoding verifier for GB300 (sm_103a).
+ *
+ * One call verifies one round for a batch of B requests. Request i proposed K_i draft tokens
+ * (K_i may differ per request, and may be 0). The caller has run the target model over the
+ * round and passes K_i+1 target logit rows for request i (positions 1..K_i+1) and the K_i
+ * draft logit rows its drafter sampled the tokens from. The verifier applies the rule of
+ * "SOTA-227: Decode with a draft model and an accept-reject rule" (section "What to do",
+ * steps 3-4), which is Rule 2 of "Speculative Decoding Coordination Protocol (SDCP)"
+ * (section "Acceptance Rules"):
+ *   - p_j = softmax(z^target_j / T), q_j = softmax(z^draft_j / T) (SDCP "Session Model":
+ *     temperature is applied first);
+ *   - walking j = 1..K_i left to right, draft x_j is accepted when u_j <= p_j(x_j)/q_j(x_j);
+ *   - at the first rejection the frontier token is drawn from max(p_j - q_j, 0) normalised,
+ *     and the walk stops; if all K_i are accepted it is drawn from p_{K_i+1};
+ *   - with T == 0 the greedy rule applies (SDCP Rule 1): x_j is accepted when it is the
+ *     argmax of p_j (ties to the smallest id) and the frontier token is argmax p_{A+1}.
+ * Every draw is an inverse-CDF lookup in ascending token order: the token chosen is the
+ * smallest v whose inclusive prefix mass exceeds u * (total mass).
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless stated otherwise. The caller owns all memory;
+ *     no entry point allocates, frees or synchronises. Work is enqueued on `stream` in order.
+ *   - Host-detectable argument errors return SPEC_ERR_INVALID_ARG (or SPEC_ERR_UNSUPPORTED)
+ *     before anything is enqueued. A failed launch returns SPEC_ERR_CUDA.
+ *   - Errors in the data of one request (found on the device) are reported per request in
+ *     req_status and never disturb the other requests of the batch (SDCP "Error Handling":
+ *     sdcp-bad-proposal is per proposal).
+ *   - Logit rows must start on 16-byte boundaries: both logits pointers 16-byte aligned and
+ *     V * sizeof(logit) a multiple of 16 (true for V = 32000, 128256, 151936, 256000 ...).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = -1, /* a host-checkable argument is wrong; nothing was enqueued   */
+    SPEC_ERR_WORKSPACE = -2,   /* workspace missing, too small or misaligned                  */
+    SPEC_ERR_CUDA = -3,        /* a CUDA call or launch failed                                */
+    SPEC_ERR_UNSUPPORTED = -4  /* valid request this build cannot serve (e.g. unaligned rows) */
+} spec_status;
+
+/* req_status bits. A request with any bit set emits nothing: accept_len = n_emitted = 0 and
+ * all its out_tokens slots are -1. */
+enum {
+    SPEC_REQ_OK = 0,
+    SPEC_REQ_BAD_PROPOSAL = 1, /* a draft token outside [0, V), or q(x) == 0 (draft logit -inf),
+                                  found before any uniform is used (SDCP Rule 2)             */
+    SPEC_REQ_BAD_LOGITS = 2,   /* a row of the request holds NaN or +inf, or no finite logit  */
+    SPEC_REQ_BAD_SHAPE = 4,    /* K_i < 0, K_i > K_max, or row_off inconsistent               */
+    SPEC_REQ_BAD_PARAM = 8,    /* temperature NaN, infinite or negative                       */
+    SPEC_REQ_BAD_BLOCKS = 16   /* spec_compact: a committed position has no page             */
+};
+
+/* ---- spec_verify ------------------------------------------------------------------------
+ * Layout: target logits are T = sum_i (K_i+1) rows of V values; request i owns rows
+ * row_off[i] .. row_off[i+1]-1, row row_off[i]+j holding position j+1. Draft logits are
+ * T - B rows; request i owns rows row_off[i]-i .. row_off[i+1]-i-2. draft_tokens and the
+ * per-draft outputs use the draft-row index; uniforms and out_tokens use the target-row index.
+ */
+typedef struct {
+    int32_t B;                   /* requests, >= 1                                             */
+    int32_t V;                   /* vocabulary size, >= 1                                      */
+    int32_t K_max;               /* upper bound on every K_i, 0..64 (SDCP: m_max <= 64)         */
+    int32_t total_rows;          /* T = row_off[B] = sum_i (K_i + 1), as known to the host      */
+    spec_dtype dtype;            /* type of both logits tensors                                */
+    const void *target_logits;   /* [T][V]                                                    */
+    const void *draft_logits;    /* [T-B][V] (may be NULL when T == B)                          */
+    const int32_t *row_off;      /* [B+1], row_off[0] = 0, K_i = row_off[i+1]-row_off[i]-1     */
+    const int32_t *draft_tokens; /* [T-B] x_j, sampled by the drafter from q_j                  */
+    const double *uniforms;      /* [T] in [0,1): slot row_off[i]+j, j < K_i, is the accept draw
+                                    of draft j; slot row_off[i]+K_i is the frontier draw       */
+    const float *temperature;    /* [B] per request, or NULL to use temperature_scalar         */
+    float temperature_scalar;
+    const int32_t *stop_token;   /* [B] or NULL: emission stops after this token (-1: none)     */
+    const int32_t *max_new;      /* [B] or NULL: most tokens request i may still emit           */
+    /* outputs */
+    int32_t *accept_len;         /* [B] A_i, drafts accepted by the rule                        */
+    int32_t *n_emitted;          /* [B] tokens emitted: A_i + 1 unless a stop token or max_new
+                                    truncated the round (SDCP "Verification and Commit" step 7)
+                                    (may be NULL)                                              */
+    int32_t *out_tokens;         /* [T] slot row_off[i]+j: emitted token j, -1 past n_emitted   */
+    int32_t *req_status;         /* [B] SPEC_REQ_* bits                                        */
+    float *alpha_rows;           /* [T-B] sum_v min(p_j(v), q_j(v)) per draft row (may be NULL) */
+    double *alpha_sum;           /* device scalar: sum of alpha over draft rows of OK requests
+                                    (may be NULL)                                              */
+    int32_t *alpha_count;        /* device scalar: number of those rows (may be NULL)           */
+    /* diagnostics (each may be NULL) */
+    float *rho_rows;             /* [T-B] p_j(x_j)/q_j(x_j) (greedy: 1 accepted / 0 rejected)   */
+    float *resid_rows;           /* [T-B] sum_v max(p_j - q_j, 0) where the kernel formed the
+                                    residual (rejected positions), else -1                     */
+    float *frontier_prob;        /* [B] probability of the frontier token in the law it was
+                                    drawn from                                                 */
+    float *frontier_margin;      /* [B] distance of u*Z to the nearer end of the frontier
+                                    token's CDF interval, over Z                                */
+    int32_t *fallback;           /* [B] 1 when the residual had zero mass and p was used        */
+    /* profiling (may be NULL): two cudaEvent_t recorded on `stream` immediately before and after
+       the per-position kernel, so a caller can time that kernel alone */
+    cudaEvent_t rows_event_begin;
+    cudaEvent_t rows_event_end;
+} spec_verify_args;
+
+/* Bytes of device workspace spec_verify needs for a batch of total_rows target rows.
+ * The workspace must be 256-byte aligned. Its contents need no initialisation. */
+size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t total_rows, spec_dtype dtype);
+
+/* Verify one round. Enqueues two kernels on `stream`; returns without waiting. */
+spec_status spec_verify(const spec_verify_args *args, void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
+/* ---- spec_compact ------------------------------------------------------------------------
+ * Packs the ragged result of spec_verify ("M7.8 - Speculative Serving", section 0x03C): for
+ * request i with prefix length P_i (target KV rows already committed), E_i accepted drafts
+ * emitted and F_i = 1 when the frontier token was emitted:
+ *   tokens  : packed at out_off[i] .. out_off[i+1]-1, positions P_i .. P_i+n_i-1;
+ *   KV rows : the first E_i candidate rows of the round are committed: kv_src = the caller's
+ *             cand_kv_rows[row_off[i]-i+j], kv_dst = block_table[i][(P_i+j)/page]*page +
+ *             (P_i+j) % page, for j < E_i; the frontier has no KV row yet (section 0x08A);
+ *   lengths : L_out = P_i+E_i+F_i, L_target = P_i+E_i, L_draft = P_i+min(E_i, K_i-1)
+ *             (section 0x09, "EOS and length-limit stopping").
+ * A request with a nonzero req_status, or whose committed positions fall outside its block
+ * table (SPEC_REQ_BAD_BLOCKS), emits and commits nothing and keeps its lengths at P_i.
+ */
+typedef struct {
+    int32_t B, page_size, max_blocks, total_rows;
+    const int32_t *row_off;      /* [B+1] as for spec_verify                                    */
+    const int32_t *accept_len;   /* [B] from spec_verify                                        */
+    const int32_t *n_emitted;    /* [B] from spec_verify (NULL: accept_len + 1)                 */
+    const int32_t *out_tokens;   /* [T] from spec_verify                                        */
+    const int32_t *req_status;   /* [B] from spec_verify (NULL: all OK)                         */
+    const int32_t *prefix_len;   /* [B] P_i                                                    */
+    const int32_t *cand_kv_rows; /* [T-B] physical row holding draft j's candidate target KV    */
+    const int32_t *block_table;  /* [B][max_blocks] page ids                                   */
+    /* outputs; capacities: T tokens, T-B KV pairs */
+    int32_t *out_off;            /* [B+1] exclusive prefix of n_i                               */
+    int32_t *packed_tokens;      /* [T]                                                        */
+    int32_t *packed_pos;         /* [T]                                                        */
+    int32_t *kv_off;             /* [B+1] exclusive prefix of E_i                               */
+    int32_t *kv_src;             /* [T-B]                                                      */
+    int32_t *kv_dst;             /* [T-B]                                                      */
+    int32_t *new_seq_len;        /* [B] L_out                                                  */
+    int32_t *new_kv_len;         /* [B] L_target                                               */
+    int32_t *new_draft_len;      /* [B] L_draft (may be NULL)                                   */
+    int32_t *compact_status;     /* [B] req_status | SPEC_REQ_BAD_BLOCKS (may be NULL)           */
+} spec_compact_args;
+
+/* Enqueues one kernel on `stream`. Needs no workspace. */
+spec_status spec_compact(const spec_compact_args *args, cudaStream_t stream);
+
+/* ---- choosing gamma ---------------------------------------------------------------------
+ * SOTA-227, "Why it is free rather than a trade": with acceptance rate alpha = E[min(p,q)]
+ * and draft cost c relative to the target, drafting gamma tokens improves wall time by
+ *     f(gamma) = (1 - alpha^(gamma+1)) / ((1 - alpha)(gamma*c + 1)),
+ * f = (gamma+1)/(gamma*c+1) at alpha = 1, and gamma is chosen numerically.
+ *
+ * spec_gamma_objective evaluates f on the host (double precision).
+ * spec_choose_gamma runs on the device: alpha = alpha_sum / alpha_count read from device
+ * memory (as written by spec_verify), or alpha_prev when alpha_count == 0; it writes the
+ * maximiser of f over [gamma_min, gamma_max] to *gamma_out (an exact tie goes to the smaller
+ * gamma, as the controller of "M7.8 - Speculative Serving" section 0x07A breaks ties toward
+ * smaller K) and the alpha it used to *alpha_out. All four pointers are device pointers. */
+double spec_gamma_objective(double alpha, double c, int32_t gamma);
+spec_status spec_choose_gamma(const double *alpha_sum, const int32_t *alpha_count,
+                              double alpha_prev, double c, int32_t gamma_min, int32_t gamma_max,
+                              int32_t *gamma_out, double *alpha_out, cudaStream_t stream);
+
+/* Version string of the library build. */
+const char *spec_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,206 @@
+// Ragged compaction of a verified round (spec_compact) and the gamma controller
+// (spec_choose_gamma, spec_gamma_objective). See include/spec_verify.h for the contract.
+//
+// Compaction follows "M7.8 - Speculative Serving", sections 0x03C (L_out = P+A+1, L_kv = P+A;
+// positions stay contiguous, padding never becomes history) and 0x09 (with stopping:
+// L_out = P+E+F, L_target = P+E, L_draft = P+min(E, K-1)). One CTA scans the per-request
+// counts in tiles of 1024 requests, carrying the running offsets, then scatters each request's
+// tokens, positions and KV row moves.
+//
+// The gamma objective is the expected wall-time improvement of SOTA-227 ("Why it is free
+// rather than a trade"): (1 - alpha^(gamma+1)) / ((1 - alpha)(gamma*c + 1)).
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "spec_device.cuh"
+#include "spec_verify.h"
+
+namespace spec {
+
+constexpr int kCompactThreads = 1024;
+
+struct CompactParams {
+    int32_t B, page_size, max_blocks, total_rows;
+    const int32_t *row_off, *accept_len, *n_emitted, *out_tokens, *req_status, *prefix_len,
+        *cand_kv_rows, *block_table;
+    int32_t *out_off, *packed_tokens, *packed_pos, *kv_off, *kv_src, *kv_dst, *new_seq_len,
+        *new_kv_len, *new_draft_len, *compact_status;
+};
+
+// Block-wide exclusive scan of one int per thread; returns the exclusive prefix and the total.
+__device__ __forceinline__ int block_exscan(int v, int *warp_tot, int &total) {
+    const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == kWarp - 1) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int t = warp_tot[lane];
+        int ti = t;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o) ti += n;
+        }
+        warp_tot[lane] = ti - t;  // exclusive prefix of the warp totals
+        if (lane == kWarp - 1) warp_tot[kWarp] = ti;
+    }
+    __syncthreads();
+    const int ex = warp_tot[warp] + incl - v;
+    total = warp_tot[kWarp];
+    __syncthreads();
+    return ex;
+}
+
+__global__ void __launch_bounds__(kCompactThreads) spec_compact_kernel(const CompactParams P) {
+    __shared__ int tot_n[kWarp + 1];
+    __shared__ int tot_e[kWarp + 1];
+    int carry_n = 0, carry_e = 0;
+    // offsets must start at 0, end at total_rows and grow by at least one row per request;
+    // otherwise every request is BAD_SHAPE, so packed writes stay within their capacities
+    int bad_off = (P.row_off[0] != 0) || (P.row_off[P.B] != P.total_rows);
+    for (int i = threadIdx.x; i < P.B && !bad_off; i += kCompactThreads)
+        if (P.row_off[i + 1] <= P.row_off[i]) bad_off = 1;
+    const bool offsets_ok = !__syncthreads_or(bad_off);
+    for (int base = 0; base < P.B; base += kCompactThreads) {
+        const int i = base + static_cast<int>(threadIdx.x);
+        int n = 0, E = 0, status = 0, K = 0, r0 = 0, Pi = 0;
+        if (i < P.B) {
+            r0 = P.row_off[i];
+            K = P.row_off[i + 1] - r0 - 1;
+            Pi = P.prefix_len[i];
+            status = P.req_status ? P.req_status[i] : 0;
+            if (!offsets_ok || K < 0 || r0 < 0 || P.row_off[i + 1] > P.total_rows) status |= SPEC_REQ_BAD_SHAPE;
+            if (!status) {
+                const int A = P.accept_len[i];
+                n = P.n_emitted ? P.n_emitted[i] : A + 1;
+                if (A < 0 || A > K || n < 0 || n > K + 1) status |= SPEC_REQ_BAD_SHAPE;
+                E = min(A, n);
+                // every committed position P..P+E-1 needs a page of this request's table
+                if (!status && E > 0) {
+                    if (Pi < 0 || (Pi + E - 1) / P.page_size >= P.max_blocks) {
+                        status |= SPEC_REQ_BAD_BLOCKS;
+                    } else {
+                        for (int pg = Pi / P.page_size; pg <= (Pi + E - 1) / P.page_size; ++pg)
+                            if (P.block_table[static_cast<int64_t>(i) * P.max_blocks + pg] < 0) status |= SPEC_REQ_BAD_BLOCKS;
+                    }
+                }
+                if (status) n = E = 0;
+            }
+        }
+        int total_n, total_e;
+        const int off_n = carry_n + block_exscan(n, tot_n, total_n);
+        const int off_e = carry_e + block_exscan(E, tot_e, total_e);
+        if (i < P.B) {
+            P.out_off[i] = off_n;
+            P.kv_off[i] = off_e;
+            for (int j = 0; j < n; ++j) {
+                P.packed_tokens[off_n + j] = P.out_tokens[r0 + j];
+                P.packed_pos[off_n + j] = Pi + j;
+            }
+            const int d0 = r0 - i;
+            for (int j = 0; j < E; ++j) {
+                const int pos = Pi + j;
+                const int blk = P.block_table[static_cast<int64_t>(i) * P.max_blocks + pos / P.page_size];
+                P.kv_src[off_e + j] = P.cand_kv_rows[d0 + j];
+                P.kv_dst[off_e + j] = blk * P.page_size + pos % P.page_size;
+            }
+            P.new_seq_len[i] = Pi + n;
+            P.new_kv_len[i] = Pi + E;
+            if (P.new_draft_len) P.new_draft_len[i] = Pi + max(min(E, K - 1), 0);
+            if (P.compact_status) P.compact_status[i] = status;
+        }
+        carry_n += total_n;
+        carry_e += total_e;
+    }
+    if (threadIdx.x == 0) {
+        P.out_off[P.B] = carry_n;
+        P.kv_off[P.B] = carry_e;
+    }
+}
+
+__host__ __device__ inline double gamma_objective(double alpha, double c, int gamma) {
+    if (alpha == 1.0) return (gamma + 1.0) / (gamma * c + 1.0);
+    double pw = alpha;  // alpha^(gamma+1)
+    for (int k = 0; k < gamma; ++k) pw *= alpha;
+    return (1.0 - pw) / ((1.0 - alpha) * (gamma * c + 1.0));
+}
+
+__global__ void spec_gamma_kernel(const double *alpha_sum, const int32_t *alpha_count, double alpha_prev,
+                                  double c, int gmin, int gmax, int32_t *gamma_out, double *alpha_out) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const int n = *alpha_count;
+    double alpha = n > 0 ? *alpha_sum / static_cast<double>(n) : alpha_prev;
+    alpha = fmin(fmax(alpha, 0.0), 1.0);
+    int best = gmin;
+    double fb = gamma_objective(alpha, c, gmin);
+    for (int g = gmin + 1; g <= gmax; ++g) {
+        const double f = gamma_objective(alpha, c, g);
+        if (f > fb) {  // strict: an exact tie keeps the smaller gamma
+            fb = f;
+            best = g;
+        }
+    }
+    *gamma_out = best;
+    *alpha_out = alpha;
+}
+
+}  // namespace spec
+
+using namespace spec;
+
+extern "C" spec_status spec_compact(const spec_compact_args *a, cudaStream_t stream) {
+    if (!a) return SPEC_ERR_INVALID_ARG;
+    if (a->B < 1 || a->page_size < 1 || a->max_blocks < 1 || a->total_rows < a->B) return SPEC_ERR_INVALID_ARG;
+    if (!a->row_off || !a->accept_len || !a->out_tokens || !a->prefix_len || !a->block_table || !a->out_off ||
+        !a->packed_tokens || !a->packed_pos || !a->kv_off || !a->new_seq_len || !a->new_kv_len)
+        return SPEC_ERR_INVALID_ARG;
+    if (a->total_rows > a->B && (!a->cand_kv_rows || !a->kv_src || !a->kv_dst)) return SPEC_ERR_INVALID_ARG;
+    CompactParams P;
+    P.B = a->B;
+    P.page_size = a->page_size;
+    P.max_blocks = a->max_blocks;
+    P.total_rows = a->total_rows;
+    P.row_off = a->row_off;
+    P.accept_len = a->accept_len;
+    P.n_emitted = a->n_emitted;
+    P.out_tokens = a->out_tokens;
+    P.req_status = a->req_status;
+    P.prefix_len = a->prefix_len;
+    P.cand_kv_rows = a->cand_kv_rows;
+    P.block_table = a->block_table;
+    P.out_off = a->out_off;
+    P.packed_tokens = a->packed_tokens;
+    P.packed_pos = a->packed_pos;
+    P.kv_off = a->kv_off;
+    P.kv_src = a->kv_src;
+    P.kv_dst = a->kv_dst;
+    P.new_seq_len = a->new_seq_len;
+    P.new_kv_len = a->new_kv_len;
+    P.new_draft_len = a->new_draft_len;
+    P.compact_status = a->compact_status;
+    spec_compact_kernel<<<1, kCompactThreads, 0, stream>>>(P);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+extern "C" double spec_gamma_objective(double alpha, double c, int32_t gamma) {
+    return gamma_objective(alpha, c, gamma);
+}
+
+extern "C" spec_status spec_choose_gamma(const double *alpha_sum, const int32_t *alpha_count, double alpha_prev,
+                                         double c, int32_t gamma_min, int32_t gamma_max, int32_t *gamma_out,
+                                         double *alpha_out, cudaStream_t stream) {
+    if (!alpha_sum || !alpha_count || !gamma_out || !alpha_out) return SPEC_ERR_INVALID_ARG;
+    if (gamma_min < 0 || gamma_max < gamma_min || gamma_max > 4096) return SPEC_ERR_INVALID_ARG;
+    if (!(c >= 0.0) || !std::isfinite(c) || !(alpha_prev >= 0.0 && alpha_prev <= 1.0)) return SPEC_ERR_INVALID_ARG;
+    spec_gamma_kernel<<<1, 32, 0, stream>>>(alpha_sum, alpha_count, alpha_prev, c, gamma_min, gamma_max, gamma_out,
+                                            alpha_out);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}

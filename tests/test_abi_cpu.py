@@ -1,0 +1,141 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol, and rejects bad
+host arguments before touching the GPU. Also the host-side gamma objective and the seeded
+input generators. No compute call here needs a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_43_gb300 import build
+    build.build()
+    from speculative_decoding_verification_43_gb300 import _lib
+    return _lib
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "spec_verify.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(lib.EXPORTS), names
+    raw = ctypes.CDLL(lib.LIB_PATH if hasattr(lib, "LIB_PATH") else lib.lib._name)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_version_string(lib):
+    assert b"sm_103a" in lib.lib.spec_version()
+
+
+def _args(lib, **kw):
+    a = lib.SpecVerifyArgs()
+    a.B, a.V, a.K_max, a.total_rows, a.dtype = 4, 1024, 4, 8, lib.SPEC_BF16
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    for f in ("target_logits", "draft_logits", "row_off", "draft_tokens", "uniforms", "accept_len",
+              "out_tokens", "req_status"):
+        setattr(a, f, fake)
+    a.temperature_scalar = 1.0
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,want", [
+    ("B", 0, -1), ("V", 0, -1), ("K_max", 65, -1), ("K_max", -1, -1), ("total_rows", 3, -1),
+    ("total_rows", 100, -1), ("dtype", 7, -1), ("target_logits", None, -1), ("uniforms", None, -1),
+    ("row_off", None, -1), ("accept_len", None, -1), ("draft_logits", None, -1),
+    ("temperature_scalar", float("nan"), -1), ("temperature_scalar", -1.0, -1),
+    ("V", 1001, -4),                                     # bf16 row of 2002 bytes: not 16-aligned
+    ("target_logits", ctypes.c_void_p(0x10008), -4),     # misaligned base
+])
+def test_host_argument_checks(lib, field, value, want):
+    a = _args(lib, **{field: value})
+    ws = ctypes.c_void_p(0x20000)
+    rc = lib.lib.spec_verify(ctypes.byref(a), ws, 1 << 20, None)
+    assert rc == want
+
+
+def test_workspace_checks(lib):
+    a = _args(lib)
+    need = lib.lib.spec_verify_workspace_size(4, 1024, 8, lib.SPEC_BF16)
+    assert need > 0 and need % 256 == 0
+    assert lib.lib.spec_verify(ctypes.byref(a), None, need, None) == -2
+    assert lib.lib.spec_verify(ctypes.byref(a), ctypes.c_void_p(0x20000), need - 1, None) == -2
+    assert lib.lib.spec_verify(ctypes.byref(a), ctypes.c_void_p(0x20010), need, None) == -2
+
+
+def test_compact_and_gamma_argument_checks(lib):
+    c = lib.SpecCompactArgs()
+    c.B, c.page_size, c.max_blocks, c.total_rows = 4, 0, 8, 8
+    assert lib.lib.spec_compact(ctypes.byref(c), None) == -1
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.lib.spec_choose_gamma(fake, fake, 0.5, -1.0, 0, 8, fake, fake, None) == -1
+    assert lib.lib.spec_choose_gamma(fake, fake, 0.5, 0.1, 5, 2, fake, fake, None) == -1
+    assert lib.lib.spec_choose_gamma(None, fake, 0.5, 0.1, 0, 8, fake, fake, None) == -1
+    assert lib.lib.spec_choose_gamma(fake, fake, 1.5, 0.1, 0, 8, fake, fake, None) == -1
+
+
+def test_gamma_objective_matches_oracle(lib):
+    import oracle
+    rng = np.random.default_rng(0)
+    for _ in range(500):
+        a = float(rng.choice([rng.random(), 1.0, 0.0]))
+        c = float(rng.random() * rng.choice([0.01, 0.3, 2.0]))
+        g = int(rng.integers(0, 20))
+        want = oracle.gamma_objective(a, c, g)
+        got = lib.lib.spec_gamma_objective(a, c, g)
+        assert abs(got - want) <= 1e-14 * max(1.0, abs(want))
+
+
+def test_workload_generator_is_seeded_and_shaped():
+    from speculative_decoding_verification_43_gb300 import workloads as W
+    wl = W.scaled(W.WORKLOADS["c3"], B=8, V=2048)
+    a = W.make_round(wl, seed=4, rnd=1)
+    b = W.make_round(wl, seed=4, rnd=1)
+    c = W.make_round(wl, seed=4, rnd=2)
+    assert torch.equal(a.target, b.target) and torch.equal(a.draft_tokens, b.draft_tokens)
+    assert not torch.equal(a.target, c.target)
+    np.testing.assert_array_equal(a.K, c.K)  # the batch shape depends on the seed only
+    assert a.target.dtype == torch.bfloat16 and a.target.shape == (int(a.row_off[-1]), 2048)
+    assert a.draft.shape == (int(a.row_off[-1]) - 8, 2048)
+    assert ((a.draft_tokens >= 0) & (a.draft_tokens < 2048)).all()
+    u = a.uniforms.numpy()
+    assert ((u >= 0) & (u < 1)).all()
+    assert np.all(np.floor(u * 2.0 ** 53) == u * 2.0 ** 53)  # 53-bit values k / 2^53
+
+
+def test_workload_k_distributions():
+    from speculative_decoding_verification_43_gb300 import workloads as W
+    k3 = W.WORKLOADS["c3"].k_values(0)
+    assert len(k3) == 64 and k3.min() >= 0 and k3.max() <= 7
+    k5 = W.WORKLOADS["c5"].k_values(0)
+    assert (k5 == 2).sum() == 128 and (k5 == 1).sum() == 128 and (k5 == 0).sum() == 256
+    assert (W.WORKLOADS["c4"].k_values(0) == 3).all()
+    assert W.WORKLOADS["c5"].bytes_per_round(0) == 1280 * 256000 * 2
+
+
+def test_zipf_rows_follow_the_recipe():
+    from speculative_decoding_verification_43_gb300 import workloads as W
+    wl = W.Workload("z", B=4, V=4096, dtype=torch.float32, temperature=1.0, logits="zipf", sigma=1.0,
+                    draft_sigma=0.0, K="fixed:1")
+    rd = W.make_round(wl, seed=1)
+    row = rd.target[0].double().numpy()
+    # sorted logits track -1.1 ln(rank) up to the N(0,1) noise
+    ranks = np.arange(1, 4097)
+    srt = np.sort(row)[::-1]
+    assert np.abs(np.mean(srt[1000:3000] + 1.1 * np.log(ranks[1000:3000]))) < 0.5
+    # draft noise 0 gives the same row
+    assert torch.equal(rd.draft[0], rd.target[0])
