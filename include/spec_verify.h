@@ -119,6 +119,19 @@ size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t total_rows, spec
 spec_status spec_verify(const spec_verify_args *args, void *workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 
+/* spec_verify without a caller-supplied workspace, for callers that cannot allocate device
+ * memory where they verify (a memory planner that owns all device memory, a callback inside
+ * another runtime, a path where cudaMalloc's synchronisation is not acceptable). The pages have
+ * no counterpart to this entry point: it is an interface convenience of this library.
+ * Scratch comes from one fixed array of 448 KiB in the library's device memory, present on
+ * every GPU that loads the library until exit. Limit: total_rows <= 16384 target rows per
+ * call; larger batches return SPEC_ERR_UNSUPPORTED before anything is enqueued. The array's
+ * address is looked up on the first call on each device (make that call before any stream
+ * capture). All calls share the array: calls that overlap on the GPU (other streams, other
+ * threads) race on it and must be serialised by the caller. Arguments, outputs and errors are
+ * otherwise those of spec_verify. */
+spec_status spec_verify_noalloc(const spec_verify_args *args, cudaStream_t stream);
+
 /* ---- spec_compact ------------------------------------------------------------------------
  * Packs the ragged result of spec_verify ("M7.8 - Speculative Serving", section 0x03C): for
  * request i with prefix length P_i (target KV rows already committed), E_i accepted drafts

@@ -28,6 +28,8 @@ REQ_BAD_SHAPE = 4
 REQ_BAD_PARAM = 8
 REQ_BAD_BLOCKS = 16
 
+NOALLOC_MAX_ROWS = 16384
+
 STATUS_NAMES = {
     SPEC_OK: "SPEC_OK", SPEC_ERR_INVALID_ARG: "SPEC_ERR_INVALID_ARG",
     SPEC_ERR_WORKSPACE: "SPEC_ERR_WORKSPACE", SPEC_ERR_CUDA: "SPEC_ERR_CUDA",
@@ -60,8 +62,8 @@ class SpecCompactArgs(ctypes.Structure):
 
 
 # every symbol include/spec_verify.h declares
-EXPORTS = ("spec_verify_workspace_size", "spec_verify", "spec_compact", "spec_gamma_objective",
-           "spec_choose_gamma", "spec_version")
+EXPORTS = ("spec_verify_workspace_size", "spec_verify", "spec_verify_noalloc", "spec_compact",
+           "spec_gamma_objective", "spec_choose_gamma", "spec_version")
 
 
 def _load():
@@ -74,6 +76,8 @@ def _load():
     lib.spec_verify_workspace_size.restype = ctypes.c_size_t
     lib.spec_verify.argtypes = [ctypes.POINTER(SpecVerifyArgs), _p, ctypes.c_size_t, _p]
     lib.spec_verify.restype = ctypes.c_int
+    lib.spec_verify_noalloc.argtypes = [ctypes.POINTER(SpecVerifyArgs), _p]
+    lib.spec_verify_noalloc.restype = ctypes.c_int
     lib.spec_compact.argtypes = [ctypes.POINTER(SpecCompactArgs), _p]
     lib.spec_compact.restype = ctypes.c_int
     lib.spec_gamma_objective.argtypes = [ctypes.c_double, ctypes.c_double, _i32]

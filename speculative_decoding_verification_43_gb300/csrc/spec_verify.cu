@@ -1122,3 +1122,51 @@ extern "C" spec_status spec_verify(const spec_verify_args *a, void *workspace, s
 }
 
 extern "C" const char *spec_version(void) { return "spec-verify-gb300 0.1 (sm_103a)"; }
+
+// ------------------------------------------------------------------------------------------
+// spec_verify_noalloc: spec_verify for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at the point where they verify a round: a serving
+// engine whose memory planner has already reserved every byte of the device, a plugin that
+// runs inside another runtime's allocator or scheduler callbacks, or a latency-critical loop
+// where an allocation's implicit synchronisation and possible failure are not acceptable.
+// For them this entry point takes its workspace from a fixed array in the library's own
+// device memory instead of from the caller.
+//
+// The array lives in every GPU that loads the library until the process exits. Its address
+// is looked up once per device, on the first call made with that device current; make that
+// first call before any stream capture. All calls share the one array and it keeps the last
+// call's contents (the kernels write every workspace entry before reading it, so nothing
+// needs clearing); calls that overlap on the GPU, on two streams or from two threads, race
+// on it and must be serialised by the caller.
+
+namespace spec {
+constexpr int32_t kNoallocMaxRows = 16384;  // target rows per call: T = sum_i (K_i + 1)
+constexpr size_t kNoallocScratchBytes = 7 * 65536;  // = workspace of kNoallocMaxRows rows
+static __device__ __align__(256) unsigned char noalloc_scratch[kNoallocScratchBytes];
+
+static std::mutex noalloc_mu;
+static void *noalloc_ptr[64] = {nullptr};
+}  // namespace spec
+
+extern "C" spec_status spec_verify_noalloc(const spec_verify_args *a, cudaStream_t stream) {
+    if (!a) return SPEC_ERR_INVALID_ARG;
+    if (a->total_rows > kNoallocMaxRows) return SPEC_ERR_UNSUPPORTED;  // beyond the fixed scratch
+    const size_t need = ws_layout(a->B, a->total_rows).total;
+    if (need > kNoallocScratchBytes) return SPEC_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
+    void *ptr = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(noalloc_mu);
+        if (!noalloc_ptr[dev]) {
+            // host code must not use the array's name as a device address: ask the runtime
+            if (cudaGetSymbolAddress(&noalloc_ptr[dev], noalloc_scratch) != cudaSuccess) {
+                noalloc_ptr[dev] = nullptr;
+                return SPEC_ERR_CUDA;
+            }
+        }
+        ptr = noalloc_ptr[dev];
+    }
+    return spec_verify(a, ptr, kNoallocScratchBytes, stream);
+}
