@@ -32,7 +32,7 @@
 
 namespace spec {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / kWarp;
 constexpr int kVecPerLane = 4;                   // 16-byte vectors per lane in one group
 constexpr int kGroupVecs = kWarp * kVecPerLane;  // 128 vectors = 2 KiB per row per group
@@ -48,21 +48,19 @@ struct Elt;
 template <>
 struct Elt<SPEC_F32> {
     static constexpr int kPerVec = 4;
-    static constexpr int kBytes = 4;
     __device__ static __forceinline__ void unpack(const uint4 &w, float *y) {
         y[0] = __uint_as_float(w.x);
         y[1] = __uint_as_float(w.y);
         y[2] = __uint_as_float(w.z);
         y[3] = __uint_as_float(w.w);
     }
-    __device__ static __forceinline__ float load1(const void *base, size_t k) {
-        return __ldg(static_cast<const float *>(base) + k);
+    __device__ static __forceinline__ float at(const uint4 *buf, int e) {
+        return reinterpret_cast<const float *>(buf)[e];
     }
 };
 template <>
 struct Elt<SPEC_BF16> {
     static constexpr int kPerVec = 8;
-    static constexpr int kBytes = 2;
     // bfloat16 is the upper half of a binary32: widening is a shift. The element at the lower
     // address is the low half of each 32-bit word.
     __device__ static __forceinline__ void unpack(const uint4 &w, float *y) {
@@ -73,11 +71,55 @@ struct Elt<SPEC_BF16> {
             y[2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
         }
     }
-    __device__ static __forceinline__ float load1(const void *base, size_t k) {
-        const uint16_t b = __ldg(static_cast<const unsigned short *>(base) + k);
+    __device__ static __forceinline__ float at(const uint4 *buf, int e) {
+        const uint16_t b = reinterpret_cast<const uint16_t *>(buf)[e];
         return __uint_as_float(static_cast<uint32_t>(b) << 16);
     }
 };
+
+// ---- two-float arithmetic: a value hi + lo carried in float32 (about 48 significant bits).
+// FP64 runs at a small fraction of the FP32 rate on this part, so sums that need more than
+// float32 precision are kept as float pairs instead.
+struct F2 {
+    float hi, lo;
+};
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+    const float s = a.hi + b.hi;
+    const float bb = s - a.hi;
+    float e = (a.hi - (s - bb)) + (b.hi - bb);
+    e += a.lo + b.lo;
+    const float hi = s + e;
+    return {hi, e - (hi - s)};
+}
+// a * 2^k, exact; k is clamped so that a wild exponent gives 0 rather than undefined behaviour
+__device__ __forceinline__ F2 f2_scale(F2 a, float k) {
+    const int kk = static_cast<int>(fminf(fmaxf(k, -300.0f), 300.0f));
+    return {ldexpf(a.hi, kk), ldexpf(a.lo, kk)};
+}
+__device__ __forceinline__ float scale2(float a, float k) {
+    return ldexpf(a, static_cast<int>(fminf(fmaxf(k, -300.0f), 300.0f)));
+}
+__device__ __forceinline__ F2 warp_sum_f2(F2 v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        F2 w;
+        w.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+        w.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+        v = f2_add(v, w);
+    }
+    return v;
+}
+// a / b for positive a, b: a first quotient, then the quotient of the exact remainder
+__device__ __forceinline__ F2 f2_div(F2 a, F2 b) {
+    const float q1 = a.hi / b.hi;
+    const float p_hi = q1 * b.hi;
+    const float p_err = fmaf(q1, b.hi, -p_hi);
+    const float r = ((a.hi - p_hi) - p_err) + a.lo - q1 * b.lo;
+    const float q2 = r / b.hi;
+    const float hi = q1 + q2;
+    return {hi, q2 - (hi - q1)};
+}
+__device__ __forceinline__ double f2_d(F2 a) { return static_cast<double>(a.hi) + static_cast<double>(a.lo); }
 
 struct RowsParams {
     const void *target;
@@ -105,34 +147,45 @@ struct RowsParams {
     float *resid_rows;
 };
 
-// What every CTA of a cluster publishes to its peers (read through DSMEM).
-struct Exchange {
-    double S[2];       // sum over the slice of 2^(y*s - Bref[r]) (stats path)
-    double part_alpha; // this slice's share of alpha (normalised)
-    double part_Z;     // this slice's residual mass, in units of 2^Bref[0]
-    float Bref[2];     // reference exponent of S[r] (log2 units)
-    float gmax[2];     // greedy: max logit of the slice
-    int32_t garg[2];   // greedy: smallest index attaining it (global token id)
-    int32_t bad[2];    // a NaN / +inf was seen in the slice
+// What a CTA publishes after pass 1; it writes its record into slot `rank` of every CTA of
+// the cluster (distributed shared memory), so that after the cluster barrier all reads are
+// local. Fields are 32-bit words.
+struct Ex1 {
+    float B[2];      // integral reference exponent of S[r] (-inf: no mass)
+    float S_hi[2];   // sum over the slice of 2^(y*s - B[r]), as a float pair
+    float S_lo[2];
+    int32_t bad[2];  // a NaN / +inf was seen in row r's slice
+    float yx[2];     // target / draft logit at the draft token, from the CTA that holds it
+    int32_t has_x;
+    float gmax[2];   // greedy rule: max logit of the slice and the smallest index attaining it
+    int32_t garg[2];
 };
+constexpr int kEx1Words = sizeof(Ex1) / 4;
+// What a CTA publishes after pass 2.
+struct Ex2 {
+    float alpha;     // this slice's share of alpha (normalised)
+    float Z_hi;      // this slice's residual mass, units of 2^B_t (float pair)
+    float Z_lo;
+};
+constexpr int kEx2Words = sizeof(Ex2) / 4;
 
 // Item-wide values, computed once and broadcast through shared memory.
 struct ItemInfo {
     int32_t req, pos, K, drow, status, pair, greedy, accept, x, sample_kind;
-    int32_t lo;        // first vector of this CTA's slice
-    int32_t nvec;      // vectors in this CTA's slice
-    int32_t groups;    // groups in this CTA's slice
+    int32_t lo;      // first vector of this CTA's slice
+    int32_t nvec;    // vectors in this CTA's slice
+    int32_t groups;  // groups in this CTA's slice
     int32_t nchunk;
-    int32_t owner;     // CTA that draws the candidate (-1: none)
+    int32_t owner;   // CTA that draws the candidate (-1: none)
     double u_acc, u_s;
-    float s_hi, s_lo, s32;
-    float B_t, B_d;    // cluster-wide reference exponents
-    double S_t, S_d;   // cluster-wide sums
+    float s_hi, s_lo;  // log2(e)/T = s_hi + s_lo, s_hi rounded toward zero (s_lo > 0)
+    float B_t, B_d;    // cluster-wide integral reference exponents
+    F2 S_t, S_d;       // cluster-wide sums in those units
     float c_t, c_d;    // B + log2 S, for the alpha-only path
-    float lam_hi, lam_lo;
-    double rho, alpha, Zres, target_t, owner_prefix, Ztot;
+    F2 lam;            // S_t / S_d
+    float rho, alpha, inv_St;
+    double target_t, owner_prefix, Ztot, Zres;
     int32_t argmax_t, argmax_d;
-    float yx_t, yx_d;
 };
 
 enum { SAMPLE_NONE = 0, SAMPLE_RESIDUAL = 1, SAMPLE_P = 2 };
@@ -171,8 +224,8 @@ __device__ __forceinline__ float vec_max(const uint4 &w) {
     }
 }
 
-// 2^(y*s - b) with s held as s_hi + s_lo (s_lo > 0): the product with s_hi and the subtraction
-// of b round once, to the small result, then the s_lo term is added. y = -inf gives -inf.
+// y*s - b with s = s_hi + s_lo (s_lo > 0): the product with s_hi and the subtraction of b round
+// once, to the small result, then the s_lo term is added. y = -inf gives -inf.
 __device__ __forceinline__ float exp_arg(float y, float s_hi, float s_lo, float b) {
     return fmaf(y, s_lo, fmaf(y, s_hi, -b));
 }
@@ -194,7 +247,7 @@ __device__ __forceinline__ void vec_weights(int kind, const uint4 *buf_t, const 
         for (int e = 0; e < E; ++e) {
             const float et = ex2(exp_arg(yt[e], I.s_hi, I.s_lo, I.B_t));
             const float ed = ex2(exp_arg(yd[e], I.s_hi, I.s_lo, I.B_d));
-            w[e] = fmaxf(fmaf(-I.lam_lo, ed, fmaf(-I.lam_hi, ed, et)), 0.0f);
+            w[e] = fmaxf(fmaf(-I.lam.lo, ed, fmaf(-I.lam.hi, ed, et)), 0.0f);
         }
     } else {
 #pragma unroll
@@ -202,18 +255,35 @@ __device__ __forceinline__ void vec_weights(int kind, const uint4 *buf_t, const 
     }
 }
 
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Lane l < C copies `words` 32-bit words of the local record into slot `rank` of CTA l.
+__device__ __forceinline__ void push_record(const void *mine, void *slot_base, int rank, int words, int C,
+                                            int lane) {
+    if (lane < C) {
+        const uint32_t *src = static_cast<const uint32_t *>(mine);
+        const uint32_t dst = dsmem_map(static_cast<uint32_t *>(slot_base) + rank * words, lane);
+        for (int w = 0; w < words; ++w) st_cluster_u32(dst + 4 * w, src[w]);
+    }
+}
+
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams P) {
+__global__ void __launch_bounds__(kThreads, 6) spec_rows_kernel(const RowsParams P) {
     constexpr int E = Elt<DT>::kPerVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[2][kMaxChunks];
-    __shared__ Exchange xch;
+    __shared__ Ex1 xch1[kMaxCluster];
+    __shared__ Ex2 xch2[kMaxCluster];
+    __shared__ Ex1 mine1;
+    __shared__ Ex2 mine2;
     __shared__ ItemInfo I;
-    __shared__ double red_f64[kWarps];
+    __shared__ float red_f[kWarps];
 
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-    const uint32_t C = cluster_nctarank();
-    const uint32_t crank = cluster_ctarank();
+    const int C = static_cast<int>(cluster_nctarank());
+    const int crank = static_cast<int>(cluster_ctarank());
     const int item = static_cast<int>(cluster_id_x());
 
     uint4 *buf_t = reinterpret_cast<uint4 *>(smem_raw);
@@ -231,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
         I.lo = lo;
         I.nvec = hi - lo;
         I.groups = (I.nvec + kGroupVecs - 1) / kGroupVecs;
-        I.nchunk = min(kMaxChunks, I.groups);
+        I.nchunk = max(1, min(kMaxChunks, I.groups / kWarps));
         for (int r = 0; r < 2; ++r)
             for (int k = 0; k < kMaxChunks; ++k) mbar_init(&bars[r][k], 1);
         fence_mbar_init();
@@ -247,24 +317,45 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
         }
     }
 
-    // ---- which request and position this item is (warp 0: a 32-way search of row_off) ----
+    // ---- which request and position this item is (warp 0) ----
+    // Loads whose values are needed only after pass 1 (the draft token, the uniforms) are
+    // issued here and consumed later, so their latency hides behind the copies.
+    int x_reg = -1;
+    double u_acc_reg = 0.0, u_s_reg = 0.0;
     if (warp == 0) {
-        int lo = 0, hi = P.B;  // answer i in [lo, hi): row_off[i] <= item < row_off[i+1]
-        while (hi - lo > kWarp) {
-            const int step = (hi - lo + kWarp - 1) / kWarp;
-            const int idx = lo + lane * step;
+        int i;
+        if (P.B < 8 * kWarp) {
+            // one round trip: lane l holds row_off[8l .. 8l+7]; i + 1 offsets are <= item
+            int vals[8];
+            int cnt = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int idx = lane * 8 + k;
+                vals[k] = idx <= P.B ? __ldg(P.row_off + idx) : INT_MAX;
+                cnt += vals[k] <= item;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+            i = cnt - 1;
+        } else {
+            int lo = 0, hi = P.B;  // answer i in [lo, hi): row_off[i] <= item < row_off[i+1]
+            while (hi - lo > kWarp) {
+                const int step = (hi - lo + kWarp - 1) / kWarp;
+                const int idx = lo + lane * step;
+                const int v = idx < hi ? __ldg(P.row_off + idx) : INT_MAX;
+                const unsigned m = __ballot_sync(0xffffffffu, v <= item);
+                const int l = m ? 31 - __clz(static_cast<int>(m)) : 0;
+                lo = lo + l * step;
+                hi = min(lo + step, hi);
+            }
+            const int idx = lo + lane;
             const int v = idx < hi ? __ldg(P.row_off + idx) : INT_MAX;
             const unsigned m = __ballot_sync(0xffffffffu, v <= item);
-            const int l = m ? 31 - __clz(static_cast<int>(m)) : 0;
-            lo = lo + l * step;
-            hi = min(lo + step, hi);
+            i = m ? lo + 31 - __clz(static_cast<int>(m)) : -1;
         }
-        const int idx = lo + lane;
-        const int v = idx < hi ? __ldg(P.row_off + idx) : INT_MAX;
-        const unsigned m = __ballot_sync(0xffffffffu, v <= item);
         if (lane == 0) {
             int status = 0;
-            const int i = m ? lo + 31 - __clz(static_cast<int>(m)) : -1;
+            if (i < 0 || i >= P.B) i = -1;
             int r0 = 0, r1 = 0, K = -1, j = -1, d = -1;
             if (i >= 0) {
                 r0 = __ldg(P.row_off + i);
@@ -281,8 +372,7 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
             I.K = K;
             I.drow = d;
             I.pair = (status == 0 && j < K) ? 1 : 0;
-            const float T = (i >= 0) ? (P.temperature ? __ldg(P.temperature + i) : P.temperature_scalar)
-                                     : 1.0f;
+            const float T = (i >= 0) ? (P.temperature ? __ldg(P.temperature + i) : P.temperature_scalar) : 1.0f;
             if (!(T >= 0.0f) || isinf(T)) status |= SPEC_REQ_BAD_PARAM;
             I.greedy = (T == 0.0f) ? 1 : 0;
             const double s64 = (T > 0.0f && !isinf(T)) ? kLog2e / static_cast<double>(T) : 0.0;
@@ -290,32 +380,17 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
             // gives -inf in both terms of exp_arg (a negative s_lo would make it NaN)
             I.s_hi = __double2float_rz(s64);
             I.s_lo = fmaxf(static_cast<float>(s64 - static_cast<double>(I.s_hi)), 1.401298464e-45f);
-            I.s32 = I.s_hi;
-            I.x = -1;
-            I.yx_t = I.yx_d = 0.0f;
             if (status == 0) {
-                I.u_acc = __ldg(P.uniforms + item);
-                I.u_s = __ldg(P.uniforms + r1 - 1);
-                if (I.pair) {
-                    const int x = __ldg(P.draft_tokens + d);
-                    I.x = x;
-                    if (x < 0 || x >= P.V) {
-                        status |= SPEC_REQ_BAD_PROPOSAL;
-                    } else {
-                        I.yx_t = Elt<DT>::load1(P.target, static_cast<size_t>(item) * P.V + x);
-                        I.yx_d = Elt<DT>::load1(P.draft, static_cast<size_t>(d) * P.V + x);
-                        // q(x) == 0 is a bad proposal for Rule 2 (checked before any draw)
-                        if (!I.greedy && I.yx_d == -INFINITY) status |= SPEC_REQ_BAD_PROPOSAL;
-                    }
-                }
+                u_acc_reg = __ldg(P.uniforms + item);
+                u_s_reg = __ldg(P.uniforms + r1 - 1);
+                if (I.pair) x_reg = __ldg(P.draft_tokens + d);
             }
             I.status = status;
             // draft copies, once the draft row is known
             if (I.pair) {
                 const uint64_t pol = policy_evict_first();
                 const unsigned char *src = static_cast<const unsigned char *>(P.draft) +
-                                           static_cast<size_t>(d) * row_bytes +
-                                           static_cast<size_t>(I.lo) * 16;
+                                           static_cast<size_t>(d) * row_bytes + static_cast<size_t>(I.lo) * 16;
                 for (int k = 0; k < I.nchunk; ++k) {
                     int g0, g1, v0, v1;
                     chunk_range(I.groups, I.nchunk, k, I.nvec, g0, g1, v0, v1);
@@ -377,8 +452,9 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
                         if (vi < nvec) mx = fmaxf(mx, vec_max<DT>(buf[vi]));
                     }
                     mx = warp_max(mx);
-                    // reference exponent: all -inf group -> 0 (its sum is 0, or NaN if a NaN hides)
-                    const float b = (mx == -INFINITY) ? 0.0f : mx * s_hi;
+                    // integral reference exponent, so that rescaling groups is exact (ldexp);
+                    // an all -inf group gets 0 (its sum is 0, or NaN if a NaN hides in it)
+                    const float b = (mx == -INFINITY) ? 0.0f : floorf(mx * s_hi);
                     float acc = 0.0f;
 #pragma unroll
                     for (int q = 0; q < kVecPerLane; ++q) {
@@ -396,9 +472,10 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
             }
         }
     }
+    if (warp == 0 && lane == 0) I.x = x_reg;
     __syncthreads();
 
-    // ---- combine the groups of this CTA (warp r handles row r) ----
+    // ---- this CTA's record: per-row statistics (warp r), the logits at x (warp 2) ----
     if (warp < nrows) {
         const int r = warp;
         if (greedy) {
@@ -417,40 +494,53 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
             const int widx = warp_min_i32(best == wbest ? bidx : INT_MAX);
             const int wbad = __any_sync(0xffffffffu, bad);
             if (lane == 0) {
-                xch.gmax[r] = wbest;
-                xch.garg[r] = widx;
-                xch.bad[r] = wbad;
+                mine1.gmax[r] = wbest;
+                mine1.garg[r] = widx;
+                mine1.bad[r] = wbad;
             }
         } else {
             float Bc = -INFINITY;
-            for (int g = lane; g < groups; g += kWarp) Bc = fmaxf(Bc, gref[r * P.groups_max + g]);
-            Bc = warp_max(Bc);
-            double acc = 0.0;
+            int bad = 0;
             for (int g = lane; g < groups; g += kWarp) {
                 const float sg = gsum[r * P.groups_max + g];
-                if (sg != 0.0f)
-                    acc += static_cast<double>(sg) * static_cast<double>(ex2(gref[r * P.groups_max + g] - Bc));
+                if (!(sg >= 0.0f) || isinf(sg)) bad = 1;  // NaN or inf
+                if (sg > 0.0f) Bc = fmaxf(Bc, gref[r * P.groups_max + g]);
             }
-            acc = warp_sum_f64(acc);
+            Bc = warp_max(Bc);
+            F2 acc = {0.0f, 0.0f};
+            for (int g = lane; g < groups; g += kWarp) {
+                const float sg = gsum[r * P.groups_max + g];
+                if (sg > 0.0f && !isinf(sg)) acc = f2_add(acc, {scale2(sg, gref[r * P.groups_max + g] - Bc), 0.0f});
+            }
+            acc = warp_sum_f2(acc);
+            const int wbad = __any_sync(0xffffffffu, bad);
             if (lane == 0) {
-                xch.Bref[r] = Bc;
-                xch.S[r] = acc;
+                mine1.B[r] = Bc;
+                mine1.S_hi[r] = acc.hi;
+                mine1.S_lo[r] = acc.lo;
+                mine1.bad[r] = wbad;
             }
         }
+    } else if (warp == 2 && lane == 0) {
+        const int x = I.x;
+        const int xl = x - I.lo * E;  // position of x in this slice
+        const int has = I.pair && x >= 0 && xl >= 0 && xl < nvec * E;
+        mine1.has_x = has;
+        mine1.yx[0] = has ? Elt<DT>::at(buf_t, xl) : 0.0f;
+        mine1.yx[1] = has ? Elt<DT>::at(buf_d, xl) : 0.0f;
     }
-    cluster_sync_all();  // #1: every slice's statistics are published
+    __syncthreads();
+    if (warp == 0) push_record(&mine1, xch1, crank, kEx1Words, C, lane);
+    cluster_sync_all();  // #1: every slice's record is in every CTA
 
-    // ---- combine the cluster (warp 0, lane c reads CTA c), decide the accept test ----
+    // ---- combine the cluster (warp 0, lane c holds CTA c's record), decide the accept test ----
     if (warp == 0) {
+        const bool in = lane < C;
         for (int r = 0; r < nrows; ++r) {
             if (greedy) {
-                float v = -INFINITY;
-                int ix = INT_MAX, bad = 0;
-                if (lane < static_cast<int>(C)) {
-                    v = dsmem_ld_f32(dsmem_map(&xch.gmax[r], lane));
-                    ix = dsmem_ld_s32(dsmem_map(&xch.garg[r], lane));
-                    bad = dsmem_ld_s32(dsmem_map(&xch.bad[r], lane));
-                }
+                const float v = in ? xch1[lane].gmax[r] : -INFINITY;
+                const int ix = in ? xch1[lane].garg[r] : INT_MAX;
+                const int bad = in ? xch1[lane].bad[r] : 0;
                 const float wv = warp_max(v);
                 const int wix = warp_min_i32(v == wv ? ix : INT_MAX);
                 const int wbad = __any_sync(0xffffffffu, bad);
@@ -460,62 +550,78 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
                     else I.argmax_d = am;
                 }
             } else {
-                float Bc = -INFINITY;
-                double Sc = 0.0;
-                if (lane < static_cast<int>(C)) {
-                    Bc = dsmem_ld_f32(dsmem_map(&xch.Bref[r], lane));
-                    Sc = dsmem_ld_f64(dsmem_map(&xch.S[r], lane));
-                }
+                const F2 Sc = in ? F2{xch1[lane].S_hi[r], xch1[lane].S_lo[r]} : F2{0.0f, 0.0f};
+                const float Bc = (in && Sc.hi > 0.0f) ? xch1[lane].B[r] : -INFINITY;
+                const int bad = in ? xch1[lane].bad[r] : 0;
                 const float Bw = warp_max(Bc);
-                const double term = (Sc != 0.0) ? Sc * static_cast<double>(ex2(Bc - Bw)) : 0.0;
-                const double S = warp_sum_f64(term);
+                const F2 S = warp_sum_f2(Sc.hi > 0.0f ? f2_scale(Sc, Bc - Bw) : F2{0.0f, 0.0f});
+                const int wbad = __any_sync(0xffffffffu, bad);
                 if (lane == 0) {
                     if (r == 0) {
-                        I.B_t = Bw;
+                        I.B_t = wbad ? NAN : Bw;
                         I.S_t = S;
                     } else {
-                        I.B_d = Bw;
+                        I.B_d = wbad ? NAN : Bw;
                         I.S_d = S;
                     }
                 }
             }
         }
+        const unsigned xm = __ballot_sync(0xffffffffu, in && xch1[lane].has_x);
+        const int xo = xm ? __ffs(xm) - 1 : 0;
+        const float yx_t = __shfl_sync(0xffffffffu, in ? xch1[lane].yx[0] : 0.0f, xo);
+        const float yx_d = __shfl_sync(0xffffffffu, in ? xch1[lane].yx[1] : 0.0f, xo);
         if (lane == 0) {
             int status = I.status | (timed_out ? REQ_TIMEOUT : 0);
             I.accept = 0;
             I.sample_kind = SAMPLE_NONE;
-            I.rho = 0.0;
+            I.rho = 0.0f;
+            I.u_acc = u_acc_reg;
+            I.u_s = u_s_reg;
             // row validity is reported together with a bad proposal (both are preconditions)
             if (!(status & (SPEC_REQ_BAD_SHAPE | SPEC_REQ_BAD_PARAM | REQ_TIMEOUT))) {
                 if (greedy) {
                     if (I.argmax_t < 0 || (I.pair && I.argmax_d < 0)) status |= SPEC_REQ_BAD_LOGITS;
+                    if (I.pair && (I.x < 0 || I.x >= P.V)) status |= SPEC_REQ_BAD_PROPOSAL;
                 } else {
-                    const bool ok_t = isfinite(I.S_t) && I.S_t > 0.0 && isfinite(I.B_t);
-                    const bool ok_d = !I.pair || (isfinite(I.S_d) && I.S_d > 0.0 && isfinite(I.B_d));
+                    const bool ok_t = isfinite(I.B_t) && I.S_t.hi > 0.0f && isfinite(I.S_t.hi);
+                    const bool ok_d = !I.pair || (isfinite(I.B_d) && I.S_d.hi > 0.0f && isfinite(I.S_d.hi));
                     if (!ok_t || !ok_d) status |= SPEC_REQ_BAD_LOGITS;
+                    // q(x) == 0 is a bad proposal for Rule 2 (checked before any draw)
+                    if (I.pair && (I.x < 0 || I.x >= P.V || yx_d == -INFINITY)) status |= SPEC_REQ_BAD_PROPOSAL;
                 }
             }
             if (status == 0) {
                 if (greedy) {
                     if (I.pair) {
                         I.accept = (I.x == I.argmax_t);
-                        I.rho = I.accept ? 1.0 : 0.0;
-                        I.alpha = (I.argmax_t == I.argmax_d) ? 1.0 : 0.0;
+                        I.rho = I.accept ? 1.0f : 0.0f;
+                        I.alpha = (I.argmax_t == I.argmax_d) ? 1.0f : 0.0f;
                     }
                 } else {
-                    const double s64 = static_cast<double>(s_hi) + static_cast<double>(s_lo);
+                    I.inv_St = 1.0f / I.S_t.hi;
                     if (I.pair) {
-                        // log2 p(x) = y_x s - B - log2 S  (and the same for q)
-                        const double lp = static_cast<double>(I.yx_t) * s64 - static_cast<double>(I.B_t) - log2(I.S_t);
-                        const double lq = static_cast<double>(I.yx_d) * s64 - static_cast<double>(I.B_d) - log2(I.S_d);
-                        const double rho = (I.yx_t == -INFINITY) ? 0.0 : exp2(lp - lq);
+                        // rho = p(x)/q(x) = 2^E * S_d/S_t with E = (y_t - y_d) s - (B_t - B_d):
+                        // E in float64 (three operations), 2^E from the integer part and ex2 of
+                        // the fraction with a first-order correction for its float rounding
+                        const F2 lam = f2_div(I.S_t, I.S_d);
+                        I.lam = lam;
+                        float rho = 0.0f;
+                        if (yx_t != -INFINITY) {
+                            const double s64 = static_cast<double>(s_hi) + static_cast<double>(s_lo);
+                            const double Ed = fma(static_cast<double>(yx_t) - static_cast<double>(yx_d), s64,
+                                                  -(static_cast<double>(I.B_t) - static_cast<double>(I.B_d)));
+                            const double n = floor(Ed);
+                            const double fd = Ed - n;
+                            const float f = static_cast<float>(fd);
+                            const float flo = static_cast<float>(fd - static_cast<double>(f));
+                            const float m = ex2(f) * fmaf(flo, 0.69314718f, 1.0f);
+                            rho = scale2(m / lam.hi * (1.0f - lam.lo / lam.hi), static_cast<float>(fmax(fmin(n, 300.0), -300.0)));
+                        }
                         I.rho = rho;
-                        I.accept = (rho > 0.0) && (I.u_acc <= rho);
-                        const double lam = I.S_t / I.S_d;
-                        I.lam_hi = static_cast<float>(lam);
-                        I.lam_lo = static_cast<float>(lam - static_cast<double>(I.lam_hi));
-                        I.c_t = static_cast<float>(static_cast<double>(I.B_t) + log2(I.S_t));
-                        I.c_d = static_cast<float>(static_cast<double>(I.B_d) + log2(I.S_d));
+                        I.accept = (rho > 0.0f) && (I.u_acc <= static_cast<double>(rho));
+                        I.c_t = I.B_t + __log2f(I.S_t.hi);
+                        I.c_d = I.B_d + __log2f(I.S_d.hi);
                         if (!I.accept) I.sample_kind = SAMPLE_RESIDUAL;
                     } else {
                         I.sample_kind = SAMPLE_P;
@@ -528,13 +634,13 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
     __syncthreads();
 
     // ---- pass 2 (pairs under Rule 2): alpha, and the residual where this position rejects ----
-    double my_alpha = 0.0;
+    float my_alpha = 0.0f;
     if (I.status == 0 && I.pair && !greedy) {
-        float acc_a = 0.0f;
         if (I.sample_kind == SAMPLE_RESIDUAL) {
-            const float B_t = I.B_t, B_d = I.B_d, lam_hi = I.lam_hi, lam_lo = I.lam_lo;
+            const float B_t = I.B_t, B_d = I.B_d, lam_hi = I.lam.hi, lam_lo = I.lam.lo;
+            float acc_a = 0.0f;
             for (int g = warp; g < groups; g += kWarps) {
-                float racc = 0.0f, aacc = 0.0f;
+                float racc = 0.0f;
 #pragma unroll
                 for (int q = 0; q < kVecPerLane; ++q) {
                     const int vi = g * kGroupVecs + q * kWarp + lane;
@@ -545,18 +651,16 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
                     for (int e = 0; e < E; ++e) {
                         const float et = ex2(exp_arg(yt[e], s_hi, s_lo, B_t));
                         const float ed = ex2(exp_arg(yd[e], s_hi, s_lo, B_d));
-                        const float rr = fmaxf(fmaf(-lam_lo, ed, fmaf(-lam_hi, ed, et)), 0.0f);
-                        racc += rr;
-                        aacc += fminf(et, lam_hi * ed);  // S_t * min(p, q), no cancellation
+                        racc += fmaxf(fmaf(-lam_lo, ed, fmaf(-lam_hi, ed, et)), 0.0f);
+                        acc_a += fminf(et, lam_hi * ed);  // S_t * min(p, q), no cancellation
                     }
                 }
                 racc = warp_sum(racc);
                 if (lane == 0) gres[g] = racc;
-                acc_a += aacc;
             }
-            my_alpha = static_cast<double>(acc_a) / I.S_t;
+            my_alpha = acc_a * I.inv_St;
         } else {
-            const float s32 = I.s32, c_t = I.c_t, c_d = I.c_d;
+            const float c_t = I.c_t, c_d = I.c_d;
             for (int g = warp; g < groups; g += kWarps) {
 #pragma unroll
                 for (int q = 0; q < kVecPerLane; ++q) {
@@ -567,81 +671,79 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
                     Elt<DT>::unpack(buf_d[vi], yd);
 #pragma unroll
                     for (int e = 0; e < E; ++e)
-                        acc_a += ex2(fminf(fmaf(yt[e], s32, -c_t), fmaf(yd[e], s32, -c_d)));
+                        my_alpha += ex2(fminf(fmaf(yt[e], s_hi, -c_t), fmaf(yd[e], s_hi, -c_d)));
                 }
             }
-            my_alpha = static_cast<double>(acc_a);
         }
     }
-    my_alpha = warp_sum_f64(my_alpha);
-    if (lane == 0) red_f64[warp] = my_alpha;
+    my_alpha = warp_sum(my_alpha);
+    if (lane == 0) red_f[warp] = my_alpha;
     __syncthreads();
     if (warp == 0) {
-        double a = lane < kWarps ? red_f64[lane] : 0.0;
-        a = warp_sum_f64(a);
-        double z = 0.0;
+        float a = lane < kWarps ? red_f[lane] : 0.0f;
+        a = warp_sum(a);
+        F2 z = {0.0f, 0.0f};
         if (I.sample_kind == SAMPLE_RESIDUAL)
-            for (int g = lane; g < groups; g += kWarp) z += static_cast<double>(gres[g]);
-        z = warp_sum_f64(z);
+            for (int g = lane; g < groups; g += kWarp) z = f2_add(z, {gres[g], 0.0f});
+        z = warp_sum_f2(z);
         if (lane == 0) {
-            xch.part_alpha = a;
-            xch.part_Z = z;
+            mine2.alpha = a;
+            mine2.Z_hi = z.hi;
+            mine2.Z_lo = z.lo;
         }
+        __syncwarp();
+        push_record(&mine2, xch2, crank, kEx2Words, C, lane);
     }
-    cluster_sync_all();  // #2: alpha and residual shares are published
+    cluster_sync_all();  // #2: alpha and residual shares are in every CTA; no remote access after this
 
     // ---- cluster totals, the owner of the draw, item results ----
     if (warp == 0) {
-        double a = 0.0, z = 0.0, wp = 0.0;
-        if (lane < static_cast<int>(C)) {
-            a = dsmem_ld_f64(dsmem_map(&xch.part_alpha, lane));
-            z = dsmem_ld_f64(dsmem_map(&xch.part_Z, lane));
-            if (I.sample_kind != SAMPLE_NONE && !greedy) {
-                const float Bc = dsmem_ld_f32(dsmem_map(&xch.Bref[0], lane));
-                const double Sc = dsmem_ld_f64(dsmem_map(&xch.S[0], lane));
-                wp = (Sc != 0.0) ? Sc * static_cast<double>(ex2(Bc - I.B_t)) : 0.0;
-            }
+        const bool in = lane < C;
+        const float a = in ? xch2[lane].alpha : 0.0f;
+        const F2 z = in ? F2{xch2[lane].Z_hi, xch2[lane].Z_lo} : F2{0.0f, 0.0f};
+        F2 wp = {0.0f, 0.0f};
+        if (in && I.sample_kind != SAMPLE_NONE && !greedy) {
+            const F2 Sc = {xch1[lane].S_hi[0], xch1[lane].S_lo[0]};
+            if (Sc.hi > 0.0f) wp = f2_scale(Sc, xch1[lane].B[0] - I.B_t);
         }
-        const double alpha_sum = warp_sum_f64(a);
+        const float alpha_sum = warp_sum(a);
         int kind = I.sample_kind;
-        const double Zres = warp_sum_f64(z);
+        const F2 Zres = warp_sum_f2(z);
         int fb = 0;
-        if (kind == SAMPLE_RESIDUAL && !(Zres > 0.0)) {
+        if (kind == SAMPLE_RESIDUAL && !(Zres.hi > 0.0f)) {
             kind = SAMPLE_P;  // zero residual mass: draw from p and say so
             fb = 1;
         }
         // masses of the law the draw uses, per CTA, accumulated in CTA order
-        const double mine = (kind == SAMPLE_RESIDUAL) ? z : wp;
-        const double incl = warp_inclusive_scan_f64(lane < static_cast<int>(C) ? mine : 0.0, lane);
+        const double mine = (kind == SAMPLE_RESIDUAL) ? f2_d(z) : f2_d(wp);
+        const double incl = warp_inclusive_scan_f64(in ? mine : 0.0, lane);
         const double Ztot = __shfl_sync(0xffffffffu, incl, C - 1);
         const double t = I.u_s * Ztot;
-        const unsigned hit = __ballot_sync(0xffffffffu, lane < static_cast<int>(C) && mine > 0.0 && incl > t);
-        const unsigned posm = __ballot_sync(0xffffffffu, lane < static_cast<int>(C) && mine > 0.0);
+        const unsigned hit = __ballot_sync(0xffffffffu, in && mine > 0.0 && incl > t);
+        const unsigned posm = __ballot_sync(0xffffffffu, in && mine > 0.0);
         int owner = -1;
         if (kind != SAMPLE_NONE && I.status == 0 && !greedy)
             owner = hit ? __ffs(hit) - 1 : (posm ? 31 - __clz(static_cast<int>(posm)) : -1);
         const double prefix = __shfl_sync(0xffffffffu, incl - mine, owner < 0 ? 0 : owner);
-        __syncwarp();
         if (lane == 0) {
             I.sample_kind = kind;
             I.owner = owner;
             I.Ztot = Ztot;
             I.target_t = t;
             I.owner_prefix = prefix;
-            I.Zres = Zres;
             if (crank == 0) {
                 const int st = I.status;
                 P.item_status[item] = st;
                 P.item_fb[item] = fb;
                 if (I.pair) {
-                    const double alpha = greedy ? I.alpha : alpha_sum;
+                    const float alpha = greedy ? I.alpha : alpha_sum;
                     P.item_flag[item] = (st == 0) ? I.accept : 0;
-                    P.alpha_ws[I.drow] = (st == 0) ? static_cast<float>(alpha) : 0.0f;
-                    if (P.alpha_rows) P.alpha_rows[I.drow] = (st == 0) ? static_cast<float>(alpha) : NAN;
-                    if (P.rho_rows) P.rho_rows[I.drow] = (st == 0) ? static_cast<float>(I.rho) : NAN;
+                    P.alpha_ws[I.drow] = (st == 0) ? alpha : 0.0f;
+                    if (P.alpha_rows) P.alpha_rows[I.drow] = (st == 0) ? alpha : NAN;
+                    if (P.rho_rows) P.rho_rows[I.drow] = (st == 0) ? I.rho : NAN;
                     if (P.resid_rows)
                         P.resid_rows[I.drow] = (st == 0 && kind == SAMPLE_RESIDUAL && !greedy)
-                                                   ? static_cast<float>(Zres / I.S_t)
+                                                   ? static_cast<float>(f2_d(Zres) / f2_d(I.S_t))
                                                    : -1.0f;
                 } else {
                     P.item_flag[item] = 0;
@@ -666,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
     __syncthreads();
 
     // ---- the draw: the owner CTA finds the group, then the vector, then the element ----
-    if (warp == 0 && I.owner == static_cast<int>(crank)) {
+    if (warp == 0 && I.owner == crank) {
         const int kind = I.sample_kind;
         const double local = I.target_t - I.owner_prefix;
         int gsel = -1, last_g = -1;
@@ -679,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
                     m = static_cast<double>(gres[g]);
                 } else {
                     const float sg = gsum[g];
-                    m = (sg != 0.0f) ? static_cast<double>(sg) * static_cast<double>(ex2(gref[g] - I.B_t)) : 0.0;
+                    m = (sg > 0.0f) ? static_cast<double>(scale2(sg, gref[g] - I.B_t)) : 0.0;
                 }
             }
             const double incl = run + warp_inclusive_scan_f64(m, lane);
@@ -707,11 +809,13 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
         double wsel = 0.0, margin = 0.0, unit = 1.0;
         if (gsel >= 0) {
             const float bg = (kind == SAMPLE_RESIDUAL) ? 0.0f : gref[gsel];
-            unit = (kind == SAMPLE_RESIDUAL) ? 1.0 : static_cast<double>(ex2(bg - I.B_t));
-            const double lt = (local - before) / unit;  // the target inside the group, group units
-            double run2 = 0.0;
+            // group units: residual weights are already in cluster units; P weights are in
+            // units of 2^b_g, 2^(b_g - B_t) cluster units each (exact power of two)
+            unit = (kind == SAMPLE_RESIDUAL) ? 1.0 : static_cast<double>(scale2(1.0f, bg - I.B_t));
+            const float lt = static_cast<float>((local - before) / unit);  // target inside the group
+            float run2 = 0.0f;
             int last_tok = -1;
-            double last_w = 0.0;
+            float last_w = 0.0f;
             for (int q = 0; q < kVecPerLane; ++q) {
                 const int vi = gsel * kGroupVecs + q * kWarp + lane;
                 float w[E];
@@ -719,44 +823,46 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
                 float ls = 0.0f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) ls += w[e];
-                const double incl = run2 + warp_inclusive_scan_f64(static_cast<double>(ls), lane);
-                const double start = incl - static_cast<double>(ls);
+                float incl = ls;
+#pragma unroll
+                for (int o = 1; o < kWarp; o <<= 1) {
+                    const float n = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += n;
+                }
+                incl += run2;
+                const float start = incl - ls;
                 // this lane's element that takes the target, if any; and its last with mass
                 int found = -1, lastp = -1;
-                double fprev = 0.0, c = start;
+                float fprev = 0.0f, c = start, wf = 0.0f, wl = 0.0f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    const double we = static_cast<double>(w[e]);
-                    if (we > 0.0) {
-                        if (found < 0 && !clamped && c + we > lt) {
+                    if (w[e] > 0.0f) {
+                        if (found < 0 && !clamped && c + w[e] > lt) {
                             found = e;
                             fprev = c;
+                            wf = w[e];
                         }
                         lastp = e;
+                        wl = w[e];
                     }
-                    c += we;
-                }
-                float wf = 0.0f, wl = 0.0f;
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    if (e == found) wf = w[e];
-                    if (e == lastp) wl = w[e];
+                    c += w[e];
                 }
                 const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
                 const unsigned posm = __ballot_sync(0xffffffffu, lastp >= 0);
                 if (hit) {
                     const int l = __ffs(hit) - 1;
                     const int e_sel = __shfl_sync(0xffffffffu, found, l);
-                    const double c0 = __shfl_sync(0xffffffffu, fprev, l);
-                    wsel = static_cast<double>(__shfl_sync(0xffffffffu, wf, l));
+                    const float c0 = __shfl_sync(0xffffffffu, fprev, l);
+                    const float ws = __shfl_sync(0xffffffffu, wf, l);
+                    wsel = ws;
                     tok = (I.lo + gsel * kGroupVecs + q * kWarp + l) * E + e_sel;
-                    margin = fmin(lt - c0, c0 + wsel - lt) * unit / I.Ztot;
+                    margin = fmin(static_cast<double>(lt - c0), static_cast<double>(c0 + ws - lt)) * unit / I.Ztot;
                     break;
                 }
                 if (posm) {
                     const int l = 31 - __clz(static_cast<int>(posm));
                     last_tok = (I.lo + gsel * kGroupVecs + q * kWarp + l) * E + __shfl_sync(0xffffffffu, lastp, l);
-                    last_w = static_cast<double>(__shfl_sync(0xffffffffu, wl, l));
+                    last_w = __shfl_sync(0xffffffffu, wl, l);
                 }
                 run2 = __shfl_sync(0xffffffffu, incl, kWarp - 1);
             }
@@ -777,7 +883,6 @@ __global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams
         for (int r = 0; r < nrows; ++r)
             for (int k = 0; k < nchunk; ++k) mbar_wait_bounded(&bars[r][k], 0, kWaitLimitNs);
     }
-    cluster_sync_all();  // #3: no CTA leaves while a peer may still read its shared memory
 }
 
 // ------------------------------------------------------------------------------------------
@@ -962,8 +1067,8 @@ static cudaError_t pick_shape(int nvec_row, LaunchShape &out) {
         if (e != cudaSuccess) return e;
         nonportable_set = true;
     }
-    // the smallest cluster whose slices fit three CTAs per SM, else two, else one
-    const size_t budgets[3] = {72 * 1024, 110 * 1024, static_cast<size_t>(max_optin) - 2048};
+    // the smallest cluster whose slices fit six CTAs per SM, else three, two, one
+    const size_t budgets[4] = {36 * 1024, 72 * 1024, 110 * 1024, static_cast<size_t>(max_optin) - 4096};
     for (size_t budget : budgets) {
         for (int C = 1; C <= kMaxCluster; C *= 2) {
             if (C > nvec_row) break;
