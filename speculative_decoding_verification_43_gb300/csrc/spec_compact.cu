@@ -16,6 +16,7 @@
 #include <cstdint>
 
 #include "spec_device.cuh"
+#include "spec_math.cuh"
 #include "spec_verify.h"
 
 namespace spec {
@@ -62,6 +63,8 @@ __device__ __forceinline__ int block_exscan(int v, int *warp_tot, int &total) {
 __global__ void __launch_bounds__(kCompactThreads) spec_compact_kernel(const CompactParams P) {
     __shared__ int tot_n[kWarp + 1];
     __shared__ int tot_e[kWarp + 1];
+    griddep_launch_dependents();
+    griddep_wait();  // launched behind the previous kernel of the stream: its outputs are ready now
     int carry_n = 0, carry_e = 0;
     // offsets must start at 0, end at total_rows and grow by at least one row per request;
     // otherwise every request is BAD_SHAPE, so packed writes stay within their capacities
@@ -126,30 +129,41 @@ __global__ void __launch_bounds__(kCompactThreads) spec_compact_kernel(const Com
     }
 }
 
-__host__ __device__ inline double gamma_objective(double alpha, double c, int gamma) {
-    if (alpha == 1.0) return (gamma + 1.0) / (gamma * c + 1.0);
-    double pw = alpha;  // alpha^(gamma+1)
-    for (int k = 0; k < gamma; ++k) pw *= alpha;
-    return (1.0 - pw) / ((1.0 - alpha) * (gamma * c + 1.0));
-}
-
-__global__ void spec_gamma_kernel(const double *alpha_sum, const int32_t *alpha_count, double alpha_prev,
-                                  double c, int gmin, int gmax, int32_t *gamma_out, double *alpha_out) {
+// The objective in float pairs on the device (float64 is slow here): the committed count as the
+// tail sum 1 + alpha + ... + alpha^gamma (M7.8 section 0x02), which needs no division and is
+// gamma + 1 exactly at alpha = 1, and candidates compared by cross-multiplication:
+// f(g1) > f(g2)  <=>  committed(g1) (g2 c + 1) > committed(g2) (g1 c + 1).
+__global__ void spec_gamma_kernel(const double *alpha_sum, const int32_t *alpha_count, float prev_hi, float prev_lo,
+                                  float c_hi, float c_lo, int gmin, int gmax, int32_t *gamma_out, double *alpha_out) {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    griddep_wait();
     const int n = *alpha_count;
-    double alpha = n > 0 ? *alpha_sum / static_cast<double>(n) : alpha_prev;
-    alpha = fmin(fmax(alpha, 0.0), 1.0);
+    const float n_hi = static_cast<float>(n);
+    const F2 nf = f2_norm(n_hi, static_cast<float>(n - static_cast<int>(n_hi)));  // exact above 2^24 too
+    F2 alpha = n > 0 ? f2_div(d2f2(*alpha_sum), nf) : F2{prev_hi, prev_lo};
+    if (!(alpha.hi > 0.0f)) alpha = {0.0f, 0.0f};
+    if (alpha.hi > 1.0f || (alpha.hi == 1.0f && alpha.lo > 0.0f)) alpha = {1.0f, 0.0f};
+    const F2 c = {c_hi, c_lo};
+    F2 pw = {1.0f, 0.0f}, committed = {1.0f, 0.0f};  // gamma = 0
+    for (int g = 1; g <= gmin; ++g) {
+        pw = f2_mul(pw, alpha);
+        committed = f2_add(committed, pw);
+    }
     int best = gmin;
-    double fb = gamma_objective(alpha, c, gmin);
+    F2 best_c = committed;
+    F2 best_den = f2_add(f2_mul({static_cast<float>(gmin), 0.0f}, c), {1.0f, 0.0f});
     for (int g = gmin + 1; g <= gmax; ++g) {
-        const double f = gamma_objective(alpha, c, g);
-        if (f > fb) {  // strict: an exact tie keeps the smaller gamma
-            fb = f;
+        pw = f2_mul(pw, alpha);
+        committed = f2_add(committed, pw);
+        const F2 den = f2_add(f2_mul({static_cast<float>(g), 0.0f}, c), {1.0f, 0.0f});
+        if (f2_gt(f2_mul(committed, best_den), f2_mul(best_c, den))) {  // strict: a tie keeps the smaller
             best = g;
+            best_c = committed;
+            best_den = den;
         }
     }
     *gamma_out = best;
-    *alpha_out = alpha;
+    *alpha_out = static_cast<double>(alpha.hi) + static_cast<double>(alpha.lo);
 }
 
 }  // namespace spec
@@ -186,12 +200,16 @@ extern "C" spec_status spec_compact(const spec_compact_args *a, cudaStream_t str
     P.new_kv_len = a->new_kv_len;
     P.new_draft_len = a->new_draft_len;
     P.compact_status = a->compact_status;
-    spec_compact_kernel<<<1, kCompactThreads, 0, stream>>>(P);
-    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    return launch_after(spec_compact_kernel, dim3(1), dim3(kCompactThreads), stream, P) == cudaSuccess ? SPEC_OK
+                                                                                                     : SPEC_ERR_CUDA;
 }
 
+// Host evaluation in double precision (the closed form of SOTA-227).
 extern "C" double spec_gamma_objective(double alpha, double c, int32_t gamma) {
-    return gamma_objective(alpha, c, gamma);
+    if (alpha == 1.0) return (gamma + 1.0) / (gamma * c + 1.0);
+    double pw = alpha;  // alpha^(gamma+1)
+    for (int k = 0; k < gamma; ++k) pw *= alpha;
+    return (1.0 - pw) / ((1.0 - alpha) * (gamma * c + 1.0));
 }
 
 extern "C" spec_status spec_choose_gamma(const double *alpha_sum, const int32_t *alpha_count, double alpha_prev,
@@ -200,7 +218,11 @@ extern "C" spec_status spec_choose_gamma(const double *alpha_sum, const int32_t 
     if (!alpha_sum || !alpha_count || !gamma_out || !alpha_out) return SPEC_ERR_INVALID_ARG;
     if (gamma_min < 0 || gamma_max < gamma_min || gamma_max > 4096) return SPEC_ERR_INVALID_ARG;
     if (!(c >= 0.0) || !std::isfinite(c) || !(alpha_prev >= 0.0 && alpha_prev <= 1.0)) return SPEC_ERR_INVALID_ARG;
-    spec_gamma_kernel<<<1, 32, 0, stream>>>(alpha_sum, alpha_count, alpha_prev, c, gamma_min, gamma_max, gamma_out,
-                                            alpha_out);
-    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    // host splits of the two double parameters into float pairs
+    const float ph = static_cast<float>(alpha_prev), pl = static_cast<float>(alpha_prev - static_cast<double>(ph));
+    const float ch = static_cast<float>(c), cl = static_cast<float>(c - static_cast<double>(ch));
+    return launch_after(spec_gamma_kernel, dim3(1), dim3(32), stream, alpha_sum, alpha_count, ph, pl, ch, cl,
+                        static_cast<int>(gamma_min), static_cast<int>(gamma_max), gamma_out, alpha_out) == cudaSuccess
+               ? SPEC_OK
+               : SPEC_ERR_CUDA;
 }

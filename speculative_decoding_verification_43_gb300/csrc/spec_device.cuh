@@ -79,6 +79,38 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t phase,
     return true;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns` while the phase is
+// incomplete (the thread resumes as soon as it completes), so waiting warps do not spin.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t phase, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(phase), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase, suspended between attempts; gives up after `max_tries` attempts of up to
+// `hint_ns` each (seconds in total) and returns false. The caller records the error and still
+// reaches every block and cluster barrier, so no peer is left waiting.
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t *bar, uint32_t phase, uint32_t hint_ns,
+                                                        int max_tries) {
+    for (int t = 0; t < max_tries; ++t)
+        if (mbar_try_wait_sleep(bar, phase, hint_ns)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar` with a byte count.
 // dst, src and bytes must be multiples of 16. The policy evicts the streamed lines first.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
@@ -94,6 +126,15 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start before the kernel ahead
+// of it in the stream finishes; it must call griddep_wait() before it reads anything that
+// kernel writes. griddep_launch_dependents() lets the kernel behind this one start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- cluster
@@ -170,6 +211,25 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Host: launch `kernel` so that it may start while the kernel ahead of it in `stream` is still
+// running (programmatic stream serialisation); the kernel must call griddep_wait() first thing
+// before touching that kernel's outputs.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+                                Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 }  // namespace spec

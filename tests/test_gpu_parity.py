@@ -209,7 +209,7 @@ def test_choose_gamma_device_matches_oracle():
         g, a = api.choose_gamma(s, n, prev, c, 0, 8)
         want_g, want_a = oracle.choose_gamma(alpha * count, count, prev, c, 0, 8)
         assert int(g.item()) == want_g
-        assert abs(float(a.item()) - want_a) < 1e-15
+        assert abs(float(a.item()) - want_a) < 1e-12  # float-pair arithmetic on the device
 
 
 def test_compaction_bit_exact_c4():
