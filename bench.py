@@ -42,7 +42,9 @@ UNIT = "rows/s"
 WORKLOAD = "c3"
 GAMMA_COST = 0.05  # relative draft cost c used by the gamma controller each step
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "rows_kernel_c3_traffic.json")
-KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_43_gb300", "csrc", "spec_verify.cu")
+CSRC = os.path.join(ROOT, "speculative_decoding_verification_43_gb300", "csrc")
+# the per-position kernel's sources: a committed ncu traffic figure counts only while they match
+KERNEL_SRCS = ("spec_verify.cu", "spec_rows.cuh", "spec_rows_kernel.cuh", "spec_math.cuh", "spec_device.cuh")
 
 
 def parse():
@@ -168,7 +170,10 @@ def measured_peak():
 
 
 def kernel_hash():
-    return hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for f in KERNEL_SRCS:
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(bytes_per_launch):
