@@ -103,6 +103,53 @@ __device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t *bar, uint32_t 
     return false;
 }
 
+// try_wait with acquire at cluster scope: the waiter sees what other CTAs of the cluster wrote
+// before their (release) arrivals. Suspends for up to `hint_ns` while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t phase, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(phase), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t phase, uint32_t hint_ns,
+                                                          int max_tries) {
+    for (int t = 0; t < max_tries; ++t)
+        if (mbar_try_wait_cluster(bar, phase, hint_ns)) return true;
+    return false;
+}
+
+// Arrive on the mbarrier at a shared::cluster address (this CTA's or another's), releasing this
+// thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 16-byte store into another CTA's shared memory (a shared::cluster address) that completes its
+// bytes on that CTA's mbarrier (also a shared::cluster address). Asynchronous: the receiver sees
+// the data once the barrier's phase completes.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- named barriers
+// Barrier `id` (1..15) completes when `count` threads (a multiple of 32) have arrived: bar_sync
+// arrives and waits, bar_arrive only arrives. What a thread wrote before arriving is visible to
+// the threads that waited. The non-aligned forms: the threads of a warp may arrive apart.
+__device__ __forceinline__ void bar_sync(int id, int count) {
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(int id, int count) {
+    asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -120,6 +167,11 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
+}
+
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -22,6 +22,11 @@ struct Elt<SPEC_F32> {
         y[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
         y[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
     }
+    // the float pair of 32-bit word pair h (elements 2h, 2h + 1)
+    __device__ static __forceinline__ float2 unpack_one(const uint4 &w, int h) {
+        return h == 0 ? make_float2(__uint_as_float(w.x), __uint_as_float(w.y))
+                      : make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+    }
     __device__ static __forceinline__ float at(const uint4 *buf, int e) {
         return reinterpret_cast<const float *>(buf)[e];
     }
@@ -40,6 +45,11 @@ struct Elt<SPEC_BF16> {
         y[1] = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
         y[2] = make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
         y[3] = make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+    }
+    // the float pair of 32-bit word h (elements 2h, 2h + 1)
+    __device__ static __forceinline__ float2 unpack_one(const uint4 &w, int h) {
+        const uint32_t x = h == 0 ? w.x : h == 1 ? w.y : h == 2 ? w.z : w.w;
+        return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
     }
     __device__ static __forceinline__ float at(const uint4 *buf, int e) {
         const uint16_t b = reinterpret_cast<const uint16_t *>(buf)[e];

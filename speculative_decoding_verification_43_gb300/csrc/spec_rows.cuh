@@ -6,19 +6,30 @@
 // from p_{K+1}; with T = 0, the greedy rule.
 //
 // Work unit: one target row ("item"). Position j < K_i of request i is a pair (target row j,
-// draft row j); position K_i is the target-only row of the bonus (or plain) draw. One thread-block
-// cluster of C CTAs verifies an item; CTA c owns the c-th 16-byte-aligned slice of the vocabulary
-// of both rows and stages it in shared memory with 1-D bulk copies, so every logit crosses HBM
-// exactly once:
-//   pass 1 (as the copies land): per 1024-token group, max and sum of 2^(y*s - b) with an
-//           integral reference b, so that combining groups and CTAs is exact scaling by 2^k;
-//   exchange #1: each CTA writes its row statistics into every CTA's shared memory (DSMEM),
-//           then one cluster barrier; the accept test is computed identically everywhere;
-//   pass 2 (pairs, from shared memory): alpha = sum min(p, q), and only where this position
-//           rejects, the residual max(p - q, 0) with per-group sums;
-//   exchange #2: alpha and residual shares, then the CTA whose slice holds u*Z draws.
+// draft row j); position K_i is the target-only row of the bonus (or plain) draw.
+//
+// A persistent thread-block cluster of C CTAs (one CTA per SM) walks a list of items. CTA c owns
+// the c-th 16-byte-aligned slice of the vocabulary of every row. Rows stream into a ring of
+// shared-memory slots by 1-D bulk copies, each logit exactly once. Each CTA has 15 data warps,
+// which hold the item's slice in registers, and one control warp, which issues the copies, runs
+// the exchange and makes every scalar decision. Per item:
+//   pass 1 (data warps): the slice moves from the ring into registers (the ring slots are free
+//           at once, and the next rows' copies start) and each thread sums 2^(y*s - b) with an
+//           integral reference b of its own, so that combining threads, warps and CTAs is exact
+//           scaling by powers of two;
+//   exchange (control warp): the CTA's record (row statistics, the logits at the draft token,
+//           the alpha / residual totals of the previous item) goes into every CTA's shared
+//           memory, followed by an arrival on that CTA's barrier for the item; every CTA then
+//           computes the accept test identically;
+//   pass 2 (data warps, pairs, from registers): alpha = sum min(p, q) and, only where this
+//           position rejects, the residual max(p - q, 0) per chunk (32 contiguous vectors);
+//   draw (control warp, one item late): once the next exchange has brought every CTA's residual
+//           (or p) mass, the CTA whose slice holds u*Z fetches the one chunk that holds it with
+//           a small bulk copy and finds the token there.
+// Data and control warps meet at named barriers only; the data warps never wait on the cluster.
 // Every rejecting position prepares its own candidate (the first rejection is known only per
-// request); the selection kernel picks. Float math is packed two lanes per instruction.
+// request); the selection kernel picks. Float math is packed two lanes per instruction; no
+// float64 instruction runs on the device (it is very slow on this part).
 #pragma once
 
 #include <climits>
@@ -31,14 +42,21 @@
 
 namespace spec {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / kWarp;
-constexpr int kVecPerLane = 4;                   // 16-byte vectors per lane in one group
-constexpr int kGroupVecs = kWarp * kVecPerLane;  // 128 vectors = 2 KiB per row per group
-constexpr int kMaxChunks = 4;                    // bulk copies per row slice
+// 15 data warps and one control warp: 16 warps, four per SM sub-partition, so that every thread
+// may hold 128 registers (a 17th warp would put five warps on one sub-partition's register file)
+constexpr int kWarps = 15;                   // data warps
+constexpr int kThreads = kWarps * kWarp;     // data threads
+constexpr int kBlock = kThreads + kWarp;     // plus the control warp
+// named barriers between the data warps and the control warp (0 is __syncthreads)
+enum : int { BAR_FREE = 1, BAR_STATS = 2, BAR_DECIDED = 3, BAR_PASS2 = 4, BAR_BATCH = 5 };
+constexpr int kChunkVecs = kWarp;   // a chunk: 32 contiguous vectors, one per lane of a warp
+constexpr int kRing = 3;            // row slots per CTA
+constexpr int kMaxItems = 64;       // item descriptors held at once
 constexpr int kMaxCluster = 16;
-constexpr uint32_t kSuspendNs = 1u << 20;        // one suspended wait: at most ~1 ms
-constexpr int kMaxWaitTries = 2048;              // ~2 s in all: a copy never takes this long
+constexpr int kMaxNvt = 9;          // 16-byte vectors per thread per row
+constexpr int kMaxChunks = kMaxNvt * kWarps;
+constexpr uint32_t kSuspendNs = 1u << 20;  // one suspended wait: at most ~1 ms
+constexpr int kMaxWaitTries = 2048;        // ~2 s in all: a copy never takes this long
 // log2(e) as a float pair
 constexpr float kLog2eHi = 1.44269502162933349609375f;
 constexpr float kLog2eLo = 1.925963e-08f;
@@ -56,7 +74,7 @@ struct RowsParams {
     int32_t B, V, K_max, total_rows;
     int32_t nvec_row;        // 16-byte vectors per row
     int32_t slice_vecs_max;  // vectors of the largest slice
-    int32_t groups_max;      // groups of the largest slice
+    int32_t nclusters;       // persistent clusters in the grid
     // per-item results (workspace), indexed by target row
     int32_t *item_flag;    // 1: the draft at this position is accepted
     int32_t *item_tok;     // candidate frontier token of this position (-1: none)
@@ -71,98 +89,79 @@ struct RowsParams {
     float *resid_rows;
 };
 
-// A CTA's record after pass 1. It is written into slot `rank` of every CTA of the cluster, so
-// that after the cluster barrier all reads are local. Fields are 32-bit words.
-struct Ex1 {
+// One item of this cluster's list, prepared before its rows arrive.
+struct Desc {
+    int32_t item, req, pos, K, drow, pair, status, x;
+    float s_hi, s_lo;  // log2(e)/T = s_hi + s_lo, s_hi rounded toward zero (s_lo > 0)
+    int32_t greedy;
+    F2 u_acc, u_s;     // the position's accept draw and the request's frontier draw
+};
+
+// A CTA's message for item k, stored into slot k % 3 of every CTA of the cluster (distributed
+// shared memory, asynchronous stores that complete bytes on that CTA's barrier of the slot).
+// Twenty 32-bit words, 16-byte aligned: five vector stores per destination.
+struct __align__(16) Msg {
     float B[2];      // integral reference exponent of S[r] (-inf: no mass)
-    float S_hi[2];   // sum over the slice of 2^(y*s - B[r]), a float pair
+    float S_hi[2];   // this slice's sum of 2^(y*s - B[r]), a float pair
     float S_lo[2];
-    int32_t bad[2];  // a NaN / +inf was seen in row r's slice
-    float yx[2];     // target / draft logit at the draft token, from the CTA that holds it
-    int32_t has_x;
+    int32_t bad[2];  // a NaN / +inf was seen in row r
     float gmax[2];   // greedy rule: max logit of the slice and the smallest index attaining it
     int32_t garg[2];
+    float yx[2];     // target / draft logit at the draft token, from the CTA that holds it
+    int32_t has_x;
+    int32_t tmo;       // a bulk copy of this CTA did not land in time
+    float prev_alpha;  // previous item: this slice's share of alpha (normalised)
+    float prev_Zhi;    // previous item: this slice's residual mass (units 2^B_t), a float pair
+    float prev_Zlo;
+    int32_t pad;
 };
-constexpr int kEx1Words = sizeof(Ex1) / 4;
-// A CTA's record after pass 2.
-struct Ex2 {
-    float alpha;  // this slice's share of alpha (normalised)
-    float Z_hi;   // this slice's residual mass, units of 2^B_t (a float pair)
-    float Z_lo;
-};
-constexpr int kEx2Words = sizeof(Ex2) / 4;
+constexpr int kMsgBytes = sizeof(Msg);
+static_assert(kMsgBytes == 80, "a message is five 16-byte vectors");
 
-// Item-wide values, computed once and broadcast through shared memory.
-struct ItemInfo {
-    int32_t req, pos, K, drow, status, pair, greedy, accept, x, sample_kind;
-    int32_t lo;      // first vector of this CTA's slice
-    int32_t nvec;    // vectors in this CTA's slice
-    int32_t groups;  // groups in this CTA's slice
-    int32_t nchunk;
-    int32_t owner;   // CTA that draws the candidate (-1: none)
-    F2 u_acc, u_s;     // the position's accept draw and the request's frontier draw
-    float s_hi, s_lo;  // log2(e)/T = s_hi + s_lo, s_hi rounded toward zero (s_lo > 0)
-    float B_t, B_d;    // cluster-wide integral reference exponents
-    F2 S_t, S_d;       // cluster-wide sums in those units
-    float c_t, c_d;    // B + log2 S, for the alpha-only pass
-    F2 lam;            // S_t / S_d
-    float rho, alpha, inv_St;
-    F2 target_t, owner_prefix, Ztot;
-    int32_t argmax_t, argmax_d;
+// The decision of an item, kept until its draw is finished (one item later).
+struct Decision {
+    int32_t item, drow, pair, greedy, status, accept, kind, valid;
+    float B_t, B_d, s_hi, s_lo, rho, inv_St, c_t, c_d;
+    F2 S_t, S_d, lam, u_s;
+    int32_t argmax_t;
+    float alpha_g;  // greedy rule: alpha of the two point masses
 };
 
 enum { SAMPLE_NONE = 0, SAMPLE_RESIDUAL = 1, SAMPLE_P = 2 };
 
-__device__ __forceinline__ void chunk_range(int groups, int nchunk, int k, int nvec, int &g0, int &g1, int &v0,
-                                            int &v1) {
-    g0 = (groups * k) / nchunk;
-    g1 = (groups * (k + 1)) / nchunk;
-    v0 = g0 * kGroupVecs;
-    v1 = min(g1 * kGroupVecs, nvec);
-}
+// Per-warp statistics of one row after pass 1.
+struct WarpStat {
+    float B;  // integral reference (-inf: no mass)
+    float S_hi, S_lo;
+    float gmax;
+    int32_t garg;
+    int32_t bad;
+};
 
-// Lane l < C copies `words` 32-bit words of the local record into slot `rank` of CTA l.
-__device__ __forceinline__ void push_record(const void *mine, void *slot_base, int rank, int words, int C, int lane) {
+// Lane l < C stores the local record into slot `rank` of CTA l (five asynchronous 16-byte
+// stores, each completing its bytes on CTA l's barrier of that slot).
+__device__ __forceinline__ void push_record(const Msg *mine, Msg *slot_base, uint64_t *bar, int rank, int C,
+                                            int lane) {
     if (lane < C) {
-        const uint32_t *src = static_cast<const uint32_t *>(mine);
-        const uint32_t dst = dsmem_map(static_cast<uint32_t *>(slot_base) + rank * words, lane);
-        for (int w = 0; w < words; ++w) st_cluster_u32(dst + 4 * w, src[w]);
+        const uint4 *src = reinterpret_cast<const uint4 *>(mine);
+        const uint32_t dst = dsmem_map(slot_base + rank, lane);
+        const uint32_t rbar = dsmem_map(bar, lane);
+#pragma unroll
+        for (int q = 0; q < kMsgBytes / 16; ++q) st_async_v4(dst + 16 * q, src[q], rbar);
     }
 }
 
-// Weights of this lane's elements of vector vi in the law the candidate is drawn from:
-// RESIDUAL: max(e_t - lambda*e_d, 0) = S_t * max(p - q, 0) in units of 2^B_t;
-// P: 2^(y*s - b_g), the pass-1 terms of the group (units of 2^b_g).
-// Same operations, in the same order, as passes 1 and 2: the values are bitwise those summed.
 template <int DT>
-__device__ __forceinline__ void vec_weights(int kind, const uint4 *buf_t, const uint4 *buf_d, int vi, int nvec,
-                                            const ItemInfo &I, float bg, float *w) {
-    constexpr int H = Elt<DT>::kPerVec / 2;
-    const float2 shi = f2splat(I.s_hi), slo = f2splat(I.s_lo);
-    float2 yt[H];
-    load_vec2<DT>(buf_t, vi, nvec, yt);
-    if (kind == SAMPLE_RESIDUAL) {
-        float2 yd[H];
-        load_vec2<DT>(buf_d, vi, nvec, yd);
-        const float2 nbt = f2splat(-I.B_t), nbd = f2splat(-I.B_d);
-        const float2 nlh = f2splat(-I.lam.hi), nll = f2splat(-I.lam.lo);
+__device__ __forceinline__ float vec_elem(const uint4 &w, int e) {
+    float2 y[Elt<DT>::kPerVec / 2];
+    Elt<DT>::unpack2(w, y);
+    float r = 0.0f;
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-            const float2 et = ex2x2(exp_arg2(yt[h], shi, slo, nbt));
-            const float2 ed = ex2x2(exp_arg2(yd[h], shi, slo, nbd));
-            const float2 r = __ffma2_rn(ed, nll, __ffma2_rn(ed, nlh, et));
-            w[2 * h] = fmaxf(r.x, 0.0f);
-            w[2 * h + 1] = fmaxf(r.y, 0.0f);
-        }
-    } else {
-        const float2 nb = f2splat(-bg);
-#pragma unroll
-        for (int h = 0; h < H; ++h) {
-            const float2 e = ex2x2(exp_arg2(yt[h], shi, slo, nb));
-            w[2 * h] = e.x;
-            w[2 * h + 1] = e.y;
-        }
+    for (int h = 0; h < Elt<DT>::kPerVec / 2; ++h) {
+        if (e == 2 * h) r = y[h].x;
+        if (e == 2 * h + 1) r = y[h].y;
     }
+    return r;
 }
 
 }  // namespace spec

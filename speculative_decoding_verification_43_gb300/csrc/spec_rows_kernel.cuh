@@ -5,659 +5,1015 @@
 
 namespace spec {
 
+// Static shared state of one CTA. The row ring (dynamic shared memory) holds kRing slices.
+struct CtaShared {
+    uint64_t full[kRing];                 // a ring slot's bulk copy has landed
+    uint64_t draw_bar;                    // the draw chunk's bulk copy has landed
+    uint64_t msg_bar[3];                  // all C records of the slot's item have arrived
+    Msg slot[3][kMaxCluster];             // exchange slots, written by every CTA of the cluster
+    Msg mine;
+    Desc desc[kMaxItems];
+    WarpStat ws[2][16];                   // per-warp row statistics of the current item
+    float wal[kWarps];                    // per-warp alpha partials
+    float pm[3][kMaxChunks];              // target-row chunk sums (units 2^pref), by item number % 3
+    float pref[3][kMaxChunks];            // their integral reference exponents
+    float rm[2][kMaxChunks];              // residual chunk sums (units 2^B_t), by item parity
+    float tpm[kMaxNvt * kThreads];        // rejecting pair: per (vector, thread) sums of p (units 2^B_t)
+    Decision dec[2];                      // by item parity
+    uint4 draw_buf[2][kChunkVecs];        // target / draft chunk of the pending draw
+    float yx[2];
+    int32_t x_stamp;                      // item number + 1 when this CTA holds the draft token
+    int32_t timed_out;
+    float prev_alpha;                     // this slice's totals of the previous item
+    F2 prev_Z;
+    // the pending draw (owner CTA only)
+    int32_t draw_pending, draw_chunk, draw_count, draw_clamped, draw_kind, draw_item, draw_par;
+    float draw_lt, draw_unit, draw_bg, draw_invZ;
+    uint32_t draw_phase;
+};
+
+// Items of cluster `cid`: cid, cid + ncl, cid + 2 ncl, ... Batch `nb` holds list entries
+// [nb, nb + nbatch). Every CTA of the cluster computes the same descriptors. Control warp.
+__device__ void load_batch(CtaShared &sh, const RowsParams &P, int cid, int nb, int nbatch, int lane) {
+    for (int s = lane; s < kMaxItems; s += kWarp) {
+        Desc &d = sh.desc[s];
+        d.item = cid + (nb + s) * P.nclusters;
+        d.req = -1;
+        d.pos = d.K = d.drow = -1;
+        d.pair = 0;
+        d.status = SPEC_REQ_BAD_SHAPE;  // until a request claims the item
+        d.x = -1;
+        d.greedy = 0;
+        d.s_hi = d.s_lo = 0.0f;
+        d.u_acc = d.u_s = {0.0f, 0.0f};
+    }
+    __syncwarp();
+    // every request writes the descriptors of its rows that belong to this batch
+    const int first = cid + nb * P.nclusters;
+    const int last = cid + (nb + nbatch) * P.nclusters;  // exclusive
+    for (int i = lane; i < P.B; i += kWarp) {
+        const int r0 = __ldg(P.row_off + i), r1 = __ldg(P.row_off + i + 1);
+        int lo = max(max(r0, first), 0);
+        lo += ((cid - lo) % P.nclusters + P.nclusters) % P.nclusters;  // next item of this cluster
+        const int hi = min(min(r1, last), P.total_rows);
+        for (int it = lo; it < hi; it += P.nclusters) {
+            const int s = (it - cid) / P.nclusters - nb;
+            if (s < 0 || s >= nbatch) continue;
+            Desc &d = sh.desc[s];
+            const int K = r1 - r0 - 1, j = it - r0, dr = r0 - i + j;
+            int status = 0;
+            if (K < 0 || K > P.K_max || j < 0 || j > K || r1 > P.total_rows ||
+                (j < K && (dr < 0 || dr >= P.total_rows - P.B)))
+                status = SPEC_REQ_BAD_SHAPE;
+            d.req = i;
+            d.pos = j;
+            d.K = K;
+            d.drow = dr;
+            d.pair = (status == 0 && j < K) ? 1 : 0;
+            d.status = status;
+            d.x = r1;  // the request's end row, for the frontier draw below
+        }
+    }
+    __syncwarp();
+    // per item: temperature, draws and draft token (loads issued in parallel, one thread each)
+    for (int s = lane; s < nbatch; s += kWarp) {
+        Desc &d = sh.desc[s];
+        int status = d.status;
+        const int r1 = d.x;
+        d.x = -1;
+        const float T = (d.req >= 0) ? (P.temperature ? __ldg(P.temperature + d.req) : P.temperature_scalar) : 1.0f;
+        if (!(T >= 0.0f) || isinf(T)) status |= SPEC_REQ_BAD_PARAM;
+        d.greedy = (T == 0.0f) ? 1 : 0;
+        F2 sv = {0.0f, 0.0f};
+        if (T > 0.0f && !isinf(T)) sv = f2_div({kLog2eHi, kLog2eLo}, {T, 0.0f});
+        if (sv.hi > 0.0f && sv.lo < 0.0f) {
+            // s_hi moved toward zero so that s_lo > 0: a -inf logit then gives -inf in both terms
+            // of exp_arg2 (a negative s_lo would make it NaN)
+            const float down = __uint_as_float(__float_as_uint(sv.hi) - 1u);
+            sv.lo += sv.hi - down;
+            sv.hi = down;
+        }
+        d.s_hi = sv.hi;
+        d.s_lo = fmaxf(sv.lo, 1.401298464e-45f);
+        if (status == 0 && d.req >= 0) {
+            d.u_acc = d2f2(__ldg(P.uniforms + d.item));
+            d.u_s = d2f2(__ldg(P.uniforms + r1 - 1));
+            if (d.pair) d.x = __ldg(P.draft_tokens + d.drow);
+        }
+        d.status = status;
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ int desc_rows(const Desc &d) {
+    return (d.status & (SPEC_REQ_BAD_SHAPE | SPEC_REQ_BAD_PARAM)) ? 0 : (d.pair ? 2 : 1);
+}
+
+// Control warp, lane 0: issue the bulk copies of the cluster's row sequence up to row `limit`
+// (exclusive).
+// The sequence runs through the batch's items in order: target row, then draft row for a pair.
+__device__ __forceinline__ void produce_rows(CtaShared &sh, uint4 *ring, const RowsParams &P, int slice_max, int lo,
+                                             int nvec, int nbatch, long long &issued, long long limit,
+                                             int &cur_item, int &cur_row) {
+    const size_t row_bytes = static_cast<size_t>(P.nvec_row) * 16;
+    const uint64_t pol = policy_evict_first();
+    while (issued < limit && cur_item < nbatch) {
+        const Desc &d = sh.desc[cur_item];
+        if (cur_row >= desc_rows(d)) {
+            ++cur_item;
+            cur_row = 0;
+            continue;
+        }
+        const int slot = static_cast<int>(issued % kRing);
+        const unsigned char *src =
+            (cur_row == 0) ? static_cast<const unsigned char *>(P.target) + static_cast<size_t>(d.item) * row_bytes
+                           : static_cast<const unsigned char *>(P.draft) + static_cast<size_t>(d.drow) * row_bytes;
+        const uint32_t bytes = static_cast<uint32_t>(nvec) * 16;
+        mbar_arrive_expect_tx(&sh.full[slot], bytes);
+        bulk_g2s(ring + static_cast<size_t>(slot) * slice_max, src + static_cast<size_t>(lo) * 16, bytes,
+                 &sh.full[slot], pol);
+        ++issued;
+        ++cur_row;
+    }
+}
+
+// A row of the item as pass 1 and pass 2 see it: vector v of thread t is vector t + 480 v of the
+// slice (a warp covers 32 contiguous vectors, a chunk). The target row is held in registers; the
+// draft row stays in its ring slot (so that only one row occupies registers).
+template <int NVT>
+struct RegRow {
+    const uint4 (&vv)[NVT];
+    __device__ __forceinline__ uint4 operator()(int v) const { return vv[v]; }
+};
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 3) spec_rows_kernel(const RowsParams P) {
+struct SmemRow {
+    const uint4 *src;
+    int tid, nvec;
+    __device__ __forceinline__ uint4 operator()(int v) const {
+        const int vi = tid + v * kThreads;
+        return vi < nvec ? src[vi] : kNegInfVec<DT>();
+    }
+};
+
+// Pass-1 statistics of one row. Each thread takes an integral reference b = floor(max * s) over
+// its own vectors (a first sweep, max only), then sums 2^(y*s - b) with every exponential
+// independent of the others (a second sweep, two accumulators); a warp combines its threads by
+// exact powers of two (one max and one sum across the lanes). For a row that a draw from p may
+// need (CHUNKS), also the per-chunk sums (chunk (v, warp), units 2^B_w with B_w the warp's
+// reference).
+template <int DT, int NVT, bool CHUNKS, class Row>
+__device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int r, int pb, const Desc &d, int lo,
+                                          int warp, int lane, int tid) {
     constexpr int E = Elt<DT>::kPerVec;
     constexpr int H = E / 2;
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t bars[2][kMaxChunks];
-    __shared__ Ex1 xch1[kMaxCluster];
-    __shared__ Ex2 xch2[kMaxCluster];
-    __shared__ Ex1 mine1;
-    __shared__ Ex2 mine2;
-    __shared__ ItemInfo I;
-    __shared__ float red_f[kWarps];
-
-    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-    griddep_launch_dependents();  // the selection kernel may be scheduled behind the last wave
-    const int C = static_cast<int>(cluster_nctarank());
-    const int crank = static_cast<int>(cluster_ctarank());
-    const int item = static_cast<int>(cluster_id_x());
-
-    uint4 *buf_t = reinterpret_cast<uint4 *>(smem_raw);
-    uint4 *buf_d = buf_t + P.slice_vecs_max;
-    float *gref = reinterpret_cast<float *>(buf_d + P.slice_vecs_max);  // [2][groups_max]
-    float *gsum = gref + 2 * P.groups_max;                              // [2][groups_max]
-    float *gres = gsum + 2 * P.groups_max;                              // [groups_max]
-    const size_t row_bytes = static_cast<size_t>(P.nvec_row) * 16;
-
-    // ---- slice, barriers, target copies (the target row is known without any lookup) ----
-    if (tid == 0) {
-        const int lo = static_cast<int>((static_cast<int64_t>(P.nvec_row) * crank) / C);
-        const int hi = static_cast<int>((static_cast<int64_t>(P.nvec_row) * (crank + 1)) / C);
-        I.lo = lo;
-        I.nvec = hi - lo;
-        I.groups = (I.nvec + kGroupVecs - 1) / kGroupVecs;
-        I.nchunk = max(1, min(kMaxChunks, I.groups / kWarps));
-        for (int r = 0; r < 2; ++r)
-            for (int k = 0; k < kMaxChunks; ++k) mbar_init(&bars[r][k], 1);
-        fence_mbar_init();
-        const uint64_t pol = policy_evict_first();
-        const unsigned char *src = static_cast<const unsigned char *>(P.target) + static_cast<size_t>(item) * row_bytes +
-                                   static_cast<size_t>(lo) * 16;
-        for (int k = 0; k < I.nchunk; ++k) {
-            int g0, g1, v0, v1;
-            chunk_range(I.groups, I.nchunk, k, I.nvec, g0, g1, v0, v1);
-            const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16;
-            mbar_arrive_expect_tx(&bars[0][k], bytes);
-            bulk_g2s(buf_t + v0, src + static_cast<size_t>(v0) * 16, bytes, &bars[0][k], pol);
-        }
-    }
-
-    // ---- which request and position this item is (warp 0) ----
-    // Loads whose values are needed only after pass 1 (the draft token, the uniforms) are
-    // issued here and consumed later, so their latency hides behind the copies.
-    int x_reg = -1;
-    double u_acc_reg = 0.0, u_s_reg = 0.0;
-    if (warp == 0) {
-        int i;
-        if (P.B < 8 * kWarp) {
-            // one round trip: lane l holds row_off[8l .. 8l+7]; i + 1 offsets are <= item
-            int cnt = 0;
+    if (d.greedy) {
+        // smallest index attaining the max; NaN / +inf make the row invalid
+        float best = -INFINITY;
+        int bidx = INT_MAX, bad = 0;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int idx = lane * 8 + k;
-                cnt += (idx <= P.B ? __ldg(P.row_off + idx) : INT_MAX) <= item;
+        for (int v = 0; v < NVT; ++v) {
+            const uint4 w = row(v);
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const float2 y = Elt<DT>::unpack_one(w, h);
+                bad |= (y.x != y.x) || (y.x == INFINITY) || (y.y != y.y) || (y.y == INFINITY);
+                if (y.x > best) {
+                    best = y.x;
+                    bidx = (lo + tid + v * kThreads) * E + 2 * h;
+                }
+                if (y.y > best) {
+                    best = y.y;
+                    bidx = (lo + tid + v * kThreads) * E + 2 * h + 1;
+                }
             }
+        }
+        const float wbest = warp_max(best);
+        const int widx = warp_min_i32(best == wbest ? bidx : INT_MAX);
+        const int wbad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            sh.ws[r][warp].gmax = wbest;
+            sh.ws[r][warp].garg = widx;
+            sh.ws[r][warp].bad = wbad;
+        }
+        return;
+    }
+    const float2 shi2 = f2splat(d.s_hi), slo2 = f2splat(d.s_lo);
+    float m = -INFINITY;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-            i = cnt - 1;
+    for (int v = 0; v < NVT; ++v) m = fmaxf(m, Elt<DT>::vmax(row(v)));
+    // an all -inf thread gets reference 0: its sum is 0 (or NaN if a NaN hides in it)
+    const float b = (m == -INFINITY) ? 0.0f : floorf(m * d.s_hi);
+    const float2 nb2 = f2splat(-b);
+    float sv[CHUNKS ? NVT : 1];
+    float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int v = 0; v < NVT; ++v) {
+        const uint4 w = row(v);
+        if (CHUNKS) {
+            float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const float2 e = ex2x2(exp_arg2(Elt<DT>::unpack_one(w, h), shi2, slo2, nb2));
+                if (h & 1) a1 = __fadd2_rn(a1, e);
+                else a0 = __fadd2_rn(a0, e);
+            }
+            const float2 a = __fadd2_rn(a0, a1);
+            sv[CHUNKS ? v : 0] = a.x + a.y;
         } else {
-            int lo = 0, hi = P.B;  // answer i in [lo, hi): row_off[i] <= item < row_off[i+1]
-            while (hi - lo > kWarp) {
-                const int step = (hi - lo + kWarp - 1) / kWarp;
-                const int idx = lo + lane * step;
-                const int v = idx < hi ? __ldg(P.row_off + idx) : INT_MAX;
-                const unsigned m = __ballot_sync(0xffffffffu, v <= item);
-                const int l = m ? 31 - __clz(static_cast<int>(m)) : 0;
-                lo = lo + l * step;
-                hi = min(lo + step, hi);
-            }
-            const int idx = lo + lane;
-            const int v = idx < hi ? __ldg(P.row_off + idx) : INT_MAX;
-            const unsigned m = __ballot_sync(0xffffffffu, v <= item);
-            i = m ? lo + 31 - __clz(static_cast<int>(m)) : -1;
-        }
-        if (lane == 0) {
-            int status = 0;
-            if (i < 0 || i >= P.B) i = -1;
-            int r0 = 0, r1 = 0, K = -1, j = -1, d = -1;
-            if (i >= 0) {
-                r0 = __ldg(P.row_off + i);
-                r1 = __ldg(P.row_off + i + 1);
-                K = r1 - r0 - 1;
-                j = item - r0;
-                d = r0 - i + j;
-            }
-            if (i < 0 || K < 0 || K > P.K_max || j < 0 || j > K || r1 > P.total_rows ||
-                (j < K && (d < 0 || d >= P.total_rows - P.B)))
-                status |= SPEC_REQ_BAD_SHAPE;
-            I.req = i;
-            I.pos = j;
-            I.K = K;
-            I.drow = d;
-            I.pair = (status == 0 && j < K) ? 1 : 0;
-            const float T = (i >= 0) ? (P.temperature ? __ldg(P.temperature + i) : P.temperature_scalar) : 1.0f;
-            if (!(T >= 0.0f) || isinf(T)) status |= SPEC_REQ_BAD_PARAM;
-            I.greedy = (T == 0.0f) ? 1 : 0;
-            // s = log2(e)/T as a float pair, then s_hi moved toward zero so that s_lo > 0: a -inf
-            // logit then gives -inf in both terms of exp_arg2 (a negative s_lo would make it NaN)
-            F2 s = {0.0f, 0.0f};
-            if (T > 0.0f && !isinf(T)) s = f2_div({kLog2eHi, kLog2eLo}, {T, 0.0f});
-            if (s.hi > 0.0f && s.lo < 0.0f) {
-                const float down = __uint_as_float(__float_as_uint(s.hi) - 1u);
-                s.lo += s.hi - down;
-                s.hi = down;
-            }
-            I.s_hi = s.hi;
-            I.s_lo = fmaxf(s.lo, 1.401298464e-45f);
-            if (status == 0) {
-                u_acc_reg = __ldg(P.uniforms + item);
-                u_s_reg = __ldg(P.uniforms + r1 - 1);
-                if (I.pair) x_reg = __ldg(P.draft_tokens + d);
-            }
-            I.status = status;
-            if (I.pair) {  // draft copies, once the draft row is known
-                const uint64_t pol = policy_evict_first();
-                const unsigned char *src = static_cast<const unsigned char *>(P.draft) +
-                                           static_cast<size_t>(d) * row_bytes + static_cast<size_t>(I.lo) * 16;
-                for (int k = 0; k < I.nchunk; ++k) {
-                    int g0, g1, v0, v1;
-                    chunk_range(I.groups, I.nchunk, k, I.nvec, g0, g1, v0, v1);
-                    const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16;
-                    mbar_arrive_expect_tx(&bars[1][k], bytes);
-                    bulk_g2s(buf_d + v0, src + static_cast<size_t>(v0) * 16, bytes, &bars[1][k], pol);
-                }
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const float2 e = ex2x2(exp_arg2(Elt<DT>::unpack_one(w, h), shi2, slo2, nb2));
+                if (h & 1) acc1 = __fadd2_rn(acc1, e);
+                else acc0 = __fadd2_rn(acc0, e);
             }
         }
     }
-    __syncthreads();
-
-    const int nrows = 1 + I.pair;
-    const int groups = I.groups, nvec = I.nvec, nchunk = I.nchunk;
-    const bool greedy = I.greedy != 0;
-    const float s_hi = I.s_hi, s_lo = I.s_lo;
-    const float2 shi2 = f2splat(s_hi), slo2 = f2splat(s_lo);
-    bool timed_out = false;
-
-    // ---- pass 1: per-group statistics as the chunks land ----
-    for (int r = 0; r < nrows; ++r) {
-        const uint4 *buf = r ? buf_d : buf_t;
-        for (int k = 0; k < nchunk; ++k) {
-            if (!mbar_wait_sleep_bounded(&bars[r][k], 0, kSuspendNs, kMaxWaitTries)) timed_out = true;
-            int g0, g1, v0, v1;
-            chunk_range(groups, nchunk, k, nvec, g0, g1, v0, v1);
-            for (int g = g0 + warp; g < g1; g += kWarps) {
-                const int vbase = g * kGroupVecs + lane;
-                if (greedy) {
-                    // smallest index attaining the max; NaN / +inf make the row invalid
-                    float best = -INFINITY;
-                    int bidx = INT_MAX, bad = 0;
+    float s;
+    if (CHUNKS) {
+        s = 0.0f;
 #pragma unroll
-                    for (int q = 0; q < kVecPerLane; ++q) {
-                        const int vi = vbase + q * kWarp;
-                        float2 y[H];
-                        load_vec2<DT>(buf, vi, nvec, y);
+        for (int v = 0; v < NVT; ++v) s += sv[CHUNKS ? v : 0];
+    } else {
+        const float2 a = __fadd2_rn(acc0, acc1);
+        s = a.x + a.y;
+    }
+    const bool ok = s > 0.0f && !isinf(s);  // NaN, inf and empty are not ok
+    const int bad = __any_sync(0xffffffffu, !(s >= 0.0f) || isinf(s));
+    const float Bw = warp_max(ok ? b : -INFINITY);
+    const float scale = ok ? pow2i(b - Bw) : 0.0f;
+    const float Sw = warp_sum(ok ? s * scale : 0.0f);
+    if (CHUNKS) {
 #pragma unroll
-                        for (int e = 0; e < E; ++e) {
-                            const float v = (e & 1) ? y[e / 2].y : y[e / 2].x;
-                            bad |= (v != v) || (v == INFINITY);
-                            if (v > best) {
-                                best = v;
-                                bidx = (I.lo + vi) * E + e;
-                            }
-                        }
-                    }
-                    const float wbest = warp_max(best);
-                    const int widx = warp_min_i32(best == wbest ? bidx : INT_MAX);
-                    const int wbad = __any_sync(0xffffffffu, bad);
-                    if (lane == 0) {
-                        gref[r * P.groups_max + g] = wbest;
-                        gsum[r * P.groups_max + g] = __int_as_float(wbad ? -1 : widx);
-                    }
-                } else {
-                    // the group's vectors stay in registers between the max and the sums
-                    uint4 wv[kVecPerLane];
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int q = 0; q < kVecPerLane; ++q) {
-                        const int vi = vbase + q * kWarp;
-                        wv[q] = vi < nvec ? buf[vi] : kNegInfVec<DT>();
-                        mx = fmaxf(mx, Elt<DT>::vmax(wv[q]));
-                    }
-                    mx = warp_max(mx);
-                    // integral reference exponent: rescaling groups and CTAs is then exact; an
-                    // all -inf group gets 0 (its sum is 0, or NaN if a NaN hides in it)
-                    const float b = (mx == -INFINITY) ? 0.0f : floorf(mx * s_hi);
-                    const float2 nb = f2splat(-b);
-                    float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-                    for (int q = 0; q < kVecPerLane; ++q) {
-                        float2 y[H];
-                        Elt<DT>::unpack2(wv[q], y);
-#pragma unroll
-                        for (int h = 0; h < H; ++h) acc = __fadd2_rn(acc, ex2x2(exp_arg2(y[h], shi2, slo2, nb)));
-                    }
-                    const float a = warp_sum(acc.x + acc.y);
-                    if (lane == 0) {
-                        gref[r * P.groups_max + g] = b;
-                        gsum[r * P.groups_max + g] = a;
-                    }
-                }
+        for (int v = 0; v < NVT; ++v) {
+            const float c = warp_sum(ok ? sv[CHUNKS ? v : 0] * scale : 0.0f);
+            if (lane == 0) {
+                sh.pm[pb][v * kWarps + warp] = c;
+                sh.pref[pb][v * kWarps + warp] = Bw;
             }
         }
     }
-    if (warp == 0 && lane == 0) I.x = x_reg;
-    __syncthreads();
+    if (lane == 0) {
+        sh.ws[r][warp].B = Bw;
+        sh.ws[r][warp].S_hi = Sw;
+        sh.ws[r][warp].S_lo = 0.0f;
+        sh.ws[r][warp].bad = bad;
+    }
+}
 
-    // ---- this CTA's record: per-row statistics (lane 0 of warp r), the logits at x (warp 2) ----
-    // One thread per row walks the group results in registers: a single wait on shared memory
-    // instead of a chain of dependent warp shuffles, which queue behind the co-resident CTAs'
-    // streaming loads.
-    if (warp < nrows && lane == 0) {
-        const int r = warp;
-        const float *gr = gref + r * P.groups_max;
-        const float *gs = gsum + r * P.groups_max;
-        if (greedy) {
-            float best = -INFINITY;
-            int bidx = INT_MAX, bad = 0;
-            for (int g = 0; g < groups; ++g) {
-                const float v = gr[g];
-                const int ix = __float_as_int(gs[g]);
-                if (ix < 0) bad = 1;
-                if (v > best || (v == best && ix < bidx)) {
-                    best = v;
-                    bidx = ix;
-                }
+// Control warp: this CTA's message for item n: its row statistics over the warps (lanes 0-15 take
+// row 0, lanes 16-31 row 1, one lane per data warp), the logits at the draft token if it holds them,
+// (the previous item's totals are already in place).
+__device__ __forceinline__ void build_message(CtaShared &sh, int greedy, int nr, int n, int nch, int lane) {
+    Msg &msg = sh.mine;
+    const int r = lane >> 4, w = lane & 15;
+    const bool on = r < nr && w < kWarps;
+    const WarpStat &st = sh.ws[r][w];
+    int bad = on ? st.bad : 0;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    float B = -INFINITY, gmax = -INFINITY;
+    int garg = INT_MAX;
+    F2 S = {0.0f, 0.0f};
+    if (greedy) {
+        gmax = on ? st.gmax : -INFINITY;
+        garg = on ? st.garg : INT_MAX;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+            const float og = __shfl_xor_sync(0xffffffffu, gmax, o);
+            const int oa = __shfl_xor_sync(0xffffffffu, garg, o);
+            if (og > gmax || (og == gmax && oa < garg)) {
+                gmax = og;
+                garg = oa;
             }
-            mine1.gmax[r] = best;
-            mine1.garg[r] = bidx;
-            mine1.bad[r] = bad;
+        }
+    } else {
+        const float Sw = on ? st.S_hi : 0.0f;
+        const bool has = Sw > 0.0f;
+        const float Bw = on ? st.B : -INFINITY;
+        B = has ? Bw : -INFINITY;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) B = fmaxf(B, __shfl_xor_sync(0xffffffffu, B, o));
+        S = has ? F2{Sw * pow2i(Bw - B), 0.0f} : F2{0.0f, 0.0f};
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+            const F2 x = {__shfl_xor_sync(0xffffffffu, S.hi, o), __shfl_xor_sync(0xffffffffu, S.lo, o)};
+            S = f2_add(S, x);
+        }
+    }
+    if (w == 0) {
+        msg.B[r] = B;
+        msg.S_hi[r] = S.hi;
+        msg.S_lo[r] = S.lo;
+        msg.bad[r] = bad;
+        msg.gmax[r] = gmax;
+        msg.garg[r] = garg;
+    }
+    if (lane == 0) {
+        msg.has_x = (sh.x_stamp == n + 1) ? 1 : 0;
+        msg.yx[0] = sh.yx[0];
+        msg.yx[1] = sh.yx[1];
+        msg.tmo = sh.timed_out;
+    }
+}
+
+// Control warp, once pass 2 of item n is done: this slice's alpha share and residual mass of the
+// item, for the next message.
+__device__ __forceinline__ void stash_totals(CtaShared &sh, int n, int nch, int lane) {
+    const float pa = warp_sum(lane < kWarps ? sh.wal[lane] : 0.0f);
+    F2 pz = {0.0f, 0.0f};
+    if (sh.dec[n & 1].kind == SAMPLE_RESIDUAL) {
+#pragma unroll 1
+        for (int k = lane; k < nch; k += kWarp) pz = f2_add(pz, {sh.rm[n & 1][k], 0.0f});
+        pz = warp_sum_f2(pz);
+    }
+    if (lane == 0) {
+        sh.mine.prev_alpha = pa;
+        sh.mine.prev_Zhi = pz.hi;
+        sh.mine.prev_Zlo = pz.lo;
+    }
+}
+
+// Control warp, after the exchange of item n: combine the C records (lanes 0-15 take row 0,
+// lanes 16-31 row 1, one lane per CTA, in CTA order; C is a power of two, so log2(C) butterfly
+// steps combine them) and decide the accept test (lane 0). Every CTA runs the same reductions on
+// the same records, so all reach the same decision.
+__device__ __forceinline__ void decide_item(CtaShared &sh, const Desc &d, int nr, int n, int C, const RowsParams &P,
+                                            int lane) {
+    const Msg *M = sh.slot[n % 3];
+    const int r = lane >> 4, c = lane & 15;
+    const bool on = c < C && r < nr;
+    const Msg &m = M[c < C ? c : 0];
+    const unsigned tmo = __ballot_sync(0xffffffffu, r == 0 && c < C && m.tmo);
+    const unsigned hx = __ballot_sync(0xffffffffu, r == 0 && c < C && m.has_x);
+    float yx_t = 0.0f, yx_d = 0.0f;
+    if (hx) {
+        const int l = 31 - __clz(static_cast<int>(hx));
+        yx_t = __shfl_sync(0xffffffffu, m.yx[0], l);
+        yx_d = __shfl_sync(0xffffffffu, m.yx[1], l);
+    }
+    int bad = on ? m.bad[r] : 0;
+    for (int o = C >> 1; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    float Bv = -INFINITY, gm = -INFINITY;
+    int ga = INT_MAX;
+    F2 S = {0.0f, 0.0f};
+    if (d.greedy) {
+        gm = on ? m.gmax[r] : -INFINITY;
+        ga = on ? m.garg[r] : INT_MAX;
+        for (int o = C >> 1; o > 0; o >>= 1) {
+            const float og = __shfl_xor_sync(0xffffffffu, gm, o);
+            const int oa = __shfl_xor_sync(0xffffffffu, ga, o);
+            if (og > gm || (og == gm && oa < ga)) {
+                gm = og;
+                ga = oa;
+            }
+        }
+    } else {
+        const float Sh = on ? m.S_hi[r] : 0.0f;
+        const bool has = Sh > 0.0f;
+        const float Bc = on ? m.B[r] : -INFINITY;
+        Bv = has ? Bc : -INFINITY;
+        for (int o = C >> 1; o > 0; o >>= 1) Bv = fmaxf(Bv, __shfl_xor_sync(0xffffffffu, Bv, o));
+        S = has ? f2_scale({Sh, m.S_lo[r]}, Bc - Bv) : F2{0.0f, 0.0f};
+        for (int o = C >> 1; o > 0; o >>= 1)
+            S = f2_add(S, {__shfl_xor_sync(0xffffffffu, S.hi, o), __shfl_xor_sync(0xffffffffu, S.lo, o)});
+    }
+    // row 1 (lane 16) to lane 0
+    const int bad1 = __shfl_sync(0xffffffffu, bad, 16);
+    const float Bv1 = __shfl_sync(0xffffffffu, Bv, 16);
+    const F2 S1 = shfl_f2(S, 16);
+    const float gm1 = __shfl_sync(0xffffffffu, gm, 16);
+    const int ga1 = __shfl_sync(0xffffffffu, ga, 16);
+    if (lane != 0) return;
+    Decision &D = sh.dec[n & 1];
+    D.item = d.item;
+    D.drow = d.drow;
+    D.pair = d.pair;
+    D.greedy = d.greedy;
+    D.s_hi = d.s_hi;
+    D.s_lo = d.s_lo;
+    D.u_s = d.u_s;
+    D.valid = 1;
+    D.accept = 0;
+    D.kind = SAMPLE_NONE;
+    D.rho = 0.0f;
+    D.argmax_t = -1;
+    D.alpha_g = 0.0f;
+    int status = d.status | (tmo ? REQ_TIMEOUT : 0);
+    int am[2] = {-1, -1};
+    float Bw[2] = {NAN, NAN};
+    F2 Sr[2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+    if (nr >= 1) {
+        am[0] = (bad || gm == -INFINITY) ? -1 : ga;
+        Bw[0] = bad ? NAN : Bv;
+        Sr[0] = S;
+    }
+    if (nr >= 2) {
+        am[1] = (bad1 || gm1 == -INFINITY) ? -1 : ga1;
+        Bw[1] = bad1 ? NAN : Bv1;
+        Sr[1] = S1;
+    }
+    D.B_t = Bw[0];
+    D.B_d = Bw[1];
+    D.S_t = Sr[0];
+    D.S_d = Sr[1];
+    // row validity is reported together with a bad proposal (both are preconditions)
+    if (!(status & (SPEC_REQ_BAD_SHAPE | SPEC_REQ_BAD_PARAM | REQ_TIMEOUT))) {
+        if (d.greedy) {
+            if (am[0] < 0 || (d.pair && am[1] < 0)) status |= SPEC_REQ_BAD_LOGITS;
+            if (d.pair && (d.x < 0 || d.x >= P.V)) status |= SPEC_REQ_BAD_PROPOSAL;
         } else {
-            float Bc = -INFINITY;
-            int bad = 0;
-            for (int g = 0; g < groups; ++g) {
-                const float sg = gs[g];
-                if (!(sg >= 0.0f) || isinf(sg)) bad = 1;  // NaN or inf
-                if (sg > 0.0f) Bc = fmaxf(Bc, gr[g]);
-            }
-            F2 acc = {0.0f, 0.0f};
-            for (int g = 0; g < groups; ++g) {
-                const float sg = gs[g];
-                if (sg > 0.0f && !isinf(sg)) acc = f2_add(acc, {sg * pow2i(gr[g] - Bc), 0.0f});
-            }
-            mine1.B[r] = Bc;
-            mine1.S_hi[r] = acc.hi;
-            mine1.S_lo[r] = acc.lo;
-            mine1.bad[r] = bad;
+            const bool ok_t = isfinite(D.B_t) && D.S_t.hi > 0.0f && isfinite(D.S_t.hi);
+            const bool ok_d = !d.pair || (isfinite(D.B_d) && D.S_d.hi > 0.0f && isfinite(D.S_d.hi));
+            if (!ok_t || !ok_d) status |= SPEC_REQ_BAD_LOGITS;
+            // q(x) == 0 is a bad proposal for Rule 2 (checked before any draw)
+            if (d.pair && (d.x < 0 || d.x >= P.V || yx_d == -INFINITY)) status |= SPEC_REQ_BAD_PROPOSAL;
         }
-    } else if (warp == 2 && lane == 0) {
-        const int x = I.x;
-        const int xl = x - I.lo * E;  // position of x in this slice
-        const int has = I.pair && x >= 0 && xl >= 0 && xl < nvec * E;
-        mine1.has_x = has;
-        mine1.yx[0] = has ? Elt<DT>::at(buf_t, xl) : 0.0f;
-        mine1.yx[1] = has ? Elt<DT>::at(buf_d, xl) : 0.0f;
     }
-    __syncthreads();
-    if (warp == 0) push_record(&mine1, xch1, crank, kEx1Words, C, lane);
-    cluster_sync_all();  // #1: every slice's record is in every CTA
+    if (status == 0) {
+        if (d.greedy) {
+            D.argmax_t = am[0];
+            if (d.pair) {
+                D.accept = (d.x == am[0]);
+                D.rho = D.accept ? 1.0f : 0.0f;
+                D.alpha_g = (am[0] == am[1]) ? 1.0f : 0.0f;
+            }
+        } else {
+            D.inv_St = rcp_approx(D.S_t.hi);
+            if (d.pair) {
+                // rho = p(x)/q(x) = 2^E * S_d/S_t with E = (y_t - y_d) s - (B_t - B_d), in float
+                // pairs; 2^E from ex2 of its fraction and an exact power of two
+                D.lam = f2_div(D.S_t, D.S_d);
+                float rho = 0.0f;
+                if (yx_t != -INFINITY) {
+                    F2 Ex = f2_mul(f2_add({yx_t, 0.0f}, {-yx_d, 0.0f}), {d.s_hi, d.s_lo});
+                    Ex = f2_add(Ex, {-(D.B_t - D.B_d), 0.0f});
+                    const float nn = floorf(Ex.hi);
+                    const float f = (Ex.hi - nn) + Ex.lo;
+                    const F2 ratio = f2_div(D.S_d, D.S_t);
+                    const float m = ex2(f) * (ratio.hi + ratio.lo);
+                    if (nn > 254.0f) {
+                        rho = INFINITY;
+                    } else if (nn >= -252.0f) {
+                        const float h = floorf(0.5f * nn);
+                        rho = m * pow2i(h) * pow2i(nn - h);
+                    }
+                }
+                D.rho = rho;
+                D.accept = (rho > 0.0f) && !f2_gt(d.u_acc, {rho, 0.0f});
+                D.c_t = D.B_t + __log2f(D.S_t.hi);
+                D.c_d = D.B_d + __log2f(D.S_d.hi);
+                if (!D.accept) D.kind = SAMPLE_RESIDUAL;
+            } else {
+                D.kind = SAMPLE_P;
+            }
+        }
+    }
+    D.status = status;
+}
 
-    // ---- combine the cluster (thread 0 walks the C records in CTA order), decide the accept test ----
-    if (warp == 0) {
-        float yx_t = 0.0f, yx_d = 0.0f;
-        if (lane == 0) {
-            for (int r = 0; r < nrows; ++r) {
-                if (greedy) {
-                    float best = -INFINITY;
-                    int bidx = INT_MAX, bad = 0;
-                    for (int c = 0; c < C; ++c) {
-                        const float v = xch1[c].gmax[r];
-                        const int ix = xch1[c].garg[r];
-                        bad |= xch1[c].bad[r];
-                        if (v > best || (v == best && ix < bidx)) {
-                            best = v;
-                            bidx = ix;
-                        }
-                    }
-                    const int am = (bad || best == -INFINITY) ? -1 : bidx;
-                    if (r == 0) I.argmax_t = am;
-                    else I.argmax_d = am;
-                } else {
-                    float Bw = -INFINITY;
-                    int bad = 0;
-                    for (int c = 0; c < C; ++c) {
-                        bad |= xch1[c].bad[r];
-                        if (xch1[c].S_hi[r] > 0.0f) Bw = fmaxf(Bw, xch1[c].B[r]);
-                    }
-                    F2 S = {0.0f, 0.0f};
-                    for (int c = 0; c < C; ++c) {
-                        const F2 Sc = {xch1[c].S_hi[r], xch1[c].S_lo[r]};
-                        if (Sc.hi > 0.0f) S = f2_add(S, f2_scale(Sc, xch1[c].B[r] - Bw));
-                    }
-                    if (r == 0) {
-                        I.B_t = bad ? NAN : Bw;
-                        I.S_t = S;
-                    } else {
-                        I.B_d = bad ? NAN : Bw;
-                        I.S_d = S;
-                    }
-                }
-            }
-            for (int c = 0; c < C; ++c)
-                if (xch1[c].has_x) {
-                    yx_t = xch1[c].yx[0];
-                    yx_d = xch1[c].yx[1];
-                }
-        }
-        if (lane == 0) {
-            int status = I.status | (timed_out ? REQ_TIMEOUT : 0);
-            I.accept = 0;
-            I.sample_kind = SAMPLE_NONE;
-            I.rho = 0.0f;
-            I.u_acc = d2f2(u_acc_reg);
-            I.u_s = d2f2(u_s_reg);
-            // row validity is reported together with a bad proposal (both are preconditions)
-            if (!(status & (SPEC_REQ_BAD_SHAPE | SPEC_REQ_BAD_PARAM | REQ_TIMEOUT))) {
-                if (greedy) {
-                    if (I.argmax_t < 0 || (I.pair && I.argmax_d < 0)) status |= SPEC_REQ_BAD_LOGITS;
-                    if (I.pair && (I.x < 0 || I.x >= P.V)) status |= SPEC_REQ_BAD_PROPOSAL;
-                } else {
-                    const bool ok_t = isfinite(I.B_t) && I.S_t.hi > 0.0f && isfinite(I.S_t.hi);
-                    const bool ok_d = !I.pair || (isfinite(I.B_d) && I.S_d.hi > 0.0f && isfinite(I.S_d.hi));
-                    if (!ok_t || !ok_d) status |= SPEC_REQ_BAD_LOGITS;
-                    // q(x) == 0 is a bad proposal for Rule 2 (checked before any draw)
-                    if (I.pair && (I.x < 0 || I.x >= P.V || yx_d == -INFINITY)) status |= SPEC_REQ_BAD_PROPOSAL;
-                }
-            }
-            if (status == 0) {
-                if (greedy) {
-                    if (I.pair) {
-                        I.accept = (I.x == I.argmax_t);
-                        I.rho = I.accept ? 1.0f : 0.0f;
-                        I.alpha = (I.argmax_t == I.argmax_d) ? 1.0f : 0.0f;
-                    }
-                } else {
-                    I.inv_St = rcp_approx(I.S_t.hi);
-                    if (I.pair) {
-                        // rho = p(x)/q(x) = 2^E * S_d/S_t with E = (y_t - y_d) s - (B_t - B_d), all
-                        // in float pairs; 2^E from ex2 of its fraction and an exact power of two
-                        I.lam = f2_div(I.S_t, I.S_d);
-                        float rho = 0.0f;
-                        if (yx_t != -INFINITY) {
-                            F2 Ex = f2_mul(f2_add({yx_t, 0.0f}, {-yx_d, 0.0f}), {s_hi, s_lo});
-                            Ex = f2_add(Ex, {-(I.B_t - I.B_d), 0.0f});
-                            const float n = floorf(Ex.hi);
-                            const float f = (Ex.hi - n) + Ex.lo;
-                            const F2 ratio = f2_div(I.S_d, I.S_t);
-                            const float m = ex2(f) * (ratio.hi + ratio.lo);
-                            if (n > 254.0f) {
-                                rho = INFINITY;
-                            } else if (n >= -252.0f) {
-                                const float h = floorf(0.5f * n);
-                                rho = m * pow2i(h) * pow2i(n - h);
-                            }
-                        }
-                        I.rho = rho;
-                        I.accept = (rho > 0.0f) && !f2_gt(I.u_acc, {rho, 0.0f});
-                        I.c_t = I.B_t + __log2f(I.S_t.hi);
-                        I.c_d = I.B_d + __log2f(I.S_d.hi);
-                        if (!I.accept) I.sample_kind = SAMPLE_RESIDUAL;
-                    } else {
-                        I.sample_kind = SAMPLE_P;
-                    }
-                }
-            }
-            I.status = status;
-        }
-    }
-    __syncthreads();
-    // ---- pass 2 (pairs under Rule 2): alpha, and the residual where this position rejects ----
+// Pass 2 of a pair under Rule 2, from the registers of pass 1. Where the position rejects:
+// e_t = 2^(y_t s - B_t), e_d = 2^(y_d s - B_d), lambda = S_t / S_d; the residual
+// max(e_t - lambda e_d, 0) per chunk, S_t * min(p, q) = min(e_t, lambda e_d) (no cancellation),
+// and per (vector, thread) the sums of e_t (a draw from p when the residual has no mass). Where it
+// accepts, only alpha: min(p, q) = 2^min(y_t s - c_t, y_d s - c_d), c = B + log2 S.
+template <int DT, int NVT>
+__device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> &rd, CtaShared &sh,
+                                      const Decision &D, int par, int warp, int lane, int tid) {
+    constexpr int H = Elt<DT>::kPerVec / 2;
     float my_alpha = 0.0f;
-    if (I.status == 0 && I.pair && !greedy) {
-        if (I.sample_kind == SAMPLE_RESIDUAL) {
-            const float2 nbt = f2splat(-I.B_t), nbd = f2splat(-I.B_d);
-            const float2 nlh = f2splat(-I.lam.hi), nll = f2splat(-I.lam.lo), lh = f2splat(I.lam.hi);
+    if (D.status == 0 && D.pair && !D.greedy) {
+        const float2 shi2 = f2splat(D.s_hi), slo2 = f2splat(D.s_lo);
+        if (D.kind == SAMPLE_RESIDUAL) {
+            const float2 nbt = f2splat(-D.B_t), nbd = f2splat(-D.B_d);
+            const float2 nlh = f2splat(-D.lam.hi), nll = f2splat(-D.lam.lo);
             float2 acc_a = make_float2(0.0f, 0.0f);
-            for (int g = warp; g < groups; g += kWarps) {
-                float2 racc = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int q = 0; q < kVecPerLane; ++q) {
-                    const int vi = g * kGroupVecs + q * kWarp + lane;
-                    float2 yt[H], yd[H];
-                    load_vec2<DT>(buf_t, vi, nvec, yt);
-                    load_vec2<DT>(buf_d, vi, nvec, yd);
+            for (int v = 0; v < NVT; ++v) {
+                const uint4 wd = rd(v);
+                float2 racc = make_float2(0.0f, 0.0f), pacc = make_float2(0.0f, 0.0f);
 #pragma unroll
-                    for (int h = 0; h < H; ++h) {
-                        const float2 et = ex2x2(exp_arg2(yt[h], shi2, slo2, nbt));
-                        const float2 ed = ex2x2(exp_arg2(yd[h], shi2, slo2, nbd));
-                        const float2 r = __ffma2_rn(ed, nll, __ffma2_rn(ed, nlh, et));
-                        racc = __fadd2_rn(racc, make_float2(fmaxf(r.x, 0.0f), fmaxf(r.y, 0.0f)));
-                        const float2 m = __fmul2_rn(ed, lh);  // S_t * min(p, q): no cancellation
-                        acc_a = __fadd2_rn(acc_a, make_float2(fminf(et.x, m.x), fminf(et.y, m.y)));
-                    }
+                for (int h = 0; h < H; ++h) {
+                    const float2 yt = Elt<DT>::unpack_one(vt[v], h), yd = Elt<DT>::unpack_one(wd, h);
+                    const float2 et = ex2x2(exp_arg2(yt, shi2, slo2, nbt));
+                    const float2 ed = ex2x2(exp_arg2(yd, shi2, slo2, nbd));
+                    const float2 r = __ffma2_rn(ed, nll, __ffma2_rn(ed, nlh, et));
+                    const float2 nq = __fmul2_rn(ed, nlh);  // -lambda_hi * e_d, for min(p, q)
+                    racc = __fadd2_rn(racc, make_float2(fmaxf(r.x, 0.0f), fmaxf(r.y, 0.0f)));
+                    pacc = __fadd2_rn(pacc, et);
+                    acc_a = __fadd2_rn(acc_a, make_float2(fminf(et.x, -nq.x), fminf(et.y, -nq.y)));
                 }
+                sh.tpm[v * kThreads + tid] = pacc.x + pacc.y;
                 const float rs = warp_sum(racc.x + racc.y);
-                if (lane == 0) gres[g] = rs;
+                if (lane == 0) sh.rm[par][v * kWarps + warp] = rs;
             }
-            my_alpha = (acc_a.x + acc_a.y) * I.inv_St;
+            my_alpha = (acc_a.x + acc_a.y) * D.inv_St;
         } else {
-            const float2 nct = f2splat(-I.c_t), ncd = f2splat(-I.c_d);
+            const float2 nct = f2splat(-D.c_t), ncd = f2splat(-D.c_d);
             float2 acc = make_float2(0.0f, 0.0f);
-            for (int g = warp; g < groups; g += kWarps) {
 #pragma unroll
-                for (int q = 0; q < kVecPerLane; ++q) {
-                    const int vi = g * kGroupVecs + q * kWarp + lane;
-                    if (vi >= nvec) continue;
-                    float2 yt[H], yd[H];
-                    Elt<DT>::unpack2(buf_t[vi], yt);
-                    Elt<DT>::unpack2(buf_d[vi], yd);
+            for (int v = 0; v < NVT; ++v) {
+                const uint4 wd = rd(v);
 #pragma unroll
-                    for (int h = 0; h < H; ++h) {
-                        const float2 at = __ffma2_rn(yt[h], shi2, nct), ad = __ffma2_rn(yd[h], shi2, ncd);
-                        acc = __fadd2_rn(acc, make_float2(ex2(fminf(at.x, ad.x)), ex2(fminf(at.y, ad.y))));
-                    }
+                for (int h = 0; h < H; ++h) {
+                    const float2 at = __ffma2_rn(Elt<DT>::unpack_one(vt[v], h), shi2, nct);
+                    const float2 ad = __ffma2_rn(Elt<DT>::unpack_one(wd, h), shi2, ncd);
+                    acc = __fadd2_rn(acc, make_float2(ex2(fminf(at.x, ad.x)), ex2(fminf(at.y, ad.y))));
                 }
             }
             my_alpha = acc.x + acc.y;
         }
     }
     my_alpha = warp_sum(my_alpha);
-    if (lane == 0) red_f[warp] = my_alpha;
-    __syncthreads();
-    if (warp == 0) {
-        float a = lane < kWarps ? red_f[lane] : 0.0f;
-        a = warp_sum(a);
-        F2 z = {0.0f, 0.0f};
-        if (I.sample_kind == SAMPLE_RESIDUAL)
-            for (int g = lane; g < groups; g += kWarp) z = f2_add(z, {gres[g], 0.0f});
-        z = warp_sum_f2(z);
-        if (lane == 0) {
-            mine2.alpha = a;
-            mine2.Z_hi = z.hi;
-            mine2.Z_lo = z.lo;
-        }
-        __syncwarp();
-        push_record(&mine2, xch2, crank, kEx2Words, C, lane);
-    }
-    cluster_sync_all();  // #2: alpha and residual shares are in every CTA; no remote access after this
+    if (lane == 0) sh.wal[warp] = my_alpha;
+}
 
-    // ---- cluster totals, the owner of the draw, item results (thread 0, CTAs in order) ----
-    if (warp == 0) {
-        float alpha_sum = 0.0f;
-        int kind = I.sample_kind, fb = 0, owner = -1;
-        F2 Zres = {0.0f, 0.0f}, Ztot = {0.0f, 0.0f}, t = {0.0f, 0.0f}, prefix = {0.0f, 0.0f};
-        if (lane == 0) {
-            for (int c = 0; c < C; ++c) {
-                alpha_sum += xch2[c].alpha;
-                Zres = f2_add(Zres, {xch2[c].Z_hi, xch2[c].Z_lo});
-            }
-            if (kind == SAMPLE_RESIDUAL && !(Zres.hi > 0.0f)) {
-                kind = SAMPLE_P;  // zero residual mass: draw from p and say so
-                fb = 1;
-            }
-            if (kind != SAMPLE_NONE && I.status == 0 && !greedy) {
-                // masses of the law the draw uses, per CTA; the owner is the CTA whose running
-                // total first exceeds u * Z (else the last CTA with mass, when rounding put u*Z
-                // at the very end)
-                for (int c = 0; c < C; ++c) {
-                    const F2 Sc = {xch1[c].S_hi[0], xch1[c].S_lo[0]};
-                    const F2 m = (kind == SAMPLE_RESIDUAL) ? F2{xch2[c].Z_hi, xch2[c].Z_lo}
-                                                           : (Sc.hi > 0.0f ? f2_scale(Sc, xch1[c].B[0] - I.B_t)
-                                                                           : F2{0.0f, 0.0f});
-                    Ztot = f2_add(Ztot, m);
-                }
-                t = f2_mul(Ztot, I.u_s);
-                F2 run = {0.0f, 0.0f}, last_run = {0.0f, 0.0f};
-                int last = -1;
-                for (int c = 0; c < C; ++c) {
-                    const F2 Sc = {xch1[c].S_hi[0], xch1[c].S_lo[0]};
-                    const F2 m = (kind == SAMPLE_RESIDUAL) ? F2{xch2[c].Z_hi, xch2[c].Z_lo}
-                                                           : (Sc.hi > 0.0f ? f2_scale(Sc, xch1[c].B[0] - I.B_t)
-                                                                           : F2{0.0f, 0.0f});
-                    const F2 next = f2_add(run, m);
-                    if (m.hi > 0.0f) {
-                        last = c;
-                        last_run = run;
-                        if (owner < 0 && f2_gt(next, t)) {
-                            owner = c;
-                            prefix = run;
-                        }
-                    }
-                    run = next;
-                }
-                if (owner < 0) {
-                    owner = last;
-                    prefix = last_run;
-                }
-            }
+// The draw weights of one vector, exactly as the passes summed them: the residual in units of
+// 2^B_t, or p in units of 2^bg (bg: the chunk's reference).
+template <int DT>
+__device__ __forceinline__ void draw_weights(int kind, const uint4 &wt, const uint4 &wd, const Decision &D, float bg,
+                                             float *w) {
+    constexpr int H = Elt<DT>::kPerVec / 2;
+    const float2 shi2 = f2splat(D.s_hi), slo2 = f2splat(D.s_lo);
+    float2 yt[H];
+    Elt<DT>::unpack2(wt, yt);
+    if (kind == SAMPLE_RESIDUAL) {
+        float2 yd[H];
+        Elt<DT>::unpack2(wd, yd);
+        const float2 nbt = f2splat(-D.B_t), nbd = f2splat(-D.B_d);
+        const float2 nlh = f2splat(-D.lam.hi), nll = f2splat(-D.lam.lo);
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const float2 et = ex2x2(exp_arg2(yt[h], shi2, slo2, nbt));
+            const float2 ed = ex2x2(exp_arg2(yd[h], shi2, slo2, nbd));
+            const float2 r = __ffma2_rn(ed, nll, __ffma2_rn(ed, nlh, et));
+            w[2 * h] = fmaxf(r.x, 0.0f);
+            w[2 * h + 1] = fmaxf(r.y, 0.0f);
         }
-        if (lane == 0) {
-            I.sample_kind = kind;
-            I.owner = owner;
-            I.Ztot = Ztot;
-            I.target_t = t;
-            I.owner_prefix = prefix;
-            if (crank == 0) {
-                const int st = I.status;
-                P.item_status[item] = st;
-                P.item_fb[item] = fb;
-                if (I.pair) {
-                    const float alpha = greedy ? I.alpha : alpha_sum;
-                    P.item_flag[item] = (st == 0) ? I.accept : 0;
-                    P.alpha_ws[I.drow] = (st == 0) ? alpha : 0.0f;
-                    if (P.alpha_rows) P.alpha_rows[I.drow] = (st == 0) ? alpha : NAN;
-                    if (P.rho_rows) P.rho_rows[I.drow] = (st == 0) ? I.rho : NAN;
-                    if (P.resid_rows)
-                        P.resid_rows[I.drow] = (st == 0 && kind == SAMPLE_RESIDUAL && !greedy)
-                                                   ? f2_div(Zres, I.S_t).hi
-                                                   : -1.0f;
+    } else {
+        const float2 nb = f2splat(-bg);
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const float2 e = ex2x2(exp_arg2(yt[h], shi2, slo2, nb));
+            w[2 * h] = e.x;
+            w[2 * h + 1] = e.y;
+        }
+    }
+}
+
+// Mass of CTA c's slice in the law a draw of item m uses (units 2^B_t).
+__device__ __forceinline__ F2 cta_mass(const Msg &Mi, const Msg &Mn, int kind, float B_t) {
+    if (kind == SAMPLE_RESIDUAL) return {Mn.prev_Zhi, Mn.prev_Zlo};
+    const F2 Sc = {Mi.S_hi[0], Mi.S_lo[0]};
+    return Sc.hi > 0.0f ? f2_scale(Sc, Mi.B[0] - B_t) : F2{0.0f, 0.0f};
+}
+
+// What the control warp knows about item m's draw after the exchange that carries its totals.
+struct FinState {
+    int kind, fb, owner;
+    F2 local, Ztot;  // u*Z less the mass of the CTAs before the owner; Z (units 2^B_t)
+};
+
+// Control warp: item m rejected and the next exchange reports no residual mass in any slice.
+__device__ __forceinline__ bool zero_residual(const CtaShared &sh, int m, int C, int lane) {
+    if (sh.dec[m & 1].kind != SAMPLE_RESIDUAL) return false;
+    const Msg *Mn = sh.slot[(m + 1) % 3];
+    return __ballot_sync(0xffffffffu, lane < C && Mn[lane < C ? lane : 0].prev_Zhi > 0.0f) == 0u;
+}
+
+// Control warp, once the exchange that carries item m's alpha and residual shares is done: the
+// item's results. They are written by the owner of its draw (the CTA whose slice holds u*Z),
+// else by CTA 0. Returns the draw's state in every lane.
+__device__ __forceinline__ FinState finalize_head(CtaShared &sh, const RowsParams &P, int m, int C, int crank,
+                                                  int lane) {
+    const Decision &D = sh.dec[m & 1];
+    const Msg *Mi = sh.slot[m % 3];
+    const Msg *Mn = sh.slot[(m + 1) % 3];
+    FinState f;
+    f.kind = D.kind;
+    f.fb = 0;
+    f.owner = -1;
+    f.local = f.Ztot = {0.0f, 0.0f};
+    // one lane per CTA record, in CTA order
+    const bool on = lane < C;
+    const Msg &mi = Mi[on ? lane : 0], &mn = Mn[on ? lane : 0];
+    const float alpha_sum = warp_sum(on ? mn.prev_alpha : 0.0f);
+    const F2 Zres = shfl_f2(warp_sum_f2(on ? F2{mn.prev_Zhi, mn.prev_Zlo} : F2{0.0f, 0.0f}), 0);
+    if (f.kind == SAMPLE_RESIDUAL && !(Zres.hi > 0.0f)) {
+        f.kind = SAMPLE_P;  // zero residual mass: draw from p and say so
+        f.fb = 1;
+    }
+    if (f.kind != SAMPLE_NONE) {
+        // the first CTA whose running total exceeds u*Z (else the last with mass: rounding put
+        // u*Z at the very end)
+        const F2 mc = on ? cta_mass(mi, mn, f.kind, D.B_t) : F2{0.0f, 0.0f};
+        const F2 incl = warp_scan_f2(mc, lane);
+        f.Ztot = shfl_f2(incl, kWarp - 1);
+        const F2 t = f2_mul(f.Ztot, D.u_s);
+        const unsigned hit = __ballot_sync(0xffffffffu, on && mc.hi > 0.0f && f2_gt(incl, t));
+        const unsigned posm = __ballot_sync(0xffffffffu, on && mc.hi > 0.0f);
+        f.owner = hit ? __ffs(hit) - 1 : (posm ? 31 - __clz(static_cast<int>(posm)) : -1);
+        if (f.owner >= 0) {
+            const F2 prefix = shfl_f2(f2_sub(incl, mc), f.owner);
+            f.local = f2_sub(t, prefix);
+        }
+    }
+    if (lane == 0) {
+        const int writer = f.owner >= 0 ? f.owner : 0;
+        if (writer == crank) {
+            const int item = D.item, st = D.status;
+            P.item_status[item] = st;
+            P.item_fb[item] = f.fb;
+            if (D.pair) {
+                const float alpha = D.greedy ? D.alpha_g : alpha_sum;
+                P.item_flag[item] = (st == 0) ? D.accept : 0;
+                P.alpha_ws[D.drow] = (st == 0) ? alpha : 0.0f;
+                if (P.alpha_rows) P.alpha_rows[D.drow] = (st == 0) ? alpha : NAN;
+                if (P.rho_rows) P.rho_rows[D.drow] = (st == 0) ? D.rho : NAN;
+                if (P.resid_rows)
+                    P.resid_rows[D.drow] =
+                        (st == 0 && f.kind == SAMPLE_RESIDUAL && !D.greedy) ? f2_div(Zres, D.S_t).hi : -1.0f;
+            } else {
+                P.item_flag[item] = 0;
+            }
+            if (f.owner < 0) {
+                if (st == 0 && D.greedy && !(D.pair && D.accept)) {
+                    // Rule 1: the correction (or the extra token) is argmax p
+                    P.item_tok[item] = D.argmax_t;
+                    P.item_prob[item] = 1.0f;
                 } else {
-                    P.item_flag[item] = 0;
-                }
-                if (st != 0 || (I.pair && I.accept)) {
                     P.item_tok[item] = -1;
                     P.item_prob[item] = NAN;
-                    P.item_margin[item] = NAN;
-                } else if (greedy) {
-                    // Rule 1: the correction (or the extra token) is argmax p
-                    P.item_tok[item] = I.argmax_t;
-                    P.item_prob[item] = 1.0f;
-                    P.item_margin[item] = NAN;
-                } else if (owner < 0) {
-                    P.item_tok[item] = -1;  // unreachable for a valid row: p always has mass
-                    P.item_prob[item] = NAN;
-                    P.item_margin[item] = NAN;
                 }
+                P.item_margin[item] = NAN;
             }
         }
     }
-    __syncthreads();
+    f.local = shfl_f2(f.local, 0);
+    f.Ztot = shfl_f2(f.Ztot, 0);
+    return f;
+}
 
-    // ---- the draw: the owner CTA finds the group, then the vector, then the element ----
-    if (warp == 0 && I.owner == crank) {
-        const int kind = I.sample_kind;
-        const F2 local = f2_sub(I.target_t, I.owner_prefix);
-        int gsel = -1, last_g = -1;
-        F2 before = {0.0f, 0.0f}, last_before = {0.0f, 0.0f}, run = {0.0f, 0.0f};
-        for (int base = 0; base < groups; base += kWarp) {
-            const int g = base + lane;
-            float m = 0.0f;
-            if (g < groups) {
-                if (kind == SAMPLE_RESIDUAL) {
-                    m = gres[g];
-                } else {
-                    const float sg = gsum[g];
-                    m = (sg > 0.0f) ? sg * pow2i(gref[g] - I.B_t) : 0.0f;
-                }
-            }
-            const F2 incl = f2_add(run, warp_scan_f2({m, 0.0f}, lane));
-            const unsigned hit = __ballot_sync(0xffffffffu, g < groups && m > 0.0f && f2_gt(incl, local));
-            const unsigned posm = __ballot_sync(0xffffffffu, g < groups && m > 0.0f);
-            if (hit) {
-                const int l = __ffs(hit) - 1;
-                gsel = base + l;
-                before = shfl_f2(f2_sub(incl, {m, 0.0f}), l);
-                break;
-            }
-            if (posm) {
-                const int l = 31 - __clz(static_cast<int>(posm));
-                last_g = base + l;
-                last_before = shfl_f2(f2_sub(incl, {m, 0.0f}), l);
-            }
-            run = shfl_f2(incl, kWarp - 1);
-        }
-        const bool clamped = gsel < 0;  // rounding put u*Z past the last group with mass
-        if (clamped) {
-            gsel = last_g;
-            before = last_before;
-        }
-        int tok = -1;
-        float wsel = 0.0f, margin = 0.0f, unit = 1.0f;
-        if (gsel >= 0) {
-            const float bg = (kind == SAMPLE_RESIDUAL) ? 0.0f : gref[gsel];
-            // group units: residual weights are already in cluster units; P weights are in units
-            // of 2^b_g, which is 2^(b_g - B_t) cluster units (an exact power of two)
-            unit = (kind == SAMPLE_RESIDUAL) ? 1.0f : pow2i(bg - I.B_t);
-            const F2 rem = f2_sub(local, before);
-            const float lt = (rem.hi + rem.lo) * ((kind == SAMPLE_RESIDUAL) ? 1.0f : pow2i(I.B_t - bg));
-            float run2 = 0.0f, last_w = 0.0f;
-            int last_tok = -1;
-            for (int q = 0; q < kVecPerLane; ++q) {
-                const int vi = gsel * kGroupVecs + q * kWarp + lane;
-                float w[E];
-                vec_weights<DT>(kind, buf_t, buf_d, vi, nvec, I, bg, w);
-                float ls = 0.0f;
-#pragma unroll
-                for (int e = 0; e < E; ++e) ls += w[e];
-                float incl = ls;
-#pragma unroll
-                for (int o = 1; o < kWarp; o <<= 1) {
-                    const float n = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += n;
-                }
-                incl += run2;
-                // this lane's element that takes the target, if any; and its last with mass
-                int found = -1, lastp = -1;
-                float fprev = 0.0f, c = incl - ls, wf = 0.0f, wl = 0.0f;
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    if (w[e] > 0.0f) {
-                        if (found < 0 && !clamped && c + w[e] > lt) {
-                            found = e;
-                            fprev = c;
-                            wf = w[e];
-                        }
-                        lastp = e;
-                        wl = w[e];
-                    }
-                    c += w[e];
-                }
-                const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
-                const unsigned posm = __ballot_sync(0xffffffffu, lastp >= 0);
-                if (hit) {
-                    const int l = __ffs(hit) - 1;
-                    const int e_sel = __shfl_sync(0xffffffffu, found, l);
-                    const float c0 = __shfl_sync(0xffffffffu, fprev, l);
-                    wsel = __shfl_sync(0xffffffffu, wf, l);
-                    tok = (I.lo + gsel * kGroupVecs + q * kWarp + l) * E + e_sel;
-                    margin = fminf(lt - c0, c0 + wsel - lt) * unit * rcp_approx(I.Ztot.hi);
-                    break;
-                }
-                if (posm) {
-                    const int l = 31 - __clz(static_cast<int>(posm));
-                    last_tok = (I.lo + gsel * kGroupVecs + q * kWarp + l) * E + __shfl_sync(0xffffffffu, lastp, l);
-                    last_w = __shfl_sync(0xffffffffu, wl, l);
-                }
-                run2 = __shfl_sync(0xffffffffu, incl, kWarp - 1);
-            }
-            if (tok < 0) {  // rounding: the last element with mass
-                tok = last_tok;
-                wsel = last_w;
-                margin = 0.0f;
+// Control warp of the owner CTA: the chunk that holds u*Z (an inclusive scan over the slice's
+// chunk masses, in vocabulary order), fetched with a small bulk copy; `complete_draw` finds the
+// token once it has landed.
+__device__ __forceinline__ void draw_chunk(CtaShared &sh, const RowsParams &P, int m, const FinState &f, int lane,
+                                           int nch, int lo, int nvec) {
+    const int par = m & 1, pb = m % 3;
+    const Decision &D = sh.dec[par];
+    int ksel = -1, klast = -1;
+    F2 before = {0.0f, 0.0f}, last_before = {0.0f, 0.0f}, run = {0.0f, 0.0f};
+#pragma unroll 1
+    for (int base = 0; base < nch; base += kWarp) {
+        const int k = base + lane;
+        float mk = 0.0f;
+        if (k < nch) {
+            if (f.kind == SAMPLE_RESIDUAL) {
+                mk = sh.rm[par][k];
+            } else if (f.fb) {
+                // a rejecting pair: sum the chunk's (vector, thread) partials of p; lanes start at
+                // different words so that they read different banks
+                const float *src = sh.tpm + (k / kWarps) * kThreads + (k % kWarps) * kWarp;
+                float a = 0.0f;
+#pragma unroll 4
+                for (int j = 0; j < kWarp; ++j) a += src[(j + lane) & (kWarp - 1)];
+                mk = a;
+            } else {
+                const float pmk = sh.pm[pb][k];
+                mk = pmk > 0.0f ? pmk * pow2i(sh.pref[pb][k] - D.B_t) : 0.0f;
             }
         }
-        if (lane == 0) {
+        const bool pos = k < nch && mk > 0.0f;
+        const F2 incl = f2_add(run, warp_scan_f2({mk, 0.0f}, lane));
+        const unsigned hit = __ballot_sync(0xffffffffu, pos && f2_gt(incl, f.local));
+        const unsigned posm = __ballot_sync(0xffffffffu, pos);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            ksel = base + l;
+            before = shfl_f2(f2_sub(incl, {mk, 0.0f}), l);
+            break;
+        }
+        if (posm) {
+            const int l = 31 - __clz(static_cast<int>(posm));
+            klast = base + l;
+            last_before = shfl_f2(f2_sub(incl, {mk, 0.0f}), l);
+        }
+        run = shfl_f2(incl, kWarp - 1);
+    }
+    const int clamped = ksel < 0;  // rounding put u*Z past the last chunk with mass
+    if (clamped) {
+        ksel = klast;
+        before = last_before;
+    }
+    if (lane == 0) {
+        const int start = (ksel >= 0) ? (ksel / kWarps) * kThreads + (ksel % kWarps) * kWarp : 0;
+        const int count = (ksel >= 0) ? max(0, min(kWarp, nvec - start)) : 0;
+        float bg = 0.0f, unit = 1.0f, lt = 0.0f;
+        const F2 rem = f2_sub(f.local, before);
+        if (f.kind == SAMPLE_RESIDUAL || f.fb) {
+            bg = D.B_t;
+            lt = rem.hi + rem.lo;
+        } else if (ksel >= 0) {
+            // p weights of the chunk are in units of 2^bg: 2^(bg - B_t) cluster units
+            bg = sh.pref[pb][ksel];
+            unit = pow2i(bg - D.B_t);
+            lt = (rem.hi + rem.lo) * pow2i(D.B_t - bg);
+        }
+        sh.draw_pending = 1;
+        sh.draw_item = D.item;
+        sh.draw_par = par;
+        sh.draw_kind = f.kind;
+        sh.draw_chunk = start;
+        sh.draw_count = count;
+        sh.draw_clamped = clamped;
+        sh.draw_lt = lt;
+        sh.draw_unit = unit;
+        sh.draw_bg = bg;
+        sh.draw_invZ = rcp_approx(f.Ztot.hi);
+        if (count > 0) {
+            const size_t row_bytes = static_cast<size_t>(P.nvec_row) * 16;
+            const size_t off = static_cast<size_t>(lo + start) * 16;
+            const uint32_t bytes = static_cast<uint32_t>(count) * 16;
+            const bool two = f.kind == SAMPLE_RESIDUAL;
+            mbar_arrive_expect_tx(&sh.draw_bar, two ? 2 * bytes : bytes);
+            bulk_g2s(sh.draw_buf[0],
+                     static_cast<const unsigned char *>(P.target) + static_cast<size_t>(D.item) * row_bytes + off,
+                     bytes, &sh.draw_bar, policy_evict_first());
+            if (two)
+                bulk_g2s(sh.draw_buf[1],
+                         static_cast<const unsigned char *>(P.draft) + static_cast<size_t>(D.drow) * row_bytes + off,
+                         bytes, &sh.draw_bar, policy_evict_first());
+        }
+    }
+    __syncwarp();
+}
+
+// Control warp of the owner CTA: the token of the pending draw within its chunk (one vector per
+// lane).
+template <int DT>
+__device__ __forceinline__ void complete_draw(CtaShared &sh, const RowsParams &P, int lo, int lane) {
+    constexpr int E = Elt<DT>::kPerVec;
+    if (!sh.draw_pending) return;
+    const Decision &D = sh.dec[sh.draw_par];
+    const int kind = sh.draw_kind, count = sh.draw_count, clamped = sh.draw_clamped;
+    bool ok = true;
+    if (count > 0) {
+        ok = mbar_wait_sleep_bounded(&sh.draw_bar, sh.draw_phase, kSuspendNs, kMaxWaitTries);
+        ok = __all_sync(0xffffffffu, ok);
+    }
+    const uint4 wt = lane < count ? sh.draw_buf[0][lane] : kNegInfVec<DT>();
+    const uint4 wd = (lane < count && kind == SAMPLE_RESIDUAL) ? sh.draw_buf[1][lane] : kNegInfVec<DT>();
+    float w[E];
+    draw_weights<DT>(kind, wt, wd, D, sh.draw_bg, w);
+    float ls = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ls += w[e];
+    float incl = ls;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const float x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    const float lt = sh.draw_lt;
+    int found = -1, lastp = -1;
+    float c = incl - ls, fprev = 0.0f, wf = 0.0f, wl = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        if (w[e] > 0.0f) {
+            if (found < 0 && !clamped && c + w[e] > lt) {
+                found = e;
+                fprev = c;
+                wf = w[e];
+            }
+            lastp = e;
+            wl = w[e];
+        }
+        c += w[e];
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
+    const unsigned posm = __ballot_sync(0xffffffffu, lastp >= 0);
+    int tok = -1;
+    float wsel = 0.0f, margin = 0.0f;
+    const int base = lo + sh.draw_chunk;
+    if (hit) {
+        const int l = __ffs(hit) - 1;
+        const float c0 = __shfl_sync(0xffffffffu, fprev, l);
+        wsel = __shfl_sync(0xffffffffu, wf, l);
+        tok = (base + l) * E + __shfl_sync(0xffffffffu, found, l);
+        margin = fminf(lt - c0, c0 + wsel - lt) * sh.draw_unit * sh.draw_invZ;
+    } else if (posm) {  // rounding: the last element with mass
+        const int l = 31 - __clz(static_cast<int>(posm));
+        wsel = __shfl_sync(0xffffffffu, wl, l);
+        tok = (base + l) * E + __shfl_sync(0xffffffffu, lastp, l);
+    }
+    if (lane == 0) {
+        const int item = sh.draw_item;
+        if (ok) {
             P.item_tok[item] = tok;
-            P.item_prob[item] = tok >= 0 ? wsel * unit * rcp_approx(I.Ztot.hi) : NAN;
+            P.item_prob[item] = tok >= 0 ? wsel * sh.draw_unit * sh.draw_invZ : NAN;
             P.item_margin[item] = tok >= 0 ? margin : NAN;
+        } else {
+            P.item_status[item] = D.status | REQ_TIMEOUT;
+            P.item_tok[item] = -1;
+            P.item_prob[item] = NAN;
+            P.item_margin[item] = NAN;
+        }
+        if (count > 0) sh.draw_phase ^= 1u;
+        sh.draw_pending = 0;
+    }
+    __syncwarp();
+}
+
+// Load the slice of one ring slot into registers: thread t takes vectors t, t + 480, ... so that
+// a warp reads 32 contiguous vectors (a chunk); past the slice end, -inf.
+template <int DT, int NVT>
+__device__ __forceinline__ bool load_row(CtaShared &sh, const uint4 *ring, int slice_max, int nvec, long long row,
+                                         int tid, uint4 (&vv)[NVT]) {
+    const int slot = static_cast<int>(row % kRing);
+    const bool ok =
+        mbar_wait_sleep_bounded(&sh.full[slot], static_cast<uint32_t>((row / kRing) & 1), kSuspendNs, kMaxWaitTries);
+    const uint4 *src = ring + static_cast<size_t>(slot) * slice_max;
+#pragma unroll
+    for (int v = 0; v < NVT; ++v) {
+        const int vi = tid + v * kThreads;
+        vv[v] = vi < nvec ? src[vi] : kNegInfVec<DT>();
+    }
+    return ok;
+}
+
+template <int DT, int NVT>
+__global__ void __launch_bounds__(kBlock, 1) spec_rows_kernel(const RowsParams P) {
+    constexpr int E = Elt<DT>::kPerVec;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ CtaShared sh;
+    uint4 *ring = reinterpret_cast<uint4 *>(smem_raw);
+
+    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+    griddep_launch_dependents();  // the selection kernel may be scheduled behind this grid
+    const int C = static_cast<int>(cluster_nctarank());
+    const int crank = static_cast<int>(cluster_ctarank());
+    const int cid = static_cast<int>(cluster_id_x());
+    const int lo = static_cast<int>((static_cast<int64_t>(P.nvec_row) * crank) / C);
+    const int nvec = static_cast<int>((static_cast<int64_t>(P.nvec_row) * (crank + 1)) / C) - lo;
+    const int slice_max = P.slice_vecs_max;
+    const int nch = NVT * kWarps;
+    const int ncl = P.nclusters;
+    const int nitems = cid < P.total_rows ? (P.total_rows - 1 - cid) / ncl + 1 : 0;
+
+    if (tid == 0) {
+        for (int k = 0; k < kRing; ++k) mbar_init(&sh.full[k], 1);
+        for (int k = 0; k < 3; ++k) mbar_init(&sh.msg_bar[k], 1);
+        mbar_init(&sh.draw_bar, 1);
+        fence_mbar_init();
+        sh.timed_out = 0;
+        sh.x_stamp = 0;
+        sh.draw_pending = 0;
+        sh.draw_phase = 0;
+        sh.dec[0].kind = sh.dec[1].kind = SAMPLE_NONE;
+        sh.mine.prev_alpha = sh.mine.prev_Zhi = sh.mine.prev_Zlo = 0.0f;
+        sh.mine.pad = 0;
+    }
+    cluster_sync_all();  // every CTA of the cluster runs, its barriers ready, before any remote access
+
+    if (warp < kWarps) {
+        // ================= data warps: registers, pass 1, pass 2 =================
+        long long R = 0;  // ring row of the item's target row
+        int nb = 0, nbatch = 0;
+        for (int n = 0; n < nitems; ++n) {
+            if (n == nb + nbatch) {
+                nb = n;
+                nbatch = min(kMaxItems, nitems - n);
+                bar_sync(BAR_BATCH, kBlock);  // the control warp has the batch's descriptors
+            }
+            const Desc &d = sh.desc[n - nb];
+            const int nr = desc_rows(d);
+            uint4 vt[NVT];
+            bool ok = true;
+            if (nr >= 1) ok = load_row<DT, NVT>(sh, ring, slice_max, nvec, R, tid, vt);
+            bar_arrive(BAR_FREE, kBlock);  // the target row's slot may be refilled
+            if (nr == 1) row_stats<DT, NVT, true>(RegRow<NVT>{vt}, sh, 0, n % 3, d, lo, warp, lane, tid);
+            const SmemRow<DT> rd = {ring + static_cast<size_t>((R + 1) % kRing) * slice_max, tid, nvec};
+            if (nr == 2) {
+                row_stats<DT, NVT, false>(RegRow<NVT>{vt}, sh, 0, n % 3, d, lo, warp, lane, tid);
+                ok &= mbar_wait_sleep_bounded(&sh.full[(R + 1) % kRing], static_cast<uint32_t>(((R + 1) / kRing) & 1),
+                                              kSuspendNs, kMaxWaitTries);
+                row_stats<DT, NVT, false>(rd, sh, 1, n % 3, d, lo, warp, lane, tid);
+                // the logits at the draft token, from the thread that holds them
+                const int x = d.x;
+                if (x >= 0 && x < P.V) {
+                    const int xv = x / E - lo;
+                    if (xv >= 0 && xv < nvec && (xv % kThreads) == tid) {
+                        const int vx = xv / kThreads, e = x % E;
+#pragma unroll
+                        for (int v = 0; v < NVT; ++v)
+                            if (v == vx) sh.yx[0] = vec_elem<DT>(vt[v], e);
+                        sh.yx[1] = vec_elem<DT>(rd.src[xv], e);
+                        sh.x_stamp = n + 1;
+                    }
+                }
+            }
+            if (!ok) sh.timed_out = 1;
+            bar_arrive(BAR_STATS, kBlock);
+            bar_sync(BAR_DECIDED, kBlock);
+            if (nr == 2) {
+                pass2<DT, NVT>(vt, rd, sh, sh.dec[n & 1], n & 1, warp, lane, tid);
+            } else if (lane == 0) {
+                sh.wal[warp] = 0.0f;
+            }
+            bar_arrive(BAR_PASS2, kBlock);  // the draft row's slot may be refilled
+            R += nr;
+        }
+    } else {
+        // ================= control warp: copies, exchange, decisions, draws =================
+        long long issued = 0, released = 0;  // rows copied; rows whose slots are free again (in order)
+        int cur_item = 0, cur_row = 0, nb = 0, nbatch = 0;
+        if (lane < kRing && lane < nitems) {
+            // the first target rows' slices into L2 while the descriptors load
+            const size_t row_bytes = static_cast<size_t>(P.nvec_row) * 16;
+            bulk_prefetch_l2(static_cast<const unsigned char *>(P.target) +
+                                 static_cast<size_t>(cid + lane * ncl) * row_bytes + static_cast<size_t>(lo) * 16,
+                             static_cast<uint32_t>(nvec) * 16);
+        }
+        for (int n = 0; n < nitems; ++n) {
+            if (n == nb + nbatch) {  // the next batch of descriptors (the ring is empty here)
+                nb = n;
+                nbatch = min(kMaxItems, nitems - n);
+                load_batch(sh, P, cid, nb, nbatch, lane);
+                if (lane == 0) {
+                    cur_item = 0;
+                    cur_row = 0;
+                    produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, issued, released + kRing, cur_item,
+                                 cur_row);
+                }
+                __syncwarp();
+                bar_arrive(BAR_BATCH, kBlock);
+            }
+            const Desc &d = sh.desc[n - nb];
+            const int nr = desc_rows(d);
+            bar_sync(BAR_FREE, kBlock);
+            released += (nr >= 1);
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, issued, released + kRing, cur_item, cur_row);
+            }
+            bar_sync(BAR_STATS, kBlock);
+            build_message(sh, d.greedy, nr, n, nch, lane);
+            __syncwarp();
+            push_record(&sh.mine, sh.slot[n % 3], &sh.msg_bar[n % 3], crank, C, lane);
+            if (lane == 0) mbar_arrive_expect_tx(&sh.msg_bar[n % 3], static_cast<uint32_t>(C * kMsgBytes));
+            complete_draw<DT>(sh, P, lo, lane);  // the draw of item n - 2, fetched one item ago
+            if (!mbar_wait_sleep_bounded(&sh.msg_bar[n % 3], static_cast<uint32_t>((n / 3) & 1), kSuspendNs,
+                                         kMaxWaitTries))
+                sh.timed_out = 1;
+            __syncwarp();
+            decide_item(sh, d, nr, n, C, P, lane);
+            __syncwarp();
+            // the previous item's results wait until pass 2 runs, unless its residual had no mass:
+            // that draw uses the per-thread sums of p, which the next pass 2 overwrites
+            const bool early = n > 0 && zero_residual(sh, n - 1, C, lane);
+            if (early) {
+                const FinState f = finalize_head(sh, P, n - 1, C, crank, lane);
+                if (f.owner == crank) draw_chunk(sh, P, n - 1, f, lane, nch, lo, nvec);
+            }
+            bar_arrive(BAR_DECIDED, kBlock);
+            if (n > 0 && !early) {
+                const FinState f = finalize_head(sh, P, n - 1, C, crank, lane);
+                if (f.owner == crank) draw_chunk(sh, P, n - 1, f, lane, nch, lo, nvec);
+            }
+            bar_sync(BAR_PASS2, kBlock);
+            stash_totals(sh, n, nch, lane);
+            if (nr == 2) {
+                released += 1;
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, issued, released + kRing, cur_item,
+                                 cur_row);
+                }
+            }
+        }
+        if (nitems > 0) {
+            // the last item's totals travel in one more exchange
+            build_message(sh, 0, 0, nitems, nch, lane);
+            __syncwarp();
+            push_record(&sh.mine, sh.slot[nitems % 3], &sh.msg_bar[nitems % 3], crank, C, lane);
+            if (lane == 0) mbar_arrive_expect_tx(&sh.msg_bar[nitems % 3], static_cast<uint32_t>(C * kMsgBytes));
+            complete_draw<DT>(sh, P, lo, lane);
+            if (!mbar_wait_sleep_bounded(&sh.msg_bar[nitems % 3], static_cast<uint32_t>((nitems / 3) & 1),
+                                         kSuspendNs, kMaxWaitTries))
+                sh.timed_out = 1;
+            __syncwarp();
+            const FinState f = finalize_head(sh, P, nitems - 1, C, crank, lane);
+            if (f.owner == crank) draw_chunk(sh, P, nitems - 1, f, lane, nch, lo, nvec);
+            complete_draw<DT>(sh, P, lo, lane);
+        }
+        if (lane == 0 && sh.timed_out) {
+            // a copy did not land in time: wait (bounded) once more so that none is left in flight
+            for (long long r = max(0LL, issued - kRing); r < issued; ++r)
+                mbar_wait_sleep_bounded(&sh.full[r % kRing], static_cast<uint32_t>((r / kRing) & 1), kSuspendNs,
+                                        kMaxWaitTries);
         }
     }
-    if (timed_out) {
-        // a copy did not land in time: wait (bounded) once more so none is left in flight
-        for (int r = 0; r < nrows; ++r)
-            for (int k = 0; k < nchunk; ++k) mbar_wait_sleep_bounded(&bars[r][k], 0, kSuspendNs, kMaxWaitTries);
-    }
+    __syncwarp();
+    cluster_sync_all();  // no CTA leaves while another may still write into its shared memory
 }
 
 }  // namespace spec

@@ -5,7 +5,7 @@
 // conventions are documented in include/spec_verify.h.
 //
 // Two kernels per call: the per-position kernel (spec_rows.cuh, spec_rows_kernel.cuh) verifies
-// every (request, position) with one thread-block cluster each; the selection kernel below walks
+// every (request, position) on a persistent grid of thread-block clusters; the selection kernel walks
 // each request's accept flags left to right (a warp ballot), picks the candidate of the first
 // rejection or the bonus, applies stop-token / max_new truncation and reduces alpha for the
 // gamma controller.
@@ -15,6 +15,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <mutex>
 
 #include "spec_device.cuh"
@@ -178,60 +179,74 @@ static WsLayout ws_layout(int32_t B, int32_t total_rows) {
     return L;
 }
 
-struct LaunchShape {
-    int C = 0;
-    int slice_vecs_max = 0;
-    int groups_max = 0;
-    size_t smem = 0;
-};
-
-static size_t rows_smem_bytes(int slice_vecs_max, int groups_max) {
-    return static_cast<size_t>(2) * slice_vecs_max * 16 + static_cast<size_t>(5) * groups_max * 4;
-}
+using RowsKernel = void (*)(const RowsParams);
 
 template <int DT>
-static cudaError_t pick_shape(int nvec_row, LaunchShape &out) {
+static RowsKernel rows_kernel_for(int nvt) {
+    switch (nvt) {
+        case 2: return spec_rows_kernel<DT, 2>;
+        case 4: return spec_rows_kernel<DT, 4>;
+        default: return spec_rows_kernel<DT, kMaxNvt>;
+    }
+}
+
+// One cluster size of the per-position kernel: its slices, registers per thread and the number
+// of clusters that can be resident at once (occupancy API; one CTA per SM).
+struct ClusterOption {
+    int C = 0;
+    int nvt = 0;
+    int slice_vecs_max = 0;
+    size_t smem = 0;
+    int active = 0;
+};
+
+struct ShapeTable {
+    int dev = -1, nvec_row = -1;
+    ClusterOption opt[5];  // C = 1, 2, 4, 8, 16
+};
+
+template <int DT>
+static cudaError_t shape_table(int nvec_row, ShapeTable &out) {
     static std::mutex mu;
-    static int cached_dev = -1, cached_nvec = -1;
-    static LaunchShape cached;
-    static size_t smem_set = 0;
+    static ShapeTable cached;
+    static bool attrs_set[4] = {false, false, false, false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    if (dev == cached_dev && nvec_row == cached_nvec) {
+    if (cached.dev == dev && cached.nvec_row == nvec_row) {
         out = cached;
         return cudaSuccess;
     }
     int max_optin = 0;
     e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    static bool nonportable_set = false;
-    if (!nonportable_set) {
-        e = cudaFuncSetAttribute(spec_rows_kernel<DT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    ShapeTable t;
+    t.dev = dev;
+    t.nvec_row = nvec_row;
+    for (int ci = 0; ci < 5; ++ci) {
+        const int C = 1 << ci;
+        ClusterOption &o = t.opt[ci];
+        if (C > nvec_row) continue;
+        const int slice = (nvec_row + C - 1) / C;
+        // vectors per data thread: 2, 4 or 9 (the largest slice that fits the registers)
+        const int nvt = (slice <= 2 * kThreads) ? 2 : (slice <= 4 * kThreads) ? 4 : kMaxNvt;
+        if (nvt * kThreads < slice) continue;  // a slice must fit the registers of one CTA
+        const RowsKernel k = rows_kernel_for<DT>(nvt);
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, k);
         if (e != cudaSuccess) return e;
-        nonportable_set = true;
-    }
-    // Cluster size: every size whose slices fit is scored by the logit bytes that the resident
-    // clusters hold at once (clusters co-resident x C x slice bytes), from the occupancy API.
-    // Large clusters strand SMs: a cluster lives in one GPC, so at sixteen CTAs only about three
-    // quarters of the SMs can be busy. Ties go to the smaller cluster (less work per CTA).
-    const int smem_cap = max_optin - 4096;
-    if (smem_set < static_cast<size_t>(smem_cap)) {
-        e = cudaFuncSetAttribute(spec_rows_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_cap);
-        if (e != cudaSuccess) return e;
-        smem_set = static_cast<size_t>(smem_cap);
-    }
-    LaunchShape best;
-    double best_score = 0.0;
-    for (int C = 1; C <= kMaxCluster; C *= 2) {
-        if (C > nvec_row) break;
-        LaunchShape s;
-        s.C = C;
-        s.slice_vecs_max = (nvec_row + C - 1) / C;
-        s.groups_max = (s.slice_vecs_max + kGroupVecs - 1) / kGroupVecs;
-        s.smem = rows_smem_bytes(s.slice_vecs_max, s.groups_max);
-        if (s.smem > static_cast<size_t>(smem_cap)) continue;
+        const size_t smem = static_cast<size_t>(kRing) * slice * 16;
+        if (smem + fa.sharedSizeBytes > static_cast<size_t>(max_optin)) continue;
+        const int ki = (nvt == 2) ? 0 : (nvt == 4) ? 1 : 2;
+        if (!attrs_set[ki]) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     max_optin - static_cast<int>(fa.sharedSizeBytes));
+            if (e != cudaSuccess) return e;
+            attrs_set[ki] = true;
+        }
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -239,51 +254,62 @@ static cudaError_t pick_shape(int nvec_row, LaunchShape &out) {
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(C * 16, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = s.smem;
+        cfg.blockDim = dim3(kBlock, 1, 1);
+        cfg.dynamicSmemBytes = smem;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        int nclusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&nclusters, spec_rows_kernel<DT>, &cfg) != cudaSuccess) {
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, k, &cfg) != cudaSuccess) {
             cudaGetLastError();
             continue;
         }
-        const double score = static_cast<double>(nclusters) * C * s.slice_vecs_max;
-        if (nclusters > 0 && score > best_score * 1.001) {
-            best_score = score;
-            best = s;
-        }
+        o.C = C;
+        o.nvt = nvt;
+        o.slice_vecs_max = slice;
+        o.smem = smem;
+        o.active = active;
     }
-    if (best.C > 0) {
-        cached_dev = dev;
-        cached_nvec = nvec_row;
-        cached = best;
-        out = best;
-        return cudaSuccess;
-    }
-    return cudaErrorInvalidConfiguration;
+    cached = t;
+    out = t;
+    return cudaSuccess;
 }
 
+// The persistent grid: the cluster size that keeps the most SMs busy on this many target rows
+// (a cluster lives in one GPC, so large clusters strand SMs; too few rows leave clusters idle).
+// Ties go to the smaller cluster (fewer barriers per logit).
 template <int DT>
 static spec_status launch_rows(const RowsParams &P, cudaStream_t stream) {
-    LaunchShape s;
-    if (pick_shape<DT>(P.nvec_row, s) != cudaSuccess) return SPEC_ERR_UNSUPPORTED;
+    ShapeTable t;
+    if (shape_table<DT>(P.nvec_row, t) != cudaSuccess) return SPEC_ERR_UNSUPPORTED;
+    int best = -1;
+    long long best_score = 0;
+    for (int ci = 0; ci < 5; ++ci) {
+        const ClusterOption &o = t.opt[ci];
+        if (o.C == 0 || o.active <= 0) continue;
+        const long long score = static_cast<long long>(std::min(o.active, P.total_rows)) * o.C;
+        if (score > best_score) {
+            best_score = score;
+            best = ci;
+        }
+    }
+    if (best < 0) return SPEC_ERR_UNSUPPORTED;
+    const ClusterOption &o = t.opt[best];
     RowsParams Q = P;
-    Q.slice_vecs_max = s.slice_vecs_max;
-    Q.groups_max = s.groups_max;
+    Q.slice_vecs_max = o.slice_vecs_max;
+    Q.nclusters = std::min(o.active, P.total_rows);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = s.C;
+    attr[0].val.clusterDim.x = o.C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(P.total_rows) * s.C, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = s.smem;
+    cfg.gridDim = dim3(static_cast<unsigned>(Q.nclusters * o.C), 1, 1);
+    cfg.blockDim = dim3(kBlock, 1, 1);
+    cfg.dynamicSmemBytes = o.smem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, spec_rows_kernel<DT>, Q) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, rows_kernel_for<DT>(o.nvt), Q) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
 
