@@ -178,6 +178,18 @@ __device__ __forceinline__ F2 shfl_f2(F2 v, int src) {
     return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
 }
 
+// log2(2^B * S) for S >= 1 a float pair and B integral, as an integral part (exact) and a
+// fraction in [0, 1): the exponent of S.hi is split off exactly, the logarithm of its mantissa
+// in [1, 2) is taken on the special-function unit (absolute error about 2^-22), and S.lo enters
+// to first order. The error does not grow with the size of S.
+__device__ __forceinline__ float2 log2_split(F2 S, float B) {
+    const int bits = __float_as_int(S.hi);
+    const int ex = ((bits >> 23) & 0xff) - 127;
+    const float m = __int_as_float((bits & 0x007fffff) | 0x3f800000);
+    const float frac = __log2f(m) + S.lo * rcp_approx(S.hi) * 1.44269504f;
+    return make_float2(B + static_cast<float>(ex), frac);
+}
+
 __device__ __forceinline__ F2 f2_scale(F2 a, float k) {
     const float m = pow2i(k);
     return {a.hi * m, a.lo * m};

@@ -42,8 +42,9 @@
 
 namespace spec {
 
-// 15 data warps and one control warp: 16 warps, four per SM sub-partition, so that every thread
-// may hold 128 registers (a 17th warp would put five warps on one sub-partition's register file)
+// 15 data warps and one control warp (512 threads, 64 registers each), two CTAs per SM: each SM
+// works on two items of two clusters at once, so that one CTA's exchange and decision latency
+// hides behind the other's exponentials
 constexpr int kWarps = 15;                   // data warps
 constexpr int kThreads = kWarps * kWarp;     // data threads
 constexpr int kBlock = kThreads + kWarp;     // plus the control warp
@@ -51,9 +52,9 @@ constexpr int kBlock = kThreads + kWarp;     // plus the control warp
 enum : int { BAR_FREE = 1, BAR_STATS = 2, BAR_DECIDED = 3, BAR_PASS2 = 4, BAR_BATCH = 5 };
 constexpr int kChunkVecs = kWarp;   // a chunk: 32 contiguous vectors, one per lane of a warp
 constexpr int kRing = 3;            // row slots per CTA
-constexpr int kMaxItems = 64;       // item descriptors held at once
+constexpr int kMaxItems = 32;       // item descriptors held at once
 constexpr int kMaxCluster = 16;
-constexpr int kMaxNvt = 9;          // 16-byte vectors per thread per row
+constexpr int kMaxNvt = 5;          // 16-byte vectors per thread per row
 constexpr int kMaxChunks = kMaxNvt * kWarps;
 constexpr uint32_t kSuspendNs = 1u << 20;  // one suspended wait: at most ~1 ms
 constexpr int kMaxWaitTries = 2048;        // ~2 s in all: a copy never takes this long
@@ -121,7 +122,8 @@ static_assert(kMsgBytes == 80, "a message is five 16-byte vectors");
 // The decision of an item, kept until its draw is finished (one item later).
 struct Decision {
     int32_t item, drow, pair, greedy, status, accept, kind, valid;
-    float B_t, B_d, s_hi, s_lo, rho, inv_St, c_t, c_d;
+    float B_t, B_d, s_hi, s_lo, rho, inv_St;
+    float c_t, c_d, c_tf, c_df;  // log2 of each row's normaliser: integral part, fraction
     F2 S_t, S_d, lam, u_s;
     int32_t argmax_t;
     float alpha_g;  // greedy rule: alpha of the two point masses

@@ -13,12 +13,11 @@ struct CtaShared {
     Msg slot[3][kMaxCluster];             // exchange slots, written by every CTA of the cluster
     Msg mine;
     Desc desc[kMaxItems];
-    WarpStat ws[2][16];                   // per-warp row statistics of the current item
+    WarpStat ws[2][kWarp];                // per-warp row statistics of the current item
     float wal[kWarps];                    // per-warp alpha partials
     float pm[3][kMaxChunks];              // target-row chunk sums (units 2^pref), by item number % 3
     float pref[3][kMaxChunks];            // their integral reference exponents
     float rm[2][kMaxChunks];              // residual chunk sums (units 2^B_t), by item parity
-    float tpm[kMaxNvt * kThreads];        // rejecting pair: per (vector, thread) sums of p (units 2^B_t)
     Decision dec[2];                      // by item parity
     uint4 draw_buf[2][kChunkVecs];        // target / draft chunk of the pending draw
     float yx[2];
@@ -137,6 +136,10 @@ __device__ __forceinline__ void produce_rows(CtaShared &sh, uint4 *ring, const R
     }
 }
 
+// Whether warp `warp` has any vector v of the slice (its 32 vectors start at v * 480 + 32 warp):
+// warps past the slice end skip the vector altogether (a warp-uniform branch).
+__device__ __forceinline__ bool warp_has(int v, int warp, int nvec) { return v * kThreads + warp * kWarp < nvec; }
+
 // A row of the item as pass 1 and pass 2 see it: vector v of thread t is vector t + 480 v of the
 // slice (a warp covers 32 contiguous vectors, a chunk). The target row is held in registers; the
 // draft row stays in its ring slot (so that only one row occupies registers).
@@ -155,38 +158,106 @@ struct SmemRow {
     }
 };
 
-// Pass-1 statistics of one row. Each thread takes an integral reference b = floor(max * s) over
-// its own vectors (a first sweep, max only), then sums 2^(y*s - b) with every exponential
-// independent of the others (a second sweep, two accumulators); a warp combines its threads by
-// exact powers of two (one max and one sum across the lanes). For a row that a draw from p may
-// need (CHUNKS), also the per-chunk sums (chunk (v, warp), units 2^B_w with B_w the warp's
-// reference).
+// The sums of 2^(y*s - b) over a thread's vectors of one row, b an integral reference.
+// Fast path: b comes from the thread's first vector alone, so no exponential waits on a running
+// max; a larger value later in the row only makes its term larger than 1. Should the first vector
+// be all -inf or the sum exceed 2^64 (so that every term later taken against the row's reference
+// stays far inside float range; a +inf or NaN logit lands here too), the exact path takes b from
+// the thread's max over all its vectors (a first sweep) and sums again.
+// CHUNKS: also the per-vector sums, at the same reference.
+// The exact path of the sums: b from the thread's max over all its vectors, then the sums.
+template <int DT, int NVT, bool CHUNKS, class Row>
+__device__ __forceinline__ float exact_sums(const Row &row, float s_hi, float2 shi2, float2 slo2, int warp, int nvec,
+                                            float &b, float (&sv)[CHUNKS ? NVT : 1]) {
+    constexpr int H = Elt<DT>::kPerVec / 2;
+    float m = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < NVT; ++v)
+        if (warp_has(v, warp, nvec)) m = fmaxf(m, Elt<DT>::vmax(row(v)));
+    // an all -inf thread gets reference 0: its sum is 0 (or NaN if a NaN hides in it)
+    b = (m == -INFINITY) ? 0.0f : floorf(m * s_hi);
+    const float2 nb2 = f2splat(-b);
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int v = 0; v < NVT; ++v) {
+        if (CHUNKS) sv[CHUNKS ? v : 0] = 0.0f;
+        if (!warp_has(v, warp, nvec)) continue;
+        const uint4 w = row(v);
+        float2 a = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int h = 0; h < H; ++h) a = __fadd2_rn(a, ex2x2(exp_arg2(Elt<DT>::unpack_one(w, h), shi2, slo2, nb2)));
+        if (CHUNKS) sv[CHUNKS ? v : 0] = a.x + a.y;
+        acc = __fadd2_rn(acc, a);
+    }
+    return acc.x + acc.y;
+}
+
+template <int DT, int NVT, bool CHUNKS, class Row>
+__device__ __forceinline__ float sweep_sums(const Row &row, float s_hi, float2 shi2, float2 slo2, int warp, int nvec,
+                                            float &b, float (&sv)[CHUNKS ? NVT : 1]) {
+    constexpr int H = Elt<DT>::kPerVec / 2;
+    // an all -inf first vector gives b = -inf, hence inf or NaN sums: the exact path below
+    b = floorf((warp_has(0, warp, nvec) ? Elt<DT>::vmax(row(0)) : -INFINITY) * s_hi);
+    float s;
+    {
+        const float2 nb2 = f2splat(-b);
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int v = 0; v < NVT; ++v) {
+            if (CHUNKS) sv[CHUNKS ? v : 0] = 0.0f;
+            if (!warp_has(v, warp, nvec)) continue;
+            const uint4 w = row(v);
+            float2 a = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int h = 0; h < H; ++h) a = __fadd2_rn(a, ex2x2(exp_arg2(Elt<DT>::unpack_one(w, h), shi2, slo2, nb2)));
+            if (CHUNKS) sv[CHUNKS ? v : 0] = a.x + a.y;
+            acc = __fadd2_rn(acc, a);
+        }
+        s = acc.x + acc.y;
+    }
+    // the exact path, for the whole warp when any of its threads needs it (a warp-uniform branch:
+    // a per-thread one costs the common path twice its time on this compiler)
+    if (__any_sync(0xffffffffu, !(s <= 0x1p64f))) s = exact_sums<DT, NVT, CHUNKS>(row, s_hi, shi2, slo2, warp, nvec, b, sv);
+    return s;
+}
+
+// Pass-1 statistics of one row: each thread's sum at its integral reference (sweep_sums), then
+// a warp combines its threads by exact powers of two (one max and one sum across the lanes). For
+// a row that a draw from p may need (CHUNKS), also the per-chunk sums (chunk (v, warp), units
+// 2^B_w with B_w the warp's reference).
 template <int DT, int NVT, bool CHUNKS, class Row>
 __device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int r, int pb, const Desc &d, int lo,
-                                          int warp, int lane, int tid) {
+                                          int nvec, int warp, int lane, int tid) {
     constexpr int E = Elt<DT>::kPerVec;
     constexpr int H = E / 2;
     if (d.greedy) {
-        // smallest index attaining the max; NaN / +inf make the row invalid
+        // smallest index attaining the max; NaN / +inf make the row invalid. The running max
+        // picks the thread's first vector attaining it, the element is found in that vector.
         float best = -INFINITY;
-        int bidx = INT_MAX, bad = 0;
+        int vbest = -1, bad = 0;
 #pragma unroll
         for (int v = 0; v < NVT; ++v) {
+            if (!warp_has(v, warp, nvec)) continue;
             const uint4 w = row(v);
 #pragma unroll
             for (int h = 0; h < H; ++h) {
                 const float2 y = Elt<DT>::unpack_one(w, h);
                 bad |= (y.x != y.x) || (y.x == INFINITY) || (y.y != y.y) || (y.y == INFINITY);
-                if (y.x > best) {
-                    best = y.x;
-                    bidx = (lo + tid + v * kThreads) * E + 2 * h;
-                }
-                if (y.y > best) {
-                    best = y.y;
-                    bidx = (lo + tid + v * kThreads) * E + 2 * h + 1;
-                }
+            }
+            const float mv = Elt<DT>::vmax(w);
+            if (mv > best) {
+                best = mv;
+                vbest = v;
             }
         }
+        int bidx = INT_MAX;
+#pragma unroll
+        for (int v = 0; v < NVT; ++v)
+            if (v == vbest) {
+                const uint4 w = row(v);
+                for (int e = E - 1; e >= 0; --e)
+                    if (vec_elem<DT>(w, e) == best) bidx = (lo + tid + v * kThreads) * E + e;
+            }
         const float wbest = warp_max(best);
         const int widx = warp_min_i32(best == wbest ? bidx : INT_MAX);
         const int wbad = __any_sync(0xffffffffu, bad);
@@ -198,45 +269,9 @@ __device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int r, 
         return;
     }
     const float2 shi2 = f2splat(d.s_hi), slo2 = f2splat(d.s_lo);
-    float m = -INFINITY;
-#pragma unroll
-    for (int v = 0; v < NVT; ++v) m = fmaxf(m, Elt<DT>::vmax(row(v)));
-    // an all -inf thread gets reference 0: its sum is 0 (or NaN if a NaN hides in it)
-    const float b = (m == -INFINITY) ? 0.0f : floorf(m * d.s_hi);
-    const float2 nb2 = f2splat(-b);
     float sv[CHUNKS ? NVT : 1];
-    float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int v = 0; v < NVT; ++v) {
-        const uint4 w = row(v);
-        if (CHUNKS) {
-            float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int h = 0; h < H; ++h) {
-                const float2 e = ex2x2(exp_arg2(Elt<DT>::unpack_one(w, h), shi2, slo2, nb2));
-                if (h & 1) a1 = __fadd2_rn(a1, e);
-                else a0 = __fadd2_rn(a0, e);
-            }
-            const float2 a = __fadd2_rn(a0, a1);
-            sv[CHUNKS ? v : 0] = a.x + a.y;
-        } else {
-#pragma unroll
-            for (int h = 0; h < H; ++h) {
-                const float2 e = ex2x2(exp_arg2(Elt<DT>::unpack_one(w, h), shi2, slo2, nb2));
-                if (h & 1) acc1 = __fadd2_rn(acc1, e);
-                else acc0 = __fadd2_rn(acc0, e);
-            }
-        }
-    }
-    float s;
-    if (CHUNKS) {
-        s = 0.0f;
-#pragma unroll
-        for (int v = 0; v < NVT; ++v) s += sv[CHUNKS ? v : 0];
-    } else {
-        const float2 a = __fadd2_rn(acc0, acc1);
-        s = a.x + a.y;
-    }
+    float b;
+    float s = sweep_sums<DT, NVT, CHUNKS>(row, d.s_hi, shi2, slo2, warp, nvec, b, sv);
     const bool ok = s > 0.0f && !isinf(s);  // NaN, inf and empty are not ok
     const int bad = __any_sync(0xffffffffu, !(s >= 0.0f) || isinf(s));
     const float Bw = warp_max(ok ? b : -INFINITY);
@@ -260,53 +295,92 @@ __device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int r, 
     }
 }
 
-// Control warp: this CTA's message for item n: its row statistics over the warps (lanes 0-15 take
-// row 0, lanes 16-31 row 1, one lane per data warp), the logits at the draft token if it holds them,
-// (the previous item's totals are already in place).
-__device__ __forceinline__ void build_message(CtaShared &sh, int greedy, int nr, int n, int nch, int lane) {
-    Msg &msg = sh.mine;
-    const int r = lane >> 4, w = lane & 15;
-    const bool on = r < nr && w < kWarps;
-    const WarpStat &st = sh.ws[r][w];
-    int bad = on ? st.bad : 0;
+// A warp's statistics of one row from each thread's sum s at its reference b.
+__device__ __forceinline__ void warp_row_stats(CtaShared &sh, int r, int warp, int lane, float s, float b) {
+    const bool ok = s > 0.0f && !isinf(s);  // NaN, inf and empty are not ok
+    const int bad = __any_sync(0xffffffffu, !(s >= 0.0f) || isinf(s));
+    const float Bw = warp_max(ok ? b : -INFINITY);
+    const float Sw = warp_sum(ok ? s * pow2i(b - Bw) : 0.0f);
+    if (lane == 0) {
+        sh.ws[r][warp].B = Bw;
+        sh.ws[r][warp].S_hi = Sw;
+        sh.ws[r][warp].S_lo = 0.0f;
+        sh.ws[r][warp].bad = bad;
+    }
+}
+
+// Pass 1 of a pair under Rule 2 (target in registers, draft in its ring slot).
+template <int DT, int NVT>
+__device__ __forceinline__ void pair_stats(const uint4 (&vt)[NVT], const SmemRow<DT> &rd, CtaShared &sh,
+                                           const Desc &d, int nvec, int warp, int lane) {
+    constexpr int H = Elt<DT>::kPerVec / 2;
+    const float2 shi2 = f2splat(d.s_hi), slo2 = f2splat(d.s_lo);
+    // one loop over both rows: the loads of the draft row and the exponentials of the target row
+    // hide each other's latency. References from each thread's first vectors (see sweep_sums).
+    const bool h0 = warp_has(0, warp, nvec);
+    float bt = floorf((h0 ? Elt<DT>::vmax(vt[0]) : -INFINITY) * d.s_hi);
+    float bd = floorf((h0 ? Elt<DT>::vmax(rd(0)) : -INFINITY) * d.s_hi);
+    float st, sd;
+    {
+        const float2 nbt = f2splat(-bt), nbd = f2splat(-bd);
+        float2 ta = make_float2(0.0f, 0.0f), qa = ta;
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-    float B = -INFINITY, gmax = -INFINITY;
-    int garg = INT_MAX;
-    F2 S = {0.0f, 0.0f};
-    if (greedy) {
-        gmax = on ? st.gmax : -INFINITY;
-        garg = on ? st.garg : INT_MAX;
+        for (int v = 0; v < NVT; ++v) {
+            if (!warp_has(v, warp, nvec)) continue;
+            const uint4 wt = vt[v], wd = rd(v);
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) {
-            const float og = __shfl_xor_sync(0xffffffffu, gmax, o);
-            const int oa = __shfl_xor_sync(0xffffffffu, garg, o);
-            if (og > gmax || (og == gmax && oa < garg)) {
-                gmax = og;
-                garg = oa;
+            for (int h = 0; h < H; ++h) {
+                ta = __fadd2_rn(ta, ex2x2(exp_arg2(Elt<DT>::unpack_one(wt, h), shi2, slo2, nbt)));
+                qa = __fadd2_rn(qa, ex2x2(exp_arg2(Elt<DT>::unpack_one(wd, h), shi2, slo2, nbd)));
             }
         }
-    } else {
-        const float Sw = on ? st.S_hi : 0.0f;
-        const bool has = Sw > 0.0f;
-        const float Bw = on ? st.B : -INFINITY;
-        B = has ? Bw : -INFINITY;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) B = fmaxf(B, __shfl_xor_sync(0xffffffffu, B, o));
-        S = has ? F2{Sw * pow2i(Bw - B), 0.0f} : F2{0.0f, 0.0f};
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) {
-            const F2 x = {__shfl_xor_sync(0xffffffffu, S.hi, o), __shfl_xor_sync(0xffffffffu, S.lo, o)};
-            S = f2_add(S, x);
-        }
+        st = ta.x + ta.y;
+        sd = qa.x + qa.y;
     }
-    if (w == 0) {
-        msg.B[r] = B;
-        msg.S_hi[r] = S.hi;
-        msg.S_lo[r] = S.lo;
-        msg.bad[r] = bad;
-        msg.gmax[r] = gmax;
-        msg.garg[r] = garg;
+    float none[1];
+    if (__any_sync(0xffffffffu, !(st <= 0x1p64f))) st = exact_sums<DT, NVT, false>(RegRow<NVT>{vt}, d.s_hi, shi2, slo2, warp, nvec, bt, none);
+    if (__any_sync(0xffffffffu, !(sd <= 0x1p64f))) sd = exact_sums<DT, NVT, false>(rd, d.s_hi, shi2, slo2, warp, nvec, bd, none);
+    warp_row_stats(sh, 0, warp, lane, st, bt);
+    warp_row_stats(sh, 1, warp, lane, sd, bd);
+}
+
+// Control warp: this CTA's message for item n: its row statistics over the data warps (lane w
+// takes warp w, both rows) and the logits at the draft token if it holds them (the previous
+// item's totals are already in place).
+__device__ __forceinline__ void build_message(CtaShared &sh, int greedy, int nr, int n, int lane) {
+    Msg &msg = sh.mine;
+    const bool on = lane < kWarps;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const bool use = on && r < nr;
+        const WarpStat &st = sh.ws[r][on ? lane : 0];
+        int bad = use ? st.bad : 0;
+        float B = -INFINITY, gmax = -INFINITY;
+        int garg = INT_MAX;
+        F2 S = {0.0f, 0.0f};
+        if (greedy) {
+            gmax = use ? st.gmax : -INFINITY;
+            garg = use ? st.garg : INT_MAX;
+        } else {
+            const float Sw = use ? st.S_hi : 0.0f;
+            const float Bw = use ? st.B : -INFINITY;
+            B = warp_max(Sw > 0.0f ? Bw : -INFINITY);
+            S = warp_sum_f2(Sw > 0.0f ? F2{Sw * pow2i(Bw - B), 0.0f} : F2{0.0f, 0.0f});
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (greedy) {
+            const float wbest = warp_max(gmax);
+            garg = warp_min_i32(gmax == wbest ? garg : INT_MAX);
+            gmax = wbest;
+        }
+        if (lane == 0) {
+            msg.B[r] = B;
+            msg.S_hi[r] = S.hi;
+            msg.S_lo[r] = S.lo;
+            msg.bad[r] = bad;
+            msg.gmax[r] = gmax;
+            msg.garg[r] = garg;
+        }
     }
     if (lane == 0) {
         msg.has_x = (sh.x_stamp == n + 1) ? 1 : 0;
@@ -460,8 +534,11 @@ __device__ __forceinline__ void decide_item(CtaShared &sh, const Desc &d, int nr
                 }
                 D.rho = rho;
                 D.accept = (rho > 0.0f) && !f2_gt(d.u_acc, {rho, 0.0f});
-                D.c_t = D.B_t + __log2f(D.S_t.hi);
-                D.c_d = D.B_d + __log2f(D.S_d.hi);
+                const float2 ct = log2_split(D.S_t, D.B_t), cd = log2_split(D.S_d, D.B_d);
+                D.c_t = ct.x;
+                D.c_tf = ct.y;
+                D.c_d = cd.x;
+                D.c_df = cd.y;
                 if (!D.accept) D.kind = SAMPLE_RESIDUAL;
             } else {
                 D.kind = SAMPLE_P;
@@ -473,9 +550,8 @@ __device__ __forceinline__ void decide_item(CtaShared &sh, const Desc &d, int nr
 
 // Pass 2 of a pair under Rule 2, from the registers of pass 1. Where the position rejects:
 // e_t = 2^(y_t s - B_t), e_d = 2^(y_d s - B_d), lambda = S_t / S_d; the residual
-// max(e_t - lambda e_d, 0) per chunk, S_t * min(p, q) = min(e_t, lambda e_d) (no cancellation),
-// and per (vector, thread) the sums of e_t (a draw from p when the residual has no mass). Where it
-// accepts, only alpha: min(p, q) = 2^min(y_t s - c_t, y_d s - c_d), c = B + log2 S.
+// max(e_t - lambda e_d, 0) per chunk and S_t * min(p, q) = min(e_t, lambda e_d) (no
+// cancellation). Where it accepts, only alpha: min(p, q) = 2^min(y_t s - c_t, y_d s - c_d), c = log2 of the normaliser.
 template <int DT, int NVT>
 __device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> &rd, CtaShared &sh,
                                       const Decision &D, int par, int warp, int lane, int tid) {
@@ -489,8 +565,12 @@ __device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> 
             float2 acc_a = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int v = 0; v < NVT; ++v) {
+                if (!warp_has(v, warp, rd.nvec)) {
+                    if (lane == 0) sh.rm[par][v * kWarps + warp] = 0.0f;
+                    continue;
+                }
                 const uint4 wd = rd(v);
-                float2 racc = make_float2(0.0f, 0.0f), pacc = make_float2(0.0f, 0.0f);
+                float2 racc = make_float2(0.0f, 0.0f);
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
                     const float2 yt = Elt<DT>::unpack_one(vt[v], h), yd = Elt<DT>::unpack_one(wd, h);
@@ -499,24 +579,26 @@ __device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> 
                     const float2 r = __ffma2_rn(ed, nll, __ffma2_rn(ed, nlh, et));
                     const float2 nq = __fmul2_rn(ed, nlh);  // -lambda_hi * e_d, for min(p, q)
                     racc = __fadd2_rn(racc, make_float2(fmaxf(r.x, 0.0f), fmaxf(r.y, 0.0f)));
-                    pacc = __fadd2_rn(pacc, et);
                     acc_a = __fadd2_rn(acc_a, make_float2(fminf(et.x, -nq.x), fminf(et.y, -nq.y)));
                 }
-                sh.tpm[v * kThreads + tid] = pacc.x + pacc.y;
                 const float rs = warp_sum(racc.x + racc.y);
                 if (lane == 0) sh.rm[par][v * kWarps + warp] = rs;
             }
             my_alpha = (acc_a.x + acc_a.y) * D.inv_St;
         } else {
+            // y*s - c with c split: the product less the integral part rounds once (to a small
+            // result near the top of the row), then the fraction
             const float2 nct = f2splat(-D.c_t), ncd = f2splat(-D.c_d);
+            const float2 nctf = f2splat(-D.c_tf), ncdf = f2splat(-D.c_df);
             float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int v = 0; v < NVT; ++v) {
+                if (!warp_has(v, warp, rd.nvec)) continue;
                 const uint4 wd = rd(v);
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
-                    const float2 at = __ffma2_rn(Elt<DT>::unpack_one(vt[v], h), shi2, nct);
-                    const float2 ad = __ffma2_rn(Elt<DT>::unpack_one(wd, h), shi2, ncd);
+                    const float2 at = __fadd2_rn(__ffma2_rn(Elt<DT>::unpack_one(vt[v], h), shi2, nct), nctf);
+                    const float2 ad = __fadd2_rn(__ffma2_rn(Elt<DT>::unpack_one(wd, h), shi2, ncd), ncdf);
                     acc = __fadd2_rn(acc, make_float2(ex2(fminf(at.x, ad.x)), ex2(fminf(at.y, ad.y))));
                 }
             }
@@ -572,13 +654,6 @@ struct FinState {
     int kind, fb, owner;
     F2 local, Ztot;  // u*Z less the mass of the CTAs before the owner; Z (units 2^B_t)
 };
-
-// Control warp: item m rejected and the next exchange reports no residual mass in any slice.
-__device__ __forceinline__ bool zero_residual(const CtaShared &sh, int m, int C, int lane) {
-    if (sh.dec[m & 1].kind != SAMPLE_RESIDUAL) return false;
-    const Msg *Mn = sh.slot[(m + 1) % 3];
-    return __ballot_sync(0xffffffffu, lane < C && Mn[lane < C ? lane : 0].prev_Zhi > 0.0f) == 0u;
-}
 
 // Control warp, once the exchange that carries item m's alpha and residual shares is done: the
 // item's results. They are written by the owner of its draw (the CTA whose slice holds u*Z),
@@ -653,13 +728,37 @@ __device__ __forceinline__ FinState finalize_head(CtaShared &sh, const RowsParam
     return f;
 }
 
+// Control warp of the owner CTA, for a rejecting pair whose residual has no mass (p <= q at every
+// token, up to rounding): the draw is from p, whose chunk masses (units 2^B_t) are computed here
+// from the target row in global memory, in the place of the (zero) residual chunk sums. A path
+// that ordinary inputs never take; it reads the slice once more.
+template <int DT>
+__device__ __noinline__ void fb_chunk_masses(CtaShared &sh, const RowsParams &P, const Decision &D, int par, int lane,
+                                             int nch, int lo, int nvec) {
+    constexpr int E = Elt<DT>::kPerVec;
+    const uint4 *row = static_cast<const uint4 *>(P.target) + static_cast<size_t>(D.item) * P.nvec_row + lo;
+    for (int k = 0; k < nch; ++k) {
+        const int vi = (k / kWarps) * kThreads + (k % kWarps) * kWarp + lane;
+        float w[E];
+        draw_weights<DT>(SAMPLE_P, vi < nvec ? row[vi] : kNegInfVec<DT>(), kNegInfVec<DT>(), D, D.B_t, w);
+        float a = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) a += w[e];
+        a = warp_sum(a);
+        if (lane == 0) sh.rm[par][k] = a;
+    }
+    __syncwarp();
+}
+
 // Control warp of the owner CTA: the chunk that holds u*Z (an inclusive scan over the slice's
 // chunk masses, in vocabulary order), fetched with a small bulk copy; `complete_draw` finds the
 // token once it has landed.
+template <int DT>
 __device__ __forceinline__ void draw_chunk(CtaShared &sh, const RowsParams &P, int m, const FinState &f, int lane,
                                            int nch, int lo, int nvec) {
     const int par = m & 1, pb = m % 3;
     const Decision &D = sh.dec[par];
+    if (f.fb) fb_chunk_masses<DT>(sh, P, D, par, lane, nch, lo, nvec);
     int ksel = -1, klast = -1;
     F2 before = {0.0f, 0.0f}, last_before = {0.0f, 0.0f}, run = {0.0f, 0.0f};
 #pragma unroll 1
@@ -670,13 +769,7 @@ __device__ __forceinline__ void draw_chunk(CtaShared &sh, const RowsParams &P, i
             if (f.kind == SAMPLE_RESIDUAL) {
                 mk = sh.rm[par][k];
             } else if (f.fb) {
-                // a rejecting pair: sum the chunk's (vector, thread) partials of p; lanes start at
-                // different words so that they read different banks
-                const float *src = sh.tpm + (k / kWarps) * kThreads + (k % kWarps) * kWarp;
-                float a = 0.0f;
-#pragma unroll 4
-                for (int j = 0; j < kWarp; ++j) a += src[(j + lane) & (kWarp - 1)];
-                mk = a;
+                mk = sh.rm[par][k];  // p masses, from fb_chunk_masses
             } else {
                 const float pmk = sh.pm[pb][k];
                 mk = pmk > 0.0f ? pmk * pow2i(sh.pref[pb][k] - D.B_t) : 0.0f;
@@ -841,7 +934,7 @@ __device__ __forceinline__ bool load_row(CtaShared &sh, const uint4 *ring, int s
 }
 
 template <int DT, int NVT>
-__global__ void __launch_bounds__(kBlock, 1) spec_rows_kernel(const RowsParams P) {
+__global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P) {
     constexpr int E = Elt<DT>::kPerVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ CtaShared sh;
@@ -890,13 +983,17 @@ __global__ void __launch_bounds__(kBlock, 1) spec_rows_kernel(const RowsParams P
             bool ok = true;
             if (nr >= 1) ok = load_row<DT, NVT>(sh, ring, slice_max, nvec, R, tid, vt);
             bar_arrive(BAR_FREE, kBlock);  // the target row's slot may be refilled
-            if (nr == 1) row_stats<DT, NVT, true>(RegRow<NVT>{vt}, sh, 0, n % 3, d, lo, warp, lane, tid);
+            if (nr == 1) row_stats<DT, NVT, true>(RegRow<NVT>{vt}, sh, 0, n % 3, d, lo, nvec, warp, lane, tid);
             const SmemRow<DT> rd = {ring + static_cast<size_t>((R + 1) % kRing) * slice_max, tid, nvec};
             if (nr == 2) {
-                row_stats<DT, NVT, false>(RegRow<NVT>{vt}, sh, 0, n % 3, d, lo, warp, lane, tid);
                 ok &= mbar_wait_sleep_bounded(&sh.full[(R + 1) % kRing], static_cast<uint32_t>(((R + 1) / kRing) & 1),
                                               kSuspendNs, kMaxWaitTries);
-                row_stats<DT, NVT, false>(rd, sh, 1, n % 3, d, lo, warp, lane, tid);
+                if (d.greedy) {
+                    row_stats<DT, NVT, false>(RegRow<NVT>{vt}, sh, 0, n % 3, d, lo, nvec, warp, lane, tid);
+                    row_stats<DT, NVT, false>(rd, sh, 1, n % 3, d, lo, nvec, warp, lane, tid);
+                } else {
+                    pair_stats<DT, NVT>(vt, rd, sh, d, nvec, warp, lane);
+                }
                 // the logits at the draft token, from the thread that holds them
                 const int x = d.x;
                 if (x >= 0 && x < P.V) {
@@ -956,7 +1053,7 @@ __global__ void __launch_bounds__(kBlock, 1) spec_rows_kernel(const RowsParams P
                 produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, issued, released + kRing, cur_item, cur_row);
             }
             bar_sync(BAR_STATS, kBlock);
-            build_message(sh, d.greedy, nr, n, nch, lane);
+            build_message(sh, d.greedy, nr, n, lane);
             __syncwarp();
             push_record(&sh.mine, sh.slot[n % 3], &sh.msg_bar[n % 3], crank, C, lane);
             if (lane == 0) mbar_arrive_expect_tx(&sh.msg_bar[n % 3], static_cast<uint32_t>(C * kMsgBytes));
@@ -967,17 +1064,11 @@ __global__ void __launch_bounds__(kBlock, 1) spec_rows_kernel(const RowsParams P
             __syncwarp();
             decide_item(sh, d, nr, n, C, P, lane);
             __syncwarp();
-            // the previous item's results wait until pass 2 runs, unless its residual had no mass:
-            // that draw uses the per-thread sums of p, which the next pass 2 overwrites
-            const bool early = n > 0 && zero_residual(sh, n - 1, C, lane);
-            if (early) {
-                const FinState f = finalize_head(sh, P, n - 1, C, crank, lane);
-                if (f.owner == crank) draw_chunk(sh, P, n - 1, f, lane, nch, lo, nvec);
-            }
             bar_arrive(BAR_DECIDED, kBlock);
-            if (n > 0 && !early) {
+            // the previous item's results, while pass 2 runs
+            if (n > 0) {
                 const FinState f = finalize_head(sh, P, n - 1, C, crank, lane);
-                if (f.owner == crank) draw_chunk(sh, P, n - 1, f, lane, nch, lo, nvec);
+                if (f.owner == crank) draw_chunk<DT>(sh, P, n - 1, f, lane, nch, lo, nvec);
             }
             bar_sync(BAR_PASS2, kBlock);
             stash_totals(sh, n, nch, lane);
@@ -992,7 +1083,7 @@ __global__ void __launch_bounds__(kBlock, 1) spec_rows_kernel(const RowsParams P
         }
         if (nitems > 0) {
             // the last item's totals travel in one more exchange
-            build_message(sh, 0, 0, nitems, nch, lane);
+            build_message(sh, 0, 0, nitems, lane);
             __syncwarp();
             push_record(&sh.mine, sh.slot[nitems % 3], &sh.msg_bar[nitems % 3], crank, C, lane);
             if (lane == 0) mbar_arrive_expect_tx(&sh.msg_bar[nitems % 3], static_cast<uint32_t>(C * kMsgBytes));
@@ -1002,7 +1093,7 @@ __global__ void __launch_bounds__(kBlock, 1) spec_rows_kernel(const RowsParams P
                 sh.timed_out = 1;
             __syncwarp();
             const FinState f = finalize_head(sh, P, nitems - 1, C, crank, lane);
-            if (f.owner == crank) draw_chunk(sh, P, nitems - 1, f, lane, nch, lo, nvec);
+            if (f.owner == crank) draw_chunk<DT>(sh, P, nitems - 1, f, lane, nch, lo, nvec);
             complete_draw<DT>(sh, P, lo, lane);
         }
         if (lane == 0 && sh.timed_out) {

@@ -229,7 +229,7 @@ static cudaError_t shape_table(int nvec_row, ShapeTable &out) {
         ClusterOption &o = t.opt[ci];
         if (C > nvec_row) continue;
         const int slice = (nvec_row + C - 1) / C;
-        // vectors per data thread: 2, 4 or 9 (the largest slice that fits the registers)
+        // vectors per data thread: 2, 4 or 5 (the largest slice that fits the registers)
         const int nvt = (slice <= 2 * kThreads) ? 2 : (slice <= 4 * kThreads) ? 4 : kMaxNvt;
         if (nvt * kThreads < slice) continue;  // a slice must fit the registers of one CTA
         const RowsKernel k = rows_kernel_for<DT>(nvt);

@@ -127,6 +127,54 @@ def test_greedy_and_mixed_temperatures():
     assert_report(check_round(rd))
 
 
+def _resample_drafts(rd, seed):
+    """Draft tokens drawn again from q = softmax(draft / T) after the logits were rewritten."""
+    gen = torch.Generator(device=rd.draft.device)
+    gen.manual_seed(seed)
+    K = np.asarray(rd.K)
+    req = torch.as_tensor(np.repeat(np.arange(rd.B), K), device=rd.draft.device)
+    t = rd.temperature[req].unsqueeze(1)
+    z = rd.draft.float()
+    u = torch.rand(z.shape, generator=gen, device=z.device).clamp_(min=1e-38)
+    score = torch.where(t > 0, z / t.clamp(min=1e-30) - torch.log(-torch.log(u)), z)
+    rd.draft_tokens = score.argmax(dim=1).to(torch.int32)
+
+
+@pytest.mark.parametrize("dtype,V", [(torch.bfloat16, 131072), (torch.float32, 65536)])
+def test_wide_logit_ranges(dtype, V):
+    """Rows whose logits span hundreds of units within one thread's share of the slice (a ramp
+    across the vocabulary, rising and falling), and rows whose vocabulary is mostly masked to
+    -inf: the per-thread reference of pass 1 then takes its exact path."""
+    base = W.Workload("t", B=64, V=V, dtype=dtype, temperature=1.0, logits="normal", sigma=1.0,
+                      draft_sigma=0.5, K="uniform:0:3")
+    rd = W.make_round(base, seed=21, device="cuda")
+    ramp = torch.linspace(-300.0, 300.0, V, device="cuda")
+    tz = rd.target.float()
+    dz = rd.draft.float()
+    # rising ramp on even requests, falling ramp on odd ones; every third request mostly masked
+    row_req = np.repeat(np.arange(rd.B), np.asarray(rd.K) + 1)
+    drow_req = np.repeat(np.arange(rd.B), np.asarray(rd.K))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    mask = torch.rand(rd.B, V, generator=gen, device="cuda") < 0.9
+    for i in range(rd.B):
+        rr = torch.as_tensor(np.nonzero(row_req == i)[0], device="cuda")
+        dr = torch.as_tensor(np.nonzero(drow_req == i)[0], device="cuda")
+        if i % 3 == 2:
+            tz[rr] = tz[rr].masked_fill(mask[i], float("-inf"))
+            if len(dr):
+                dz[dr] = dz[dr].masked_fill(mask[i], float("-inf"))
+        else:
+            sgn = 1.0 if i % 2 == 0 else -1.0
+            tz[rr] += sgn * ramp
+            if len(dr):
+                dz[dr] += sgn * ramp
+    rd.target = tz.to(dtype).contiguous()
+    rd.draft = dz.to(dtype).contiguous()
+    _resample_drafts(rd, 17)
+    assert_report(check_round(rd))
+
+
 def test_bad_requests():
     base = W.Workload("t", B=10, V=3000, dtype=torch.bfloat16, temperature=1.0, logits="normal",
                       sigma=2.0, draft_sigma=0.6, K="fixed:3")
