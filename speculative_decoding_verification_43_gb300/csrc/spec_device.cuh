@@ -191,6 +191,15 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // ---------------------------------------------------------------- cluster
 
+// The two halves of a cluster barrier: every thread of the cluster arrives once, then waits once
+// (possibly much later) before it arrives again.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::

@@ -32,8 +32,10 @@ struct CtaShared {
 };
 
 // Items of cluster `cid`: cid, cid + ncl, cid + 2 ncl, ... Batch `nb` holds list entries
-// [nb, nb + nbatch). Every CTA of the cluster computes the same descriptors. Control warp.
-__device__ void load_batch(CtaShared &sh, const RowsParams &P, int cid, int nb, int nbatch, int lane) {
+// [nb, nb + nbatch). Every CTA of the cluster computes the same descriptors. Control warp, in two
+// steps: the shapes (which request and position, the draft row), enough to issue the row copies,
+// then the per-item values (temperature, draws, draft token).
+__device__ void load_batch_shapes(CtaShared &sh, const RowsParams &P, int cid, int nb, int nbatch, int lane) {
     for (int s = lane; s < kMaxItems; s += kWarp) {
         Desc &d = sh.desc[s];
         d.item = cid + (nb + s) * P.nclusters;
@@ -70,10 +72,13 @@ __device__ void load_batch(CtaShared &sh, const RowsParams &P, int cid, int nb, 
             d.drow = dr;
             d.pair = (status == 0 && j < K) ? 1 : 0;
             d.status = status;
-            d.x = r1;  // the request's end row, for the frontier draw below
+            d.x = r1;  // the request's end row, for the frontier draw
         }
     }
     __syncwarp();
+}
+
+__device__ void load_batch_values(CtaShared &sh, const RowsParams &P, int nbatch, int lane) {
     // per item: temperature, draws and draft token (loads issued in parallel, one thread each)
     for (int s = lane; s < nbatch; s += kWarp) {
         Desc &d = sh.desc[s];
@@ -104,8 +109,11 @@ __device__ void load_batch(CtaShared &sh, const RowsParams &P, int cid, int nb, 
     __syncwarp();
 }
 
+// Rows an item streams through the ring: its target row, and its draft row for a pair. Only a bad
+// shape has none (its rows may not exist); a bad temperature streams them and discards the
+// result, so that the ring order is fixed before the temperatures are read.
 __device__ __forceinline__ int desc_rows(const Desc &d) {
-    return (d.status & (SPEC_REQ_BAD_SHAPE | SPEC_REQ_BAD_PARAM)) ? 0 : (d.pair ? 2 : 1);
+    return (d.status & SPEC_REQ_BAD_SHAPE) ? 0 : (d.pair ? 2 : 1);
 }
 
 // Control warp, lane 0: issue the bulk copies of the cluster's row sequence up to row `limit`
@@ -409,8 +417,9 @@ __device__ __forceinline__ void stash_totals(CtaShared &sh, int n, int nch, int 
 
 // Control warp, after the exchange of item n: combine the C records (lanes 0-15 take row 0,
 // lanes 16-31 row 1, one lane per CTA, in CTA order; C is a power of two, so log2(C) butterfly
-// steps combine them) and decide the accept test (lane 0). Every CTA runs the same reductions on
-// the same records, so all reach the same decision.
+// steps combine them) and decide the accept test. The scalar tail is spread over four lanes: the
+// accept test (lane 0), lambda (lane 1), log2 of the two normalisers (lanes 2, 3). Every CTA runs
+// the same reductions on the same records, so all reach the same decision.
 __device__ __forceinline__ void decide_item(CtaShared &sh, const Desc &d, int nr, int n, int C, const RowsParams &P,
                                             int lane) {
     const Msg *M = sh.slot[n % 3];
@@ -426,126 +435,130 @@ __device__ __forceinline__ void decide_item(CtaShared &sh, const Desc &d, int nr
         yx_d = __shfl_sync(0xffffffffu, m.yx[1], l);
     }
     int bad = on ? m.bad[r] : 0;
-    for (int o = C >> 1; o > 0; o >>= 1) bad |= __shfl_xor_sync(0xffffffffu, bad, o);
     float Bv = -INFINITY, gm = -INFINITY;
     int ga = INT_MAX;
     F2 S = {0.0f, 0.0f};
     if (d.greedy) {
         gm = on ? m.gmax[r] : -INFINITY;
         ga = on ? m.garg[r] : INT_MAX;
-        for (int o = C >> 1; o > 0; o >>= 1) {
-            const float og = __shfl_xor_sync(0xffffffffu, gm, o);
-            const int oa = __shfl_xor_sync(0xffffffffu, ga, o);
-            if (og > gm || (og == gm && oa < ga)) {
-                gm = og;
-                ga = oa;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1)
+            if (o < C) {
+                bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+                const float og = __shfl_xor_sync(0xffffffffu, gm, o);
+                const int oa = __shfl_xor_sync(0xffffffffu, ga, o);
+                if (og > gm || (og == gm && oa < ga)) {
+                    gm = og;
+                    ga = oa;
+                }
             }
-        }
     } else {
         const float Sh = on ? m.S_hi[r] : 0.0f;
         const bool has = Sh > 0.0f;
         const float Bc = on ? m.B[r] : -INFINITY;
         Bv = has ? Bc : -INFINITY;
-        for (int o = C >> 1; o > 0; o >>= 1) Bv = fmaxf(Bv, __shfl_xor_sync(0xffffffffu, Bv, o));
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1)
+            if (o < C) {
+                bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+                Bv = fmaxf(Bv, __shfl_xor_sync(0xffffffffu, Bv, o));
+            }
         S = has ? f2_scale({Sh, m.S_lo[r]}, Bc - Bv) : F2{0.0f, 0.0f};
-        for (int o = C >> 1; o > 0; o >>= 1)
-            S = f2_add(S, {__shfl_xor_sync(0xffffffffu, S.hi, o), __shfl_xor_sync(0xffffffffu, S.lo, o)});
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1)
+            if (o < C) S = f2_add(S, {__shfl_xor_sync(0xffffffffu, S.hi, o), __shfl_xor_sync(0xffffffffu, S.lo, o)});
     }
-    // row 1 (lane 16) to lane 0
-    const int bad1 = __shfl_sync(0xffffffffu, bad, 16);
-    const float Bv1 = __shfl_sync(0xffffffffu, Bv, 16);
-    const F2 S1 = shfl_f2(S, 16);
-    const float gm1 = __shfl_sync(0xffffffffu, gm, 16);
-    const int ga1 = __shfl_sync(0xffffffffu, ga, 16);
-    if (lane != 0) return;
-    Decision &D = sh.dec[n & 1];
-    D.item = d.item;
-    D.drow = d.drow;
-    D.pair = d.pair;
-    D.greedy = d.greedy;
-    D.s_hi = d.s_hi;
-    D.s_lo = d.s_lo;
-    D.u_s = d.u_s;
-    D.valid = 1;
-    D.accept = 0;
-    D.kind = SAMPLE_NONE;
-    D.rho = 0.0f;
-    D.argmax_t = -1;
-    D.alpha_g = 0.0f;
+    // rows 0 and 1 from lanes 0 and 16, to every lane
+    const int bad0 = __shfl_sync(0xffffffffu, bad, 0), bad1 = __shfl_sync(0xffffffffu, bad, 16);
+    const float B0 = __shfl_sync(0xffffffffu, Bv, 0), B1 = __shfl_sync(0xffffffffu, Bv, 16);
+    const F2 S0 = shfl_f2(S, 0), S1 = shfl_f2(S, 16);
+    const float gm0 = __shfl_sync(0xffffffffu, gm, 0), gm1 = __shfl_sync(0xffffffffu, gm, 16);
+    const int ga0 = __shfl_sync(0xffffffffu, ga, 0), ga1 = __shfl_sync(0xffffffffu, ga, 16);
+    const int am0 = (nr >= 1 && !(bad0 || gm0 == -INFINITY)) ? ga0 : -1;
+    const int am1 = (nr >= 2 && !(bad1 || gm1 == -INFINITY)) ? ga1 : -1;
+    const float B_t = (nr >= 1) ? (bad0 ? NAN : B0) : NAN, B_d = (nr >= 2) ? (bad1 ? NAN : B1) : NAN;
+    const F2 S_t = (nr >= 1) ? S0 : F2{0.0f, 0.0f}, S_d = (nr >= 2) ? S1 : F2{0.0f, 0.0f};
+    // the status, the same in every lane; row validity is reported together with a bad proposal
+    // (both are preconditions)
     int status = d.status | (tmo ? REQ_TIMEOUT : 0);
-    int am[2] = {-1, -1};
-    float Bw[2] = {NAN, NAN};
-    F2 Sr[2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
-    if (nr >= 1) {
-        am[0] = (bad || gm == -INFINITY) ? -1 : ga;
-        Bw[0] = bad ? NAN : Bv;
-        Sr[0] = S;
-    }
-    if (nr >= 2) {
-        am[1] = (bad1 || gm1 == -INFINITY) ? -1 : ga1;
-        Bw[1] = bad1 ? NAN : Bv1;
-        Sr[1] = S1;
-    }
-    D.B_t = Bw[0];
-    D.B_d = Bw[1];
-    D.S_t = Sr[0];
-    D.S_d = Sr[1];
-    // row validity is reported together with a bad proposal (both are preconditions)
     if (!(status & (SPEC_REQ_BAD_SHAPE | SPEC_REQ_BAD_PARAM | REQ_TIMEOUT))) {
         if (d.greedy) {
-            if (am[0] < 0 || (d.pair && am[1] < 0)) status |= SPEC_REQ_BAD_LOGITS;
+            if (am0 < 0 || (d.pair && am1 < 0)) status |= SPEC_REQ_BAD_LOGITS;
             if (d.pair && (d.x < 0 || d.x >= P.V)) status |= SPEC_REQ_BAD_PROPOSAL;
         } else {
-            const bool ok_t = isfinite(D.B_t) && D.S_t.hi > 0.0f && isfinite(D.S_t.hi);
-            const bool ok_d = !d.pair || (isfinite(D.B_d) && D.S_d.hi > 0.0f && isfinite(D.S_d.hi));
+            const bool ok_t = isfinite(B_t) && S_t.hi > 0.0f && isfinite(S_t.hi);
+            const bool ok_d = !d.pair || (isfinite(B_d) && S_d.hi > 0.0f && isfinite(S_d.hi));
             if (!ok_t || !ok_d) status |= SPEC_REQ_BAD_LOGITS;
             // q(x) == 0 is a bad proposal for Rule 2 (checked before any draw)
             if (d.pair && (d.x < 0 || d.x >= P.V || yx_d == -INFINITY)) status |= SPEC_REQ_BAD_PROPOSAL;
         }
     }
-    if (status == 0) {
-        if (d.greedy) {
-            D.argmax_t = am[0];
-            if (d.pair) {
-                D.accept = (d.x == am[0]);
-                D.rho = D.accept ? 1.0f : 0.0f;
-                D.alpha_g = (am[0] == am[1]) ? 1.0f : 0.0f;
-            }
-        } else {
-            D.inv_St = rcp_approx(D.S_t.hi);
-            if (d.pair) {
+    Decision &D = sh.dec[n & 1];
+    const bool rule2 = status == 0 && !d.greedy;
+    if (lane == 1 && rule2) {
+        D.inv_St = rcp_approx(S_t.hi);
+        if (d.pair) D.lam = f2_div(S_t, S_d);
+    } else if (lane == 2 && rule2 && d.pair) {
+        const float2 ct = log2_split(S_t, B_t);
+        D.c_t = ct.x;
+        D.c_tf = ct.y;
+    } else if (lane == 3 && rule2 && d.pair) {
+        const float2 cd = log2_split(S_d, B_d);
+        D.c_d = cd.x;
+        D.c_df = cd.y;
+    } else if (lane == 0) {
+        D.item = d.item;
+        D.drow = d.drow;
+        D.pair = d.pair;
+        D.greedy = d.greedy;
+        D.s_hi = d.s_hi;
+        D.s_lo = d.s_lo;
+        D.u_s = d.u_s;
+        D.valid = 1;
+        D.B_t = B_t;
+        D.B_d = B_d;
+        D.S_t = S_t;
+        D.S_d = S_d;
+        int accept = 0, kind = SAMPLE_NONE;
+        float rho = 0.0f;
+        D.argmax_t = -1;
+        D.alpha_g = 0.0f;
+        if (status == 0) {
+            if (d.greedy) {
+                D.argmax_t = am0;
+                if (d.pair) {
+                    accept = (d.x == am0);
+                    rho = accept ? 1.0f : 0.0f;
+                    D.alpha_g = (am0 == am1) ? 1.0f : 0.0f;
+                }
+            } else if (d.pair) {
                 // rho = p(x)/q(x) = 2^E * S_d/S_t with E = (y_t - y_d) s - (B_t - B_d), in float
                 // pairs; 2^E from ex2 of its fraction and an exact power of two
-                D.lam = f2_div(D.S_t, D.S_d);
-                float rho = 0.0f;
                 if (yx_t != -INFINITY) {
                     F2 Ex = f2_mul(f2_add({yx_t, 0.0f}, {-yx_d, 0.0f}), {d.s_hi, d.s_lo});
-                    Ex = f2_add(Ex, {-(D.B_t - D.B_d), 0.0f});
+                    Ex = f2_add(Ex, {-(B_t - B_d), 0.0f});
                     const float nn = floorf(Ex.hi);
                     const float f = (Ex.hi - nn) + Ex.lo;
-                    const F2 ratio = f2_div(D.S_d, D.S_t);
-                    const float m = ex2(f) * (ratio.hi + ratio.lo);
+                    const F2 ratio = f2_div(S_d, S_t);
+                    const float mm = ex2(f) * (ratio.hi + ratio.lo);
                     if (nn > 254.0f) {
                         rho = INFINITY;
                     } else if (nn >= -252.0f) {
                         const float h = floorf(0.5f * nn);
-                        rho = m * pow2i(h) * pow2i(nn - h);
+                        rho = mm * pow2i(h) * pow2i(nn - h);
                     }
                 }
-                D.rho = rho;
-                D.accept = (rho > 0.0f) && !f2_gt(d.u_acc, {rho, 0.0f});
-                const float2 ct = log2_split(D.S_t, D.B_t), cd = log2_split(D.S_d, D.B_d);
-                D.c_t = ct.x;
-                D.c_tf = ct.y;
-                D.c_d = cd.x;
-                D.c_df = cd.y;
-                if (!D.accept) D.kind = SAMPLE_RESIDUAL;
+                accept = (rho > 0.0f) && !f2_gt(d.u_acc, {rho, 0.0f});
+                if (!accept) kind = SAMPLE_RESIDUAL;
             } else {
-                D.kind = SAMPLE_P;
+                kind = SAMPLE_P;
             }
         }
+        D.rho = rho;
+        D.accept = accept;
+        D.kind = kind;
+        D.status = status;
     }
-    D.status = status;
 }
 
 // Pass 2 of a pair under Rule 2, from the registers of pass 1. Where the position rejects:
@@ -965,7 +978,10 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
         sh.mine.prev_alpha = sh.mine.prev_Zhi = sh.mine.prev_Zlo = 0.0f;
         sh.mine.pad = 0;
     }
-    cluster_sync_all();  // every CTA of the cluster runs, its barriers ready, before any remote access
+    __syncthreads();  // the barriers are initialised
+    // every CTA of the cluster must run, its barriers ready, before any remote access: all threads
+    // arrive now; the control warp waits before its first remote store, the data warps at the end
+    cluster_arrive();
 
     if (warp < kWarps) {
         // ================= data warps: registers, pass 1, pass 2 =================
@@ -1019,6 +1035,7 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
             bar_arrive(BAR_PASS2, kBlock);  // the draft row's slot may be refilled
             R += nr;
         }
+        cluster_wait();
     } else {
         // ================= control warp: copies, exchange, decisions, draws =================
         long long issued = 0, released = 0;  // rows copied; rows whose slots are free again (in order)
@@ -1034,7 +1051,7 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
             if (n == nb + nbatch) {  // the next batch of descriptors (the ring is empty here)
                 nb = n;
                 nbatch = min(kMaxItems, nitems - n);
-                load_batch(sh, P, cid, nb, nbatch, lane);
+                load_batch_shapes(sh, P, cid, nb, nbatch, lane);
                 if (lane == 0) {
                     cur_item = 0;
                     cur_row = 0;
@@ -1042,6 +1059,7 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
                                  cur_row);
                 }
                 __syncwarp();
+                load_batch_values(sh, P, nbatch, lane);  // while the first copies are in flight
                 bar_arrive(BAR_BATCH, kBlock);
             }
             const Desc &d = sh.desc[n - nb];
@@ -1055,6 +1073,7 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
             bar_sync(BAR_STATS, kBlock);
             build_message(sh, d.greedy, nr, n, lane);
             __syncwarp();
+            if (n == 0) cluster_wait();  // the peers run and their barriers are ready
             push_record(&sh.mine, sh.slot[n % 3], &sh.msg_bar[n % 3], crank, C, lane);
             if (lane == 0) mbar_arrive_expect_tx(&sh.msg_bar[n % 3], static_cast<uint32_t>(C * kMsgBytes));
             complete_draw<DT>(sh, P, lo, lane);  // the draw of item n - 2, fetched one item ago
@@ -1081,6 +1100,7 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
                 }
             }
         }
+        if (nitems == 0) cluster_wait();
         if (nitems > 0) {
             // the last item's totals travel in one more exchange
             build_message(sh, 0, 0, nitems, lane);
