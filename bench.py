@@ -80,6 +80,12 @@ def barrier(world):
         torch.distributed.barrier()
 
 
+def job_value(world: int, rows_per_step: int, steps: int, ms_total_max: float) -> float:
+    """Whole-job throughput: every rank verifies its own batch each step (weak scaling); the
+    slowest rank's time (the max over ranks) bounds the job."""
+    return world * rows_per_step * steps / (ms_total_max / 1e3)
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     if world == 1:
         return x
@@ -326,7 +332,7 @@ def run_ours(args):
     ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
     rows_ms = statistics.fmean(ev_b[s].elapsed_time(ev_e[s]) for s in range(args.steps))
-    value = world * rows * args.steps / (ms_total / 1e3)
+    value = job_value(world, rows, args.steps, ms_total)
 
     # end to end through the public API, host buffers in, host results out
     e2e = run_e2e(args, sets, verifiers, compactors, gout, stream, dev, world) if args.e2e_steps > 0 else None

@@ -93,6 +93,18 @@ def _load():
                                             ctypes.c_double, _i32, _i32,
                                             ctypes.POINTER(ctypes.c_double)]
         lib.oracle_choose_gamma.restype = _i32
+        _vp = ctypes.c_void_p
+        lib.oracle_depth_counts.argtypes = [_i32, _vp, _vp, _vp, _i32, _vp, _vp]
+        lib.oracle_depth_counts.restype = None
+        lib.oracle_depth_alpha.argtypes = [_vp, _vp, _i32, ctypes.c_double, _i32, _vp]
+        lib.oracle_depth_alpha.restype = None
+        lib.oracle_depth_expected_accept.argtypes = [_vp, _vp, _i32, ctypes.c_double, _i32]
+        lib.oracle_depth_expected_accept.restype = ctypes.c_double
+        lib.oracle_depth_objective.argtypes = [_vp, _vp, _i32, ctypes.c_double, ctypes.c_double, _i32]
+        lib.oracle_depth_objective.restype = ctypes.c_double
+        lib.oracle_choose_gamma_depth.argtypes = [_vp, _vp, _i32, ctypes.c_double, ctypes.c_double,
+                                                  _i32, _i32, ctypes.POINTER(ctypes.c_double)]
+        lib.oracle_choose_gamma_depth.restype = _i32
         _lib = lib
     return _lib
 
@@ -195,3 +207,39 @@ def choose_gamma(alpha_sum: float, alpha_count: int, alpha_prev: float, c: float
     g = _load().oracle_choose_gamma(float(alpha_sum), int(alpha_count), float(alpha_prev),
                                     float(c), int(gamma_min), int(gamma_max), ctypes.byref(a))
     return int(g), float(a.value)
+
+
+def depth_counts(row_off, accept_len, req_status, depth_max: int):
+    """Per-depth counts of requests that reached / accepted depth j = 1..depth_max."""
+    ro, al, rs = _c(row_off, np.int32), _c(accept_len, np.int32), _c(req_status, np.int32)
+    nr = np.zeros(depth_max, np.int32)
+    na = np.zeros(depth_max, np.int32)
+    _load().oracle_depth_counts(len(al), _ptr(ro), _ptr(al), _ptr(rs), int(depth_max), _ptr(nr), _ptr(na))
+    return nr, na
+
+
+def depth_alpha(n_reached, n_accepted, alpha_prev: float, n_out: int):
+    nr, na = _c(n_reached, np.int32), _c(n_accepted, np.int32)
+    out = np.zeros(n_out, np.float64)
+    _load().oracle_depth_alpha(_ptr(nr), _ptr(na), len(nr), float(alpha_prev), int(n_out), _ptr(out))
+    return out
+
+
+def depth_expected_accept(n_reached, n_accepted, alpha_prev: float, gamma: int) -> float:
+    nr, na = _c(n_reached, np.int32), _c(n_accepted, np.int32)
+    return float(_load().oracle_depth_expected_accept(_ptr(nr), _ptr(na), len(nr), float(alpha_prev), int(gamma)))
+
+
+def depth_objective(n_reached, n_accepted, alpha_prev: float, c: float, gamma: int) -> float:
+    nr, na = _c(n_reached, np.int32), _c(n_accepted, np.int32)
+    return float(_load().oracle_depth_objective(_ptr(nr), _ptr(na), len(nr), float(alpha_prev), float(c),
+                                                int(gamma)))
+
+
+def choose_gamma_depth(n_reached, n_accepted, alpha_prev: float, c: float, gamma_min: int = 0,
+                       gamma_max: int = 8):
+    nr, na = _c(n_reached, np.int32), _c(n_accepted, np.int32)
+    ea = ctypes.c_double(0.0)
+    g = _load().oracle_choose_gamma_depth(_ptr(nr), _ptr(na), len(nr), float(alpha_prev), float(c),
+                                          int(gamma_min), int(gamma_max), ctypes.byref(ea))
+    return int(g), float(ea.value)

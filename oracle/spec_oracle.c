@@ -394,3 +394,71 @@ int32_t oracle_choose_gamma(double alpha_sum, int32_t alpha_count, double alpha_
     }
     return best;
 }
+
+/* ---- depth statistics ("M7.8 - Speculative Serving", 0x02D "Estimation Bias And Censoring" and
+ * 0x07B): a deeper position is observed only when every earlier draft was accepted, so its rate
+ * divides by the requests that reached it, not by the rounds. */
+void oracle_depth_counts(int32_t B, const int32_t *row_off, const int32_t *accept_len,
+                         const int32_t *req_status, int32_t depth_max, int32_t *n_reached,
+                         int32_t *n_accepted) {
+    for (int32_t j = 0; j < depth_max; ++j) n_reached[j] = n_accepted[j] = 0;
+    for (int32_t i = 0; i < B; ++i) {
+        if (req_status[i] != 0) continue;
+        const int32_t K = row_off[i + 1] - row_off[i] - 1, A = accept_len[i];
+        for (int32_t j = 1; j <= depth_max; ++j) {
+            if (K >= j && A >= j - 1) n_reached[j - 1] += 1;
+            if (A >= j) n_accepted[j - 1] += 1;
+        }
+    }
+}
+
+void oracle_depth_alpha(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                        double alpha_prev, int32_t n_out, double *alpha_hat) {
+    double sr = 0.0, sa = 0.0;
+    for (int32_t j = 0; j < depth_max; ++j) {
+        sr += (double)n_reached[j];
+        sa += (double)n_accepted[j];
+    }
+    const double pooled = sr > 0.0 ? sa / sr : alpha_prev;
+    for (int32_t j = 0; j < n_out; ++j) {
+        const int32_t r = j < depth_max ? n_reached[j] : 0;
+        alpha_hat[j] = r > 0 ? (double)n_accepted[j] / (double)r : pooled;
+    }
+}
+
+double oracle_depth_expected_accept(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                                    double alpha_prev, int32_t gamma) {
+    double ah[4096];
+    if (gamma > 4096) gamma = 4096;
+    oracle_depth_alpha(n_reached, n_accepted, depth_max, alpha_prev, gamma, ah);
+    double ea = 0.0, prod = 1.0;
+    for (int32_t j = 0; j < gamma; ++j) {
+        prod *= ah[j];
+        ea += prod;
+    }
+    return ea;
+}
+
+double oracle_depth_objective(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                              double alpha_prev, double c, int32_t gamma) {
+    const double ea = oracle_depth_expected_accept(n_reached, n_accepted, depth_max, alpha_prev, gamma);
+    return (1.0 + ea) / ((double)gamma * c + 1.0);
+}
+
+/* The same choice as oracle_choose_gamma (maximiser, ties to the smaller gamma) with E[A] from the
+ * per-depth rates in place of the constant-alpha closed form. */
+int32_t oracle_choose_gamma_depth(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                                  double alpha_prev, double c, int32_t gamma_min, int32_t gamma_max,
+                                  double *ea_out) {
+    int32_t best = gamma_min;
+    double best_f = oracle_depth_objective(n_reached, n_accepted, depth_max, alpha_prev, c, gamma_min);
+    for (int32_t g = gamma_min + 1; g <= gamma_max; ++g) {
+        const double f = oracle_depth_objective(n_reached, n_accepted, depth_max, alpha_prev, c, g);
+        if (f > best_f) {
+            best_f = f;
+            best = g;
+        }
+    }
+    if (ea_out) *ea_out = oracle_depth_expected_accept(n_reached, n_accepted, depth_max, alpha_prev, best);
+    return best;
+}

@@ -96,6 +96,27 @@ typedef struct {
 int oracle_compact(const oracle_compact_args *a);
 
 double oracle_gamma_objective(double alpha, double c, int32_t gamma);
+
+/* Depth statistics ("M7.8 - Speculative Serving", sections 0x02D and 0x07B): depth j = 1..depth_max
+ * of request i (no status bits) was reached when K_i >= j and its first j-1 drafts were accepted
+ * (A_i >= j-1), and accepted when A_i >= j. n_reached[j-1], n_accepted[j-1] count requests. */
+void oracle_depth_counts(int32_t B, const int32_t *row_off, const int32_t *accept_len,
+                         const int32_t *req_status, int32_t depth_max, int32_t *n_reached,
+                         int32_t *n_accepted);
+/* alpha_hat_j = n_accepted_j / n_reached_j (censoring-aware); a depth nobody reached takes the
+ * pooled estimate over all depths, and with no depth reached at all alpha_prev. j = 1..n_out. */
+void oracle_depth_alpha(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                        double alpha_prev, int32_t n_out, double *alpha_hat);
+/* Expected accepted drafts with gamma drafts, E[A] = sum_{j<=gamma} prod_{m<=j} alpha_hat_m, and
+ * the depth-aware objective (1 + E[A]) / (gamma*c + 1), which for a constant alpha_hat is
+ * oracle_gamma_objective. */
+double oracle_depth_expected_accept(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                                    double alpha_prev, int32_t gamma);
+double oracle_depth_objective(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                              double alpha_prev, double c, int32_t gamma);
+int32_t oracle_choose_gamma_depth(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                                  double alpha_prev, double c, int32_t gamma_min, int32_t gamma_max,
+                                  double *ea_out);
 int32_t oracle_choose_gamma(double alpha_sum, int32_t alpha_count, double alpha_prev, double c,
                             int32_t gamma_min, int32_t gamma_max, double *alpha_out);
 
