@@ -109,6 +109,12 @@ typedef struct {
        the per-position kernel, so a caller can time that kernel alone */
     cudaEvent_t rows_event_begin;
     cudaEvent_t rows_event_end;
+    /* depth statistics ("M7.8 - Speculative Serving", sections 0x02D and 0x07B; each may be
+       NULL): over the requests without status bits, depth j = 1..K_max (index j-1) was reached
+       when K_i >= j and the first j-1 drafts were accepted, and accepted when A_i >= j. Written
+       (not accumulated) by each call; the ratio is the censoring-aware acceptance rate. */
+    int32_t *depth_reached;      /* [K_max]                                                    */
+    int32_t *depth_accepted;     /* [K_max]                                                    */
 } spec_verify_args;
 
 /* Bytes of device workspace spec_verify needs for a batch of total_rows target rows.
@@ -184,6 +190,24 @@ spec_status spec_compact(const spec_compact_args *args, cudaStream_t stream);
  * gamma, as the controller of "M7.8 - Speculative Serving" section 0x07A breaks ties toward
  * smaller K) and the alpha it used to *alpha_out. All four pointers are device pointers. */
 double spec_gamma_objective(double alpha, double c, int32_t gamma);
+
+/* spec_choose_gamma with the per-depth rates in place of one alpha ("M7.8 - Speculative
+ * Serving", section 0x07B): alpha_hat_j = n_accepted[j-1] / n_reached[j-1] (device arrays of
+ * depth_max counts, as written by spec_verify); a depth nobody reached takes the pooled rate
+ * sum(n_accepted) / sum(n_reached), and with nothing reached alpha_prev. E[A](gamma) =
+ * sum_{j<=gamma} prod_{m<=j} alpha_hat_m; gamma maximises (1 + E[A]) / (gamma*c + 1) over
+ * [gamma_min, gamma_max] (ties to the smaller). Writes *gamma_out and *ea_out = E[A] at that gamma
+ * (device scalars). Runs on the device, one thread; SPEC_ERR_INVALID_ARG for a null output, a
+ * negative depth_max (or null counts with depth_max > 0), gamma_min < 0, gamma_max < gamma_min or
+ * > 4096, c < 0 or not finite, alpha_prev outside [0, 1]. */
+spec_status spec_choose_gamma_depth(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                                    double alpha_prev, double c, int32_t gamma_min, int32_t gamma_max,
+                                    int32_t *gamma_out, double *ea_out, cudaStream_t stream);
+
+/* Host, double precision: the objective (1 + E[A](gamma)) / (gamma*c + 1) of
+ * spec_choose_gamma_depth from HOST arrays of counts. */
+double spec_depth_objective(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                            double alpha_prev, double c, int32_t gamma);
 spec_status spec_choose_gamma(const double *alpha_sum, const int32_t *alpha_count,
                               double alpha_prev, double c, int32_t gamma_min, int32_t gamma_max,
                               int32_t *gamma_out, double *alpha_out, cudaStream_t stream);

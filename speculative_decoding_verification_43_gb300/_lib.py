@@ -47,6 +47,7 @@ class SpecVerifyArgs(ctypes.Structure):
         ("alpha_rows", _p), ("alpha_sum", _p), ("alpha_count", _p),
         ("rho_rows", _p), ("resid_rows", _p), ("frontier_prob", _p), ("frontier_margin", _p),
         ("fallback", _p), ("rows_event_begin", _p), ("rows_event_end", _p),
+        ("depth_reached", _p), ("depth_accepted", _p),
     ]
 
 
@@ -63,7 +64,8 @@ class SpecCompactArgs(ctypes.Structure):
 
 # every symbol include/spec_verify.h declares
 EXPORTS = ("spec_verify_workspace_size", "spec_verify", "spec_verify_noalloc", "spec_compact",
-           "spec_gamma_objective", "spec_choose_gamma", "spec_version")
+           "spec_gamma_objective", "spec_choose_gamma", "spec_choose_gamma_depth", "spec_depth_objective",
+           "spec_version")
 
 
 def _load():
@@ -84,6 +86,10 @@ def _load():
     lib.spec_gamma_objective.restype = ctypes.c_double
     lib.spec_choose_gamma.argtypes = [_p, _p, ctypes.c_double, ctypes.c_double, _i32, _i32, _p, _p, _p]
     lib.spec_choose_gamma.restype = ctypes.c_int
+    lib.spec_choose_gamma_depth.argtypes = [_p, _p, _i32, ctypes.c_double, ctypes.c_double, _i32, _i32, _p, _p, _p]
+    lib.spec_choose_gamma_depth.restype = ctypes.c_int
+    lib.spec_depth_objective.argtypes = [_p, _p, _i32, ctypes.c_double, ctypes.c_double, _i32]
+    lib.spec_depth_objective.restype = ctypes.c_double
     lib.spec_version.argtypes = []
     lib.spec_version.restype = ctypes.c_char_p
     return lib

@@ -50,6 +50,8 @@ class VerifyOutputs:
     frontier_prob: torch.Tensor | None = None
     frontier_margin: torch.Tensor | None = None
     fallback: torch.Tensor | None = None
+    depth_reached: torch.Tensor | None = None   # [K_max] requests that reached depth j
+    depth_accepted: torch.Tensor | None = None  # [K_max] requests that accepted depth j
 
 
 class Verifier:
@@ -72,7 +74,8 @@ class Verifier:
             out_tokens=torch.empty(total_rows, **i32), req_status=torch.empty(B, **i32),
             alpha_rows=torch.empty(nd, **f32),
             alpha_sum=torch.empty(1, dtype=torch.float64, device=device),
-            alpha_count=torch.empty(1, **i32))
+            alpha_count=torch.empty(1, **i32),
+            depth_reached=torch.empty(max(K_max, 1), **i32), depth_accepted=torch.empty(max(K_max, 1), **i32))
         if diagnostics:
             self.out.rho_rows = torch.empty(nd, **f32)
             self.out.resid_rows = torch.empty(nd, **f32)
@@ -88,7 +91,7 @@ class Verifier:
         o = self.out
         for name in ("accept_len", "n_emitted", "out_tokens", "req_status", "alpha_rows", "alpha_sum",
                      "alpha_count", "rho_rows", "resid_rows", "frontier_prob", "frontier_margin",
-                     "fallback"):
+                     "fallback", "depth_reached", "depth_accepted"):
             setattr(a, name, _ptr(getattr(o, name)))
         self._keep = ()
 
@@ -222,6 +225,34 @@ def choose_gamma(alpha_sum, alpha_count, alpha_prev: float, c: float, gamma_min:
                                int(gamma_min), int(gamma_max), _ptr(g), _ptr(a), _stream_handle(stream))
     check(rc, "spec_choose_gamma")
     return g, a
+
+
+def choose_gamma_depth(depth_reached, depth_accepted, alpha_prev: float, c: float, gamma_min: int = 0,
+                       gamma_max: int = 8, *, out=None, stream=None):
+    """Device-side gamma choice from per-depth counts (as spec_verify writes them); returns
+    (gamma int32[1], E[A] float64[1]) device tensors."""
+    dev = depth_reached.device
+    _i32(depth_reached)
+    _i32(depth_accepted)
+    assert depth_reached.numel() == depth_accepted.numel()
+    if out is None:
+        out = (torch.empty(1, dtype=torch.int32, device=dev), torch.empty(1, dtype=torch.float64, device=dev))
+    g, ea = out
+    rc = lib.spec_choose_gamma_depth(_ptr(depth_reached), _ptr(depth_accepted), int(depth_reached.numel()),
+                                     float(alpha_prev), float(c), int(gamma_min), int(gamma_max), _ptr(g),
+                                     _ptr(ea), _stream_handle(stream))
+    check(rc, "spec_choose_gamma_depth")
+    return g, ea
+
+
+def depth_objective(n_reached, n_accepted, alpha_prev: float, c: float, gamma: int) -> float:
+    """Host evaluation (double) of the depth-aware objective from host integer arrays."""
+    import numpy as np
+    nr = np.ascontiguousarray(n_reached, np.int32)
+    na = np.ascontiguousarray(n_accepted, np.int32)
+    assert nr.shape == na.shape
+    return float(lib.spec_depth_objective(nr.ctypes.data_as(ctypes.c_void_p), na.ctypes.data_as(ctypes.c_void_p),
+                                          int(nr.size), float(alpha_prev), float(c), int(gamma)))
 
 
 def gamma_objective(alpha: float, c: float, gamma: int) -> float:

@@ -1,5 +1,6 @@
 // Ragged compaction of a verified round (spec_compact) and the gamma controller
-// (spec_choose_gamma, spec_gamma_objective). See include/spec_verify.h for the contract.
+// (spec_choose_gamma, spec_gamma_objective, and their per-depth forms spec_choose_gamma_depth,
+// spec_depth_objective). See include/spec_verify.h for the contract.
 //
 // Compaction follows "M7.8 - Speculative Serving", sections 0x03C (L_out = P+A+1, L_kv = P+A;
 // positions stay contiguous, padding never becomes history) and 0x09 (with stopping:
@@ -166,6 +167,53 @@ __global__ void spec_gamma_kernel(const double *alpha_sum, const int32_t *alpha_
     *alpha_out = static_cast<double>(alpha.hi) + static_cast<double>(alpha.lo);
 }
 
+
+// Per-depth rates ("M7.8 - Speculative Serving", sections 0x02D and 0x07B): alpha_hat_j =
+// n_accepted_j / n_reached_j; a depth nobody reached takes the pooled rate over all depths, and
+// with no depth reached at all the previous estimate. E[A](gamma) = sum_{j<=gamma} prod_{m<=j}
+// alpha_hat_m replaces the constant-alpha sum in the objective (1 + E[A]) / (gamma*c + 1). One
+// thread, float pairs (no float64 arithmetic on the device).
+__device__ __forceinline__ F2 int_f2(int n) {
+    const float hi = static_cast<float>(n);
+    return f2_norm(hi, static_cast<float>(n - static_cast<int>(hi)));  // exact above 2^24 too
+}
+
+__global__ void spec_gamma_depth_kernel(const int32_t *n_reached, const int32_t *n_accepted, int depth_max,
+                                        float prev_hi, float prev_lo, float c_hi, float c_lo, int gmin, int gmax,
+                                        int32_t *gamma_out, double *ea_out) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    griddep_wait();
+    long long sr = 0, sa = 0;
+    for (int j = 0; j < depth_max; ++j) {
+        sr += n_reached[j];
+        sa += n_accepted[j];
+    }
+    const F2 pooled = sr > 0 ? f2_div(int_f2(static_cast<int>(sa)), int_f2(static_cast<int>(sr))) : F2{prev_hi, prev_lo};
+    const F2 c = {c_hi, c_lo};
+    F2 prod = {1.0f, 0.0f}, ea = {0.0f, 0.0f};
+    int best = -1;
+    F2 best_num = {0.0f, 0.0f}, best_den = {1.0f, 0.0f}, best_ea = {0.0f, 0.0f};
+    for (int g = 0; g <= gmax; ++g) {
+        if (g > 0) {
+            const int j = g - 1;
+            const int r = j < depth_max ? n_reached[j] : 0;
+            const F2 ah = r > 0 ? f2_div(int_f2(n_accepted[j]), int_f2(r)) : pooled;
+            prod = f2_mul(prod, ah);
+            ea = f2_add(ea, prod);
+        }
+        if (g < gmin) continue;
+        const F2 num = f2_add({1.0f, 0.0f}, ea);
+        const F2 den = f2_add(f2_mul({static_cast<float>(g), 0.0f}, c), {1.0f, 0.0f});
+        if (best < 0 || f2_gt(f2_mul(num, best_den), f2_mul(best_num, den))) {  // strict: a tie keeps the smaller
+            best = g;
+            best_num = num;
+            best_den = den;
+            best_ea = ea;
+        }
+    }
+    *gamma_out = best;
+    *ea_out = static_cast<double>(best_ea.hi) + static_cast<double>(best_ea.lo);
+}
 }  // namespace spec
 
 using namespace spec;
@@ -223,6 +271,41 @@ extern "C" spec_status spec_choose_gamma(const double *alpha_sum, const int32_t 
     const float ch = static_cast<float>(c), cl = static_cast<float>(c - static_cast<double>(ch));
     return launch_after(spec_gamma_kernel, dim3(1), dim3(32), stream, alpha_sum, alpha_count, ph, pl, ch, cl,
                         static_cast<int>(gamma_min), static_cast<int>(gamma_max), gamma_out, alpha_out) == cudaSuccess
+               ? SPEC_OK
+               : SPEC_ERR_CUDA;
+}
+
+// Host evaluation in double precision of the depth-aware objective (for tests and callers that
+// choose on the host). Host pointers.
+extern "C" double spec_depth_objective(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                                       double alpha_prev, double c, int32_t gamma) {
+    double sr = 0.0, sa = 0.0;
+    for (int j = 0; j < depth_max; ++j) {
+        sr += n_reached[j];
+        sa += n_accepted[j];
+    }
+    const double pooled = sr > 0.0 ? sa / sr : alpha_prev;
+    double prod = 1.0, ea = 0.0;
+    for (int j = 0; j < gamma; ++j) {
+        const int r = j < depth_max ? n_reached[j] : 0;
+        prod *= r > 0 ? static_cast<double>(n_accepted[j]) / r : pooled;
+        ea += prod;
+    }
+    return (1.0 + ea) / (gamma * c + 1.0);
+}
+
+extern "C" spec_status spec_choose_gamma_depth(const int32_t *n_reached, const int32_t *n_accepted, int32_t depth_max,
+                                               double alpha_prev, double c, int32_t gamma_min, int32_t gamma_max,
+                                               int32_t *gamma_out, double *ea_out, cudaStream_t stream) {
+    if (!gamma_out || !ea_out || depth_max < 0 || (depth_max > 0 && (!n_reached || !n_accepted)))
+        return SPEC_ERR_INVALID_ARG;
+    if (gamma_min < 0 || gamma_max < gamma_min || gamma_max > 4096) return SPEC_ERR_INVALID_ARG;
+    if (!(c >= 0.0) || !std::isfinite(c) || !(alpha_prev >= 0.0 && alpha_prev <= 1.0)) return SPEC_ERR_INVALID_ARG;
+    const float ph = static_cast<float>(alpha_prev), pl = static_cast<float>(alpha_prev - static_cast<double>(ph));
+    const float ch = static_cast<float>(c), cl = static_cast<float>(c - static_cast<double>(ch));
+    return launch_after(spec_gamma_depth_kernel, dim3(1), dim3(32), stream, n_reached, n_accepted,
+                        static_cast<int>(depth_max), ph, pl, ch, cl, static_cast<int>(gamma_min),
+                        static_cast<int>(gamma_max), gamma_out, ea_out) == cudaSuccess
                ? SPEC_OK
                : SPEC_ERR_CUDA;
 }

@@ -39,6 +39,7 @@ struct FinParams {
     int32_t *accept_len, *n_emitted, *out_tokens, *req_status, *fallback, *alpha_count;
     float *frontier_prob, *frontier_margin;
     double *alpha_sum;
+    int32_t *depth_reached, *depth_accepted;  // [K_max] each, or NULL
 };
 
 constexpr int kFinThreads = 1024;
@@ -47,8 +48,12 @@ __global__ void __launch_bounds__(kFinThreads) spec_select_kernel(const FinParam
     __shared__ float red_hi[kFinThreads / kWarp];
     __shared__ float red_lo[kFinThreads / kWarp];
     __shared__ int red_n[kFinThreads / kWarp];
+    // depth statistics ("M7.8 - Speculative Serving", 0x02D): requests that reached / accepted
+    // depth j = 1..K_max
+    __shared__ int hist_r[64], hist_a[64];
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     griddep_launch_dependents();
+    if (threadIdx.x < 64) hist_r[threadIdx.x] = hist_a[threadIdx.x] = 0;
     // Inputs first (they do not depend on the per-position kernel): the offsets must start at 0,
     // end at total_rows and grow by at least one row per request; otherwise every request is
     // BAD_SHAPE and nothing is read through them.
@@ -117,7 +122,12 @@ __global__ void __launch_bounds__(kFinThreads) spec_select_kernel(const FinParam
             if (j < n) tok = (j < A) ? __ldg(P.draft_tokens + d0 + j) : frontier;
             P.out_tokens[r0 + j] = tok;
         }
-        for (int j = lane; j < K; j += kWarp) asum = f2_add(asum, {P.alpha_ws[d0 + j], 0.0f});
+        for (int j = lane; j < K; j += kWarp) {
+            asum = f2_add(asum, {P.alpha_ws[d0 + j], 0.0f});
+            // depth j + 1 was reached when the first j drafts were accepted, accepted when j < A
+            if (P.depth_reached && j <= A) atomicAdd(&hist_r[j], 1);
+            if (P.depth_accepted && j < A) atomicAdd(&hist_a[j], 1);
+        }
         if (lane == 0) {
             acnt += K;
             P.req_status[i] = 0;
@@ -135,6 +145,10 @@ __global__ void __launch_bounds__(kFinThreads) spec_select_kernel(const FinParam
         red_n[warp] = acnt;
     }
     __syncthreads();
+    for (int j = threadIdx.x; j < P.K_max; j += kFinThreads) {
+        if (P.depth_reached) P.depth_reached[j] = hist_r[j];
+        if (P.depth_accepted) P.depth_accepted[j] = hist_a[j];
+    }
     if (warp == 0) {
         F2 a = {red_hi[lane], red_lo[lane]};
         int c = red_n[lane];
@@ -399,6 +413,8 @@ extern "C" spec_status spec_verify(const spec_verify_args *a, void *workspace, s
     F.frontier_prob = a->frontier_prob;
     F.frontier_margin = a->frontier_margin;
     F.alpha_sum = a->alpha_sum;
+    F.depth_reached = a->depth_reached;
+    F.depth_accepted = a->depth_accepted;
     if (launch_after(spec_select_kernel, dim3(1), dim3(kFinThreads), stream, F) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
 }

@@ -100,6 +100,37 @@ def test_gamma_objective_matches_oracle(lib):
         assert abs(got - want) <= 1e-14 * max(1.0, abs(want))
 
 
+def test_depth_objective_matches_oracle(lib):
+    import oracle
+    from speculative_decoding_verification_43_gb300 import api
+    rng = np.random.default_rng(1)
+    for _ in range(300):
+        D = int(rng.integers(0, 10))
+        nr = rng.integers(0, 50, size=D).astype(np.int32)
+        na = np.array([rng.integers(0, r + 1) for r in nr], np.int32)
+        nr[rng.random(D) < 0.2] = 0  # unobserved depths
+        na[nr == 0] = 0
+        prev = float(rng.random())
+        c = float(rng.random() * rng.choice([0.01, 0.3, 2.0]))
+        g = int(rng.integers(0, 16))
+        want = oracle.depth_objective(nr, na, prev, c, g)
+        got = api.depth_objective(nr, na, prev, c, g)
+        assert abs(got - want) <= 1e-13 * max(1.0, abs(want))
+
+
+def test_choose_gamma_depth_rejects_bad_arguments(lib):
+    fake = ctypes.c_void_p(16)
+    f = lib.lib.spec_choose_gamma_depth
+    assert f(fake, fake, 4, 0.5, 0.1, 0, 8, None, fake, None) == -1
+    assert f(fake, fake, 4, 0.5, 0.1, 0, 8, fake, None, None) == -1
+    assert f(None, fake, 4, 0.5, 0.1, 0, 8, fake, fake, None) == -1
+    assert f(fake, fake, -1, 0.5, 0.1, 0, 8, fake, fake, None) == -1
+    assert f(fake, fake, 4, 0.5, -1.0, 0, 8, fake, fake, None) == -1
+    assert f(fake, fake, 4, 0.5, 0.1, 5, 2, fake, fake, None) == -1
+    assert f(fake, fake, 4, 1.5, 0.1, 0, 8, fake, fake, None) == -1
+    assert f(fake, fake, 4, 0.5, 0.1, 0, 5000, fake, fake, None) == -1
+
+
 def test_workload_generator_is_seeded_and_shaped():
     from speculative_decoding_verification_43_gb300 import workloads as W
     wl = W.scaled(W.WORKLOADS["c3"], B=8, V=2048)

@@ -260,6 +260,40 @@ def test_choose_gamma_device_matches_oracle():
         assert abs(float(a.item()) - want_a) < 1e-12  # float-pair arithmetic on the device
 
 
+def test_depth_counts_and_depth_gamma():
+    """Per-depth counts written by spec_verify equal the censored counts of its own accept
+    lengths (requests with status bits excluded), and the device's depth-aware gamma choice
+    equals the oracle's on those counts and on constructed ones."""
+    wl = W.WORKLOADS["c3"]
+    rd = W.make_round(wl, seed=0, device="cuda")
+    temps = rd.temperature.clone()
+    temps[5] = -1.0  # a bad request: excluded from the counts
+    gpu = run_gpu(rd, temperature=temps)
+    ro = rd.row_off.cpu().numpy()
+    nr, na = oracle.depth_counts(ro, gpu["accept_len"], gpu["req_status"], 64)
+    assert gpu["req_status"][5] != 0
+    np.testing.assert_array_equal(gpu["depth_reached"], nr)
+    np.testing.assert_array_equal(gpu["depth_accepted"], na)
+    assert nr[0] > 0 and nr[7] == 0  # K_i <= 7 in this workload
+    cases = [(nr, na)]
+    rng = np.random.default_rng(3)
+    for _ in range(6):
+        D = int(rng.integers(1, 12))
+        r = rng.integers(0, 200, size=D).astype(np.int32)
+        r[rng.random(D) < 0.25] = 0
+        a = np.array([rng.integers(0, x + 1) for x in r], np.int32)
+        cases.append((r, a))
+    cases.append((np.zeros(4, np.int32), np.zeros(4, np.int32)))          # nothing observed
+    cases.append((np.array([64, 32, 16], np.int32), np.array([32, 16, 8], np.int32)))  # constant 1/2
+    for r, a in cases:
+        for prev, c, gmin, gmax in ((0.5, 0.05, 0, 8), (0.2, 0.3, 1, 12), (0.9, 0.01, 0, 20)):
+            g, ea = api.choose_gamma_depth(torch.as_tensor(r, device="cuda"), torch.as_tensor(a, device="cuda"),
+                                           prev, c, gmin, gmax)
+            og, oea = oracle.choose_gamma_depth(r, a, prev, c, gmin, gmax)
+            assert int(g.item()) == og, (r, a, prev, c)
+            assert abs(float(ea.item()) - oea) <= 1e-6 * max(1.0, oea)
+
+
 def test_compaction_bit_exact_c4():
     wl = W.WORKLOADS["c4"]
     rd = W.make_round(wl, seed=0, device="cuda")
