@@ -8,25 +8,24 @@
 // Work unit: one target row ("item"). Position j < K_i of request i is a pair (target row j,
 // draft row j); position K_i is the target-only row of the bonus (or plain) draw.
 //
-// A persistent thread-block cluster of C CTAs (one CTA per SM) walks a list of items. CTA c owns
-// the c-th 16-byte-aligned slice of the vocabulary of every row. Rows stream into a ring of
-// shared-memory slots by 1-D bulk copies, each logit exactly once. Each CTA has 15 data warps,
-// which hold the item's slice in registers, and one control warp, which issues the copies, runs
-// the exchange and makes every scalar decision. Per item:
-//   pass 1 (data warps): the slice moves from the ring into registers (the ring slots are free
-//           at once, and the next rows' copies start) and each thread sums 2^(y*s - b) with an
+// A persistent thread-block cluster of C CTAs (two CTAs per SM) walks a list of items. CTA c
+// owns the c-th 16-byte-aligned slice of the vocabulary of every row. Each CTA has 15 data warps
+// and one control warp.
+//   pass 1 (data warps): the item's rows arrive in a ring of shared-memory slots by 1-D bulk
+//           copies (issued by whichever data warp releases a slot last), the target row moves
+//           into registers (its slot refills at once), and each thread sums 2^(y*s - b) with an
 //           integral reference b of its own, so that combining threads, warps and CTAs is exact
 //           scaling by powers of two;
-//   exchange (control warp): the CTA's record (row statistics, the logits at the draft token,
-//           the alpha / residual totals of the previous item) goes into every CTA's shared
-//           memory, followed by an arrival on that CTA's barrier for the item; every CTA then
-//           computes the accept test identically;
-//   pass 2 (data warps, pairs, from registers): alpha = sum min(p, q) and, only where this
-//           position rejects, the residual max(p - q, 0) per chunk (32 contiguous vectors);
-//   draw (control warp, one item late): once the next exchange has brought every CTA's residual
-//           (or p) mass, the CTA whose slice holds u*Z fetches the one chunk that holds it with
-//           a small bulk copy and finds the token there.
-// Data and control warps meet at named barriers only; the data warps never wait on the cluster.
+//   exchange (control warp): the CTA's record (row statistics, the logits at the draft token, the
+//           alpha / residual totals of the previous item) goes into every CTA's shared memory with
+//           asynchronous stores completing on that CTA's barrier; every CTA then computes the
+//           accept test identically;
+//   pass 2 (data warps, pairs): from the same registers and slot: alpha = sum min(p, q) and, only
+//           where the position rejects, the residual max(p - q, 0) per chunk (32 vectors);
+//   draw (control warp): once an exchange has brought every CTA's residual (or p) mass, the CTA
+//           whose slice holds u*Z fetches the one chunk that holds it and finds the token there.
+// The roles meet at mbarriers keyed by item (statistics ready, decision ready): the control warp
+// finishes an item (its results and draw) while the data warps run the next one.
 // Every rejecting position prepares its own candidate (the first rejection is known only per
 // request); the selection kernel picks. Float math is packed two lanes per instruction; no
 // float64 instruction runs on the device (it is very slow on this part).
@@ -48,11 +47,11 @@ namespace spec {
 constexpr int kWarps = 15;                   // data warps
 constexpr int kThreads = kWarps * kWarp;     // data threads
 constexpr int kBlock = kThreads + kWarp;     // plus the control warp
-// named barriers between the data warps and the control warp (0 is __syncthreads)
-enum : int { BAR_FREE = 1, BAR_STATS = 2, BAR_DECIDED = 3, BAR_PASS2 = 4, BAR_BATCH = 5 };
+// named barrier (0 is __syncthreads): a batch's descriptors are loaded (all 512 threads)
+enum : int { BAR_BATCH = 1 };
 constexpr int kChunkVecs = kWarp;   // a chunk: 32 contiguous vectors, one per lane of a warp
 constexpr int kRing = 3;            // row slots per CTA
-constexpr int kMaxItems = 32;       // item descriptors held at once
+constexpr int kMaxItems = 32;       // item descriptors held at once (one batch)
 constexpr int kMaxCluster = 16;
 constexpr int kMaxNvt = 5;          // 16-byte vectors per thread per row
 constexpr int kMaxChunks = kMaxNvt * kWarps;
@@ -63,6 +62,18 @@ constexpr float kLog2eHi = 1.44269502162933349609375f;
 constexpr float kLog2eLo = 1.925963e-08f;
 
 enum : int32_t { REQ_TIMEOUT = 32 };  // internal: a bulk copy did not complete in time
+
+// The pipeline: an item's rows stay on chip from pass 1 to pass 2 (the target row in registers,
+// the draft row in its ring slot), so that nothing is read twice; the data warps wait for the
+// item's decision between the passes while the other CTA on the SM computes. The control warp
+// decides item g, signals it, and only then finishes item g - 1 (its results and draw), in the
+// shadow of pass 2. Ring depths of the per-item buffers:
+constexpr int kWS = 2;   // pass-1 statistics (read by the item's exchange)
+constexpr int kPM = 4;   // bonus-row chunk sums (read by the draw, one item later)
+constexpr int kRM = 3;   // pass-2 residual chunk sums and alpha partials (read one item later)
+constexpr int kND = 3;   // decisions (read by pass 2, the results and the draw)
+constexpr int kNMS = 3;  // exchange slots (a record is read again one exchange later)
+constexpr int kSB = 2;   // barriers: pass-1 statistics ready
 
 struct RowsParams {
     const void *target;
@@ -98,33 +109,32 @@ struct Desc {
     F2 u_acc, u_s;     // the position's accept draw and the request's frontier draw
 };
 
-// A CTA's message for item k, stored into slot k % 3 of every CTA of the cluster (distributed
-// shared memory, asynchronous stores that complete bytes on that CTA's barrier of the slot).
-// Twenty 32-bit words, 16-byte aligned: five vector stores per destination.
+// A CTA's record for item k, stored into exchange slot k % kNMS of every CTA of the cluster
+// (distributed shared memory, asynchronous stores that complete bytes on that CTA's barrier of
+// the slot). Sixteen 32-bit words, 16-byte aligned: four vector stores per destination. Sums are
+// plain floats: a record adds at most log2(16) + 4 roundings to sums of thousands of terms.
 struct __align__(16) Msg {
     float B[2];      // integral reference exponent of S[r] (-inf: no mass)
-    float S_hi[2];   // this slice's sum of 2^(y*s - B[r]), a float pair
-    float S_lo[2];
+    float S[2];      // this slice's sum of 2^(y*s - B[r])
     int32_t bad[2];  // a NaN / +inf was seen in row r
     float gmax[2];   // greedy rule: max logit of the slice and the smallest index attaining it
     int32_t garg[2];
     float yx[2];     // target / draft logit at the draft token, from the CTA that holds it
     int32_t has_x;
     int32_t tmo;       // a bulk copy of this CTA did not land in time
-    float prev_alpha;  // previous item: this slice's share of alpha (normalised)
-    float prev_Zhi;    // previous item: this slice's residual mass (units 2^B_t), a float pair
-    float prev_Zlo;
-    int32_t pad;
+    float prev_alpha;  // an earlier item: this slice's share of alpha (normalised)
+    float prev_Z;      // an earlier item: this slice's residual mass (units 2^B_t)
 };
 constexpr int kMsgBytes = sizeof(Msg);
-static_assert(kMsgBytes == 80, "a message is five 16-byte vectors");
+static_assert(kMsgBytes == 64, "a record is four 16-byte vectors");
 
 // The decision of an item, kept until its draw is finished (one item later).
 struct Decision {
     int32_t item, drow, pair, greedy, status, accept, kind, valid;
     float B_t, B_d, s_hi, s_lo, rho, inv_St;
     float c_t, c_d, c_tf, c_df;  // log2 of each row's normaliser: integral part, fraction
-    F2 S_t, S_d, lam, u_s;
+    float S_t, S_d;  // each row's sum of 2^(y*s - B) over the whole vocabulary
+    F2 lam, u_s;
     int32_t argmax_t;
     float alpha_g;  // greedy rule: alpha of the two point masses
 };
@@ -134,7 +144,7 @@ enum { SAMPLE_NONE = 0, SAMPLE_RESIDUAL = 1, SAMPLE_P = 2 };
 // Per-warp statistics of one row after pass 1.
 struct WarpStat {
     float B;  // integral reference (-inf: no mass)
-    float S_hi, S_lo;
+    float S;  // sum of 2^(y*s - B)
     float gmax;
     int32_t garg;
     int32_t bad;

@@ -5,28 +5,32 @@
 
 namespace spec {
 
-// Static shared state of one CTA. The row ring (dynamic shared memory) holds kRing slices.
+// Static shared state of one CTA. Dynamic shared memory holds the row ring (kRing slices) and the
+// exchange slots (kNMS x C records, written by every CTA of the cluster).
 struct CtaShared {
     uint64_t full[kRing];                 // a ring slot's bulk copy has landed
     uint64_t draw_bar;                    // the draw chunk's bulk copy has landed
-    uint64_t msg_bar[3];                  // all C records of the slot's item have arrived
-    Msg slot[3][kMaxCluster];             // exchange slots, written by every CTA of the cluster
+    uint64_t msg_bar[kNMS];               // all C records of an exchange have arrived
+    uint64_t stats_bar[kSB];              // pass 1 of an item (or, for the drain, the last pass 2)
+                                          // done: one arrival per data warp
+    uint64_t dec_bar[kND];                // the decision of an item is ready (control warp)
     Msg mine;
     Desc desc[kMaxItems];
-    WarpStat ws[2][kWarp];                // per-warp row statistics of the current item
-    float wal[kWarps];                    // per-warp alpha partials
-    float pm[3][kMaxChunks];              // target-row chunk sums (units 2^pref), by item number % 3
-    float pref[3][kMaxChunks];            // their integral reference exponents
-    float rm[2][kMaxChunks];              // residual chunk sums (units 2^B_t), by item parity
-    Decision dec[2];                      // by item parity
+    WarpStat ws[kWS][2][kWarps];          // per-warp row statistics, by item % kWS
+    float yx[kWS][2];                     // logits at the draft token, from the thread holding it
+    int32_t x_stamp[kWS];                 // item number + 1 when this CTA holds the draft token
+    float wal[kRM][kWarps];               // per-warp alpha partials, by item % kRM
+    float rm[kRM][kMaxChunks];            // residual chunk sums (units 2^B_t), by item % kRM
+    float pm[kPM][kMaxChunks];            // bonus-row chunk sums (units 2^pref), by item % kPM
+    float pref[kPM][kWarps];              // their integral reference exponents (one per warp)
+    Decision dec[kND];                    // by item % kND
     uint4 draw_buf[2][kChunkVecs];        // target / draft chunk of the pending draw
-    float yx[2];
-    int32_t x_stamp;                      // item number + 1 when this CTA holds the draft token
     int32_t timed_out;
-    float prev_alpha;                     // this slice's totals of the previous item
-    F2 prev_Z;
+    long long prod_issued;                // the producer (see release_row): rows copied; batch cursor
+    int32_t prod_item, prod_row;
+    int32_t free_cnt[kRing];              // data warps done with the row in each slot
     // the pending draw (owner CTA only)
-    int32_t draw_pending, draw_chunk, draw_count, draw_clamped, draw_kind, draw_item, draw_par;
+    int32_t draw_pending, draw_chunk, draw_count, draw_clamped, draw_kind, draw_item, draw_dec;
     float draw_lt, draw_unit, draw_bg, draw_invZ;
     uint32_t draw_phase;
 };
@@ -116,9 +120,9 @@ __device__ __forceinline__ int desc_rows(const Desc &d) {
     return (d.status & SPEC_REQ_BAD_SHAPE) ? 0 : (d.pair ? 2 : 1);
 }
 
-// Control warp, lane 0: issue the bulk copies of the cluster's row sequence up to row `limit`
-// (exclusive).
-// The sequence runs through the batch's items in order: target row, then draft row for a pair.
+// Data thread 0: issue the bulk copies of the cluster's row sequence up to row `limit`
+// (exclusive). The sequence runs through the batch's items in order: target row, then draft row
+// for a pair. Each row is read once (evict-first).
 __device__ __forceinline__ void produce_rows(CtaShared &sh, uint4 *ring, const RowsParams &P, int slice_max, int lo,
                                              int nvec, int nbatch, long long &issued, long long limit,
                                              int &cur_item, int &cur_row) {
@@ -144,18 +148,39 @@ __device__ __forceinline__ void produce_rows(CtaShared &sh, uint4 *ring, const R
     }
 }
 
+// A data warp is done with ring row `row` (its lanes' reads of the slot are complete): the last
+// of the 15 warps to get here refills the slot, issuing the copy of row + kRing. No warp waits
+// for another; successive releases of a slot are ordered by the copies they issue (a warp reaches
+// row + kRing only after the copy that the last release issued has landed).
+__device__ __forceinline__ void release_row(CtaShared &sh, uint4 *ring, const RowsParams &P, int slice_max, int lo,
+                                            int nvec, int nbatch, long long row, int lane) {
+    __syncwarp();
+    if (lane == 0) {
+        const int slot = static_cast<int>(row % kRing);
+        __threadfence_block();
+        if (atomicAdd(&sh.free_cnt[slot], 1) == kWarps - 1) {
+            sh.free_cnt[slot] = 0;
+            __threadfence_block();
+            fence_proxy_async_smem();
+            produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, sh.prod_issued, row + 1 + kRing, sh.prod_item,
+                         sh.prod_row);
+        }
+    }
+}
+
 // Whether warp `warp` has any vector v of the slice (its 32 vectors start at v * 480 + 32 warp):
 // warps past the slice end skip the vector altogether (a warp-uniform branch).
 __device__ __forceinline__ bool warp_has(int v, int warp, int nvec) { return v * kThreads + warp * kWarp < nvec; }
 
-// A row of the item as pass 1 and pass 2 see it: vector v of thread t is vector t + 480 v of the
-// slice (a warp covers 32 contiguous vectors, a chunk). The target row is held in registers; the
-// draft row stays in its ring slot (so that only one row occupies registers).
+// A row of the item as pass 1 sees it, in registers: vector v of thread t is vector t + 480 v of
+// the slice (a warp covers 32 contiguous vectors, a chunk).
 template <int NVT>
 struct RegRow {
     const uint4 (&vv)[NVT];
     __device__ __forceinline__ uint4 operator()(int v) const { return vv[v]; }
 };
+// The draft row as pass 1 sees it: in its ring slot, vector v of thread t at t + 480 v; past the
+// slice end, -inf.
 template <int DT>
 struct SmemRow {
     const uint4 *src;
@@ -234,7 +259,7 @@ __device__ __forceinline__ float sweep_sums(const Row &row, float s_hi, float2 s
 // a row that a draw from p may need (CHUNKS), also the per-chunk sums (chunk (v, warp), units
 // 2^B_w with B_w the warp's reference).
 template <int DT, int NVT, bool CHUNKS, class Row>
-__device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int r, int pb, const Desc &d, int lo,
+__device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int wb, int r, int pb, const Desc &d, int lo,
                                           int nvec, int warp, int lane, int tid) {
     constexpr int E = Elt<DT>::kPerVec;
     constexpr int H = E / 2;
@@ -270,9 +295,9 @@ __device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int r, 
         const int widx = warp_min_i32(best == wbest ? bidx : INT_MAX);
         const int wbad = __any_sync(0xffffffffu, bad);
         if (lane == 0) {
-            sh.ws[r][warp].gmax = wbest;
-            sh.ws[r][warp].garg = widx;
-            sh.ws[r][warp].bad = wbad;
+            sh.ws[wb][r][warp].gmax = wbest;
+            sh.ws[wb][r][warp].garg = widx;
+            sh.ws[wb][r][warp].bad = wbad;
         }
         return;
     }
@@ -289,42 +314,39 @@ __device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int r, 
 #pragma unroll
         for (int v = 0; v < NVT; ++v) {
             const float c = warp_sum(ok ? sv[CHUNKS ? v : 0] * scale : 0.0f);
-            if (lane == 0) {
-                sh.pm[pb][v * kWarps + warp] = c;
-                sh.pref[pb][v * kWarps + warp] = Bw;
-            }
+            if (lane == 0) sh.pm[pb][v * kWarps + warp] = c;
         }
     }
     if (lane == 0) {
-        sh.ws[r][warp].B = Bw;
-        sh.ws[r][warp].S_hi = Sw;
-        sh.ws[r][warp].S_lo = 0.0f;
-        sh.ws[r][warp].bad = bad;
+        if (CHUNKS) sh.pref[pb][warp] = Bw;
+        sh.ws[wb][r][warp].B = Bw;
+        sh.ws[wb][r][warp].S = Sw;
+        sh.ws[wb][r][warp].bad = bad;
     }
 }
 
 // A warp's statistics of one row from each thread's sum s at its reference b.
-__device__ __forceinline__ void warp_row_stats(CtaShared &sh, int r, int warp, int lane, float s, float b) {
+__device__ __forceinline__ void warp_row_stats(CtaShared &sh, int wb, int r, int warp, int lane, float s, float b) {
     const bool ok = s > 0.0f && !isinf(s);  // NaN, inf and empty are not ok
     const int bad = __any_sync(0xffffffffu, !(s >= 0.0f) || isinf(s));
     const float Bw = warp_max(ok ? b : -INFINITY);
     const float Sw = warp_sum(ok ? s * pow2i(b - Bw) : 0.0f);
     if (lane == 0) {
-        sh.ws[r][warp].B = Bw;
-        sh.ws[r][warp].S_hi = Sw;
-        sh.ws[r][warp].S_lo = 0.0f;
-        sh.ws[r][warp].bad = bad;
+        sh.ws[wb][r][warp].B = Bw;
+        sh.ws[wb][r][warp].S = Sw;
+        sh.ws[wb][r][warp].bad = bad;
     }
 }
 
-// Pass 1 of a pair under Rule 2 (target in registers, draft in its ring slot).
+// Pass 1 of a pair under Rule 2: the target row in registers, the draft row in its ring slot, in
+// one loop over both (the draft's loads and the target's exponentials hide each other's latency;
+// both rows in registers would not fit 64 registers). References from each thread's first vectors
+// (see sweep_sums).
 template <int DT, int NVT>
-__device__ __forceinline__ void pair_stats(const uint4 (&vt)[NVT], const SmemRow<DT> &rd, CtaShared &sh,
+__device__ __forceinline__ void pair_stats(const uint4 (&vt)[NVT], const SmemRow<DT> &rd, CtaShared &sh, int wb,
                                            const Desc &d, int nvec, int warp, int lane) {
     constexpr int H = Elt<DT>::kPerVec / 2;
     const float2 shi2 = f2splat(d.s_hi), slo2 = f2splat(d.s_lo);
-    // one loop over both rows: the loads of the draft row and the exponentials of the target row
-    // hide each other's latency. References from each thread's first vectors (see sweep_sums).
     const bool h0 = warp_has(0, warp, nvec);
     float bt = floorf((h0 ? Elt<DT>::vmax(vt[0]) : -INFINITY) * d.s_hi);
     float bd = floorf((h0 ? Elt<DT>::vmax(rd(0)) : -INFINITY) * d.s_hi);
@@ -346,138 +368,135 @@ __device__ __forceinline__ void pair_stats(const uint4 (&vt)[NVT], const SmemRow
         sd = qa.x + qa.y;
     }
     float none[1];
-    if (__any_sync(0xffffffffu, !(st <= 0x1p64f))) st = exact_sums<DT, NVT, false>(RegRow<NVT>{vt}, d.s_hi, shi2, slo2, warp, nvec, bt, none);
-    if (__any_sync(0xffffffffu, !(sd <= 0x1p64f))) sd = exact_sums<DT, NVT, false>(rd, d.s_hi, shi2, slo2, warp, nvec, bd, none);
-    warp_row_stats(sh, 0, warp, lane, st, bt);
-    warp_row_stats(sh, 1, warp, lane, sd, bd);
+    if (__any_sync(0xffffffffu, !(st <= 0x1p64f)))
+        st = exact_sums<DT, NVT, false>(RegRow<NVT>{vt}, d.s_hi, shi2, slo2, warp, nvec, bt, none);
+    if (__any_sync(0xffffffffu, !(sd <= 0x1p64f)))
+        sd = exact_sums<DT, NVT, false>(rd, d.s_hi, shi2, slo2, warp, nvec, bd, none);
+    warp_row_stats(sh, wb, 0, warp, lane, st, bt);
+    warp_row_stats(sh, wb, 1, warp, lane, sd, bd);
 }
 
-// Control warp: this CTA's message for item n: its row statistics over the data warps (lane w
-// takes warp w, both rows) and the logits at the draft token if it holds them (the previous
-// item's totals are already in place).
-__device__ __forceinline__ void build_message(CtaShared &sh, int greedy, int nr, int n, int lane) {
-    Msg &msg = sh.mine;
-    const bool on = lane < kWarps;
+// Sum over the 16-lane half of the warp (xor steps 8, 4, 2, 1; each half sums its own lanes).
+__device__ __forceinline__ float half_sum(float v) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const bool use = on && r < nr;
-        const WarpStat &st = sh.ws[r][on ? lane : 0];
-        int bad = use ? st.bad : 0;
-        float B = -INFINITY, gmax = -INFINITY;
-        int garg = INT_MAX;
-        F2 S = {0.0f, 0.0f};
-        if (greedy) {
-            gmax = use ? st.gmax : -INFINITY;
-            garg = use ? st.garg : INT_MAX;
-        } else {
-            const float Sw = use ? st.S_hi : 0.0f;
-            const float Bw = use ? st.B : -INFINITY;
-            B = warp_max(Sw > 0.0f ? Bw : -INFINITY);
-            S = warp_sum_f2(Sw > 0.0f ? F2{Sw * pow2i(Bw - B), 0.0f} : F2{0.0f, 0.0f});
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float half_max(float v) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+// Greedy rule: the larger logit, ties to the smaller index, over lanes xor o (o < n).
+__device__ __forceinline__ void half_argmax(float &gm, int &ga, int n) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1)
+        if (o < n) {
+            const float og = __shfl_xor_sync(0xffffffffu, gm, o);
+            const int oa = __shfl_xor_sync(0xffffffffu, ga, o);
+            if (og > gm || (og == gm && oa < ga)) {
+                gm = og;
+                ga = oa;
+            }
         }
-        bad = __any_sync(0xffffffffu, bad);
-        if (greedy) {
-            const float wbest = warp_max(gmax);
-            garg = warp_min_i32(gmax == wbest ? garg : INT_MAX);
-            gmax = wbest;
-        }
-        if (lane == 0) {
-            msg.B[r] = B;
-            msg.S_hi[r] = S.hi;
-            msg.S_lo[r] = S.lo;
-            msg.bad[r] = bad;
-            msg.gmax[r] = gmax;
-            msg.garg[r] = garg;
-        }
-    }
-    if (lane == 0) {
-        msg.has_x = (sh.x_stamp == n + 1) ? 1 : 0;
-        msg.yx[0] = sh.yx[0];
-        msg.yx[1] = sh.yx[1];
-        msg.tmo = sh.timed_out;
-    }
 }
 
-// Control warp, once pass 2 of item n is done: this slice's alpha share and residual mass of the
-// item, for the next message.
-__device__ __forceinline__ void stash_totals(CtaShared &sh, int n, int nch, int lane) {
-    const float pa = warp_sum(lane < kWarps ? sh.wal[lane] : 0.0f);
-    F2 pz = {0.0f, 0.0f};
-    if (sh.dec[n & 1].kind == SAMPLE_RESIDUAL) {
+// Control warp: this CTA's record for item g, its row statistics over the data warps (row r in
+// lanes 16r .. 16r + 14, lane 16r + w taking warp w: the max reference, then the sums scaled to
+// it by exact powers of two), the logits at the draft token if it holds them, and the totals of
+// item m (its alpha share, summed alongside, and its residual mass; m < 0: none). nr = 0: no
+// item (a draining exchange).
+__device__ __forceinline__ void build_record(CtaShared &sh, int greedy, int nr, int g, int m, int nch, int lane) {
+    Msg &msg = sh.mine;
+    const int wb = g % kWS, r = lane >> 4, w = lane & 15;
+    const bool use = w < kWarps && r < nr;
+    const WarpStat &st = sh.ws[wb][r][use ? w : 0];
+    const int rb = m >= 0 ? m % kRM : 0;
+    const float pa = (m >= 0 && r == 0 && w < kWarps) ? sh.wal[rb][w] : 0.0f;
+    const unsigned badm = __ballot_sync(0xffffffffu, use && st.bad);
+    const int bad = (badm >> (16 * r)) & 0xffffu ? 1 : 0;
+    float B = -INFINITY, S = 0.0f, gmax = -INFINITY;
+    int garg = INT_MAX;
+    if (greedy) {
+        gmax = use ? st.gmax : -INFINITY;
+        garg = use ? st.garg : INT_MAX;
+        half_argmax(gmax, garg, 16);
+    } else {
+        const float Sw = use ? st.S : 0.0f;
+        const float Bw = Sw > 0.0f ? st.B : -INFINITY;
+        B = half_max(Bw);
+        S = Sw > 0.0f ? Sw * pow2i(Bw - B) : 0.0f;
+    }
+    S = half_sum(S);
+    const float alpha = half_sum(pa);
+    float pz = 0.0f;
+    if (m >= 0 && sh.dec[m % kND].kind == SAMPLE_RESIDUAL) {
 #pragma unroll 1
-        for (int k = lane; k < nch; k += kWarp) pz = f2_add(pz, {sh.rm[n & 1][k], 0.0f});
-        pz = warp_sum_f2(pz);
+        for (int k = lane; k < nch; k += kWarp) pz += sh.rm[rb][k];
+        pz = warp_sum(pz);
+    }
+    if (w == 0) {
+        msg.B[r] = B;
+        msg.S[r] = S;
+        msg.bad[r] = bad;
+        msg.gmax[r] = gmax;
+        msg.garg[r] = garg;
     }
     if (lane == 0) {
-        sh.mine.prev_alpha = pa;
-        sh.mine.prev_Zhi = pz.hi;
-        sh.mine.prev_Zlo = pz.lo;
+        const bool hx = nr > 0 && sh.x_stamp[wb] == g + 1;
+        msg.has_x = hx ? 1 : 0;
+        msg.yx[0] = hx ? sh.yx[wb][0] : 0.0f;
+        msg.yx[1] = hx ? sh.yx[wb][1] : 0.0f;
+        msg.tmo = sh.timed_out;
+        msg.prev_alpha = alpha;
+        msg.prev_Z = pz;
     }
 }
 
-// Control warp, after the exchange of item n: combine the C records (lanes 0-15 take row 0,
+// Control warp, after the exchange of item g: combine the C records (lanes 0-15 take row 0,
 // lanes 16-31 row 1, one lane per CTA, in CTA order; C is a power of two, so log2(C) butterfly
-// steps combine them) and decide the accept test. The scalar tail is spread over four lanes: the
-// accept test (lane 0), lambda (lane 1), log2 of the two normalisers (lanes 2, 3). Every CTA runs
-// the same reductions on the same records, so all reach the same decision.
-__device__ __forceinline__ void decide_item(CtaShared &sh, const Desc &d, int nr, int n, int C, const RowsParams &P,
-                                            int lane) {
-    const Msg *M = sh.slot[n % 3];
+// steps combine them) and decide the accept test. Every lane then computes the whole scalar tail
+// (the test, lambda, the log2 of both normalisers): independent chains that the compiler
+// interleaves, where a split over lanes would run them one after the other. Every CTA runs the
+// same reductions on the same records, so all reach the same decision.
+__device__ __forceinline__ void decide_item(CtaShared &sh, const Msg *M, const Desc &d, int nr, int g, int C,
+                                            const RowsParams &P, int lane) {
     const int r = lane >> 4, c = lane & 15;
     const bool on = c < C && r < nr;
     const Msg &m = M[c < C ? c : 0];
     const unsigned tmo = __ballot_sync(0xffffffffu, r == 0 && c < C && m.tmo);
     const unsigned hx = __ballot_sync(0xffffffffu, r == 0 && c < C && m.has_x);
-    float yx_t = 0.0f, yx_d = 0.0f;
-    if (hx) {
-        const int l = 31 - __clz(static_cast<int>(hx));
-        yx_t = __shfl_sync(0xffffffffu, m.yx[0], l);
-        yx_d = __shfl_sync(0xffffffffu, m.yx[1], l);
-    }
-    int bad = on ? m.bad[r] : 0;
-    float Bv = -INFINITY, gm = -INFINITY;
+    const unsigned badm = __ballot_sync(0xffffffffu, on && m.bad[r]);
+    const int lx = hx ? 31 - __clz(static_cast<int>(hx)) : 0;
+    const float yx_t = __shfl_sync(0xffffffffu, m.yx[0], lx), yx_d = __shfl_sync(0xffffffffu, m.yx[1], lx);
+    float Bv = -INFINITY, S = 0.0f, gm = -INFINITY;
     int ga = INT_MAX;
-    F2 S = {0.0f, 0.0f};
     if (d.greedy) {
         gm = on ? m.gmax[r] : -INFINITY;
         ga = on ? m.garg[r] : INT_MAX;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1)
-            if (o < C) {
-                bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-                const float og = __shfl_xor_sync(0xffffffffu, gm, o);
-                const int oa = __shfl_xor_sync(0xffffffffu, ga, o);
-                if (og > gm || (og == gm && oa < ga)) {
-                    gm = og;
-                    ga = oa;
-                }
-            }
+        half_argmax(gm, ga, C);
     } else {
-        const float Sh = on ? m.S_hi[r] : 0.0f;
-        const bool has = Sh > 0.0f;
-        const float Bc = on ? m.B[r] : -INFINITY;
-        Bv = has ? Bc : -INFINITY;
+        const float Sc = on ? m.S[r] : 0.0f;
+        const float Bc = Sc > 0.0f ? m.B[r] : -INFINITY;
+        Bv = Bc;
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1)
-            if (o < C) {
-                bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-                Bv = fmaxf(Bv, __shfl_xor_sync(0xffffffffu, Bv, o));
-            }
-        S = has ? f2_scale({Sh, m.S_lo[r]}, Bc - Bv) : F2{0.0f, 0.0f};
+            if (o < C) Bv = fmaxf(Bv, __shfl_xor_sync(0xffffffffu, Bv, o));
+        S = Sc > 0.0f ? Sc * pow2i(Bc - Bv) : 0.0f;
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1)
-            if (o < C) S = f2_add(S, {__shfl_xor_sync(0xffffffffu, S.hi, o), __shfl_xor_sync(0xffffffffu, S.lo, o)});
+            if (o < C) S += __shfl_xor_sync(0xffffffffu, S, o);
     }
     // rows 0 and 1 from lanes 0 and 16, to every lane
-    const int bad0 = __shfl_sync(0xffffffffu, bad, 0), bad1 = __shfl_sync(0xffffffffu, bad, 16);
+    const int bad0 = (badm & 0xffffu) != 0, bad1 = (badm >> 16) != 0;
     const float B0 = __shfl_sync(0xffffffffu, Bv, 0), B1 = __shfl_sync(0xffffffffu, Bv, 16);
-    const F2 S0 = shfl_f2(S, 0), S1 = shfl_f2(S, 16);
+    const float S0 = __shfl_sync(0xffffffffu, S, 0), S1 = __shfl_sync(0xffffffffu, S, 16);
     const float gm0 = __shfl_sync(0xffffffffu, gm, 0), gm1 = __shfl_sync(0xffffffffu, gm, 16);
     const int ga0 = __shfl_sync(0xffffffffu, ga, 0), ga1 = __shfl_sync(0xffffffffu, ga, 16);
     const int am0 = (nr >= 1 && !(bad0 || gm0 == -INFINITY)) ? ga0 : -1;
     const int am1 = (nr >= 2 && !(bad1 || gm1 == -INFINITY)) ? ga1 : -1;
     const float B_t = (nr >= 1) ? (bad0 ? NAN : B0) : NAN, B_d = (nr >= 2) ? (bad1 ? NAN : B1) : NAN;
-    const F2 S_t = (nr >= 1) ? S0 : F2{0.0f, 0.0f}, S_d = (nr >= 2) ? S1 : F2{0.0f, 0.0f};
+    const float S_t = (nr >= 1) ? S0 : 0.0f, S_d = (nr >= 2) ? S1 : 0.0f;
     // the status, the same in every lane; row validity is reported together with a bad proposal
     // (both are preconditions)
     int status = d.status | (tmo ? REQ_TIMEOUT : 0);
@@ -486,27 +505,52 @@ __device__ __forceinline__ void decide_item(CtaShared &sh, const Desc &d, int nr
             if (am0 < 0 || (d.pair && am1 < 0)) status |= SPEC_REQ_BAD_LOGITS;
             if (d.pair && (d.x < 0 || d.x >= P.V)) status |= SPEC_REQ_BAD_PROPOSAL;
         } else {
-            const bool ok_t = isfinite(B_t) && S_t.hi > 0.0f && isfinite(S_t.hi);
-            const bool ok_d = !d.pair || (isfinite(B_d) && S_d.hi > 0.0f && isfinite(S_d.hi));
+            const bool ok_t = isfinite(B_t) && S_t > 0.0f && isfinite(S_t);
+            const bool ok_d = !d.pair || (isfinite(B_d) && S_d > 0.0f && isfinite(S_d));
             if (!ok_t || !ok_d) status |= SPEC_REQ_BAD_LOGITS;
             // q(x) == 0 is a bad proposal for Rule 2 (checked before any draw)
             if (d.pair && (d.x < 0 || d.x >= P.V || yx_d == -INFINITY)) status |= SPEC_REQ_BAD_PROPOSAL;
         }
     }
-    Decision &D = sh.dec[n & 1];
-    const bool rule2 = status == 0 && !d.greedy;
-    if (lane == 1 && rule2) {
-        D.inv_St = rcp_approx(S_t.hi);
-        if (d.pair) D.lam = f2_div(S_t, S_d);
-    } else if (lane == 2 && rule2 && d.pair) {
-        const float2 ct = log2_split(S_t, B_t);
-        D.c_t = ct.x;
-        D.c_tf = ct.y;
-    } else if (lane == 3 && rule2 && d.pair) {
-        const float2 cd = log2_split(S_d, B_d);
-        D.c_d = cd.x;
-        D.c_df = cd.y;
-    } else if (lane == 0) {
+    // the scalar tail in every lane (values of rows that are not there are computed and unused)
+    const float inv_St = rcp_approx(S_t);
+    const F2 lam = f2_div({S_t, 0.0f}, {S_d, 0.0f});
+    const float2 ct = log2_split({S_t, 0.0f}, B_t), cd = log2_split({S_d, 0.0f}, B_d);
+    int accept = 0, kind = SAMPLE_NONE, argmax_t = -1;
+    float rho = 0.0f, alpha_g = 0.0f;
+    if (status == 0) {
+        if (d.greedy) {
+            argmax_t = am0;
+            if (d.pair) {
+                accept = (d.x == am0);
+                rho = accept ? 1.0f : 0.0f;
+                alpha_g = (am0 == am1) ? 1.0f : 0.0f;
+            }
+        } else if (d.pair) {
+            // rho = p(x)/q(x) = 2^E * S_d/S_t with E = (y_t - y_d) s - (B_t - B_d), in float
+            // pairs; 2^E from ex2 of its fraction and an exact power of two
+            if (yx_t != -INFINITY) {
+                F2 Ex = f2_mul(f2_add({yx_t, 0.0f}, {-yx_d, 0.0f}), {d.s_hi, d.s_lo});
+                Ex = f2_add(Ex, {-(B_t - B_d), 0.0f});
+                const float nn = floorf(Ex.hi);
+                const float f = (Ex.hi - nn) + Ex.lo;
+                const F2 ratio = f2_div({S_d, 0.0f}, {S_t, 0.0f});
+                const float mm = ex2(f) * (ratio.hi + ratio.lo);
+                if (nn > 254.0f) {
+                    rho = INFINITY;
+                } else if (nn >= -252.0f) {
+                    const float h = floorf(0.5f * nn);
+                    rho = mm * pow2i(h) * pow2i(nn - h);
+                }
+            }
+            accept = (rho > 0.0f) && !f2_gt(d.u_acc, {rho, 0.0f});
+            if (!accept) kind = SAMPLE_RESIDUAL;
+        } else {
+            kind = SAMPLE_P;
+        }
+    }
+    if (lane == 0) {
+        Decision &D = sh.dec[g % kND];
         D.item = d.item;
         D.drow = d.drow;
         D.pair = d.pair;
@@ -519,41 +563,14 @@ __device__ __forceinline__ void decide_item(CtaShared &sh, const Desc &d, int nr
         D.B_d = B_d;
         D.S_t = S_t;
         D.S_d = S_d;
-        int accept = 0, kind = SAMPLE_NONE;
-        float rho = 0.0f;
-        D.argmax_t = -1;
-        D.alpha_g = 0.0f;
-        if (status == 0) {
-            if (d.greedy) {
-                D.argmax_t = am0;
-                if (d.pair) {
-                    accept = (d.x == am0);
-                    rho = accept ? 1.0f : 0.0f;
-                    D.alpha_g = (am0 == am1) ? 1.0f : 0.0f;
-                }
-            } else if (d.pair) {
-                // rho = p(x)/q(x) = 2^E * S_d/S_t with E = (y_t - y_d) s - (B_t - B_d), in float
-                // pairs; 2^E from ex2 of its fraction and an exact power of two
-                if (yx_t != -INFINITY) {
-                    F2 Ex = f2_mul(f2_add({yx_t, 0.0f}, {-yx_d, 0.0f}), {d.s_hi, d.s_lo});
-                    Ex = f2_add(Ex, {-(B_t - B_d), 0.0f});
-                    const float nn = floorf(Ex.hi);
-                    const float f = (Ex.hi - nn) + Ex.lo;
-                    const F2 ratio = f2_div(S_d, S_t);
-                    const float mm = ex2(f) * (ratio.hi + ratio.lo);
-                    if (nn > 254.0f) {
-                        rho = INFINITY;
-                    } else if (nn >= -252.0f) {
-                        const float h = floorf(0.5f * nn);
-                        rho = mm * pow2i(h) * pow2i(nn - h);
-                    }
-                }
-                accept = (rho > 0.0f) && !f2_gt(d.u_acc, {rho, 0.0f});
-                if (!accept) kind = SAMPLE_RESIDUAL;
-            } else {
-                kind = SAMPLE_P;
-            }
-        }
+        D.inv_St = inv_St;
+        D.lam = lam;
+        D.c_t = ct.x;
+        D.c_tf = ct.y;
+        D.c_d = cd.x;
+        D.c_df = cd.y;
+        D.argmax_t = argmax_t;
+        D.alpha_g = alpha_g;
         D.rho = rho;
         D.accept = accept;
         D.kind = kind;
@@ -561,13 +578,15 @@ __device__ __forceinline__ void decide_item(CtaShared &sh, const Desc &d, int nr
     }
 }
 
-// Pass 2 of a pair under Rule 2, from the registers of pass 1. Where the position rejects:
+// Pass 2 of a pair under Rule 2, from the registers and the ring slot of pass 1. Thread t takes
+// vectors t + 480 v of the slice, as in pass 1. Where the position rejects:
 // e_t = 2^(y_t s - B_t), e_d = 2^(y_d s - B_d), lambda = S_t / S_d; the residual
 // max(e_t - lambda e_d, 0) per chunk and S_t * min(p, q) = min(e_t, lambda e_d) (no
-// cancellation). Where it accepts, only alpha: min(p, q) = 2^min(y_t s - c_t, y_d s - c_d), c = log2 of the normaliser.
+// cancellation). Where it accepts, only alpha: min(p, q) = 2^min(y_t s - c_t, y_d s - c_d), c the
+// log2 of the normaliser.
 template <int DT, int NVT>
 __device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> &rd, CtaShared &sh,
-                                      const Decision &D, int par, int warp, int lane, int tid) {
+                                      const Decision &D, int rb, int warp, int lane) {
     constexpr int H = Elt<DT>::kPerVec / 2;
     float my_alpha = 0.0f;
     if (D.status == 0 && D.pair && !D.greedy) {
@@ -579,7 +598,7 @@ __device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> 
 #pragma unroll
             for (int v = 0; v < NVT; ++v) {
                 if (!warp_has(v, warp, rd.nvec)) {
-                    if (lane == 0) sh.rm[par][v * kWarps + warp] = 0.0f;
+                    if (lane == 0) sh.rm[rb][v * kWarps + warp] = 0.0f;
                     continue;
                 }
                 const uint4 wd = rd(v);
@@ -595,7 +614,7 @@ __device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> 
                     acc_a = __fadd2_rn(acc_a, make_float2(fminf(et.x, -nq.x), fminf(et.y, -nq.y)));
                 }
                 const float rs = warp_sum(racc.x + racc.y);
-                if (lane == 0) sh.rm[par][v * kWarps + warp] = rs;
+                if (lane == 0) sh.rm[rb][v * kWarps + warp] = rs;
             }
             my_alpha = (acc_a.x + acc_a.y) * D.inv_St;
         } else {
@@ -619,7 +638,7 @@ __device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> 
         }
     }
     my_alpha = warp_sum(my_alpha);
-    if (lane == 0) sh.wal[warp] = my_alpha;
+    if (lane == 0) sh.wal[rb][warp] = my_alpha;
 }
 
 // The draw weights of one vector, exactly as the passes summed them: the residual in units of
@@ -657,9 +676,8 @@ __device__ __forceinline__ void draw_weights(int kind, const uint4 &wt, const ui
 
 // Mass of CTA c's slice in the law a draw of item m uses (units 2^B_t).
 __device__ __forceinline__ F2 cta_mass(const Msg &Mi, const Msg &Mn, int kind, float B_t) {
-    if (kind == SAMPLE_RESIDUAL) return {Mn.prev_Zhi, Mn.prev_Zlo};
-    const F2 Sc = {Mi.S_hi[0], Mi.S_lo[0]};
-    return Sc.hi > 0.0f ? f2_scale(Sc, Mi.B[0] - B_t) : F2{0.0f, 0.0f};
+    if (kind == SAMPLE_RESIDUAL) return {Mn.prev_Z, 0.0f};
+    return Mi.S[0] > 0.0f ? F2{Mi.S[0] * pow2i(Mi.B[0] - B_t), 0.0f} : F2{0.0f, 0.0f};
 }
 
 // What the control warp knows about item m's draw after the exchange that carries its totals.
@@ -668,14 +686,13 @@ struct FinState {
     F2 local, Ztot;  // u*Z less the mass of the CTAs before the owner; Z (units 2^B_t)
 };
 
-// Control warp, once the exchange that carries item m's alpha and residual shares is done: the
-// item's results. They are written by the owner of its draw (the CTA whose slice holds u*Z),
+// Control warp, once the exchange that carries item m's alpha and residual shares is done (Mi: the
+// records of item m's own exchange, Mn: those of the exchange carrying its totals): the item's
+// results. They are written by the owner of its draw (the CTA whose slice holds u*Z),
 // else by CTA 0. Returns the draw's state in every lane.
-__device__ __forceinline__ FinState finalize_head(CtaShared &sh, const RowsParams &P, int m, int C, int crank,
-                                                  int lane) {
-    const Decision &D = sh.dec[m & 1];
-    const Msg *Mi = sh.slot[m % 3];
-    const Msg *Mn = sh.slot[(m + 1) % 3];
+__device__ __forceinline__ FinState finalize_head(CtaShared &sh, const RowsParams &P, int m, const Msg *Mi,
+                                                  const Msg *Mn, int C, int crank, int lane) {
+    const Decision &D = sh.dec[m % kND];
     FinState f;
     f.kind = D.kind;
     f.fb = 0;
@@ -684,9 +701,17 @@ __device__ __forceinline__ FinState finalize_head(CtaShared &sh, const RowsParam
     // one lane per CTA record, in CTA order
     const bool on = lane < C;
     const Msg &mi = Mi[on ? lane : 0], &mn = Mn[on ? lane : 0];
-    const float alpha_sum = warp_sum(on ? mn.prev_alpha : 0.0f);
-    const F2 Zres = shfl_f2(warp_sum_f2(on ? F2{mn.prev_Zhi, mn.prev_Zlo} : F2{0.0f, 0.0f}), 0);
-    if (f.kind == SAMPLE_RESIDUAL && !(Zres.hi > 0.0f)) {
+    float alpha_sum = on ? mn.prev_alpha : 0.0f;
+    float Zres = on ? mn.prev_Z : 0.0f;
+    // sums over the C lanes (C a power of two: lane l < C meets only lanes below C)
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1)
+        if (o < C) {
+            alpha_sum += __shfl_xor_sync(0xffffffffu, alpha_sum, o);
+            Zres += __shfl_xor_sync(0xffffffffu, Zres, o);
+        }
+    Zres = __shfl_sync(0xffffffffu, Zres, 0);  // the same in every lane: the branches below hold warp-wide shuffles
+    if (f.kind == SAMPLE_RESIDUAL && !(Zres > 0.0f)) {
         f.kind = SAMPLE_P;  // zero residual mass: draw from p and say so
         f.fb = 1;
     }
@@ -694,8 +719,15 @@ __device__ __forceinline__ FinState finalize_head(CtaShared &sh, const RowsParam
         // the first CTA whose running total exceeds u*Z (else the last with mass: rounding put
         // u*Z at the very end)
         const F2 mc = on ? cta_mass(mi, mn, f.kind, D.B_t) : F2{0.0f, 0.0f};
-        const F2 incl = warp_scan_f2(mc, lane);
-        f.Ztot = shfl_f2(incl, kWarp - 1);
+        // inclusive scan over the C lanes, in CTA order
+        F2 incl = mc;
+#pragma unroll
+        for (int o = 1; o < kMaxCluster; o <<= 1)
+            if (o < C) {
+                const F2 w = {__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+                if (lane >= o) incl = f2_add(w, incl);
+            }
+        f.Ztot = shfl_f2(incl, C - 1);
         const F2 t = f2_mul(f.Ztot, D.u_s);
         const unsigned hit = __ballot_sync(0xffffffffu, on && mc.hi > 0.0f && f2_gt(incl, t));
         const unsigned posm = __ballot_sync(0xffffffffu, on && mc.hi > 0.0f);
@@ -719,7 +751,7 @@ __device__ __forceinline__ FinState finalize_head(CtaShared &sh, const RowsParam
                 if (P.rho_rows) P.rho_rows[D.drow] = (st == 0) ? D.rho : NAN;
                 if (P.resid_rows)
                     P.resid_rows[D.drow] =
-                        (st == 0 && f.kind == SAMPLE_RESIDUAL && !D.greedy) ? f2_div(Zres, D.S_t).hi : -1.0f;
+                        (st == 0 && f.kind == SAMPLE_RESIDUAL && !D.greedy) ? Zres * D.inv_St : -1.0f;
             } else {
                 P.item_flag[item] = 0;
             }
@@ -746,7 +778,7 @@ __device__ __forceinline__ FinState finalize_head(CtaShared &sh, const RowsParam
 // from the target row in global memory, in the place of the (zero) residual chunk sums. A path
 // that ordinary inputs never take; it reads the slice once more.
 template <int DT>
-__device__ __noinline__ void fb_chunk_masses(CtaShared &sh, const RowsParams &P, const Decision &D, int par, int lane,
+__device__ __noinline__ void fb_chunk_masses(CtaShared &sh, const RowsParams &P, const Decision &D, int rb, int lane,
                                              int nch, int lo, int nvec) {
     constexpr int E = Elt<DT>::kPerVec;
     const uint4 *row = static_cast<const uint4 *>(P.target) + static_cast<size_t>(D.item) * P.nvec_row + lo;
@@ -758,7 +790,7 @@ __device__ __noinline__ void fb_chunk_masses(CtaShared &sh, const RowsParams &P,
 #pragma unroll
         for (int e = 0; e < E; ++e) a += w[e];
         a = warp_sum(a);
-        if (lane == 0) sh.rm[par][k] = a;
+        if (lane == 0) sh.rm[rb][k] = a;
     }
     __syncwarp();
 }
@@ -767,11 +799,11 @@ __device__ __noinline__ void fb_chunk_masses(CtaShared &sh, const RowsParams &P,
 // chunk masses, in vocabulary order), fetched with a small bulk copy; `complete_draw` finds the
 // token once it has landed.
 template <int DT>
-__device__ __forceinline__ void draw_chunk(CtaShared &sh, const RowsParams &P, int m, const FinState &f, int lane,
+__device__ __noinline__ void draw_chunk(CtaShared &sh, const RowsParams &P, int m, const FinState &f, int lane,
                                            int nch, int lo, int nvec) {
-    const int par = m & 1, pb = m % 3;
-    const Decision &D = sh.dec[par];
-    if (f.fb) fb_chunk_masses<DT>(sh, P, D, par, lane, nch, lo, nvec);
+    const int rb = m % kRM, pb = m % kPM;
+    const Decision &D = sh.dec[m % kND];
+    if (f.fb) fb_chunk_masses<DT>(sh, P, D, rb, lane, nch, lo, nvec);
     int ksel = -1, klast = -1;
     F2 before = {0.0f, 0.0f}, last_before = {0.0f, 0.0f}, run = {0.0f, 0.0f};
 #pragma unroll 1
@@ -780,12 +812,12 @@ __device__ __forceinline__ void draw_chunk(CtaShared &sh, const RowsParams &P, i
         float mk = 0.0f;
         if (k < nch) {
             if (f.kind == SAMPLE_RESIDUAL) {
-                mk = sh.rm[par][k];
+                mk = sh.rm[rb][k];
             } else if (f.fb) {
-                mk = sh.rm[par][k];  // p masses, from fb_chunk_masses
+                mk = sh.rm[rb][k];  // p masses, from fb_chunk_masses
             } else {
                 const float pmk = sh.pm[pb][k];
-                mk = pmk > 0.0f ? pmk * pow2i(sh.pref[pb][k] - D.B_t) : 0.0f;
+                mk = pmk > 0.0f ? pmk * pow2i(sh.pref[pb][k % kWarps] - D.B_t) : 0.0f;
             }
         }
         const bool pos = k < nch && mk > 0.0f;
@@ -820,13 +852,13 @@ __device__ __forceinline__ void draw_chunk(CtaShared &sh, const RowsParams &P, i
             lt = rem.hi + rem.lo;
         } else if (ksel >= 0) {
             // p weights of the chunk are in units of 2^bg: 2^(bg - B_t) cluster units
-            bg = sh.pref[pb][ksel];
+            bg = sh.pref[pb][ksel % kWarps];
             unit = pow2i(bg - D.B_t);
             lt = (rem.hi + rem.lo) * pow2i(D.B_t - bg);
         }
         sh.draw_pending = 1;
         sh.draw_item = D.item;
-        sh.draw_par = par;
+        sh.draw_dec = m % kND;
         sh.draw_kind = f.kind;
         sh.draw_chunk = start;
         sh.draw_count = count;
@@ -856,10 +888,10 @@ __device__ __forceinline__ void draw_chunk(CtaShared &sh, const RowsParams &P, i
 // Control warp of the owner CTA: the token of the pending draw within its chunk (one vector per
 // lane).
 template <int DT>
-__device__ __forceinline__ void complete_draw(CtaShared &sh, const RowsParams &P, int lo, int lane) {
+__device__ __noinline__ void complete_draw(CtaShared &sh, const RowsParams &P, int lo, int lane) {
     constexpr int E = Elt<DT>::kPerVec;
     if (!sh.draw_pending) return;
-    const Decision &D = sh.dec[sh.draw_par];
+    const Decision &D = sh.dec[sh.draw_dec];
     const int kind = sh.draw_kind, count = sh.draw_count, clamped = sh.draw_clamped;
     bool ok = true;
     if (count > 0) {
@@ -929,6 +961,40 @@ __device__ __forceinline__ void complete_draw(CtaShared &sh, const RowsParams &P
     __syncwarp();
 }
 
+// Control warp, exchange g: item g's record goes out with the totals of item g - 1 (pass 2 of
+// g - 1 is done once every data warp has passed pass 1 of g); item g is decided and released to
+// the data warps at once; then item g - 1 is finished (results, draw) from this exchange's totals.
+// d == nullptr: the drain after the last item (totals only).
+template <int DT>
+__device__ __forceinline__ void control_item(CtaShared &sh, const RowsParams &P, const Desc *d, int g, Msg *slots,
+                                             int C, int crank, int lo, int nvec, int nch, int lane) {
+    const int nr = d ? desc_rows(*d) : 0, greedy = d ? d->greedy : 0;
+    if (!mbar_wait_sleep_bounded(&sh.stats_bar[g % kSB], static_cast<uint32_t>((g / kSB) & 1), kSuspendNs,
+                                 kMaxWaitTries))
+        sh.timed_out = 1;
+    __syncwarp();
+    build_record(sh, greedy, nr, g, g - 1, nch, lane);
+    __syncwarp();
+    if (g == 0) cluster_wait();  // the peers run and their barriers are ready
+    Msg *const here = slots + (g % kNMS) * C;
+    push_record(&sh.mine, here, &sh.msg_bar[g % kNMS], crank, C, lane);
+    if (lane == 0) mbar_arrive_expect_tx(&sh.msg_bar[g % kNMS], static_cast<uint32_t>(C * kMsgBytes));
+    complete_draw<DT>(sh, P, lo, lane);  // the draw fetched at the previous exchange
+    if (!mbar_wait_sleep_bounded(&sh.msg_bar[g % kNMS], static_cast<uint32_t>((g / kNMS) & 1), kSuspendNs,
+                                 kMaxWaitTries))
+        sh.timed_out = 1;
+    __syncwarp();
+    if (d) {
+        decide_item(sh, here, *d, nr, g, C, P, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.dec_bar[g % kND]);
+    }
+    if (g >= 1) {
+        const FinState f = finalize_head(sh, P, g - 1, slots + ((g - 1) % kNMS) * C, here, C, crank, lane);
+        if (f.owner == crank) draw_chunk<DT>(sh, P, g - 1, f, lane, nch, lo, nvec);
+    }
+}
+
 // Load the slice of one ring slot into registers: thread t takes vectors t, t + 480, ... so that
 // a warp reads 32 contiguous vectors (a chunk); past the slice end, -inf.
 template <int DT, int NVT>
@@ -953,7 +1019,12 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
     __shared__ CtaShared sh;
     uint4 *ring = reinterpret_cast<uint4 *>(smem_raw);
 
-    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+    // The control warp is hardware warp 0 (the schedulers favour the lowest warps when several are
+    // ready, and its chain of dependent steps gates every item); the data warps are hardware warps
+    // 1 .. 15. Logical numbering: data thread t = 0 .. 479 in warps 0 .. 14, the control warp 15.
+    const int hw_warp = static_cast<int>(threadIdx.x) / kWarp, lane = static_cast<int>(threadIdx.x) % kWarp;
+    const int warp = hw_warp == 0 ? kWarps : hw_warp - 1;
+    const int tid = warp * kWarp + lane;
     griddep_launch_dependents();  // the selection kernel may be scheduled behind this grid
     const int C = static_cast<int>(cluster_nctarank());
     const int crank = static_cast<int>(cluster_ctarank());
@@ -964,19 +1035,25 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
     const int nch = NVT * kWarps;
     const int ncl = P.nclusters;
     const int nitems = cid < P.total_rows ? (P.total_rows - 1 - cid) / ncl + 1 : 0;
+    // the exchange slots follow the ring: kNMS exchanges x C records, the same layout in every CTA
+    Msg *const slots = reinterpret_cast<Msg *>(smem_raw + static_cast<size_t>(kRing) * slice_max * 16);
 
     if (tid == 0) {
-        for (int k = 0; k < kRing; ++k) mbar_init(&sh.full[k], 1);
-        for (int k = 0; k < 3; ++k) mbar_init(&sh.msg_bar[k], 1);
+        for (int k = 0; k < kRing; ++k) {
+            mbar_init(&sh.full[k], 1);
+            sh.free_cnt[k] = 0;
+        }
+        for (int k = 0; k < kNMS; ++k) mbar_init(&sh.msg_bar[k], 1);
+        for (int k = 0; k < kSB; ++k) mbar_init(&sh.stats_bar[k], kWarps);
+        for (int k = 0; k < kND; ++k) mbar_init(&sh.dec_bar[k], 1);
         mbar_init(&sh.draw_bar, 1);
         fence_mbar_init();
         sh.timed_out = 0;
-        sh.x_stamp = 0;
         sh.draw_pending = 0;
         sh.draw_phase = 0;
-        sh.dec[0].kind = sh.dec[1].kind = SAMPLE_NONE;
-        sh.mine.prev_alpha = sh.mine.prev_Zhi = sh.mine.prev_Zlo = 0.0f;
-        sh.mine.pad = 0;
+        for (int k = 0; k < kWS; ++k) sh.x_stamp[k] = 0;
+        sh.mine.prev_alpha = sh.mine.prev_Z = 0.0f;
+        sh.prod_issued = 0;
     }
     __syncthreads();  // the barriers are initialised
     // every CTA of the cluster must run, its barriers ready, before any remote access: all threads
@@ -984,62 +1061,86 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
     cluster_arrive();
 
     if (warp < kWarps) {
-        // ================= data warps: registers, pass 1, pass 2 =================
+        // ================= data warps: pass 1, the decision, pass 2 (rows held on chip) ========
         long long R = 0;  // ring row of the item's target row
-        int nb = 0, nbatch = 0;
-        for (int n = 0; n < nitems; ++n) {
-            if (n == nb + nbatch) {
-                nb = n;
-                nbatch = min(kMaxItems, nitems - n);
-                bar_sync(BAR_BATCH, kBlock);  // the control warp has the batch's descriptors
+        int g0 = 0;       // the batch's first item, counted over the whole list
+        for (int nb = 0; nb < nitems; nb += kMaxItems) {
+            const int nbatch = min(kMaxItems, nitems - nb);
+            bar_sync(BAR_BATCH, kBlock);  // the control warp has the batch's descriptors
+            if (tid == 0) {
+                sh.prod_item = 0;
+                sh.prod_row = 0;
+                produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, sh.prod_issued, R + kRing, sh.prod_item,
+                             sh.prod_row);
             }
-            const Desc &d = sh.desc[n - nb];
-            const int nr = desc_rows(d);
-            uint4 vt[NVT];
-            bool ok = true;
-            if (nr >= 1) ok = load_row<DT, NVT>(sh, ring, slice_max, nvec, R, tid, vt);
-            bar_arrive(BAR_FREE, kBlock);  // the target row's slot may be refilled
-            if (nr == 1) row_stats<DT, NVT, true>(RegRow<NVT>{vt}, sh, 0, n % 3, d, lo, nvec, warp, lane, tid);
-            const SmemRow<DT> rd = {ring + static_cast<size_t>((R + 1) % kRing) * slice_max, tid, nvec};
-            if (nr == 2) {
-                ok &= mbar_wait_sleep_bounded(&sh.full[(R + 1) % kRing], static_cast<uint32_t>(((R + 1) / kRing) & 1),
-                                              kSuspendNs, kMaxWaitTries);
-                if (d.greedy) {
-                    row_stats<DT, NVT, false>(RegRow<NVT>{vt}, sh, 0, n % 3, d, lo, nvec, warp, lane, tid);
-                    row_stats<DT, NVT, false>(rd, sh, 1, n % 3, d, lo, nvec, warp, lane, tid);
-                } else {
-                    pair_stats<DT, NVT>(vt, rd, sh, d, nvec, warp, lane);
+            for (int i = 0; i < nbatch; ++i) {
+                const int g = g0 + i, wb = g % kWS;
+                const Desc &d = sh.desc[i];
+                const int nr = desc_rows(d);
+                uint4 vt[NVT];
+                bool ok = true;
+                if (nr >= 1) {
+                    ok = load_row<DT, NVT>(sh, ring, slice_max, nvec, R, tid, vt);
+                    // this warp holds the target row in registers: its slot may refill
+                    release_row(sh, ring, P, slice_max, lo, nvec, nbatch, R, lane);
                 }
-                // the logits at the draft token, from the thread that holds them
-                const int x = d.x;
-                if (x >= 0 && x < P.V) {
-                    const int xv = x / E - lo;
-                    if (xv >= 0 && xv < nvec && (xv % kThreads) == tid) {
-                        const int vx = xv / kThreads, e = x % E;
+                const SmemRow<DT> rd = {ring + static_cast<size_t>((R + 1) % kRing) * slice_max, tid, nvec};
+                if (nr == 2)
+                    ok &= mbar_wait_sleep_bounded(&sh.full[(R + 1) % kRing],
+                                                  static_cast<uint32_t>(((R + 1) / kRing) & 1), kSuspendNs,
+                                                  kMaxWaitTries);
+                if (!ok) sh.timed_out = 1;
+                if (nr == 1) row_stats<DT, NVT, true>(RegRow<NVT>{vt}, sh, wb, 0, g % kPM, d, lo, nvec, warp, lane, tid);
+                if (nr == 2) {
+                    if (d.greedy) {
+                        row_stats<DT, NVT, false>(RegRow<NVT>{vt}, sh, wb, 0, 0, d, lo, nvec, warp, lane, tid);
+                        row_stats<DT, NVT, false>(rd, sh, wb, 1, 0, d, lo, nvec, warp, lane, tid);
+                    } else {
+                        pair_stats<DT, NVT>(vt, rd, sh, wb, d, nvec, warp, lane);
+                    }
+                    // the logits at the draft token, from the thread that holds them
+                    const int x = d.x;
+                    if (x >= 0 && x < P.V) {
+                        const int xv = x / E - lo;
+                        if (xv >= 0 && xv < nvec && (xv % kThreads) == tid) {
+                            const int vx = xv / kThreads, e = x % E;
 #pragma unroll
-                        for (int v = 0; v < NVT; ++v)
-                            if (v == vx) sh.yx[0] = vec_elem<DT>(vt[v], e);
-                        sh.yx[1] = vec_elem<DT>(rd.src[xv], e);
-                        sh.x_stamp = n + 1;
+                            for (int v = 0; v < NVT; ++v)
+                                if (v == vx) sh.yx[wb][0] = vec_elem<DT>(vt[v], e);
+                            sh.yx[wb][1] = vec_elem<DT>(rd.src[xv], e);
+                            sh.x_stamp[wb] = g + 1;
+                        }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.stats_bar[g % kSB]);
+                // every item waits for its decision (pass 2 needs it; it also keeps the data warps
+                // within one item of each other and of the control warp)
+                if (!mbar_wait_sleep_bounded(&sh.dec_bar[g % kND], static_cast<uint32_t>((g / kND) & 1), kSuspendNs,
+                                             kMaxWaitTries))
+                    sh.timed_out = 1;
+                if (nr == 2) {
+                    pass2<DT, NVT>(vt, rd, sh, sh.dec[g % kND], g % kRM, warp, lane);
+                    release_row(sh, ring, P, slice_max, lo, nvec, nbatch, R + 1, lane);  // the draft slot
+                } else if (lane == 0) {
+                    sh.wal[g % kRM][warp] = 0.0f;
+                }
+                R += nr;
             }
-            if (!ok) sh.timed_out = 1;
-            bar_arrive(BAR_STATS, kBlock);
-            bar_sync(BAR_DECIDED, kBlock);
-            if (nr == 2) {
-                pass2<DT, NVT>(vt, rd, sh, sh.dec[n & 1], n & 1, warp, lane, tid);
-            } else if (lane == 0) {
-                sh.wal[warp] = 0.0f;
-            }
-            bar_arrive(BAR_PASS2, kBlock);  // the draft row's slot may be refilled
-            R += nr;
+            g0 += nbatch;
+        }
+        // the drain: the last pass 2 is done, its totals go out with one more exchange
+        __syncwarp();
+        if (nitems > 0 && lane == 0) mbar_arrive(&sh.stats_bar[nitems % kSB]);
+        if (tid == 0 && sh.timed_out) {
+            // a copy did not land in time: wait (bounded) once more so that none is left in flight
+            for (long long r = max(0LL, sh.prod_issued - kRing); r < sh.prod_issued; ++r)
+                mbar_wait_sleep_bounded(&sh.full[r % kRing], static_cast<uint32_t>((r / kRing) & 1), kSuspendNs,
+                                        kMaxWaitTries);
         }
         cluster_wait();
     } else {
-        // ================= control warp: copies, exchange, decisions, draws =================
-        long long issued = 0, released = 0;  // rows copied; rows whose slots are free again (in order)
-        int cur_item = 0, cur_row = 0, nb = 0, nbatch = 0;
+        // ================= control warp: exchanges, decisions, results, draws =================
         if (lane < kRing && lane < nitems) {
             // the first target rows' slices into L2 while the descriptors load
             const size_t row_bytes = static_cast<size_t>(P.nvec_row) * 16;
@@ -1047,80 +1148,21 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
                                  static_cast<size_t>(cid + lane * ncl) * row_bytes + static_cast<size_t>(lo) * 16,
                              static_cast<uint32_t>(nvec) * 16);
         }
-        for (int n = 0; n < nitems; ++n) {
-            if (n == nb + nbatch) {  // the next batch of descriptors (the ring is empty here)
-                nb = n;
-                nbatch = min(kMaxItems, nitems - n);
-                load_batch_shapes(sh, P, cid, nb, nbatch, lane);
-                if (lane == 0) {
-                    cur_item = 0;
-                    cur_row = 0;
-                    produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, issued, released + kRing, cur_item,
-                                 cur_row);
-                }
-                __syncwarp();
-                load_batch_values(sh, P, nbatch, lane);  // while the first copies are in flight
-                bar_arrive(BAR_BATCH, kBlock);
-            }
-            const Desc &d = sh.desc[n - nb];
-            const int nr = desc_rows(d);
-            bar_sync(BAR_FREE, kBlock);
-            released += (nr >= 1);
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, issued, released + kRing, cur_item, cur_row);
-            }
-            bar_sync(BAR_STATS, kBlock);
-            build_message(sh, d.greedy, nr, n, lane);
+        int g = 0;  // item (and exchange) number; exchange nitems is the drain
+        for (int nb = 0; nb < nitems; nb += kMaxItems) {
+            const int nbatch = min(kMaxItems, nitems - nb);
+            load_batch_shapes(sh, P, cid, nb, nbatch, lane);
+            load_batch_values(sh, P, nbatch, lane);
             __syncwarp();
-            if (n == 0) cluster_wait();  // the peers run and their barriers are ready
-            push_record(&sh.mine, sh.slot[n % 3], &sh.msg_bar[n % 3], crank, C, lane);
-            if (lane == 0) mbar_arrive_expect_tx(&sh.msg_bar[n % 3], static_cast<uint32_t>(C * kMsgBytes));
-            complete_draw<DT>(sh, P, lo, lane);  // the draw of item n - 2, fetched one item ago
-            if (!mbar_wait_sleep_bounded(&sh.msg_bar[n % 3], static_cast<uint32_t>((n / 3) & 1), kSuspendNs,
-                                         kMaxWaitTries))
-                sh.timed_out = 1;
-            __syncwarp();
-            decide_item(sh, d, nr, n, C, P, lane);
-            __syncwarp();
-            bar_arrive(BAR_DECIDED, kBlock);
-            // the previous item's results, while pass 2 runs
-            if (n > 0) {
-                const FinState f = finalize_head(sh, P, n - 1, C, crank, lane);
-                if (f.owner == crank) draw_chunk<DT>(sh, P, n - 1, f, lane, nch, lo, nvec);
-            }
-            bar_sync(BAR_PASS2, kBlock);
-            stash_totals(sh, n, nch, lane);
-            if (nr == 2) {
-                released += 1;
-                if (lane == 0) {
-                    fence_proxy_async_smem();
-                    produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, issued, released + kRing, cur_item,
-                                 cur_row);
-                }
-            }
+            bar_arrive(BAR_BATCH, kBlock);
+            for (int i = 0; i < nbatch; ++i, ++g)
+                control_item<DT>(sh, P, &sh.desc[i], g, slots, C, crank, lo, nvec, nch, lane);
         }
-        if (nitems == 0) cluster_wait();
         if (nitems > 0) {
-            // the last item's totals travel in one more exchange
-            build_message(sh, 0, 0, nitems, lane);
-            __syncwarp();
-            push_record(&sh.mine, sh.slot[nitems % 3], &sh.msg_bar[nitems % 3], crank, C, lane);
-            if (lane == 0) mbar_arrive_expect_tx(&sh.msg_bar[nitems % 3], static_cast<uint32_t>(C * kMsgBytes));
-            complete_draw<DT>(sh, P, lo, lane);
-            if (!mbar_wait_sleep_bounded(&sh.msg_bar[nitems % 3], static_cast<uint32_t>((nitems / 3) & 1),
-                                         kSuspendNs, kMaxWaitTries))
-                sh.timed_out = 1;
-            __syncwarp();
-            const FinState f = finalize_head(sh, P, nitems - 1, C, crank, lane);
-            if (f.owner == crank) draw_chunk<DT>(sh, P, nitems - 1, f, lane, nch, lo, nvec);
-            complete_draw<DT>(sh, P, lo, lane);
-        }
-        if (lane == 0 && sh.timed_out) {
-            // a copy did not land in time: wait (bounded) once more so that none is left in flight
-            for (long long r = max(0LL, issued - kRing); r < issued; ++r)
-                mbar_wait_sleep_bounded(&sh.full[r % kRing], static_cast<uint32_t>((r / kRing) & 1), kSuspendNs,
-                                        kMaxWaitTries);
+            control_item<DT>(sh, P, nullptr, nitems, slots, C, crank, lo, nvec, nch, lane);
+            complete_draw<DT>(sh, P, lo, lane);  // the last draw
+        } else {
+            cluster_wait();
         }
     }
     __syncwarp();
