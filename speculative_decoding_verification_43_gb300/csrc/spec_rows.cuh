@@ -52,6 +52,7 @@ enum : int { BAR_BATCH = 1 };
 constexpr int kChunkVecs = kWarp;   // a chunk: 32 contiguous vectors, one per lane of a warp
 constexpr int kRing = 3;            // row slots per CTA
 constexpr int kMaxItems = 32;       // item descriptors held at once (one batch)
+constexpr int kRoffMax = 520;       // row offsets staged in shared memory (B <= 519)
 constexpr int kMaxCluster = 16;
 constexpr int kMaxNvt = 5;          // 16-byte vectors per thread per row
 constexpr int kMaxChunks = kMaxNvt * kWarps;
@@ -63,17 +64,21 @@ constexpr float kLog2eLo = 1.925963e-08f;
 
 enum : int32_t { REQ_TIMEOUT = 32 };  // internal: a bulk copy did not complete in time
 
-// The pipeline: an item's rows stay on chip from pass 1 to pass 2 (the target row in registers,
-// the draft row in its ring slot), so that nothing is read twice; the data warps wait for the
-// item's decision between the passes while the other CTA on the SM computes. The control warp
-// decides item g, signals it, and only then finishes item g - 1 (its results and draw), in the
-// shadow of pass 2. Ring depths of the per-item buffers:
-constexpr int kWS = 2;   // pass-1 statistics (read by the item's exchange)
-constexpr int kPM = 4;   // bonus-row chunk sums (read by the draw, one item later)
-constexpr int kRM = 3;   // pass-2 residual chunk sums and alpha partials (read one item later)
-constexpr int kND = 3;   // decisions (read by pass 2, the results and the draw)
-constexpr int kNMS = 3;  // exchange slots (a record is read again one exchange later)
-constexpr int kSB = 2;   // barriers: pass-1 statistics ready
+// The pipeline. kLag = 0: an item's rows stay on chip from pass 1 to pass 2 (the target row in
+// registers, the draft row in its ring slot), and the data warps wait for the item's decision
+// between the passes while the other CTA on the SM computes. kLag > 0: pass 2 of item g runs
+// after pass 1 of item g + kLag, so that the exchange and the decision overlap other items'
+// passes; the rows of item g are read again (from L2, where pass 1's copies left them). The
+// control warp decides item g, signals it, and only then finishes an earlier item (its results
+// and draw). Ring depths of the per-item buffers follow from how far apart the roles may run:
+constexpr int kLag = 0;
+constexpr int kWS = kLag + 2;       // pass-1 statistics (read by the item's exchange)
+constexpr int kPM = 2 * kLag + 4;   // bonus-row chunk sums (read by the draw, kLag + 1 items later)
+constexpr int kRM = kLag + 3;       // pass-2 residual chunk sums and alpha partials
+constexpr int kND = kLag + 3;       // decisions (read by pass 2, the results and the draw)
+constexpr int kNMS = kLag + 3;      // exchange slots (a record is read again kLag + 1 exchanges later)
+constexpr int kSB = kLag + 2;       // barriers: pass-1 statistics ready
+constexpr int kPB = kLag + 3;       // barriers: pass 2 done (kLag > 0)
 
 struct RowsParams {
     const void *target;
@@ -109,24 +114,29 @@ struct Desc {
     F2 u_acc, u_s;     // the position's accept draw and the request's frontier draw
 };
 
+// Reference exponent of a row (or slice) with no mass.
+constexpr int32_t kNoRef = -(1 << 30);
+// Record flags: this CTA holds the draft token; a bulk copy timed out; q(x) = 0; p(x) = 0.
+enum : int32_t { XF_HAS = 1, XF_TMO = 2, XF_QZERO = 4, XF_PZERO = 8 };
+
 // A CTA's record for item k, stored into exchange slot k % kNMS of every CTA of the cluster
 // (distributed shared memory, asynchronous stores that complete bytes on that CTA's barrier of
-// the slot). Sixteen 32-bit words, 16-byte aligned: four vector stores per destination. Sums are
-// plain floats: a record adds at most log2(16) + 4 roundings to sums of thousands of terms.
+// the slot). Twelve 32-bit words, 16-byte aligned: three vector stores per destination. Sums are
+// plain floats: a record adds a handful of roundings to sums of thousands of terms.
 struct __align__(16) Msg {
-    float B[2];      // integral reference exponent of S[r] (-inf: no mass)
-    float S[2];      // this slice's sum of 2^(y*s - B[r])
-    int32_t bad[2];  // a NaN / +inf was seen in row r
-    float gmax[2];   // greedy rule: max logit of the slice and the smallest index attaining it
-    int32_t garg[2];
-    float yx[2];     // target / draft logit at the draft token, from the CTA that holds it
-    int32_t has_x;
-    int32_t tmo;       // a bulk copy of this CTA did not land in time
-    float prev_alpha;  // an earlier item: this slice's share of alpha (normalised)
-    float prev_Z;      // an earlier item: this slice's residual mass (units 2^B_t)
+    int32_t a[2];  // Rule 2: integral reference exponent B_r of row r (kNoRef: no mass);
+                   // Rule 1: smallest index attaining the max (-1: the row holds a NaN / +inf)
+    float b[2];    // Rule 2: sum S_r of 2^(y*s - B_r) (NaN: the row holds a NaN / +inf);
+                   // Rule 1: max logit (+inf with a = -1: invalid row)
+    float E_hi, E_lo;  // (y_t - y_d) s at the draft token, a float pair (from the CTA holding it)
+    int32_t flags;     // XF_* bits
+    int32_t pad0;
+    float prev_alpha;  // the previous item: this slice's share of alpha (normalised)
+    float prev_Z;      // the previous item: this slice's residual mass (units 2^B_t)
+    int32_t pad1, pad2;
 };
 constexpr int kMsgBytes = sizeof(Msg);
-static_assert(kMsgBytes == 64, "a record is four 16-byte vectors");
+static_assert(kMsgBytes == 48, "a record is three 16-byte vectors");
 
 // The decision of an item, kept until its draw is finished (one item later).
 struct Decision {
@@ -141,25 +151,25 @@ struct Decision {
 
 enum { SAMPLE_NONE = 0, SAMPLE_RESIDUAL = 1, SAMPLE_P = 2 };
 
-// Per-warp statistics of one row after pass 1.
-struct WarpStat {
-    float B;  // integral reference (-inf: no mass)
-    float S;  // sum of 2^(y*s - B)
-    float gmax;
-    int32_t garg;
-    int32_t bad;
+// Per-warp statistics of both rows after pass 1, in the record's encoding (a[r], b[r] as in
+// Msg), 16 bytes so that one vector load reads a warp's entry.
+struct __align__(16) WarpStat {
+    int32_t a[2];
+    float b[2];
 };
 
-// Lane l < C stores the local record into slot `rank` of CTA l (five asynchronous 16-byte
-// stores, each completing its bytes on CTA l's barrier of that slot).
-__device__ __forceinline__ void push_record(const Msg *mine, Msg *slot_base, uint64_t *bar, int rank, int C,
+// 2^d for an integer d <= 0 with integer operations only (0 below the normal range).
+__device__ __forceinline__ float pow2_int(int d) { return d < -126 ? 0.0f : __int_as_float((d + 127) << 23); }
+
+// Lane l < C stores this CTA's record (three vectors in registers, the same in every lane) into
+// slot `rank` of CTA l, each asynchronous store completing its bytes on CTA l's barrier.
+__device__ __forceinline__ void push_record(const uint4 (&rec)[3], Msg *slot_base, uint64_t *bar, int rank, int C,
                                             int lane) {
     if (lane < C) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(mine);
         const uint32_t dst = dsmem_map(slot_base + rank, lane);
         const uint32_t rbar = dsmem_map(bar, lane);
 #pragma unroll
-        for (int q = 0; q < kMsgBytes / 16; ++q) st_async_v4(dst + 16 * q, src[q], rbar);
+        for (int q = 0; q < 3; ++q) st_async_v4(dst + 16 * q, rec[q], rbar);
     }
 }
 

@@ -11,15 +11,18 @@ struct CtaShared {
     uint64_t full[kRing];                 // a ring slot's bulk copy has landed
     uint64_t draw_bar;                    // the draw chunk's bulk copy has landed
     uint64_t msg_bar[kNMS];               // all C records of an exchange have arrived
-    uint64_t stats_bar[kSB];              // pass 1 of an item (or, for the drain, the last pass 2)
-                                          // done: one arrival per data warp
+    uint64_t stats_bar[kSB];              // pass 1 of an item (or, held rows, the drain after the
+                                          // last pass 2) done: one arrival per data warp
+    uint64_t p2_bar[kPB];                 // kLag > 0: pass 2 of an item done (one arrival per data warp)
     uint64_t dec_bar[kND];                // the decision of an item is ready (control warp)
-    Msg mine;
     Desc desc[kMaxItems];
-    WarpStat ws[kWS][2][kWarps];          // per-warp row statistics, by item % kWS
-    float yx[kWS][2];                     // logits at the draft token, from the thread holding it
+    int32_t roff[kRoffMax];               // row_off, staged once when B + 1 entries fit
+    WarpStat ws[kWS][kWarps];             // per-warp row statistics, by item % kWS
+    float xE[kWS][2];                     // (y_t - y_d) s at the draft token, from the thread holding it
+    int32_t x_flags[kWS];                 // XF_* bits of the draft token (XF_HAS when held here)
     int32_t x_stamp[kWS];                 // item number + 1 when this CTA holds the draft token
     float wal[kRM][kWarps];               // per-warp alpha partials, by item % kRM
+    float wz[kRM][kWarps];                // per-warp residual mass (units 2^B_t), by item % kRM
     float rm[kRM][kMaxChunks];            // residual chunk sums (units 2^B_t), by item % kRM
     float pm[kPM][kMaxChunks];            // bonus-row chunk sums (units 2^pref), by item % kPM
     float pref[kPM][kWarps];              // their integral reference exponents (one per warp)
@@ -40,6 +43,23 @@ struct CtaShared {
 // steps: the shapes (which request and position, the draft row), enough to issue the row copies,
 // then the per-item values (temperature, draws, draft token).
 __device__ void load_batch_shapes(CtaShared &sh, const RowsParams &P, int cid, int nb, int nbatch, int lane) {
+    // row_off into shared memory once, eight independent loads per lane in flight
+    const bool staged = P.B + 1 <= kRoffMax;
+    if (nb == 0 && staged) {
+        for (int base = 0; base <= P.B; base += 8 * kWarp) {
+            int v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = base + k * kWarp + lane;
+                v[k] = (i <= P.B) ? __ldg(P.row_off + i) : 0;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = base + k * kWarp + lane;
+                if (i <= P.B) sh.roff[i] = v[k];
+            }
+        }
+    }
     for (int s = lane; s < kMaxItems; s += kWarp) {
         Desc &d = sh.desc[s];
         d.item = cid + (nb + s) * P.nclusters;
@@ -57,7 +77,8 @@ __device__ void load_batch_shapes(CtaShared &sh, const RowsParams &P, int cid, i
     const int first = cid + nb * P.nclusters;
     const int last = cid + (nb + nbatch) * P.nclusters;  // exclusive
     for (int i = lane; i < P.B; i += kWarp) {
-        const int r0 = __ldg(P.row_off + i), r1 = __ldg(P.row_off + i + 1);
+        const int r0 = staged ? sh.roff[i] : __ldg(P.row_off + i);
+        const int r1 = staged ? sh.roff[i + 1] : __ldg(P.row_off + i + 1);
         int lo = max(max(r0, first), 0);
         lo += ((cid - lo) % P.nclusters + P.nclusters) % P.nclusters;  // next item of this cluster
         const int hi = min(min(r1, last), P.total_rows);
@@ -89,7 +110,12 @@ __device__ void load_batch_values(CtaShared &sh, const RowsParams &P, int nbatch
         int status = d.status;
         const int r1 = d.x;
         d.x = -1;
+        // every load of the item at once (the shape decides which exist)
+        const bool shaped = status == 0 && d.req >= 0;
         const float T = (d.req >= 0) ? (P.temperature ? __ldg(P.temperature + d.req) : P.temperature_scalar) : 1.0f;
+        const double ua = shaped ? __ldg(P.uniforms + d.item) : 0.0;
+        const double us = shaped ? __ldg(P.uniforms + r1 - 1) : 0.0;
+        const int xt = (shaped && d.pair) ? __ldg(P.draft_tokens + d.drow) : -1;
         if (!(T >= 0.0f) || isinf(T)) status |= SPEC_REQ_BAD_PARAM;
         d.greedy = (T == 0.0f) ? 1 : 0;
         F2 sv = {0.0f, 0.0f};
@@ -104,9 +130,9 @@ __device__ void load_batch_values(CtaShared &sh, const RowsParams &P, int nbatch
         d.s_hi = sv.hi;
         d.s_lo = fmaxf(sv.lo, 1.401298464e-45f);
         if (status == 0 && d.req >= 0) {
-            d.u_acc = d2f2(__ldg(P.uniforms + d.item));
-            d.u_s = d2f2(__ldg(P.uniforms + r1 - 1));
-            if (d.pair) d.x = __ldg(P.draft_tokens + d.drow);
+            d.u_acc = d2f2(ua);
+            d.u_s = d2f2(us);
+            if (d.pair) d.x = xt;
         }
         d.status = status;
     }
@@ -122,12 +148,13 @@ __device__ __forceinline__ int desc_rows(const Desc &d) {
 
 // Data thread 0: issue the bulk copies of the cluster's row sequence up to row `limit`
 // (exclusive). The sequence runs through the batch's items in order: target row, then draft row
-// for a pair. Each row is read once (evict-first).
+// for a pair. With kLag > 0 pass 2 reads the rows again a few items later: the copies keep them in
+// L2 (evict-last); otherwise each row is read once (evict-first).
 __device__ __forceinline__ void produce_rows(CtaShared &sh, uint4 *ring, const RowsParams &P, int slice_max, int lo,
                                              int nvec, int nbatch, long long &issued, long long limit,
                                              int &cur_item, int &cur_row) {
     const size_t row_bytes = static_cast<size_t>(P.nvec_row) * 16;
-    const uint64_t pol = policy_evict_first();
+    const uint64_t pol = kLag > 0 ? policy_evict_last() : policy_evict_first();
     while (issued < limit && cur_item < nbatch) {
         const Desc &d = sh.desc[cur_item];
         if (cur_row >= desc_rows(d)) {
@@ -295,9 +322,8 @@ __device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int wb,
         const int widx = warp_min_i32(best == wbest ? bidx : INT_MAX);
         const int wbad = __any_sync(0xffffffffu, bad);
         if (lane == 0) {
-            sh.ws[wb][r][warp].gmax = wbest;
-            sh.ws[wb][r][warp].garg = widx;
-            sh.ws[wb][r][warp].bad = wbad;
+            sh.ws[wb][warp].b[r] = wbad ? INFINITY : wbest;
+            sh.ws[wb][warp].a[r] = wbad ? -1 : widx;
         }
         return;
     }
@@ -319,9 +345,10 @@ __device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int wb,
     }
     if (lane == 0) {
         if (CHUNKS) sh.pref[pb][warp] = Bw;
-        sh.ws[wb][r][warp].B = Bw;
-        sh.ws[wb][r][warp].S = Sw;
-        sh.ws[wb][r][warp].bad = bad;
+        // a reference beyond 2^28 (logits far outside any float32 softmax) reads as invalid
+        const bool inval = bad || (Sw > 0.0f && !(fabsf(Bw) < 0x1p28f));
+        sh.ws[wb][warp].a[r] = (Sw > 0.0f && !inval) ? static_cast<int>(Bw) : kNoRef;
+        sh.ws[wb][warp].b[r] = inval ? NAN : Sw;
     }
 }
 
@@ -332,9 +359,10 @@ __device__ __forceinline__ void warp_row_stats(CtaShared &sh, int wb, int r, int
     const float Bw = warp_max(ok ? b : -INFINITY);
     const float Sw = warp_sum(ok ? s * pow2i(b - Bw) : 0.0f);
     if (lane == 0) {
-        sh.ws[wb][r][warp].B = Bw;
-        sh.ws[wb][r][warp].S = Sw;
-        sh.ws[wb][r][warp].bad = bad;
+        // a reference beyond 2^28 (logits far outside any float32 softmax) reads as invalid
+        const bool inval = bad || (Sw > 0.0f && !(fabsf(Bw) < 0x1p28f));
+        sh.ws[wb][warp].a[r] = (Sw > 0.0f && !inval) ? static_cast<int>(Bw) : kNoRef;
+        sh.ws[wb][warp].b[r] = inval ? NAN : Sw;
     }
 }
 
@@ -401,101 +429,94 @@ __device__ __forceinline__ void half_argmax(float &gm, int &ga, int n) {
         }
 }
 
-// Control warp: this CTA's record for item g, its row statistics over the data warps (row r in
-// lanes 16r .. 16r + 14, lane 16r + w taking warp w: the max reference, then the sums scaled to
-// it by exact powers of two), the logits at the draft token if it holds them, and the totals of
-// item m (its alpha share, summed alongside, and its residual mass; m < 0: none). nr = 0: no
-// item (a draining exchange).
-__device__ __forceinline__ void build_record(CtaShared &sh, int greedy, int nr, int g, int m, int nch, int lane) {
-    Msg &msg = sh.mine;
+// Control warp: this CTA's record for item g, in registers (the same in every lane): its row
+// statistics over the data warps (row r in lanes 16r .. 16r + 14, lane 16r + w taking warp w:
+// the max reference, then the sums scaled to it by exact powers of two), the ratio exponent at
+// the draft token if this CTA holds it, and the totals of item m (its alpha share in the row-0
+// lanes and its residual mass in the row-1 lanes, summed alongside; m < 0: none). nr = 0: no item
+// (a draining exchange).
+__device__ __forceinline__ void build_record(CtaShared &sh, int greedy, int nr, int g, int m, int lane,
+                                             uint4 (&rec)[3]) {
     const int wb = g % kWS, r = lane >> 4, w = lane & 15;
     const bool use = w < kWarps && r < nr;
-    const WarpStat &st = sh.ws[wb][r][use ? w : 0];
-    const int rb = m >= 0 ? m % kRM : 0;
-    const float pa = (m >= 0 && r == 0 && w < kWarps) ? sh.wal[rb][w] : 0.0f;
-    const unsigned badm = __ballot_sync(0xffffffffu, use && st.bad);
-    const int bad = (badm >> (16 * r)) & 0xffffu ? 1 : 0;
-    float B = -INFINITY, S = 0.0f, gmax = -INFINITY;
-    int garg = INT_MAX;
+    const WarpStat &st = sh.ws[wb][use ? w : 0];
+    int a = use ? st.a[r] : (greedy ? INT_MAX : kNoRef);
+    float b = use ? st.b[r] : (greedy ? -INFINITY : 0.0f);
+    float t = 0.0f;
+    if (m >= 0 && w < kWarps) t = (r == 0) ? sh.wal[m % kRM][w] : sh.wz[m % kRM][w];
     if (greedy) {
-        gmax = use ? st.gmax : -INFINITY;
-        garg = use ? st.garg : INT_MAX;
-        half_argmax(gmax, garg, 16);
+        half_argmax(b, a, 16);
     } else {
-        const float Sw = use ? st.S : 0.0f;
-        const float Bw = Sw > 0.0f ? st.B : -INFINITY;
-        B = half_max(Bw);
-        S = Sw > 0.0f ? Sw * pow2i(Bw - B) : 0.0f;
+        int Bm = a;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) Bm = max(Bm, __shfl_xor_sync(0xffffffffu, Bm, o));
+        // no mass: 0 (a NaN sum stays NaN)
+        b = (a == kNoRef) ? b * 0.0f : b * pow2_int(a - Bm);
+        a = Bm;
     }
-    S = half_sum(S);
-    const float alpha = half_sum(pa);
-    float pz = 0.0f;
-    if (m >= 0 && sh.dec[m % kND].kind == SAMPLE_RESIDUAL) {
-#pragma unroll 1
-        for (int k = lane; k < nch; k += kWarp) pz += sh.rm[rb][k];
-        pz = warp_sum(pz);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+        if (!greedy) b += __shfl_xor_sync(0xffffffffu, b, o);
+        t += __shfl_xor_sync(0xffffffffu, t, o);
     }
-    if (w == 0) {
-        msg.B[r] = B;
-        msg.S[r] = S;
-        msg.bad[r] = bad;
-        msg.gmax[r] = gmax;
-        msg.garg[r] = garg;
-    }
-    if (lane == 0) {
-        const bool hx = nr > 0 && sh.x_stamp[wb] == g + 1;
-        msg.has_x = hx ? 1 : 0;
-        msg.yx[0] = hx ? sh.yx[wb][0] : 0.0f;
-        msg.yx[1] = hx ? sh.yx[wb][1] : 0.0f;
-        msg.tmo = sh.timed_out;
-        msg.prev_alpha = alpha;
-        msg.prev_Z = pz;
-    }
+    const int a1 = __shfl_sync(0xffffffffu, a, 16);
+    const float b1 = __shfl_sync(0xffffffffu, b, 16);
+    const float alpha = __shfl_sync(0xffffffffu, t, 0), Z = __shfl_sync(0xffffffffu, t, 16);
+    const bool hx = nr > 0 && sh.x_stamp[wb] == g + 1;
+    const int flags = (hx ? sh.x_flags[wb] : 0) | (sh.timed_out ? XF_TMO : 0);
+    rec[0] = make_uint4(static_cast<uint32_t>(a), static_cast<uint32_t>(a1), __float_as_uint(b), __float_as_uint(b1));
+    rec[1] = make_uint4(__float_as_uint(hx ? sh.xE[wb][0] : 0.0f), __float_as_uint(hx ? sh.xE[wb][1] : 0.0f),
+                        static_cast<uint32_t>(flags), 0u);
+    rec[2] = make_uint4(__float_as_uint(alpha), __float_as_uint(Z), 0u, 0u);
 }
 
 // Control warp, after the exchange of item g: combine the C records (lanes 0-15 take row 0,
 // lanes 16-31 row 1, one lane per CTA, in CTA order; C is a power of two, so log2(C) butterfly
-// steps combine them) and decide the accept test. Every lane then computes the whole scalar tail
-// (the test, lambda, the log2 of both normalisers): independent chains that the compiler
-// interleaves, where a split over lanes would run them one after the other. Every CTA runs the
+// steps combine them: the max reference, then the sums scaled to it by exact powers of two) and
+// decide the accept test. Every lane then computes the whole scalar tail (the test, lambda, the
+// log2 of both normalisers): independent chains that the compiler interleaves. Every CTA runs the
 // same reductions on the same records, so all reach the same decision.
 __device__ __forceinline__ void decide_item(CtaShared &sh, const Msg *M, const Desc &d, int nr, int g, int C,
                                             const RowsParams &P, int lane) {
     const int r = lane >> 4, c = lane & 15;
     const bool on = c < C && r < nr;
-    const Msg &m = M[c < C ? c : 0];
-    const unsigned tmo = __ballot_sync(0xffffffffu, r == 0 && c < C && m.tmo);
-    const unsigned hx = __ballot_sync(0xffffffffu, r == 0 && c < C && m.has_x);
-    const unsigned badm = __ballot_sync(0xffffffffu, on && m.bad[r]);
-    const int lx = hx ? 31 - __clz(static_cast<int>(hx)) : 0;
-    const float yx_t = __shfl_sync(0xffffffffu, m.yx[0], lx), yx_d = __shfl_sync(0xffffffffu, m.yx[1], lx);
-    float Bv = -INFINITY, S = 0.0f, gm = -INFINITY;
-    int ga = INT_MAX;
+    const Msg &m = M[c];
+    const int4 fx = *reinterpret_cast<const int4 *>(&m.E_hi);
+    const int myflags = (r == 0 && c < C) ? fx.z : 0;
+    const unsigned hx = __ballot_sync(0xffffffffu, myflags & XF_HAS);
+    int flags = myflags;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) flags |= __shfl_xor_sync(0xffffffffu, flags, o);
+    flags = __shfl_sync(0xffffffffu, flags, 0);
+    const int lx = hx ? __ffs(hx) - 1 : 0;
+    const float E_hi = __shfl_sync(0xffffffffu, __int_as_float(fx.x), lx);
+    const float E_lo = __shfl_sync(0xffffffffu, __int_as_float(fx.y), lx);
+    int a = on ? m.a[r] : (d.greedy ? INT_MAX : kNoRef);
+    float b = on ? m.b[r] : (d.greedy ? -INFINITY : 0.0f);
     if (d.greedy) {
-        gm = on ? m.gmax[r] : -INFINITY;
-        ga = on ? m.garg[r] : INT_MAX;
-        half_argmax(gm, ga, C);
+        half_argmax(b, a, C);
     } else {
-        const float Sc = on ? m.S[r] : 0.0f;
-        const float Bc = Sc > 0.0f ? m.B[r] : -INFINITY;
-        Bv = Bc;
+        int Bm = a;
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1)
-            if (o < C) Bv = fmaxf(Bv, __shfl_xor_sync(0xffffffffu, Bv, o));
-        S = Sc > 0.0f ? Sc * pow2i(Bc - Bv) : 0.0f;
+            if (o < C) Bm = max(Bm, __shfl_xor_sync(0xffffffffu, Bm, o));
+        b = (a == kNoRef) ? b * 0.0f : b * pow2_int(a - Bm);  // a NaN sum stays NaN
+        a = Bm;
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1)
-            if (o < C) S += __shfl_xor_sync(0xffffffffu, S, o);
+            if (o < C) b += __shfl_xor_sync(0xffffffffu, b, o);
     }
     // rows 0 and 1 from lanes 0 and 16, to every lane
-    const int bad0 = (badm & 0xffffu) != 0, bad1 = (badm >> 16) != 0;
-    const float B0 = __shfl_sync(0xffffffffu, Bv, 0), B1 = __shfl_sync(0xffffffffu, Bv, 16);
-    const float S0 = __shfl_sync(0xffffffffu, S, 0), S1 = __shfl_sync(0xffffffffu, S, 16);
-    const float gm0 = __shfl_sync(0xffffffffu, gm, 0), gm1 = __shfl_sync(0xffffffffu, gm, 16);
-    const int ga0 = __shfl_sync(0xffffffffu, ga, 0), ga1 = __shfl_sync(0xffffffffu, ga, 16);
-    const int am0 = (nr >= 1 && !(bad0 || gm0 == -INFINITY)) ? ga0 : -1;
-    const int am1 = (nr >= 2 && !(bad1 || gm1 == -INFINITY)) ? ga1 : -1;
-    const float B_t = (nr >= 1) ? (bad0 ? NAN : B0) : NAN, B_d = (nr >= 2) ? (bad1 ? NAN : B1) : NAN;
+    const int B0 = __shfl_sync(0xffffffffu, a, 0), B1 = __shfl_sync(0xffffffffu, a, 16);
+    const float S0 = __shfl_sync(0xffffffffu, b, 0), S1 = __shfl_sync(0xffffffffu, b, 16);
+    const int ga0 = B0, ga1 = B1;
+    const float gm0 = S0, gm1 = S1;
+    const bool tmo = (flags & XF_TMO) != 0;
+    const int am0 = (nr >= 1 && ga0 >= 0 && gm0 != -INFINITY) ? ga0 : -1;
+    const int am1 = (nr >= 2 && ga1 >= 0 && gm1 != -INFINITY) ? ga1 : -1;
+    // a NaN sum marks a row that holds a NaN / +inf
+    const float B_t = (nr >= 1 && B0 != kNoRef && !isnan(S0)) ? static_cast<float>(B0) : NAN;
+    const float B_d = (nr >= 2 && B1 != kNoRef && !isnan(S1)) ? static_cast<float>(B1) : NAN;
     const float S_t = (nr >= 1) ? S0 : 0.0f, S_d = (nr >= 2) ? S1 : 0.0f;
     // the status, the same in every lane; row validity is reported together with a bad proposal
     // (both are preconditions)
@@ -509,7 +530,7 @@ __device__ __forceinline__ void decide_item(CtaShared &sh, const Msg *M, const D
             const bool ok_d = !d.pair || (isfinite(B_d) && S_d > 0.0f && isfinite(S_d));
             if (!ok_t || !ok_d) status |= SPEC_REQ_BAD_LOGITS;
             // q(x) == 0 is a bad proposal for Rule 2 (checked before any draw)
-            if (d.pair && (d.x < 0 || d.x >= P.V || yx_d == -INFINITY)) status |= SPEC_REQ_BAD_PROPOSAL;
+            if (d.pair && (d.x < 0 || d.x >= P.V || (flags & XF_QZERO))) status |= SPEC_REQ_BAD_PROPOSAL;
         }
     }
     // the scalar tail in every lane (values of rows that are not there are computed and unused)
@@ -529,9 +550,9 @@ __device__ __forceinline__ void decide_item(CtaShared &sh, const Msg *M, const D
         } else if (d.pair) {
             // rho = p(x)/q(x) = 2^E * S_d/S_t with E = (y_t - y_d) s - (B_t - B_d), in float
             // pairs; 2^E from ex2 of its fraction and an exact power of two
-            if (yx_t != -INFINITY) {
-                F2 Ex = f2_mul(f2_add({yx_t, 0.0f}, {-yx_d, 0.0f}), {d.s_hi, d.s_lo});
-                Ex = f2_add(Ex, {-(B_t - B_d), 0.0f});
+            if (!(flags & XF_PZERO)) {
+                // (y_t - y_d) s came with the record of the CTA holding the draft token
+                const F2 Ex = f2_add({E_hi, E_lo}, {-(B_t - B_d), 0.0f});
                 const float nn = floorf(Ex.hi);
                 const float f = (Ex.hi - nn) + Ex.lo;
                 const F2 ratio = f2_div({S_d, 0.0f}, {S_t, 0.0f});
@@ -585,10 +606,10 @@ __device__ __forceinline__ void decide_item(CtaShared &sh, const Msg *M, const D
 // cancellation). Where it accepts, only alpha: min(p, q) = 2^min(y_t s - c_t, y_d s - c_d), c the
 // log2 of the normaliser.
 template <int DT, int NVT>
-__device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> &rd, CtaShared &sh,
+__device__ __forceinline__ void pass2_held(const uint4 (&vt)[NVT], const SmemRow<DT> &rd, CtaShared &sh,
                                       const Decision &D, int rb, int warp, int lane) {
     constexpr int H = Elt<DT>::kPerVec / 2;
-    float my_alpha = 0.0f;
+    float my_alpha = 0.0f, my_z = 0.0f;
     if (D.status == 0 && D.pair && !D.greedy) {
         const float2 shi2 = f2splat(D.s_hi), slo2 = f2splat(D.s_lo);
         if (D.kind == SAMPLE_RESIDUAL) {
@@ -614,6 +635,7 @@ __device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> 
                     acc_a = __fadd2_rn(acc_a, make_float2(fminf(et.x, -nq.x), fminf(et.y, -nq.y)));
                 }
                 const float rs = warp_sum(racc.x + racc.y);
+                my_z += rs;
                 if (lane == 0) sh.rm[rb][v * kWarps + warp] = rs;
             }
             my_alpha = (acc_a.x + acc_a.y) * D.inv_St;
@@ -638,7 +660,78 @@ __device__ __forceinline__ void pass2(const uint4 (&vt)[NVT], const SmemRow<DT> 
         }
     }
     my_alpha = warp_sum(my_alpha);
-    if (lane == 0) sh.wal[rb][warp] = my_alpha;
+    if (lane == 0) {
+        sh.wal[rb][warp] = my_alpha;
+        sh.wz[rb][warp] = my_z;
+    }
+}
+
+// kLag > 0: pass 2 of a pair under Rule 2, its two rows read again from global memory (pass 1's
+// copies left them in L2 a few items earlier; these loads stream them out, evict-first). Thread t
+// takes vectors t + 480 v of the slice, as in pass 1. The arithmetic is that of pass2_held.
+template <int DT, int NVT>
+__device__ __forceinline__ void pass2_l2(const RowsParams &P, CtaShared &sh, const Decision &D, int rb, int lo,
+                                         int nvec, int warp, int lane, int tid) {
+    constexpr int H = Elt<DT>::kPerVec / 2;
+    float my_alpha = 0.0f, my_z = 0.0f;
+    if (D.status == 0 && D.pair && !D.greedy) {
+        const uint4 *tr = static_cast<const uint4 *>(P.target) + static_cast<size_t>(D.item) * P.nvec_row + lo;
+        const uint4 *dr = static_cast<const uint4 *>(P.draft) + static_cast<size_t>(D.drow) * P.nvec_row + lo;
+        const float2 shi2 = f2splat(D.s_hi), slo2 = f2splat(D.s_lo);
+        if (D.kind == SAMPLE_RESIDUAL) {
+            const float2 nbt = f2splat(-D.B_t), nbd = f2splat(-D.B_d);
+            const float2 nlh = f2splat(-D.lam.hi), nll = f2splat(-D.lam.lo);
+            float2 acc_a = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int v = 0; v < NVT; ++v) {
+                if (!warp_has(v, warp, nvec)) {
+                    if (lane == 0) sh.rm[rb][v * kWarps + warp] = 0.0f;
+                    continue;
+                }
+                const int vi = tid + v * kThreads;
+                const uint4 wt = vi < nvec ? __ldcs(tr + vi) : kNegInfVec<DT>();
+                const uint4 wd = vi < nvec ? __ldcs(dr + vi) : kNegInfVec<DT>();
+                float2 racc = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float2 yt = Elt<DT>::unpack_one(wt, h), yd = Elt<DT>::unpack_one(wd, h);
+                    const float2 et = ex2x2(exp_arg2(yt, shi2, slo2, nbt));
+                    const float2 ed = ex2x2(exp_arg2(yd, shi2, slo2, nbd));
+                    const float2 r = __ffma2_rn(ed, nll, __ffma2_rn(ed, nlh, et));
+                    const float2 nq = __fmul2_rn(ed, nlh);  // -lambda_hi * e_d, for min(p, q)
+                    racc = __fadd2_rn(racc, make_float2(fmaxf(r.x, 0.0f), fmaxf(r.y, 0.0f)));
+                    acc_a = __fadd2_rn(acc_a, make_float2(fminf(et.x, -nq.x), fminf(et.y, -nq.y)));
+                }
+                const float rs = warp_sum(racc.x + racc.y);
+                my_z += rs;
+                if (lane == 0) sh.rm[rb][v * kWarps + warp] = rs;
+            }
+            my_alpha = (acc_a.x + acc_a.y) * D.inv_St;
+        } else {
+            const float2 nct = f2splat(-D.c_t), ncd = f2splat(-D.c_d);
+            const float2 nctf = f2splat(-D.c_tf), ncdf = f2splat(-D.c_df);
+            float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int v = 0; v < NVT; ++v) {
+                if (!warp_has(v, warp, nvec)) continue;
+                const int vi = tid + v * kThreads;
+                const uint4 wt = vi < nvec ? __ldcs(tr + vi) : kNegInfVec<DT>();
+                const uint4 wd = vi < nvec ? __ldcs(dr + vi) : kNegInfVec<DT>();
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const float2 at = __fadd2_rn(__ffma2_rn(Elt<DT>::unpack_one(wt, h), shi2, nct), nctf);
+                    const float2 ad = __fadd2_rn(__ffma2_rn(Elt<DT>::unpack_one(wd, h), shi2, ncd), ncdf);
+                    acc = __fadd2_rn(acc, make_float2(ex2(fminf(at.x, ad.x)), ex2(fminf(at.y, ad.y))));
+                }
+            }
+            my_alpha = acc.x + acc.y;
+        }
+    }
+    my_alpha = warp_sum(my_alpha);
+    if (lane == 0) {
+        sh.wal[rb][warp] = my_alpha;
+        sh.wz[rb][warp] = my_z;
+    }
 }
 
 // The draw weights of one vector, exactly as the passes summed them: the residual in units of
@@ -677,7 +770,9 @@ __device__ __forceinline__ void draw_weights(int kind, const uint4 &wt, const ui
 // Mass of CTA c's slice in the law a draw of item m uses (units 2^B_t).
 __device__ __forceinline__ F2 cta_mass(const Msg &Mi, const Msg &Mn, int kind, float B_t) {
     if (kind == SAMPLE_RESIDUAL) return {Mn.prev_Z, 0.0f};
-    return Mi.S[0] > 0.0f ? F2{Mi.S[0] * pow2i(Mi.B[0] - B_t), 0.0f} : F2{0.0f, 0.0f};
+    // B_t is the cluster's max of the CTA references, an integer
+    return (Mi.a[0] != kNoRef && Mi.b[0] > 0.0f) ? F2{Mi.b[0] * pow2_int(Mi.a[0] - static_cast<int>(B_t)), 0.0f}
+                                                 : F2{0.0f, 0.0f};
 }
 
 // What the control warp knows about item m's draw after the exchange that carries its totals.
@@ -973,11 +1068,11 @@ __device__ __forceinline__ void control_item(CtaShared &sh, const RowsParams &P,
                                  kMaxWaitTries))
         sh.timed_out = 1;
     __syncwarp();
-    build_record(sh, greedy, nr, g, g - 1, nch, lane);
-    __syncwarp();
+    uint4 rec[3];
+    build_record(sh, greedy, nr, g, g - 1, lane, rec);
     if (g == 0) cluster_wait();  // the peers run and their barriers are ready
-    Msg *const here = slots + (g % kNMS) * C;
-    push_record(&sh.mine, here, &sh.msg_bar[g % kNMS], crank, C, lane);
+    Msg *const here = slots + (g % kNMS) * kMaxCluster;
+    push_record(rec, here, &sh.msg_bar[g % kNMS], crank, C, lane);
     if (lane == 0) mbar_arrive_expect_tx(&sh.msg_bar[g % kNMS], static_cast<uint32_t>(C * kMsgBytes));
     complete_draw<DT>(sh, P, lo, lane);  // the draw fetched at the previous exchange
     if (!mbar_wait_sleep_bounded(&sh.msg_bar[g % kNMS], static_cast<uint32_t>((g / kNMS) & 1), kSuspendNs,
@@ -990,9 +1085,32 @@ __device__ __forceinline__ void control_item(CtaShared &sh, const RowsParams &P,
         if (lane == 0) mbar_arrive(&sh.dec_bar[g % kND]);
     }
     if (g >= 1) {
-        const FinState f = finalize_head(sh, P, g - 1, slots + ((g - 1) % kNMS) * C, here, C, crank, lane);
+        const FinState f = finalize_head(sh, P, g - 1, slots + ((g - 1) % kNMS) * kMaxCluster, here, C, crank, lane);
         if (f.owner == crank) draw_chunk<DT>(sh, P, g - 1, f, lane, nch, lo, nvec);
     }
+}
+
+// Pass 1 of a pair: the thread that holds the draft token x records (y_t - y_d) s there as a float
+// pair (for the accept ratio) and whether p(x) or q(x) is zero.
+template <int DT, int NVT>
+__device__ __forceinline__ void extract_x(CtaShared &sh, const Desc &d, const uint4 (&vt)[NVT], const SmemRow<DT> &rd,
+                                          int wb, int g, int lo, int nvec, int V, int tid) {
+    constexpr int E = Elt<DT>::kPerVec;
+    const int x = d.x;
+    if (x < 0 || x >= V) return;
+    const int xv = x / E - lo;
+    if (xv < 0 || xv >= nvec || (xv % kThreads) != tid) return;
+    const int vx = xv / kThreads, e = x % E;
+    float yt = 0.0f;
+#pragma unroll
+    for (int v = 0; v < NVT; ++v)
+        if (v == vx) yt = vec_elem<DT>(vt[v], e);
+    const float yd = vec_elem<DT>(rd.src[xv], e);
+    const F2 Ex = f2_mul(f2_add({yt, 0.0f}, {-yd, 0.0f}), {d.s_hi, d.s_lo});
+    sh.xE[wb][0] = Ex.hi;
+    sh.xE[wb][1] = Ex.lo;
+    sh.x_flags[wb] = XF_HAS | (yd == -INFINITY ? XF_QZERO : 0) | (yt == -INFINITY ? XF_PZERO : 0);
+    sh.x_stamp[wb] = g + 1;
 }
 
 // Load the slice of one ring slot into registers: thread t takes vectors t, t + 480, ... so that
@@ -1035,7 +1153,8 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
     const int nch = NVT * kWarps;
     const int ncl = P.nclusters;
     const int nitems = cid < P.total_rows ? (P.total_rows - 1 - cid) / ncl + 1 : 0;
-    // the exchange slots follow the ring: kNMS exchanges x C records, the same layout in every CTA
+    // the exchange slots follow the ring: kNMS exchanges x kMaxCluster records (C used), the same
+    // layout in every CTA
     Msg *const slots = reinterpret_cast<Msg *>(smem_raw + static_cast<size_t>(kRing) * slice_max * 16);
 
     if (tid == 0) {
@@ -1046,13 +1165,13 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
         for (int k = 0; k < kNMS; ++k) mbar_init(&sh.msg_bar[k], 1);
         for (int k = 0; k < kSB; ++k) mbar_init(&sh.stats_bar[k], kWarps);
         for (int k = 0; k < kND; ++k) mbar_init(&sh.dec_bar[k], 1);
+        for (int k = 0; k < kPB; ++k) mbar_init(&sh.p2_bar[k], kWarps);
         mbar_init(&sh.draw_bar, 1);
         fence_mbar_init();
         sh.timed_out = 0;
         sh.draw_pending = 0;
         sh.draw_phase = 0;
         for (int k = 0; k < kWS; ++k) sh.x_stamp[k] = 0;
-        sh.mine.prev_alpha = sh.mine.prev_Z = 0.0f;
         sh.prod_issued = 0;
     }
     __syncthreads();  // the barriers are initialised
@@ -1061,13 +1180,14 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
     cluster_arrive();
 
     if (warp < kWarps) {
+      if constexpr (kLag == 0) {
         // ================= data warps: pass 1, the decision, pass 2 (rows held on chip) ========
         long long R = 0;  // ring row of the item's target row
         int g0 = 0;       // the batch's first item, counted over the whole list
         for (int nb = 0; nb < nitems; nb += kMaxItems) {
             const int nbatch = min(kMaxItems, nitems - nb);
             bar_sync(BAR_BATCH, kBlock);  // the control warp has the batch's descriptors
-            if (tid == 0) {
+            if (tid == 0 && nb > 0) {  // the first batch's copies went out with its shapes
                 sh.prod_item = 0;
                 sh.prod_row = 0;
                 produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, sh.prod_issued, R + kRing, sh.prod_item,
@@ -1098,19 +1218,7 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
                     } else {
                         pair_stats<DT, NVT>(vt, rd, sh, wb, d, nvec, warp, lane);
                     }
-                    // the logits at the draft token, from the thread that holds them
-                    const int x = d.x;
-                    if (x >= 0 && x < P.V) {
-                        const int xv = x / E - lo;
-                        if (xv >= 0 && xv < nvec && (xv % kThreads) == tid) {
-                            const int vx = xv / kThreads, e = x % E;
-#pragma unroll
-                            for (int v = 0; v < NVT; ++v)
-                                if (v == vx) sh.yx[wb][0] = vec_elem<DT>(vt[v], e);
-                            sh.yx[wb][1] = vec_elem<DT>(rd.src[xv], e);
-                            sh.x_stamp[wb] = g + 1;
-                        }
-                    }
+                    extract_x<DT, NVT>(sh, d, vt, rd, wb, g, lo, nvec, P.V, tid);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.stats_bar[g % kSB]);
@@ -1120,10 +1228,11 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
                                              kMaxWaitTries))
                     sh.timed_out = 1;
                 if (nr == 2) {
-                    pass2<DT, NVT>(vt, rd, sh, sh.dec[g % kND], g % kRM, warp, lane);
+                    pass2_held<DT, NVT>(vt, rd, sh, sh.dec[g % kND], g % kRM, warp, lane);
                     release_row(sh, ring, P, slice_max, lo, nvec, nbatch, R + 1, lane);  // the draft slot
                 } else if (lane == 0) {
                     sh.wal[g % kRM][warp] = 0.0f;
+                    sh.wz[g % kRM][warp] = 0.0f;
                 }
                 R += nr;
             }
@@ -1132,6 +1241,67 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
         // the drain: the last pass 2 is done, its totals go out with one more exchange
         __syncwarp();
         if (nitems > 0 && lane == 0) mbar_arrive(&sh.stats_bar[nitems % kSB]);
+      } else {
+        // ================= data warps: pass 1 of item i, then pass 2 of item i - kLag =========
+        long long R = 0;  // ring row of the item's target row
+        int g0 = 0;       // the batch's first item, counted over the whole list
+        for (int nb = 0; nb < nitems; nb += kMaxItems) {
+            const int nbatch = min(kMaxItems, nitems - nb);
+            bar_sync(BAR_BATCH, kBlock);  // the control warp has the batch's descriptors
+            if (tid == 0 && nb > 0) {  // the first batch's copies went out with its shapes
+                sh.prod_item = 0;
+                sh.prod_row = 0;
+                produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, sh.prod_issued, R + kRing, sh.prod_item,
+                             sh.prod_row);
+            }
+            for (int i = 0; i < nbatch + kLag; ++i) {
+                if (i < nbatch) {
+                    const int g = g0 + i, wb = g % kWS;
+                    const Desc &d = sh.desc[i];
+                    const int nr = desc_rows(d);
+                    uint4 vt[NVT];
+                    bool ok = true;
+                    if (nr >= 1) {
+                        ok = load_row<DT, NVT>(sh, ring, slice_max, nvec, R, tid, vt);
+                        // this warp holds the target row in registers: its slot may refill
+                        release_row(sh, ring, P, slice_max, lo, nvec, nbatch, R, lane);
+                    }
+                    const SmemRow<DT> rd = {ring + static_cast<size_t>((R + 1) % kRing) * slice_max, tid, nvec};
+                    if (nr == 2)
+                        ok &= mbar_wait_sleep_bounded(&sh.full[(R + 1) % kRing],
+                                                      static_cast<uint32_t>(((R + 1) / kRing) & 1), kSuspendNs,
+                                                      kMaxWaitTries);
+                    if (!ok) sh.timed_out = 1;
+                    if (nr == 1)
+                        row_stats<DT, NVT, true>(RegRow<NVT>{vt}, sh, wb, 0, g % kPM, d, lo, nvec, warp, lane, tid);
+                    if (nr == 2) {
+                        if (d.greedy) {
+                            row_stats<DT, NVT, false>(RegRow<NVT>{vt}, sh, wb, 0, 0, d, lo, nvec, warp, lane, tid);
+                            row_stats<DT, NVT, false>(rd, sh, wb, 1, 0, d, lo, nvec, warp, lane, tid);
+                        } else {
+                            pair_stats<DT, NVT>(vt, rd, sh, wb, d, nvec, warp, lane);
+                        }
+                        extract_x<DT, NVT>(sh, d, vt, rd, wb, g, lo, nvec, P.V, tid);
+                        // pass 1 of this warp is done with the draft row
+                        release_row(sh, ring, P, slice_max, lo, nvec, nbatch, R + 1, lane);
+                    }
+                    R += nr;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.stats_bar[g % kSB]);
+                }
+                if (i >= kLag) {
+                    const int m = g0 + i - kLag;
+                    if (!mbar_wait_sleep_bounded(&sh.dec_bar[m % kND], static_cast<uint32_t>((m / kND) & 1),
+                                                 kSuspendNs, kMaxWaitTries))
+                        sh.timed_out = 1;
+                    pass2_l2<DT, NVT>(P, sh, sh.dec[m % kND], m % kRM, lo, nvec, warp, lane, tid);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.p2_bar[m % kPB]);
+                }
+            }
+            g0 += nbatch;
+        }
+      }
         if (tid == 0 && sh.timed_out) {
             // a copy did not land in time: wait (bounded) once more so that none is left in flight
             for (long long r = max(0LL, sh.prod_issued - kRing); r < sh.prod_issued; ++r)
@@ -1148,10 +1318,19 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
                                  static_cast<size_t>(cid + lane * ncl) * row_bytes + static_cast<size_t>(lo) * 16,
                              static_cast<uint32_t>(nvec) * 16);
         }
+      if constexpr (kLag == 0) {
         int g = 0;  // item (and exchange) number; exchange nitems is the drain
         for (int nb = 0; nb < nitems; nb += kMaxItems) {
             const int nbatch = min(kMaxItems, nitems - nb);
             load_batch_shapes(sh, P, cid, nb, nbatch, lane);
+            if (nb == 0 && lane == 0) {
+                // the first rows go out as soon as the shapes are known, while the values load (the
+                // ring is empty; later batches are started by the data warps)
+                sh.prod_item = 0;
+                sh.prod_row = 0;
+                produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, sh.prod_issued, kRing, sh.prod_item,
+                             sh.prod_row);
+            }
             load_batch_values(sh, P, nbatch, lane);
             __syncwarp();
             bar_arrive(BAR_BATCH, kBlock);
@@ -1164,6 +1343,69 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
         } else {
             cluster_wait();
         }
+      } else {
+        int e = 0;   // exchanges so far
+        int g0 = 0;  // the batch's first item
+        for (int nb = 0; nb < nitems; nb += kMaxItems) {
+            const int nbatch = min(kMaxItems, nitems - nb);
+            load_batch_shapes(sh, P, cid, nb, nbatch, lane);
+            if (nb == 0 && lane == 0) {
+                // the first rows go out as soon as the shapes are known, while the values load (the
+                // ring is empty; later batches are started by the data warps)
+                sh.prod_item = 0;
+                sh.prod_row = 0;
+                produce_rows(sh, ring, P, slice_max, lo, nvec, nbatch, sh.prod_issued, kRing, sh.prod_item,
+                             sh.prod_row);
+            }
+            load_batch_values(sh, P, nbatch, lane);
+            __syncwarp();
+            bar_arrive(BAR_BATCH, kBlock);
+            const int e0 = e;  // the exchange of the batch's item i is e0 + i
+            // exchange j carries item j's record (j < nbatch) and the totals of item j - kLag - 1;
+            // kLag + 1 draining exchanges follow the batch's last item
+            for (int j = 0; j < nbatch + kLag + 1; ++j) {
+                const int g = g0 + j, m = j - kLag - 1;
+                int nr = 0, greedy = 0;
+                if (j < nbatch) {
+                    nr = desc_rows(sh.desc[j]);
+                    greedy = sh.desc[j].greedy;
+                    if (!mbar_wait_sleep_bounded(&sh.stats_bar[g % kSB], static_cast<uint32_t>((g / kSB) & 1),
+                                                 kSuspendNs, kMaxWaitTries))
+                        sh.timed_out = 1;
+                }
+                if (m >= 0 && !mbar_wait_sleep_bounded(&sh.p2_bar[(g0 + m) % kPB],
+                                                       static_cast<uint32_t>(((g0 + m) / kPB) & 1), kSuspendNs,
+                                                       kMaxWaitTries))
+                    sh.timed_out = 1;
+                __syncwarp();
+                uint4 rec[3];
+                build_record(sh, greedy, nr, g, m >= 0 ? g0 + m : -1, lane, rec);
+                if (e == 0) cluster_wait();  // the peers run and their barriers are ready
+                Msg *const here = slots + (e % kNMS) * kMaxCluster;
+                push_record(rec, here, &sh.msg_bar[e % kNMS], crank, C, lane);
+                if (lane == 0) mbar_arrive_expect_tx(&sh.msg_bar[e % kNMS], static_cast<uint32_t>(C * kMsgBytes));
+                complete_draw<DT>(sh, P, lo, lane);  // the draw fetched at the previous exchange
+                if (!mbar_wait_sleep_bounded(&sh.msg_bar[e % kNMS], static_cast<uint32_t>((e / kNMS) & 1),
+                                             kSuspendNs, kMaxWaitTries))
+                    sh.timed_out = 1;
+                __syncwarp();
+                if (j < nbatch) {
+                    decide_item(sh, here, sh.desc[j], nr, g, C, P, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.dec_bar[g % kND]);
+                }
+                if (m >= 0) {
+                    const FinState f = finalize_head(sh, P, g0 + m, slots + ((e0 + m) % kNMS) * kMaxCluster, here,
+                                                     C, crank, lane);
+                    if (f.owner == crank) draw_chunk<DT>(sh, P, g0 + m, f, lane, nch, lo, nvec);
+                }
+                ++e;
+            }
+            complete_draw<DT>(sh, P, lo, lane);  // the batch's last draw
+            g0 += nbatch;
+        }
+        if (nitems == 0) cluster_wait();
+      }
     }
     __syncwarp();
     cluster_sync_all();  // no CTA leaves while another may still write into its shared memory

@@ -251,7 +251,7 @@ static cudaError_t shape_table(int nvec_row, ShapeTable &out) {
         e = cudaFuncGetAttributes(&fa, k);
         if (e != cudaSuccess) return e;
         // the row ring, then the exchange slots (kNMS exchanges x C records)
-        const size_t smem = static_cast<size_t>(kRing) * slice * 16 + static_cast<size_t>(kNMS) * C * sizeof(Msg);
+        const size_t smem = static_cast<size_t>(kRing) * slice * 16 + static_cast<size_t>(kNMS) * kMaxCluster * sizeof(Msg);
         if (smem + fa.sharedSizeBytes > static_cast<size_t>(max_optin)) continue;
         const int ki = (nvt == 2) ? 0 : (nvt == 4) ? 1 : 2;
         if (!attrs_set[ki]) {
