@@ -42,6 +42,7 @@ class _Batch(ctypes.Structure):
         ("B", _i32), ("V", _i32), ("K_max", _i32), ("dtype", _i32),
         ("target", _p), ("draft", _p), ("row_off", _p), ("draft_tokens", _p),
         ("uniforms", _p), ("temperature", _p), ("stop_token", _p), ("max_new", _p),
+        ("top_k", _p), ("top_p", _p),
     ]
 
 
@@ -50,6 +51,7 @@ class _Result(ctypes.Structure):
         ("accept_len", _p), ("out_tokens", _p), ("n_emitted", _p), ("req_status", _p),
         ("alpha", _p), ("rho", _p), ("resid_mass", _p), ("accept_margin", _p),
         ("sample_margin", _p), ("sample_prob", _p), ("fallback", _p),
+        ("trunc_margin", _p), ("trunc_keep", _p),
     ]
 
 
@@ -118,7 +120,7 @@ def _c(a, dtype):
 
 
 def verify(target, draft, row_off, draft_tokens, uniforms, temperature, *, V=None,
-           K_max=64, stop_token=None, max_new=None):
+           K_max=64, stop_token=None, max_new=None, top_k=None, top_p=None):
     """Run the verifier on host arrays.
 
     ``target``/``draft`` are 2-D float32 arrays, or uint16 arrays holding bfloat16 bits.
@@ -141,6 +143,8 @@ def verify(target, draft, row_off, draft_tokens, uniforms, temperature, *, V=Non
     temperature = _c(np.broadcast_to(np.asarray(temperature, np.float32), (B,)), np.float32)
     stop_token = _c(stop_token, np.int32)
     max_new = _c(max_new, np.int32)
+    top_k = None if top_k is None else _c(np.broadcast_to(np.asarray(top_k, np.int32), (B,)), np.int32)
+    top_p = None if top_p is None else _c(np.broadcast_to(np.asarray(top_p, np.float32), (B,)), np.float32)
     assert uniforms.shape[0] >= T and draft_tokens.shape[0] >= nd
 
     out = {
@@ -150,10 +154,11 @@ def verify(target, draft, row_off, draft_tokens, uniforms, temperature, *, V=Non
         "resid_mass": np.zeros(nd, np.float64), "accept_margin": np.zeros(nd, np.float64),
         "sample_margin": np.zeros(B, np.float64), "sample_prob": np.zeros(B, np.float64),
         "fallback": np.zeros(B, np.int32),
+        "trunc_margin": np.full(T, np.nan, np.float64), "trunc_keep": np.full(T, V, np.int32),
     }
     b = _Batch(B, V, K_max, 1 if bf16 else 0, _ptr(target), _ptr(draft), _ptr(row_off),
                _ptr(draft_tokens), _ptr(uniforms), _ptr(temperature), _ptr(stop_token),
-               _ptr(max_new))
+               _ptr(max_new), _ptr(top_k), _ptr(top_p))
     r = _Result(*[_ptr(out[f]) for f, _ in _Result._fields_])
     rc = lib.oracle_verify(ctypes.byref(b), ctypes.byref(r))
     if rc != 0:

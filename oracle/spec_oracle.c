@@ -41,9 +41,77 @@ typedef struct {
     double T;
     int greedy;
     int32_t argmax; /* smallest index attaining the maximum logit */
-    double m, logS; /* only for T > 0 */
+    double m, logS; /* only for T > 0; S over the kept tokens */
     int valid;      /* 0 when a logit is NaN or +inf or none is finite */
+    /* top-k / top-p: token v is kept when (z_v, v) ranks no later than (z_cut, id_cut) in the
+     * order "larger logit first, then smaller id"; without truncation every token is kept */
+    int truncated;
+    double z_cut;
+    int32_t id_cut, keep;
+    double cut_margin; /* top-p only: |top_p - nearer cumulative mass at the cut| */
 } row_law;
+
+static int row_kept(const row_law *L, double z, int32_t v) {
+    if (!L->truncated) return 1;
+    return z > L->z_cut || (z == L->z_cut && v <= L->id_cut);
+}
+
+/* Ranking of one row for the truncation: larger logit first, then smaller id. */
+typedef struct {
+    double z;
+    int32_t v;
+} ranked;
+
+static int ranked_cmp(const void *a, const void *b) {
+    const ranked *x = (const ranked *)a, *y = (const ranked *)b;
+    if (x->z > y->z) return -1;
+    if (x->z < y->z) return 1;
+    return (x->v > y->v) - (x->v < y->v);
+}
+
+/* Top-k, then top-p (SDCP "Session Model", in that order) on the row's law at temperature T:
+ * rank the tokens; keep the first n_k = k of them (all when k <= 0 or k >= V); renormalise p
+ * over them; keep the first n_p whose cumulative mass reaches top_p (n_p >= 1; all when
+ * top_p >= 1). Records the last kept token as the cut. */
+static void row_truncate(row_law *L, int32_t top_k, double top_p) {
+    const int32_t V = L->V;
+    L->truncated = 0;
+    L->keep = V;
+    L->cut_margin = NAN;
+    const int use_k = top_k > 0 && top_k < V, use_p = top_p < 1.0;
+    if (!use_k && !use_p) return;
+    ranked *r = (ranked *)malloc(sizeof(ranked) * (size_t)V);
+    if (!r) return;
+    for (int32_t v = 0; v < V; ++v) {
+        r[v].z = logit_at(L->base, L->dtype, L->row, V, v);
+        r[v].v = v;
+    }
+    qsort(r, (size_t)V, sizeof(ranked), ranked_cmp);
+    int32_t n = use_k ? top_k : V;
+    if (use_p) {
+        /* masses of the top-k head, renormalised over it */
+        double Sk = 0.0;
+        for (int32_t j = 0; j < n; ++j) Sk += exp(r[j].z / L->T - L->m);
+        double cum = 0.0, prev = 0.0;
+        int32_t np = n;
+        for (int32_t j = 0; j < n; ++j) {
+            prev = cum;
+            cum += exp(r[j].z / L->T - L->m) / Sk;
+            if (cum >= top_p) {
+                np = j + 1;
+                break;
+            }
+        }
+        const double d1 = fabs(cum - top_p), d0 = fabs(prev - top_p);
+        L->cut_margin = d1 < d0 ? d1 : d0;
+        n = np;
+    }
+    L->truncated = 1;
+    L->keep = n;
+    L->z_cut = r[n - 1].z;
+    L->id_cut = r[n - 1].v;
+    free(r);
+}
 
 static row_law row_law_make(const void *base, int32_t dtype, int64_t row, int32_t V, double T) {
     row_law L;
@@ -57,6 +125,9 @@ static row_law row_law_make(const void *base, int32_t dtype, int64_t row, int32_
     L.m = -INFINITY;
     L.logS = 0.0;
     L.valid = 1;
+    L.truncated = 0;
+    L.keep = V;
+    L.cut_margin = NAN;
 
     double zmax = -INFINITY;
     for (int32_t v = 0; v < V; ++v) {
@@ -85,9 +156,22 @@ static row_law row_law_make(const void *base, int32_t dtype, int64_t row, int32_
     return L;
 }
 
+/* Renormalise a truncated law over its kept tokens. */
+static void row_law_renormalise(row_law *L) {
+    if (!L->truncated || L->greedy || !L->valid) return;
+    double S = 0.0;
+    for (int32_t v = 0; v < L->V; ++v) {
+        double z = logit_at(L->base, L->dtype, L->row, L->V, v);
+        if (row_kept(L, z, v)) S += exp(z / L->T - L->m);
+    }
+    L->logS = log(S);
+}
+
 static double row_prob(const row_law *L, int32_t v) {
     if (L->greedy) return v == L->argmax ? 1.0 : 0.0;
-    double y = logit_at(L->base, L->dtype, L->row, L->V, v) / L->T;
+    double z = logit_at(L->base, L->dtype, L->row, L->V, v);
+    if (!row_kept(L, z, v)) return 0.0;
+    double y = z / L->T;
     return exp(y - L->m - L->logS);
 }
 
@@ -142,8 +226,14 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
         const double T = (double)in->temperature[i];
         int32_t status = 0;
 
+        const int32_t tk = in->top_k ? in->top_k[i] : 0;
+        const double tp = in->top_p ? (double)in->top_p[i] : 1.0;
         if (K < 0 || K > in->K_max) status |= ORACLE_REQ_BAD_SHAPE;
-        if (!(T >= 0.0) || isinf(T)) status |= ORACLE_REQ_BAD_PARAM;
+        if (!(T >= 0.0) || isinf(T) || isnan(tp)) status |= ORACLE_REQ_BAD_PARAM;
+        if (K >= 0 && out->trunc_margin)
+            for (int32_t j = 0; j <= K; ++j) out->trunc_margin[r0 + j] = NAN;
+        if (K >= 0 && out->trunc_keep)
+            for (int32_t j = 0; j <= K; ++j) out->trunc_keep[r0 + j] = V;
 
         out->accept_len[i] = 0;
         out->n_emitted[i] = 0;
@@ -168,6 +258,12 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
         for (int32_t j = 0; j <= K; ++j) {
             Plaw[j] = row_law_make(in->target, in->dtype, r0 + j, V, T);
             if (!Plaw[j].valid) status |= ORACLE_REQ_BAD_LOGITS;
+            if (Plaw[j].valid && !Plaw[j].greedy) {
+                row_truncate(&Plaw[j], tk, tp);
+                row_law_renormalise(&Plaw[j]);
+                if (out->trunc_margin) out->trunc_margin[r0 + j] = Plaw[j].cut_margin;
+                if (out->trunc_keep) out->trunc_keep[r0 + j] = Plaw[j].keep;
+            }
         }
         for (int32_t j = 0; j < K; ++j) {
             Qlaw[j] = row_law_make(in->draft, in->dtype, d0 + j, V, T);
@@ -209,9 +305,11 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
                 out->rho[d0 + j] = (x == P.argmax) ? 1.0 : 0.0;
                 out->accept_margin[d0 + j] = NAN;
             } else {
-                double lp = logit_at(in->target, in->dtype, r0 + j, V, x) / T - P.m - P.logS;
+                const double zx = logit_at(in->target, in->dtype, r0 + j, V, x);
+                double lp = zx / T - P.m - P.logS;
                 double lq = logit_at(in->draft, in->dtype, d0 + j, V, x) / T - Q.m - Q.logS;
-                double rho = exp(lp - lq);
+                /* p(x) = 0 where top-k / top-p removed x */
+                double rho = row_kept(&P, zx, x) ? exp(lp - lq) : 0.0;
                 out->rho[d0 + j] = rho;
                 out->accept_margin[d0 + j] = in->uniforms[r0 + j] - rho;
             }

@@ -13,7 +13,10 @@
  *   - "Speculative Decoding Coordination Protocol (SDCP)", section "Acceptance Rules",
  *     Rule 2 (speculative sampling): the same rule, q(x) must be checked non-zero before any
  *     random draw; the accept draw and the extra-token draw are separate values.
- *   - SDCP, section "Session Model": p is the target's distribution after temperature.
+ *   - SDCP, section "Session Model": p is the target's distribution after temperature, top-k
+ *     and top-p, in that order (the draft's q is not truncated). Reading of the silent points:
+ *     tokens are ranked by logit, ties by ascending token id; top-k keeps the first k; top-p
+ *     then keeps the shortest head whose mass, renormalised over the top-k set, is >= top_p.
  *   - "M7.8 - Speculative Serving", section 0x03C (ragged acceptance) and 0x09 (draft,
  *     target and frontier cache transitions): L_out = P + A + 1, L_kv = P + A.
  *   - SOTA-227, section "Why it is free rather than a trade": alpha = E[min(p, q)] and the
@@ -36,7 +39,7 @@ extern "C" {
 #define ORACLE_REQ_BAD_PROPOSAL 1 /* draft token outside [0,V) or q(x) == 0 (draft logit -inf) */
 #define ORACLE_REQ_BAD_LOGITS   2 /* a row holds NaN or +inf, or has no finite logit          */
 #define ORACLE_REQ_BAD_SHAPE    4 /* K_i < 0 or K_i > K_max                                  */
-#define ORACLE_REQ_BAD_PARAM    8 /* temperature not finite or < 0                           */
+#define ORACLE_REQ_BAD_PARAM    8 /* temperature not finite or < 0, or top_p NaN            */
 #define ORACLE_REQ_BAD_BLOCKS  16 /* compaction: a committed position has no page            */
 
 typedef struct {
@@ -51,6 +54,10 @@ typedef struct {
     const float *temperature;   /* [B]; 0 selects the greedy rule                             */
     const int32_t *stop_token;  /* [B] or NULL: token that ends generation (-1: none)         */
     const int32_t *max_new;     /* [B] or NULL: output tokens still allowed (budget)          */
+    const int32_t *top_k;       /* [B] or NULL: keep the k most probable tokens of p (k <= 0 or
+                                   k >= V: all)                                                */
+    const float *top_p;         /* [B] or NULL: then keep the shortest head of p, renormalised
+                                   over the top-k set, whose mass reaches top_p (>= 1: all)    */
 } oracle_batch;
 
 typedef struct {
@@ -67,6 +74,9 @@ typedef struct {
     double *sample_prob;        /* [B] probability of the frontier token under the law it was
                                    drawn from                                                  */
     int32_t *fallback;          /* [B] 1 when the residual had zero mass and p was used        */
+    double *trunc_margin;       /* [T] or NULL: distance of top_p to the nearer of the two
+                                   cumulative masses around the top-p cut (NaN: no top-p cut)  */
+    int32_t *trunc_keep;        /* [T] or NULL: tokens kept by top-k / top-p (V: all)          */
 } oracle_result;
 
 int oracle_verify(const oracle_batch *in, oracle_result *out);
