@@ -59,7 +59,7 @@ enum {
                                   found before any uniform is used (SDCP Rule 2)             */
     SPEC_REQ_BAD_LOGITS = 2,   /* a row of the request holds NaN or +inf, or no finite logit  */
     SPEC_REQ_BAD_SHAPE = 4,    /* K_i < 0, K_i > K_max, or row_off inconsistent               */
-    SPEC_REQ_BAD_PARAM = 8,    /* temperature NaN, infinite or negative                       */
+    SPEC_REQ_BAD_PARAM = 8,    /* temperature NaN, infinite or negative, or top_p NaN         */
     SPEC_REQ_BAD_BLOCKS = 16   /* spec_compact: a committed position has no page             */
 };
 
@@ -115,13 +115,24 @@ typedef struct {
        (not accumulated) by each call; the ratio is the censoring-aware acceptance rate. */
     int32_t *depth_reached;      /* [K_max]                                                    */
     int32_t *depth_accepted;     /* [K_max]                                                    */
+    /* top-k / top-p (SDCP "Session Model": p is the target's distribution after temperature,
+       top-k and top-p, in that order; q is not truncated). Tokens rank by logit, ties by
+       ascending id. Each may be NULL (no truncation); ignored under the greedy rule (T == 0).
+       The cut of each target row is computed by an extra kernel (one CTA per target row) and
+       every other token is treated as probability zero: the accept ratio, alpha, the residual
+       and both draws use the truncated, renormalised law. */
+    const int32_t *top_k;        /* [B] keep the k highest-ranked tokens (k <= 0 or k >= V: all) */
+    const float *top_p;          /* [B] then keep the shortest head whose mass, renormalised over
+                                    the top-k set, reaches top_p (>= 1: all; <= 0: the first
+                                    token; NaN: SPEC_REQ_BAD_PARAM)                            */
 } spec_verify_args;
 
 /* Bytes of device workspace spec_verify needs for a batch of total_rows target rows.
  * The workspace must be 256-byte aligned. Its contents need no initialisation. */
 size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t total_rows, spec_dtype dtype);
 
-/* Verify one round. Enqueues two kernels on `stream`; returns without waiting. */
+/* Verify one round. Enqueues two kernels on `stream` (three with top-k / top-p); returns
+ * without waiting. */
 spec_status spec_verify(const spec_verify_args *args, void *workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 
@@ -129,7 +140,7 @@ spec_status spec_verify(const spec_verify_args *args, void *workspace, size_t wo
  * memory where they verify (a memory planner that owns all device memory, a callback inside
  * another runtime, a path where cudaMalloc's synchronisation is not acceptable). The pages have
  * no counterpart to this entry point: it is an interface convenience of this library.
- * Scratch comes from one fixed array of 448 KiB in the library's device memory, present on
+ * Scratch comes from one fixed array of 576 KiB in the library's device memory, present on
  * every GPU that loads the library until exit. Limit: total_rows <= 16384 target rows per
  * call; larger batches return SPEC_ERR_UNSUPPORTED before anything is enqueued. The array's
  * address is looked up on the first call on each device (make that call before any stream

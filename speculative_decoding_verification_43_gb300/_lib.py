@@ -48,6 +48,7 @@ class SpecVerifyArgs(ctypes.Structure):
         ("rho_rows", _p), ("resid_rows", _p), ("frontier_prob", _p), ("frontier_margin", _p),
         ("fallback", _p), ("rows_event_begin", _p), ("rows_event_end", _p),
         ("depth_reached", _p), ("depth_accepted", _p),
+        ("top_k", _p), ("top_p", _p),
     ]
 
 

@@ -96,7 +96,7 @@ class Verifier:
         self._keep = ()
 
     def bind(self, target, draft, row_off, draft_tokens, uniforms, temperature=1.0, *,
-             stop_token=None, max_new=None):
+             stop_token=None, max_new=None, top_k=None, top_p=None):
         B, V, T = self.B, self.V, self.T
         assert target.dtype == self.dtype and target.is_cuda and target.is_contiguous()
         assert target.shape == (T, V), (target.shape, (T, V))
@@ -122,7 +122,13 @@ class Verifier:
             a.temperature_scalar = float(temperature)
         a.stop_token = _ptr(_i32(stop_token)) if stop_token is not None else None
         a.max_new = _ptr(_i32(max_new)) if max_new is not None else None
-        self._keep = (target, draft, row_off, draft_tokens, uniforms, temperature, stop_token, max_new)
+        # top-k / top-p of the target law, per request (None: no truncation)
+        if top_p is not None:
+            assert top_p.dtype == torch.float32 and top_p.is_cuda and top_p.numel() == B
+        a.top_k = _ptr(_i32(top_k)) if top_k is not None else None
+        a.top_p = _ptr(top_p) if top_p is not None else None
+        self._keep = (target, draft, row_off, draft_tokens, uniforms, temperature, stop_token, max_new,
+                      top_k, top_p)
         return self
 
     def time_rows_with(self, begin, end):
@@ -140,13 +146,14 @@ class Verifier:
 
 
 def verify(target, draft, row_off, draft_tokens, uniforms, temperature=1.0, *, K_max: int = 64,
-           stop_token=None, max_new=None, diagnostics: bool = False, stream=None) -> VerifyOutputs:
+           stop_token=None, max_new=None, top_k=None, top_p=None, diagnostics: bool = False,
+           stream=None) -> VerifyOutputs:
     """One verifier round on device tensors (see include/spec_verify.h for the layout)."""
     T, V = target.shape
     B = row_off.numel() - 1
     v = Verifier(B, V, T, target.dtype, K_max=K_max, device=target.device, diagnostics=diagnostics)
     v.bind(target, draft, row_off, draft_tokens, uniforms, temperature, stop_token=stop_token,
-           max_new=max_new)
+           max_new=max_new, top_k=top_k, top_p=top_p)
     return v.run(stream)
 
 

@@ -195,4 +195,13 @@ __device__ __forceinline__ F2 f2_scale(F2 a, float k) {
     return {a.hi * m, a.lo * m};
 }
 
+// ---- order-preserving integer keys of logits (a larger logit has a larger key; NaN sorts
+// outside the finite range) and the top-k / top-p cut: token v is kept when its key is above
+// tau, or equal to it with v <= id (ties rank by ascending token id).
+__device__ __forceinline__ uint32_t key_bf16(uint32_t b) { return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u); }
+__device__ __forceinline__ uint32_t key_f32(uint32_t u) { return (u & 0x80000000u) ? ~u : (u | 0x80000000u); }
+__device__ __forceinline__ bool cut_keeps(uint32_t key, int v, uint32_t tau, int id) {
+    return key > tau || (key == tau && v <= id);
+}
+
 }  // namespace spec

@@ -104,6 +104,10 @@ struct RowsParams {
     float *alpha_rows;
     float *rho_rows;
     float *resid_rows;
+    // top-k / top-p (each may be NULL): the cut of each target row, and the per-request top_p
+    // (read only to flag a NaN as a bad parameter)
+    const int2 *trunc;
+    const float *top_p;
 };
 
 // One item of this cluster's list, prepared before its rows arrive.
@@ -112,6 +116,8 @@ struct Desc {
     float s_hi, s_lo;  // log2(e)/T = s_hi + s_lo, s_hi rounded toward zero (s_lo > 0)
     int32_t greedy;
     F2 u_acc, u_s;     // the position's accept draw and the request's frontier draw
+    uint32_t cut_tau;  // top-k / top-p cut of the target row (see cut_keeps); trunc = 0: none
+    int32_t cut_id, trunc;
 };
 
 // Reference exponent of a row (or slice) with no mass.
@@ -147,6 +153,8 @@ struct Decision {
     F2 lam, u_s;
     int32_t argmax_t;
     float alpha_g;  // greedy rule: alpha of the two point masses
+    uint32_t cut_tau;  // the target row's top-k / top-p cut (trunc = 0: none)
+    int32_t cut_id, trunc;
 };
 
 enum { SAMPLE_NONE = 0, SAMPLE_RESIDUAL = 1, SAMPLE_P = 2 };
@@ -171,6 +179,30 @@ __device__ __forceinline__ void push_record(const uint4 (&rec)[3], Msg *slot_bas
 #pragma unroll
         for (int q = 0; q < 3; ++q) st_async_v4(dst + 16 * q, rec[q], rbar);
     }
+}
+
+// Top-k / top-p: the logits of one 16-byte vector of a target row (vector `vi` of the row)
+// that the row's cut removes become -inf, which turns every later sum, ratio and draw into
+// those of the truncated, renormalised law.
+template <int DT>
+__device__ __forceinline__ void mask_cut(uint4 &w, int vi, uint32_t tau, int id) {
+    uint32_t x[4] = {w.x, w.y, w.z, w.w};
+    if (DT == SPEC_BF16) {
+        const int base = vi * 8;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const uint32_t lo = x[h] & 0xFFFFu, hi = x[h] >> 16;
+            const uint32_t nlo = cut_keeps(key_bf16(lo), base + 2 * h, tau, id) ? lo : 0xFF80u;
+            const uint32_t nhi = cut_keeps(key_bf16(hi), base + 2 * h + 1, tau, id) ? hi : 0xFF80u;
+            x[h] = nlo | (nhi << 16);
+        }
+    } else {
+        const int base = vi * 4;
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            if (!cut_keeps(key_f32(x[h]), base + h, tau, id)) x[h] = 0xFF800000u;
+    }
+    w = make_uint4(x[0], x[1], x[2], x[3]);
 }
 
 template <int DT>

@@ -71,6 +71,9 @@ __device__ void load_batch_shapes(CtaShared &sh, const RowsParams &P, int cid, i
         d.greedy = 0;
         d.s_hi = d.s_lo = 0.0f;
         d.u_acc = d.u_s = {0.0f, 0.0f};
+        d.cut_tau = 0u;
+        d.cut_id = INT_MAX;
+        d.trunc = 0;
     }
     __syncwarp();
     // every request writes the descriptors of its rows that belong to this batch
@@ -116,7 +119,12 @@ __device__ void load_batch_values(CtaShared &sh, const RowsParams &P, int nbatch
         const double ua = shaped ? __ldg(P.uniforms + d.item) : 0.0;
         const double us = shaped ? __ldg(P.uniforms + r1 - 1) : 0.0;
         const int xt = (shaped && d.pair) ? __ldg(P.draft_tokens + d.drow) : -1;
-        if (!(T >= 0.0f) || isinf(T)) status |= SPEC_REQ_BAD_PARAM;
+        const int2 cut = (shaped && P.trunc) ? __ldg(P.trunc + d.item) : make_int2(0, INT_MAX);
+        const float tp = (d.req >= 0 && P.top_p) ? __ldg(P.top_p + d.req) : 1.0f;
+        if (!(T >= 0.0f) || isinf(T) || isnan(tp)) status |= SPEC_REQ_BAD_PARAM;
+        d.cut_tau = static_cast<uint32_t>(cut.x);
+        d.cut_id = cut.y;
+        d.trunc = (cut.x != 0 || cut.y != INT_MAX) ? 1 : 0;
         d.greedy = (T == 0.0f) ? 1 : 0;
         F2 sv = {0.0f, 0.0f};
         if (T > 0.0f && !isinf(T)) sv = f2_div({kLog2eHi, kLog2eLo}, {T, 0.0f});
@@ -574,6 +582,9 @@ __device__ __forceinline__ void decide_item(CtaShared &sh, const Msg *M, const D
         Decision &D = sh.dec[g % kND];
         D.item = d.item;
         D.drow = d.drow;
+        D.cut_tau = d.cut_tau;
+        D.cut_id = d.cut_id;
+        D.trunc = d.trunc;
         D.pair = d.pair;
         D.greedy = d.greedy;
         D.s_hi = d.s_hi;
@@ -689,7 +700,8 @@ __device__ __forceinline__ void pass2_l2(const RowsParams &P, CtaShared &sh, con
                     continue;
                 }
                 const int vi = tid + v * kThreads;
-                const uint4 wt = vi < nvec ? __ldcs(tr + vi) : kNegInfVec<DT>();
+                uint4 wt = vi < nvec ? __ldcs(tr + vi) : kNegInfVec<DT>();
+                if (D.trunc) mask_cut<DT>(wt, lo + vi, D.cut_tau, D.cut_id);
                 const uint4 wd = vi < nvec ? __ldcs(dr + vi) : kNegInfVec<DT>();
                 float2 racc = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -715,7 +727,8 @@ __device__ __forceinline__ void pass2_l2(const RowsParams &P, CtaShared &sh, con
             for (int v = 0; v < NVT; ++v) {
                 if (!warp_has(v, warp, nvec)) continue;
                 const int vi = tid + v * kThreads;
-                const uint4 wt = vi < nvec ? __ldcs(tr + vi) : kNegInfVec<DT>();
+                uint4 wt = vi < nvec ? __ldcs(tr + vi) : kNegInfVec<DT>();
+                if (D.trunc) mask_cut<DT>(wt, lo + vi, D.cut_tau, D.cut_id);
                 const uint4 wd = vi < nvec ? __ldcs(dr + vi) : kNegInfVec<DT>();
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
@@ -880,7 +893,9 @@ __device__ __noinline__ void fb_chunk_masses(CtaShared &sh, const RowsParams &P,
     for (int k = 0; k < nch; ++k) {
         const int vi = (k / kWarps) * kThreads + (k % kWarps) * kWarp + lane;
         float w[E];
-        draw_weights<DT>(SAMPLE_P, vi < nvec ? row[vi] : kNegInfVec<DT>(), kNegInfVec<DT>(), D, D.B_t, w);
+        uint4 wt = vi < nvec ? row[vi] : kNegInfVec<DT>();
+        if (D.trunc) mask_cut<DT>(wt, lo + vi, D.cut_tau, D.cut_id);
+        draw_weights<DT>(SAMPLE_P, wt, kNegInfVec<DT>(), D, D.B_t, w);
         float a = 0.0f;
 #pragma unroll
         for (int e = 0; e < E; ++e) a += w[e];
@@ -993,7 +1008,8 @@ __device__ __noinline__ void complete_draw(CtaShared &sh, const RowsParams &P, i
         ok = mbar_wait_sleep_bounded(&sh.draw_bar, sh.draw_phase, kSuspendNs, kMaxWaitTries);
         ok = __all_sync(0xffffffffu, ok);
     }
-    const uint4 wt = lane < count ? sh.draw_buf[0][lane] : kNegInfVec<DT>();
+    uint4 wt = lane < count ? sh.draw_buf[0][lane] : kNegInfVec<DT>();
+    if (D.trunc) mask_cut<DT>(wt, lo + sh.draw_chunk + lane, D.cut_tau, D.cut_id);
     const uint4 wd = (lane < count && kind == SAMPLE_RESIDUAL) ? sh.draw_buf[1][lane] : kNegInfVec<DT>();
     float w[E];
     draw_weights<DT>(kind, wt, wd, D, sh.draw_bg, w);
@@ -1113,6 +1129,14 @@ __device__ __forceinline__ void extract_x(CtaShared &sh, const Desc &d, const ui
     sh.x_stamp[wb] = g + 1;
 }
 
+// Top-k / top-p: apply the target row's cut to this thread's vectors (vector v of thread t is
+// vector lo + t + 480 v of the row).
+template <int DT, int NVT>
+__device__ __forceinline__ void mask_row(uint4 (&vt)[NVT], int lo, int tid, uint32_t tau, int id) {
+#pragma unroll
+    for (int v = 0; v < NVT; ++v) mask_cut<DT>(vt[v], lo + tid + v * kThreads, tau, id);
+}
+
 // Load the slice of one ring slot into registers: thread t takes vectors t, t + 480, ... so that
 // a warp reads 32 contiguous vectors (a chunk); past the slice end, -inf.
 template <int DT, int NVT>
@@ -1132,7 +1156,6 @@ __device__ __forceinline__ bool load_row(CtaShared &sh, const uint4 *ring, int s
 
 template <int DT, int NVT>
 __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P) {
-    constexpr int E = Elt<DT>::kPerVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ CtaShared sh;
     uint4 *ring = reinterpret_cast<uint4 *>(smem_raw);
@@ -1203,6 +1226,7 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
                     ok = load_row<DT, NVT>(sh, ring, slice_max, nvec, R, tid, vt);
                     // this warp holds the target row in registers: its slot may refill
                     release_row(sh, ring, P, slice_max, lo, nvec, nbatch, R, lane);
+                    if (d.trunc) mask_row<DT, NVT>(vt, lo, tid, d.cut_tau, d.cut_id);
                 }
                 const SmemRow<DT> rd = {ring + static_cast<size_t>((R + 1) % kRing) * slice_max, tid, nvec};
                 if (nr == 2)
@@ -1265,6 +1289,7 @@ __global__ void __launch_bounds__(kBlock, 2) spec_rows_kernel(const RowsParams P
                         ok = load_row<DT, NVT>(sh, ring, slice_max, nvec, R, tid, vt);
                         // this warp holds the target row in registers: its slot may refill
                         release_row(sh, ring, P, slice_max, lo, nvec, nbatch, R, lane);
+                        if (d.trunc) mask_row<DT, NVT>(vt, lo, tid, d.cut_tau, d.cut_id);
                     }
                     const SmemRow<DT> rd = {ring + static_cast<size_t>((R + 1) % kRing) * slice_max, tid, nvec};
                     if (nr == 2)

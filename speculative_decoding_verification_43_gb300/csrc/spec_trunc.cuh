@@ -1,0 +1,301 @@
+// spec_trunc_kernel: top-k, then top-p, of each target row's law (included once, by
+// spec_verify.cu).
+//
+// SDCP, section "Session Model": p is the target model's next-token distribution after
+// temperature, top-k and top-p, in that order (the draft's q is not truncated). Tokens rank by
+// logit, ties by ascending id; top-k keeps the first k; top-p then keeps the shortest head of
+// the law renormalised over the top-k set whose mass reaches top_p. The kept set of a row is a
+// prefix of that ranking, so it is one cut: token v is kept when key(v) > tau, or key(v) == tau
+// and v <= id, with key the order-preserving integer image of the logit. The per-position
+// kernel reads the cut and treats every other token of the row as a -inf logit, which is the
+// truncated, renormalised law.
+//
+// One CTA per target row: a radix select over the key, eight bits per pass, on counts (top-k)
+// or on masses (top-p), then an ordered search among the tokens tied at the cut. Masses are
+// 2^((z - z_max) s) in fixed point (2^-40 units, 64-bit integer sums): the sums, and so the cut,
+// do not depend on the order of the atomic additions.
+#pragma once
+
+#include <climits>
+#include <cstdint>
+
+#include "spec_device.cuh"
+#include "spec_math.cuh"
+
+namespace spec {
+
+constexpr int kTruncThreads = 512;
+constexpr int kTruncWarps = kTruncThreads / kWarp;
+// the cut that keeps every token (every key is >= 0)
+constexpr uint32_t kCutAllTau = 0u;
+constexpr int32_t kCutAllId = INT_MAX;
+
+struct TruncParams {
+    const void *target;
+    const int32_t *row_off;
+    const float *temperature;
+    float temperature_scalar;
+    const int32_t *top_k;  // [B] or NULL
+    const float *top_p;    // [B] or NULL
+    int32_t B, V, total_rows;
+    int2 *cut;             // [T] (tau, id) per target row
+};
+
+__device__ __forceinline__ float logit_of_key_bf16(uint32_t k) {
+    const uint32_t b = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+    return __uint_as_float(b << 16);
+}
+__device__ __forceinline__ float logit_of_key_f32(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+template <int DT>
+struct TruncElt;
+template <>
+struct TruncElt<SPEC_BF16> {
+    static constexpr int kBits = 16;
+    __device__ static __forceinline__ uint32_t key(const void *row, int v) {
+        return key_bf16(__ldg(static_cast<const uint16_t *>(row) + v));
+    }
+    __device__ static __forceinline__ float logit(uint32_t k) { return logit_of_key_bf16(k); }
+};
+template <>
+struct TruncElt<SPEC_F32> {
+    static constexpr int kBits = 32;
+    __device__ static __forceinline__ uint32_t key(const void *row, int v) {
+        return key_f32(__ldg(static_cast<const uint32_t *>(row) + v));
+    }
+    __device__ static __forceinline__ float logit(uint32_t k) { return logit_of_key_f32(k); }
+};
+
+// Shared state of one row's selection.
+struct TruncShared {
+    uint32_t hist[256];
+    unsigned long long hmass[256];
+    uint32_t wsum[kTruncWarps];
+    unsigned long long total;
+    uint32_t kmax;
+    int32_t req, found;
+    uint32_t chosen;
+    unsigned long long need;
+};
+
+
+// Block-wide max of a key (every thread gets it).
+__device__ __forceinline__ uint32_t block_max_u32(TruncShared &sh, uint32_t v, int tid) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (tid == 0) sh.kmax = 0u;
+    __syncthreads();
+    if ((tid & 31) == 0) atomicMax(&sh.kmax, v);
+    __syncthreads();
+    const uint32_t r = sh.kmax;
+    __syncthreads();
+    return r;
+}
+
+// Block-wide sum of 64-bit integers (every thread gets it).
+__device__ __forceinline__ unsigned long long block_sum_u64(TruncShared &sh, unsigned long long v, int tid) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (tid == 0) sh.total = 0ull;
+    __syncthreads();
+    if ((tid & 31) == 0) atomicAdd(&sh.total, v);
+    __syncthreads();
+    const unsigned long long r = sh.total;
+    __syncthreads();
+    return r;
+}
+
+// Exclusive prefix over the threads of the block, in thread order (every thread gets its own).
+__device__ __forceinline__ uint32_t block_exscan_u32(TruncShared &sh, uint32_t c, int tid) {
+    const int lane = tid & 31, w = tid >> 5;
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) sh.wsum[w] = incl;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int k = 0; k < w; ++k) before += sh.wsum[k];
+    __syncthreads();
+    return before + incl - c;
+}
+
+// Radix select from the top of the key order, eight bits per pass: the key tau at which the
+// running total (counts when MASS is false, fixed-point masses otherwise) of the tokens ranked
+// before it first reaches `need`; on return `need` is what remains to be taken among the
+// tokens tied at tau. kept(v, key) filters the tokens that take part.
+template <int DT, bool MASS, class Kept, class Mass>
+__device__ uint32_t radix_select(TruncShared &sh, const void *row, int V, unsigned long long &need, Kept kept,
+                                 Mass mass, int tid) {
+    uint32_t prefix = 0u, pmask = 0u;
+    for (int shift = TruncElt<DT>::kBits - 8; shift >= 0; shift -= 8) {
+        for (int b = tid; b < 256; b += kTruncThreads) {
+            sh.hist[b] = 0u;
+            sh.hmass[b] = 0ull;
+        }
+        __syncthreads();
+        for (int v = tid; v < V; v += kTruncThreads) {
+            const uint32_t k = TruncElt<DT>::key(row, v);
+            if ((k & pmask) != prefix || !kept(v, k)) continue;
+            const uint32_t bin = (k >> shift) & 0xFFu;
+            if (MASS)
+                atomicAdd(&sh.hmass[bin], mass(k));
+            else
+                atomicAdd(&sh.hist[bin], 1u);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long cum = 0ull, h_last = 0ull;
+            int chosen = -1, last = 0;
+            for (int b = 255; b >= 0; --b) {
+                const unsigned long long h = MASS ? sh.hmass[b] : static_cast<unsigned long long>(sh.hist[b]);
+                if (h == 0ull) continue;
+                if (cum + h >= need) {
+                    chosen = b;
+                    break;
+                }
+                cum += h;
+                last = b;
+                h_last = h;
+            }
+            if (chosen >= 0) {
+                sh.chosen = static_cast<uint32_t>(chosen);
+                sh.need = need - cum;
+            } else {
+                // the total falls short of `need` (it can only by rounding): every token counts,
+                // down to the lowest bin that holds any
+                sh.chosen = static_cast<uint32_t>(last);
+                sh.need = h_last;
+            }
+        }
+        __syncthreads();
+        prefix |= sh.chosen << shift;
+        pmask |= 0xFFu << shift;
+        need = sh.need;
+        __syncthreads();
+    }
+    return prefix;
+}
+
+// The n-th (1-based) token in id order among those with key == tau that pass kept(v, key);
+// -1 if there are fewer. Each thread scans a contiguous range of ids.
+template <int DT, class Kept>
+__device__ int nth_tied(TruncShared &sh, const void *row, int V, uint32_t tau, uint32_t n, Kept kept, int tid) {
+    const int chunk = (V + kTruncThreads - 1) / kTruncThreads;
+    const int v0 = min(V, tid * chunk), v1 = min(V, v0 + chunk);
+    uint32_t c = 0u;
+    for (int v = v0; v < v1; ++v) {
+        const uint32_t k = TruncElt<DT>::key(row, v);
+        c += (k == tau && kept(v, k)) ? 1u : 0u;
+    }
+    if (tid == 0) sh.found = -1;
+    const uint32_t before = block_exscan_u32(sh, c, tid);
+    if (before < n && n <= before + c) {
+        uint32_t seen = before;
+        for (int v = v0; v < v1; ++v) {
+            const uint32_t k = TruncElt<DT>::key(row, v);
+            if (k == tau && kept(v, k) && ++seen == n) {
+                sh.found = v;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    const int r = sh.found;
+    __syncthreads();
+    return r;
+}
+
+struct KeepAll {
+    __device__ bool operator()(int, uint32_t) const { return true; }
+};
+// a cut (tau, id): the tokens ranked no later than it
+struct KeepCut {
+    uint32_t tau;
+    int32_t id;
+    __device__ bool operator()(int v, uint32_t k) const { return cut_keeps(k, v, tau, id); }
+};
+struct NoMass {
+    __device__ unsigned long long operator()(uint32_t) const { return 0ull; }
+};
+// 2^((z - z_max) s) in units of 2^-40 (the top token weighs 2^40)
+template <int DT>
+struct FixedMass {
+    float zmax, s;
+    __device__ unsigned long long operator()(uint32_t k) const {
+        const float m = ex2((TruncElt<DT>::logit(k) - zmax) * s);
+        return __float2ull_rn(m * 0x1p40f);
+    }
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kTruncThreads) spec_trunc_kernel(const TruncParams P) {
+    __shared__ TruncShared sh;
+    const int tid = static_cast<int>(threadIdx.x), row = static_cast<int>(blockIdx.x);
+    if (tid == 0) {
+        // the request owning target row `row`: the last i with row_off[i] <= row
+        int lo = 0, hi = P.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(P.row_off + mid) <= row)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        sh.req = lo;
+    }
+    __syncthreads();
+    const int req = sh.req, V = P.V;
+    const int32_t k = P.top_k ? __ldg(P.top_k + req) : 0;
+    const float tp = P.top_p ? __ldg(P.top_p + req) : 1.0f;
+    const float T = P.temperature ? __ldg(P.temperature + req) : P.temperature_scalar;
+    const bool use_k = k > 0 && k < V;
+    const bool use_p = tp < 1.0f;  // false for NaN (the request is then invalid)
+    if ((!use_k && !use_p) || !(T > 0.0f) || isinf(T)) {  // the greedy rule ignores truncation
+        if (tid == 0) P.cut[row] = make_int2(static_cast<int>(kCutAllTau), kCutAllId);
+        return;
+    }
+    const size_t row_bytes = static_cast<size_t>(V) * (DT == SPEC_BF16 ? 2 : 4);
+    const void *rowp = static_cast<const unsigned char *>(P.target) + static_cast<size_t>(row) * row_bytes;
+
+    // top-k: the k-th key from the top, then the tokens tied there in id order
+    KeepCut kc = {kCutAllTau, kCutAllId};
+    if (use_k) {
+        unsigned long long need = static_cast<unsigned long long>(k);
+        const uint32_t tau = radix_select<DT, false>(sh, rowp, V, need, KeepAll{}, NoMass{}, tid);
+        const int id = nth_tied<DT>(sh, rowp, V, tau, static_cast<uint32_t>(need), KeepAll{}, tid);
+        kc = {tau, id};
+    }
+    KeepCut fc = kc;
+    if (use_p) {
+        // masses relative to the top token; the top-k set's total; then the shortest head whose
+        // mass reaches top_p of it (at least the top token)
+        uint32_t kmax = 0u;
+        for (int v = tid; v < V; v += kTruncThreads) kmax = max(kmax, TruncElt<DT>::key(rowp, v));
+        kmax = block_max_u32(sh, kmax, tid);
+        const FixedMass<DT> fm = {TruncElt<DT>::logit(kmax), 1.4426950408889634f / T};
+        unsigned long long part = 0ull;
+        for (int v = tid; v < V; v += kTruncThreads) {
+            const uint32_t key = TruncElt<DT>::key(rowp, v);
+            if (kc(v, key)) part += fm(key);
+        }
+        const unsigned long long Mk = block_sum_u64(sh, part, tid);
+        unsigned long long need = 1ull;
+        if (tp > 0.0f) {
+            const double t = ceil(static_cast<double>(tp) * static_cast<double>(Mk));
+            need = t < 1.0 ? 1ull : (t > static_cast<double>(Mk) ? Mk : static_cast<unsigned long long>(t));
+        }
+        const uint32_t tau = radix_select<DT, true>(sh, rowp, V, need, kc, fm, tid);
+        const unsigned long long mt = fm(tau);
+        const uint32_t n = mt > 0ull ? static_cast<uint32_t>((need + mt - 1ull) / mt) : 1u;
+        const int id = nth_tied<DT>(sh, rowp, V, tau, n, kc, tid);
+        fc = {tau, id};
+    }
+    if (tid == 0) P.cut[row] = make_int2(static_cast<int>(fc.tau), fc.id);
+}
+
+}  // namespace spec

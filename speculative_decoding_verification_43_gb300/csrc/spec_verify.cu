@@ -22,6 +22,7 @@
 #include "spec_verify.h"
 
 #include "spec_rows_kernel.cuh"
+#include "spec_trunc.cuh"
 
 namespace spec {
 
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kFinThreads) spec_select_kernel(const FinParam
 // Host side
 
 struct WsLayout {
-    size_t flag, tok, status, fb, prob, margin, alpha, total;
+    size_t flag, tok, status, fb, prob, margin, alpha, cut, total;
 };
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -189,6 +190,7 @@ static WsLayout ws_layout(int32_t B, int32_t total_rows) {
     L.prob = take(T * 4);
     L.margin = take(T * 4);
     L.alpha = take((nd > 0 ? nd : 1) * 4);
+    L.cut = take(T * 8);  // top-k / top-p cut per target row
     L.total = off;
     return L;
 }
@@ -384,6 +386,28 @@ extern "C" spec_status spec_verify(const spec_verify_args *a, void *workspace, s
     P.alpha_rows = a->alpha_rows;
     P.rho_rows = a->rho_rows;
     P.resid_rows = a->resid_rows;
+    P.top_p = a->top_p;
+    P.trunc = nullptr;
+    if (a->top_k || a->top_p) {
+        // top-k / top-p: the cut of every target row, before the per-position kernel reads it
+        TruncParams Tp = {};
+        Tp.target = a->target_logits;
+        Tp.row_off = a->row_off;
+        Tp.temperature = a->temperature;
+        Tp.temperature_scalar = a->temperature_scalar;
+        Tp.top_k = a->top_k;
+        Tp.top_p = a->top_p;
+        Tp.B = a->B;
+        Tp.V = a->V;
+        Tp.total_rows = a->total_rows;
+        Tp.cut = reinterpret_cast<int2 *>(ws + L.cut);
+        if (a->dtype == SPEC_BF16)
+            spec_trunc_kernel<SPEC_BF16><<<a->total_rows, kTruncThreads, 0, stream>>>(Tp);
+        else
+            spec_trunc_kernel<SPEC_F32><<<a->total_rows, kTruncThreads, 0, stream>>>(Tp);
+        if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+        P.trunc = Tp.cut;
+    }
 
     if (a->rows_event_begin && cudaEventRecord(a->rows_event_begin, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     const spec_status st = (a->dtype == SPEC_BF16) ? launch_rows<SPEC_BF16>(P, stream) : launch_rows<SPEC_F32>(P, stream);
@@ -441,7 +465,7 @@ extern "C" const char *spec_version(void) { return "spec-verify-gb300 0.1 (sm_10
 
 namespace spec {
 constexpr int32_t kNoallocMaxRows = 16384;  // target rows per call: T = sum_i (K_i + 1)
-constexpr size_t kNoallocScratchBytes = 7 * 65536;  // = workspace of kNoallocMaxRows rows
+constexpr size_t kNoallocScratchBytes = 9 * 65536;  // = workspace of kNoallocMaxRows rows
 static __device__ __align__(256) unsigned char noalloc_scratch[kNoallocScratchBytes];
 
 static std::mutex noalloc_mu;

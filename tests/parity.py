@@ -8,6 +8,9 @@ The bar (north star of this repository):
     1e-5 relative.
 Float decisions on each side are taken in each side's own precision (the oracle in float64,
 the kernels in float32 with float64 accumulation), which is why a band exists at all.
+With top-p, the cut of a target row is a boundary too: a request with a row whose cumulative
+mass at the oracle's cut lies within TRUNC_BAND of top_p is counted with the band (the kernel
+sums the masses of the cut in fixed point from float32 exponentials).
 """
 from __future__ import annotations
 
@@ -22,12 +25,14 @@ from speculative_decoding_verification_43_gb300.workloads import Round, to_numpy
 
 BAND = 1e-6
 RTOL = 1e-5
+TRUNC_BAND = 1e-5
 
 
-def run_gpu(rd: Round, *, K_max=64, stop_token=None, max_new=None, temperature=None):
+def run_gpu(rd: Round, *, K_max=64, stop_token=None, max_new=None, temperature=None, top_k=None, top_p=None):
     temp = rd.temperature if temperature is None else temperature
     out = api.verify(rd.target, rd.draft, rd.row_off, rd.draft_tokens, rd.uniforms, temp,
-                     K_max=K_max, stop_token=stop_token, max_new=max_new, diagnostics=True)
+                     K_max=K_max, stop_token=stop_token, max_new=max_new, top_k=top_k, top_p=top_p,
+                     diagnostics=True)
     torch.cuda.synchronize()
     return {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for k, v in out.__dict__.items()}
 
@@ -62,7 +67,7 @@ def run_oracle(rd: Round, reqs=None, **kw):
     reqs = list(range(rd.B)) if reqs is None else list(reqs)
     sb = sub_batch(rd, reqs)
     extra = {}
-    for k in ("stop_token", "max_new"):
+    for k in ("stop_token", "max_new", "top_k", "top_p"):
         if kw.get(k) is not None:
             extra[k] = np.asarray(kw[k].cpu().numpy() if isinstance(kw[k], torch.Tensor) else kw[k])[reqs]
     out = oracle.verify(sb["target"], sb["draft"], sb["row_off"], sb["draft_tokens"], sb["uniforms"],
@@ -120,6 +125,11 @@ def compare(gpu, orc, sb, reqs, full_row_off) -> Report:
                 rep.mismatches.append((i, "bad request emitted", gpu["out_tokens"][g_r0:g_r0 + K + 1]))
             continue
         greedy = float(sb["temperature"][k]) == 0.0
+        tm = orc["trunc_margin"][r0:r1]
+        if np.any(np.isfinite(tm) & (tm < TRUNC_BAND)):
+            # a top-p cut at the boundary: the two sides may keep different sets
+            rep.near_boundary += 1
+            continue
         # values: alpha and rho for every draft row, residual mass where the kernel formed it
         for j in range(K):
             a_o, a_g = orc["alpha"][d0 + j], gpu["alpha_rows"][g_d0 + j]
@@ -183,6 +193,7 @@ def compare(gpu, orc, sb, reqs, full_row_off) -> Report:
 
 
 def check_round(rd: Round, reqs=None, **kw) -> Report:
-    gpu = run_gpu(rd, K_max=kw.get("K_max", 64), stop_token=kw.get("stop_token"), max_new=kw.get("max_new"))
+    gpu = run_gpu(rd, K_max=kw.get("K_max", 64), stop_token=kw.get("stop_token"), max_new=kw.get("max_new"),
+                  top_k=kw.get("top_k"), top_p=kw.get("top_p"))
     orc, sb, reqs = run_oracle(rd, reqs, **kw)
     return compare(gpu, orc, sb, reqs, rd.row_off.cpu().numpy())

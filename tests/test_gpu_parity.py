@@ -338,3 +338,53 @@ def test_compaction_with_stops_and_bad_blocks():
         np.testing.assert_array_equal(getattr(c, k).cpu().numpy(), o[k], err_msg=k)
     for k, n in (("packed_tokens", n_out), ("packed_pos", n_out), ("kv_src", n_kv), ("kv_dst", n_kv)):
         np.testing.assert_array_equal(getattr(c, k).cpu().numpy()[:n], o[k], err_msg=k)
+
+
+def _trunc_params(B, V, seed):
+    """Per-request top-k / top-p values: off, extreme and ordinary ones, mixed."""
+    rng = np.random.default_rng(seed)
+    ks = np.array([0, 1, 3, 50, 1000, V - 1, V + 7], np.int32)
+    ps = np.array([1.0, 0.9, 0.5, 0.99, 0.0, 0.7, 0.95], np.float32)
+    top_k = torch.as_tensor(ks[rng.integers(0, len(ks), B)], device="cuda")
+    top_p = torch.as_tensor(ps[rng.integers(0, len(ps), B)], device="cuda")
+    return top_k, top_p
+
+
+@pytest.mark.parametrize("dtype,V,logits", [(torch.bfloat16, 32000, "zipf"), (torch.float32, 20000, "normal"),
+                                            (torch.bfloat16, 128256, "zipf")])
+def test_top_k_top_p(dtype, V, logits):
+    """Top-k then top-p of the target law (SDCP "Session Model"): the cut of each target row by
+    the truncation kernel, the masked rows in the per-position kernel, every draw of the
+    truncated law. Some requests use the greedy rule, which ignores truncation."""
+    base = W.Workload("t", B=48 if V < 100000 else 24, V=V, dtype=dtype, temperature=0.8, logits=logits,
+                      sigma=2.0, draft_sigma=0.7, K="uniform:0:5")
+    rd = W.make_round(base, seed=31, device="cuda")
+    temp = rd.temperature.clone()
+    temp[::11] = 0.0
+    rd.temperature = temp
+    top_k, top_p = _trunc_params(rd.B, V, 7)
+    assert_report(check_round(rd, top_k=top_k, top_p=top_p))
+
+
+def test_top_k_cuts_inside_ties():
+    """Integer-valued logits put many tokens at the cut's logit: the kept ones are the
+    smallest ids among them, on both sides."""
+    base = W.Workload("t", B=40, V=4096, dtype=torch.bfloat16, temperature=1.0, logits="normal", sigma=2.0,
+                      draft_sigma=0.5, K="uniform:0:3")
+    rd = W.make_round(base, seed=5, device="cuda")
+    rd.target = torch.round(rd.target.float()).to(torch.bfloat16).contiguous()
+    top_k = torch.as_tensor(np.random.default_rng(2).integers(1, 400, rd.B).astype(np.int32), device="cuda")
+    top_p = torch.full((rd.B,), 0.9, dtype=torch.float32, device="cuda")
+    top_p[::2] = 1.0
+    assert_report(check_round(rd, top_k=top_k, top_p=top_p))
+
+
+def test_nan_top_p_is_a_bad_parameter_on_device():
+    base = W.Workload("t", B=8, V=2048, dtype=torch.float32, temperature=1.0, logits="normal", sigma=1.0,
+                      draft_sigma=0.5, K="fixed:2")
+    rd = W.make_round(base, seed=9, device="cuda")
+    top_p = torch.ones(rd.B, dtype=torch.float32, device="cuda")
+    top_p[3] = float("nan")
+    g = run_gpu(rd, top_p=top_p)
+    assert g["req_status"][3] == 8 and g["n_emitted"][3] == 0
+    assert (np.delete(g["req_status"], 3) == 0).all()
