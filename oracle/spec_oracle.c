@@ -102,8 +102,10 @@ static void row_truncate(row_law *L, int32_t top_k, double top_p) {
                 break;
             }
         }
+        /* the cut can move only between heads of one or more tokens: the empty head (mass 0)
+         * never counts, so with n_p = 1 only the first token's mass is compared */
         const double d1 = fabs(cum - top_p), d0 = fabs(prev - top_p);
-        L->cut_margin = d1 < d0 ? d1 : d0;
+        L->cut_margin = (np >= 2 && d0 < d1) ? d0 : d1;
         n = np;
     }
     L->truncated = 1;

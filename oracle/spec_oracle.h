@@ -74,8 +74,9 @@ typedef struct {
     double *sample_prob;        /* [B] probability of the frontier token under the law it was
                                    drawn from                                                  */
     int32_t *fallback;          /* [B] 1 when the residual had zero mass and p was used        */
-    double *trunc_margin;       /* [T] or NULL: distance of top_p to the nearer of the two
-                                   cumulative masses around the top-p cut (NaN: no top-p cut)  */
+    double *trunc_margin;       /* [T] or NULL: distance of top_p to the nearer of the
+                                   cumulative masses of the kept head and of the head one token
+                                   shorter (when that has a token; NaN: no top-p cut)           */
     int32_t *trunc_keep;        /* [T] or NULL: tokens kept by top-k / top-p (V: all)          */
 } oracle_result;
 

@@ -168,3 +168,17 @@ def test_exactness_of_the_truncated_law(k, top_p):
         m = counts.sum()
         assert m > 10_000
         assert stats.chisquare(counts[keep], m * pt[d][keep]).pvalue > 1e-3, (d, counts, pt[d])
+
+
+def test_top_p_margin_ignores_the_empty_head():
+    """top_p <= 0 keeps the first token whatever the masses; the only cumulative mass at the cut
+    is that token's. For p = (0.5, 0.3, 0.15, 0.05): margin 0.5 at top_p = 0, and at top_p = 0.6
+    (cut after two tokens) min(|0.8 - 0.6|, |0.5 - 0.6|) = 0.1."""
+    tz = np.log(np.array([[0.5, 0.3, 0.15, 0.05]] * 2))
+    dz = np.zeros((1, 4))
+    o = one(tz, dz, [0], [0.9, 0.5], 1.0, top_p=0.0)
+    assert o["trunc_keep"][0] == 1
+    np.testing.assert_allclose(o["trunc_margin"][0], 0.5, rtol=1e-6)
+    o = one(tz, dz, [0], [0.9, 0.5], 1.0, top_p=0.6)
+    assert o["trunc_keep"][0] == 2
+    np.testing.assert_allclose(o["trunc_margin"][0], 0.1, rtol=1e-5)
