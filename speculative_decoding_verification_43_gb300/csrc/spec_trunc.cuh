@@ -13,7 +13,8 @@
 // One CTA per target row: a radix select over the key, eight bits per pass, on counts (top-k)
 // or on masses (top-p), then an ordered search among the tokens tied at the cut. Masses are
 // 2^((z - z_max) s) in fixed point (2^-40 units, 64-bit integer sums): the sums, and so the cut,
-// do not depend on the order of the atomic additions.
+// do not depend on the order of the atomic additions. Rows are read as 16-byte vectors; a row
+// stays in L2 across its passes (bf16 V = 128256: about six passes over 256 KB).
 #pragma once
 
 #include <climits>
@@ -53,27 +54,40 @@ template <int DT>
 struct TruncElt;
 template <>
 struct TruncElt<SPEC_BF16> {
-    static constexpr int kBits = 16;
-    __device__ static __forceinline__ uint32_t key(const void *row, int v) {
-        return key_bf16(__ldg(static_cast<const uint16_t *>(row) + v));
+    static constexpr int kBits = 16, kPerVec = 8;
+    // key of element e of a 16-byte vector
+    __device__ static __forceinline__ uint32_t key(const uint4 &w, int e) {
+        const uint32_t x = (e >> 1) == 0 ? w.x : (e >> 1) == 1 ? w.y : (e >> 1) == 2 ? w.z : w.w;
+        return key_bf16((e & 1) ? (x >> 16) : (x & 0xFFFFu));
     }
     __device__ static __forceinline__ float logit(uint32_t k) { return logit_of_key_bf16(k); }
 };
 template <>
 struct TruncElt<SPEC_F32> {
-    static constexpr int kBits = 32;
-    __device__ static __forceinline__ uint32_t key(const void *row, int v) {
-        return key_f32(__ldg(static_cast<const uint32_t *>(row) + v));
+    static constexpr int kBits = 32, kPerVec = 4;
+    __device__ static __forceinline__ uint32_t key(const uint4 &w, int e) {
+        return key_f32(e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w);
     }
     __device__ static __forceinline__ float logit(uint32_t k) { return logit_of_key_f32(k); }
 };
+
+// f(v, key) for every token of the row, each thread taking 16-byte vectors t, t + 512, ...
+// (rows are 16-byte multiples).
+template <int DT, class F>
+__device__ __forceinline__ void for_each_key(const uint4 *row, int nv, int tid, F f) {
+    constexpr int E = TruncElt<DT>::kPerVec;
+    for (int i = tid; i < nv; i += kTruncThreads) {
+        const uint4 w = __ldg(row + i);
+#pragma unroll
+        for (int e = 0; e < E; ++e) f(i * E + e, TruncElt<DT>::key(w, e));
+    }
+}
 
 // Shared state of one row's selection.
 struct TruncShared {
     uint32_t hist[256];
     unsigned long long hmass[256];
     uint32_t wsum[kTruncWarps];
-    unsigned long long total;
     uint32_t kmax;
     int32_t req, found;
     uint32_t chosen;
@@ -94,61 +108,59 @@ __device__ __forceinline__ uint32_t block_max_u32(TruncShared &sh, uint32_t v, i
     return r;
 }
 
-// Block-wide sum of 64-bit integers (every thread gets it).
-__device__ __forceinline__ unsigned long long block_sum_u64(TruncShared &sh, unsigned long long v, int tid) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (tid == 0) sh.total = 0ull;
-    __syncthreads();
-    if ((tid & 31) == 0) atomicAdd(&sh.total, v);
-    __syncthreads();
-    const unsigned long long r = sh.total;
-    __syncthreads();
-    return r;
-}
-
-// Exclusive prefix over the threads of the block, in thread order (every thread gets its own).
-__device__ __forceinline__ uint32_t block_exscan_u32(TruncShared &sh, uint32_t c, int tid) {
-    const int lane = tid & 31, w = tid >> 5;
-    uint32_t incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += x;
-    }
-    if (lane == 31) sh.wsum[w] = incl;
-    __syncthreads();
-    uint32_t before = 0;
-    for (int k = 0; k < w; ++k) before += sh.wsum[k];
-    __syncthreads();
-    return before + incl - c;
-}
-
 // Radix select from the top of the key order, eight bits per pass: the key tau at which the
 // running total (counts when MASS is false, fixed-point masses otherwise) of the tokens ranked
 // before it first reaches `need`; on return `need` is what remains to be taken among the
-// tokens tied at tau. kept(v, key) filters the tokens that take part.
+// tokens tied at tau. kept(v, key) filters the tokens that take part. With tp >= 0 (masses
+// only), `need` comes from the first pass: ceil(tp * total), at least 1 (the top token).
+// Histogram updates are aggregated per warp over lanes that hit the same bin.
 template <int DT, bool MASS, class Kept, class Mass>
-__device__ uint32_t radix_select(TruncShared &sh, const void *row, int V, unsigned long long &need, Kept kept,
-                                 Mass mass, int tid) {
+__device__ uint32_t radix_select(TruncShared &sh, const uint4 *row, int nv, unsigned long long &need, Kept kept,
+                                 Mass mass, float tp, int tid) {
+    constexpr int E = TruncElt<DT>::kPerVec;
+    const int lane = tid & 31;
     uint32_t prefix = 0u, pmask = 0u;
+    bool first = true;
     for (int shift = TruncElt<DT>::kBits - 8; shift >= 0; shift -= 8) {
         for (int b = tid; b < 256; b += kTruncThreads) {
             sh.hist[b] = 0u;
             sh.hmass[b] = 0ull;
         }
         __syncthreads();
-        for (int v = tid; v < V; v += kTruncThreads) {
-            const uint32_t k = TruncElt<DT>::key(row, v);
-            if ((k & pmask) != prefix || !kept(v, k)) continue;
-            const uint32_t bin = (k >> shift) & 0xFFu;
-            if (MASS)
-                atomicAdd(&sh.hmass[bin], mass(k));
-            else
-                atomicAdd(&sh.hist[bin], 1u);
+        for (int base = tid & ~31; base < nv; base += kTruncThreads) {  // warp-uniform
+            const int i = base + lane;
+            const bool ok = i < nv;
+            const uint4 w = ok ? __ldg(row + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const uint32_t k = TruncElt<DT>::key(w, e);
+                const bool in = ok && (k & pmask) == prefix && kept(i * E + e, k);
+                const uint32_t bin = in ? ((k >> shift) & 0xFFu) : 256u;
+                const unsigned grp = __match_any_sync(0xffffffffu, bin);
+                const bool leader = lane == __ffs(grp) - 1;
+                if (MASS) {
+                    // a mass is below 2^41: two 20-bit halves sum over 32 lanes without overflow
+                    const unsigned long long m = in ? mass(k) : 0ull;
+                    const unsigned hi = __reduce_add_sync(grp, static_cast<unsigned>(m >> 20));
+                    const unsigned lo = __reduce_add_sync(grp, static_cast<unsigned>(m & 0xFFFFFull));
+                    if (leader && bin < 256u)
+                        atomicAdd(&sh.hmass[bin], (static_cast<unsigned long long>(hi) << 20) + lo);
+                } else if (leader && bin < 256u) {
+                    atomicAdd(&sh.hist[bin], static_cast<unsigned>(__popc(grp)));
+                }
+            }
         }
         __syncthreads();
         if (tid == 0) {
+            if (MASS && first && tp >= 0.0f) {
+                unsigned long long total = 0ull;
+                for (int b = 0; b < 256; ++b) total += sh.hmass[b];
+                need = 1ull;
+                if (tp > 0.0f) {
+                    const double t = ceil(static_cast<double>(tp) * static_cast<double>(total));
+                    need = t < 1.0 ? 1ull : (t > static_cast<double>(total) ? total : static_cast<unsigned long long>(t));
+                }
+            }
             unsigned long long cum = 0ull, h_last = 0ull;
             int chosen = -1, last = 0;
             for (int b = 255; b >= 0; --b) {
@@ -176,32 +188,68 @@ __device__ uint32_t radix_select(TruncShared &sh, const void *row, int V, unsign
         prefix |= sh.chosen << shift;
         pmask |= 0xFFu << shift;
         need = sh.need;
+        first = false;
         __syncthreads();
     }
     return prefix;
 }
 
 // The n-th (1-based) token in id order among those with key == tau that pass kept(v, key);
-// -1 if there are fewer. Each thread scans a contiguous range of ids.
+// -1 if there are fewer. Warp w scans the w-th contiguous run of vectors, 32 at a time.
 template <int DT, class Kept>
-__device__ int nth_tied(TruncShared &sh, const void *row, int V, uint32_t tau, uint32_t n, Kept kept, int tid) {
-    const int chunk = (V + kTruncThreads - 1) / kTruncThreads;
-    const int v0 = min(V, tid * chunk), v1 = min(V, v0 + chunk);
+__device__ int nth_tied(TruncShared &sh, const uint4 *row, int nv, uint32_t tau, uint32_t n, Kept kept, int tid) {
+    constexpr int E = TruncElt<DT>::kPerVec;
+    const int lane = tid & 31, wp = tid >> 5;
+    const int cw = (nv + kTruncWarps - 1) / kTruncWarps;
+    const int v0 = min(nv, wp * cw), v1 = min(nv, v0 + cw);
+    auto ties = [&](int i, const uint4 &w) {
+        uint32_t c = 0u;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const uint32_t k = TruncElt<DT>::key(w, e);
+            c += (k == tau && kept(i * E + e, k)) ? 1u : 0u;
+        }
+        return c;
+    };
     uint32_t c = 0u;
-    for (int v = v0; v < v1; ++v) {
-        const uint32_t k = TruncElt<DT>::key(row, v);
-        c += (k == tau && kept(v, k)) ? 1u : 0u;
-    }
+    for (int i = v0 + lane; i < v1; i += 32) c += ties(i, __ldg(row + i));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0) sh.wsum[wp] = c;
     if (tid == 0) sh.found = -1;
-    const uint32_t before = block_exscan_u32(sh, c, tid);
-    if (before < n && n <= before + c) {
+    __syncthreads();
+    uint32_t before = 0u;
+    for (int k = 0; k < wp; ++k) before += sh.wsum[k];
+    if (before < n && n <= before + c) {  // warp-uniform: this warp's run holds the n-th
         uint32_t seen = before;
-        for (int v = v0; v < v1; ++v) {
-            const uint32_t k = TruncElt<DT>::key(row, v);
-            if (k == tau && kept(v, k) && ++seen == n) {
-                sh.found = v;
+        for (int base = v0; base < v1; base += 32) {
+            const int i = base + lane;
+            const bool ok = i < v1;
+            const uint4 w = ok ? __ldg(row + i) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t mine = ok ? ties(i, w) : 0u;
+            uint32_t incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += x;
+            }
+            const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+            if (seen + total >= n) {
+                const uint32_t r = n - seen;  // 1-based rank within these 32 vectors
+                if (mine > 0u && incl - mine < r && r <= incl) {
+                    uint32_t left = r - (incl - mine);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const uint32_t k = TruncElt<DT>::key(w, e);
+                        if (k == tau && kept(i * E + e, k) && --left == 0u) {
+                            sh.found = i * E + e;
+                            break;
+                        }
+                    }
+                }
                 break;
             }
+            seen += total;
         }
     }
     __syncthreads();
@@ -259,40 +307,30 @@ __global__ void __launch_bounds__(kTruncThreads) spec_trunc_kernel(const TruncPa
         if (tid == 0) P.cut[row] = make_int2(static_cast<int>(kCutAllTau), kCutAllId);
         return;
     }
-    const size_t row_bytes = static_cast<size_t>(V) * (DT == SPEC_BF16 ? 2 : 4);
-    const void *rowp = static_cast<const unsigned char *>(P.target) + static_cast<size_t>(row) * row_bytes;
+    const int nv = V / TruncElt<DT>::kPerVec;  // rows are 16-byte multiples
+    const uint4 *rowp = static_cast<const uint4 *>(P.target) + static_cast<size_t>(row) * nv;
 
     // top-k: the k-th key from the top, then the tokens tied there in id order
     KeepCut kc = {kCutAllTau, kCutAllId};
     if (use_k) {
         unsigned long long need = static_cast<unsigned long long>(k);
-        const uint32_t tau = radix_select<DT, false>(sh, rowp, V, need, KeepAll{}, NoMass{}, tid);
-        const int id = nth_tied<DT>(sh, rowp, V, tau, static_cast<uint32_t>(need), KeepAll{}, tid);
+        const uint32_t tau = radix_select<DT, false>(sh, rowp, nv, need, KeepAll{}, NoMass{}, -1.0f, tid);
+        const int id = nth_tied<DT>(sh, rowp, nv, tau, static_cast<uint32_t>(need), KeepAll{}, tid);
         kc = {tau, id};
     }
     KeepCut fc = kc;
     if (use_p) {
-        // masses relative to the top token; the top-k set's total; then the shortest head whose
-        // mass reaches top_p of it (at least the top token)
+        // masses relative to the top token; the shortest head of the top-k set whose mass reaches
+        // top_p of the set's total (the first pass of the select sums it; at least the top token)
         uint32_t kmax = 0u;
-        for (int v = tid; v < V; v += kTruncThreads) kmax = max(kmax, TruncElt<DT>::key(rowp, v));
+        for_each_key<DT>(rowp, nv, tid, [&](int, uint32_t key) { kmax = max(kmax, key); });
         kmax = block_max_u32(sh, kmax, tid);
         const FixedMass<DT> fm = {TruncElt<DT>::logit(kmax), 1.4426950408889634f / T};
-        unsigned long long part = 0ull;
-        for (int v = tid; v < V; v += kTruncThreads) {
-            const uint32_t key = TruncElt<DT>::key(rowp, v);
-            if (kc(v, key)) part += fm(key);
-        }
-        const unsigned long long Mk = block_sum_u64(sh, part, tid);
         unsigned long long need = 1ull;
-        if (tp > 0.0f) {
-            const double t = ceil(static_cast<double>(tp) * static_cast<double>(Mk));
-            need = t < 1.0 ? 1ull : (t > static_cast<double>(Mk) ? Mk : static_cast<unsigned long long>(t));
-        }
-        const uint32_t tau = radix_select<DT, true>(sh, rowp, V, need, kc, fm, tid);
+        const uint32_t tau = radix_select<DT, true>(sh, rowp, nv, need, kc, fm, tp, tid);
         const unsigned long long mt = fm(tau);
         const uint32_t n = mt > 0ull ? static_cast<uint32_t>((need + mt - 1ull) / mt) : 1u;
-        const int id = nth_tied<DT>(sh, rowp, V, tau, n, kc, tid);
+        const int id = nth_tied<DT>(sh, rowp, nv, tau, n, kc, tid);
         fc = {tau, id};
     }
     if (tid == 0) P.cut[row] = make_int2(static_cast<int>(fc.tau), fc.id);
