@@ -65,15 +65,57 @@ __global__ void __launch_bounds__(kFinThreads) spec_select_kernel(const FinParam
     griddep_wait();  // the per-position results are complete from here on
     F2 asum = {0.0f, 0.0f};
     int acnt = 0;
+    // one request per warp at a time, lane j taking position j (K_max <= 64: two rounds at most);
+    // every per-position value is fetched in one round of independent loads
     for (int i = warp; i < P.B; i += kFinThreads / kWarp) {
         const int r0 = __ldg(P.row_off + i), r1 = __ldg(P.row_off + i + 1);
         const int K = r1 - r0 - 1;
         const int d0 = r0 - i;
         int status = 0;
         if (!global_ok || K < 0 || K > P.K_max || r0 < 0 || r1 > P.total_rows || d0 < 0) status |= SPEC_REQ_BAD_SHAPE;
+        const int n_cap = P.max_new ? __ldg(P.max_new + i) : INT_MAX;
+        const int stop = P.stop_token ? __ldg(P.stop_token + i) : -1;
+        // positions j = lane and j = lane + 32
         int st_items = 0;
+        unsigned rej_lo = 0u, rej_hi = 0u;
+        int tok0 = -1, tok1 = -1, fb0 = 0, fb1 = 0, x0 = -1, x1 = -1;
+        float pr0 = NAN, pr1 = NAN, mg0 = NAN, mg1 = NAN, al0 = 0.0f, al1 = 0.0f;
+        int tok2 = -1, fb2 = 0;  // position 64 (lane 0), when K = 64
+        float pr2 = NAN, mg2 = NAN;
         if (!status) {
-            for (int j = lane; j <= K; j += kWarp) st_items |= P.item_status[r0 + j];
+            const int j0 = lane, j1 = lane + kWarp;
+            const bool in0 = j0 <= K, in1 = j1 <= K;
+            if (in0) {
+                st_items |= P.item_status[r0 + j0];
+                tok0 = P.item_tok[r0 + j0];
+                pr0 = P.item_prob[r0 + j0];
+                mg0 = P.item_margin[r0 + j0];
+                fb0 = P.item_fb[r0 + j0];
+                if (j0 < K) {
+                    x0 = __ldg(P.draft_tokens + d0 + j0);
+                    al0 = P.alpha_ws[d0 + j0];
+                }
+            }
+            if (in1) {
+                st_items |= P.item_status[r0 + j1];
+                tok1 = P.item_tok[r0 + j1];
+                pr1 = P.item_prob[r0 + j1];
+                mg1 = P.item_margin[r0 + j1];
+                fb1 = P.item_fb[r0 + j1];
+                if (j1 < K) {
+                    x1 = __ldg(P.draft_tokens + d0 + j1);
+                    al1 = P.alpha_ws[d0 + j1];
+                }
+            }
+            if (K == 2 * kWarp && lane == 0) {  // K_max <= 64: the frontier slot of K = 64
+                st_items |= P.item_status[r0 + K];
+                tok2 = P.item_tok[r0 + K];
+                pr2 = P.item_prob[r0 + K];
+                mg2 = P.item_margin[r0 + K];
+                fb2 = P.item_fb[r0 + K];
+            }
+            rej_lo = __ballot_sync(0xffffffffu, j0 < K && P.item_flag[r0 + j0] == 0);
+            rej_hi = __ballot_sync(0xffffffffu, j1 < K && P.item_flag[r0 + j1] == 0);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) st_items |= __shfl_xor_sync(0xffffffffu, st_items, o);
         }
@@ -91,52 +133,46 @@ __global__ void __launch_bounds__(kFinThreads) spec_select_kernel(const FinParam
             }
             continue;
         }
-        // A = index of the first rejected position (K when all are accepted): ballots over
-        // the accept flags, in position order
-        int A = K;
-        for (int base = 0; base < K; base += kWarp) {
-            const int j = base + lane;
-            const unsigned rej = __ballot_sync(0xffffffffu, j < K && P.item_flag[r0 + j] == 0);
-            if (rej) {
-                A = base + __ffs(rej) - 1;
-                break;
-            }
-        }
-        int n = A + 1;
-        if (P.max_new) n = min(n, max(__ldg(P.max_new + i), 0));
-        const int stop = P.stop_token ? __ldg(P.stop_token + i) : -1;
-        const int frontier = P.item_tok[r0 + A];
+        // A = index of the first rejected position (K when all are accepted)
+        const int A = rej_lo ? __ffs(rej_lo) - 1 : (rej_hi ? kWarp + __ffs(rej_hi) - 1 : K);
+        // the frontier's values, from the lane that holds position A
+        const int la = A & (kWarp - 1), half = A >> 5;  // 0, 1, or 2 (A = 64, lane 0)
+        const int frontier = __shfl_sync(0xffffffffu, half == 0 ? tok0 : half == 1 ? tok1 : tok2, la);
+        const float fprob = __shfl_sync(0xffffffffu, half == 0 ? pr0 : half == 1 ? pr1 : pr2, la);
+        const float fmarg = __shfl_sync(0xffffffffu, half == 0 ? mg0 : half == 1 ? mg1 : mg2, la);
+        const int ffb = __shfl_sync(0xffffffffu, half == 0 ? fb0 : half == 1 ? fb1 : fb2, la);
+        const int out0 = (lane < A) ? x0 : (lane == A ? frontier : -1);
+        const int out1 = (lane + kWarp < A) ? x1 : (lane + kWarp == A ? frontier : -1);
+        int n = min(A + 1, max(n_cap, 0));
         if (stop >= 0) {
-            for (int base = 0; base < n; base += kWarp) {
-                const int j = base + lane;
-                int tok = -1;
-                if (j < n) tok = (j < A) ? __ldg(P.draft_tokens + d0 + j) : frontier;
-                const unsigned hit = __ballot_sync(0xffffffffu, j < n && tok == stop);
-                if (hit) {
-                    n = base + __ffs(hit);
-                    break;
-                }
-            }
+            const unsigned h0 = __ballot_sync(0xffffffffu, lane < n && out0 == stop);
+            const unsigned h1 = __ballot_sync(0xffffffffu, lane + kWarp < n && out1 == stop);
+            if (h0)
+                n = __ffs(h0);
+            else if (h1)
+                n = kWarp + __ffs(h1);
         }
-        for (int j = lane; j <= K; j += kWarp) {
-            int tok = -1;
-            if (j < n) tok = (j < A) ? __ldg(P.draft_tokens + d0 + j) : frontier;
-            P.out_tokens[r0 + j] = tok;
+        if (lane <= K) P.out_tokens[r0 + lane] = lane < n ? out0 : -1;
+        if (lane + kWarp <= K) P.out_tokens[r0 + lane + kWarp] = lane + kWarp < n ? out1 : -1;
+        if (lane == 0 && K == 2 * kWarp) P.out_tokens[r0 + K] = (A == K && n > K) ? frontier : -1;
+        asum = f2_add(f2_add(asum, {al0, 0.0f}), {al1, 0.0f});
+        // depth j + 1 was reached when the first j drafts were accepted, accepted when j < A
+        if (P.depth_reached) {
+            if (lane < K && lane <= A) atomicAdd(&hist_r[lane], 1);
+            if (lane + kWarp < K && lane + kWarp <= A) atomicAdd(&hist_r[lane + kWarp], 1);
         }
-        for (int j = lane; j < K; j += kWarp) {
-            asum = f2_add(asum, {P.alpha_ws[d0 + j], 0.0f});
-            // depth j + 1 was reached when the first j drafts were accepted, accepted when j < A
-            if (P.depth_reached && j <= A) atomicAdd(&hist_r[j], 1);
-            if (P.depth_accepted && j < A) atomicAdd(&hist_a[j], 1);
+        if (P.depth_accepted) {
+            if (lane < K && lane < A) atomicAdd(&hist_a[lane], 1);
+            if (lane + kWarp < K && lane + kWarp < A) atomicAdd(&hist_a[lane + kWarp], 1);
         }
         if (lane == 0) {
             acnt += K;
             P.req_status[i] = 0;
             P.accept_len[i] = A;
             if (P.n_emitted) P.n_emitted[i] = n;
-            if (P.frontier_prob) P.frontier_prob[i] = P.item_prob[r0 + A];
-            if (P.frontier_margin) P.frontier_margin[i] = P.item_margin[r0 + A];
-            if (P.fallback) P.fallback[i] = P.item_fb[r0 + A];
+            if (P.frontier_prob) P.frontier_prob[i] = fprob;
+            if (P.frontier_margin) P.frontier_margin[i] = fmarg;
+            if (P.fallback) P.fallback[i] = ffb;
         }
     }
     asum = warp_sum_f2(asum);

@@ -388,3 +388,19 @@ def test_nan_top_p_is_a_bad_parameter_on_device():
     g = run_gpu(rd, top_p=top_p)
     assert g["req_status"][3] == 8 and g["n_emitted"][3] == 0
     assert (np.delete(g["req_status"], 3) == 0).all()
+
+
+def test_all_64_drafts_accepted():
+    """K = K_max = 64 with every accept draw at 0: A = 64 and the frontier token is drawn from
+    the 65th target row (the selection's third slot per warp)."""
+    base = W.Workload("t", B=3, V=2048, dtype=torch.float32, temperature=1.0, logits="normal",
+                      sigma=1.0, draft_sigma=0.2, K="fixed:64")
+    rd = W.make_round(base, seed=12, device="cuda")
+    u = rd.uniforms.clone()
+    for i in range(rd.B):
+        u[i * 65:i * 65 + 64] = 0.0
+    rd.uniforms = u
+    gpu = run_gpu(rd)
+    assert (gpu["accept_len"] == 64).all() and (gpu["n_emitted"] == 65).all()
+    assert (gpu["out_tokens"].reshape(rd.B, 65) >= 0).all()
+    assert_report(check_round(rd), max_near_frac=0.7)
