@@ -41,10 +41,11 @@ METRIC = "verified rows/sec (Σ(K_i+1) over V) and achieved HBM GB/s vs GB300 pe
 UNIT = "rows/s"
 WORKLOAD = "c3"
 GAMMA_COST = 0.05  # relative draft cost c used by the gamma controller each step
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "rows_kernel_c3_traffic.json")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "stream_kernel_c3_traffic.json")
 CSRC = os.path.join(ROOT, "speculative_decoding_verification_43_gb300", "csrc")
 # the per-position kernel's sources: a committed ncu traffic figure counts only while they match
-KERNEL_SRCS = ("spec_verify.cu", "spec_rows.cuh", "spec_rows_kernel.cuh", "spec_math.cuh", "spec_device.cuh")
+KERNEL_SRCS = ("spec_verify.cu", "spec_rows.cuh", "spec_rows_kernel.cuh", "spec_stream_kernel.cuh", "spec_math.cuh",
+               "spec_device.cuh")
 
 
 def parse():
@@ -191,6 +192,16 @@ def recorded_traffic(bytes_per_launch):
     if d.get("kernel_src_sha256_16") != kernel_hash():
         return None
     return d.get("dram_bytes_per_launch")
+
+
+def kernel_label(wl, rows):
+    """The per-position kernel the library launches for this workload, and its grid."""
+    from speculative_decoding_verification_43_gb300 import api
+    plan = api.verify_plan(wl.B, wl.V, rows, wl.dtype)
+    if plan is None:
+        return "none"
+    name, c, n = plan
+    return f"{name}<{'bf16' if wl.dtype == torch.bfloat16 else 'f32'}>, {n} clusters of {c}"
 
 
 def workload_config(wl, rows, logit_bytes):
@@ -348,7 +359,7 @@ def run_ours(args):
         "config": workload_config(wl, rows, logit_bytes),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(logit_bytes),
-                     "kernel": "spec_rows_kernel<bf16>", "kernel_ms_avg": rows_ms,
+                     "kernel": kernel_label(wl, rows), "kernel_ms_avg": rows_ms,
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
                      "algorithmic_bytes_per_launch": logit_bytes},
         "e2e": e2e,

@@ -149,6 +149,20 @@ spec_status spec_verify(const spec_verify_args *args, void *workspace, size_t wo
  * otherwise those of spec_verify. */
 spec_status spec_verify_noalloc(const spec_verify_args *args, cudaStream_t stream);
 
+/* Which per-position kernel spec_verify launches for a batch of this shape (B requests,
+ * total_rows target rows, vocabulary V, dtype) on the current device, and its persistent grid:
+ * *cluster CTAs per cluster and *clusters clusters (either pointer may be NULL). Returns a
+ * static string naming the kernel, "spec_stream_kernel" (row slices streamed in tiles, one CTA
+ * per SM) or "spec_rows_kernel" (row slices held whole, two CTAs per SM), or NULL when no
+ * configuration fits this device (spec_verify then returns SPEC_ERR_UNSUPPORTED) or the shape is
+ * invalid (B <= 0, V <= 0, total_rows < B, a row not a multiple of 16 bytes). A diagnostic of
+ * this library: it enqueues nothing and only queries the device's occupancy. The kernel is the
+ * streaming one whenever a CTA's row slice fits its tiles, else the rows one; the cluster size
+ * keeps the most SMs busy on total_rows items. The environment variable SPEC_VERIFY_KERNEL=rows
+ * or =stream (read on every call, here and in spec_verify) restricts the choice to one kernel. */
+const char *spec_verify_plan(int32_t B, int32_t V, int32_t total_rows, spec_dtype dtype, int32_t *cluster,
+                             int32_t *clusters);
+
 /* ---- spec_compact ------------------------------------------------------------------------
  * Packs the ragged result of spec_verify ("M7.8 - Speculative Serving", section 0x03C): for
  * request i with prefix length P_i (target KV rows already committed), E_i accepted drafts

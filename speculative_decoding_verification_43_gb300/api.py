@@ -36,6 +36,14 @@ def workspace_size(B: int, V: int, total_rows: int, dtype: torch.dtype) -> int:
     return int(lib.spec_verify_workspace_size(B, V, total_rows, _DTYPE[dtype]))
 
 
+def verify_plan(B: int, V: int, total_rows: int, dtype: torch.dtype):
+    """(kernel name, CTAs per cluster, clusters) that spec_verify launches for this shape on the
+    current device, or None when no configuration fits (or the shape is invalid)."""
+    c, n = ctypes.c_int32(0), ctypes.c_int32(0)
+    name = lib.spec_verify_plan(B, V, total_rows, _DTYPE[dtype], ctypes.byref(c), ctypes.byref(n))
+    return None if name is None else (name.decode(), c.value, n.value)
+
+
 @dataclass
 class VerifyOutputs:
     accept_len: torch.Tensor

@@ -51,11 +51,12 @@ constexpr int kBlock = kThreads + kWarp;     // plus the control warp
 enum : int { BAR_BATCH = 1 };
 constexpr int kChunkVecs = kWarp;   // a chunk: 32 contiguous vectors, one per lane of a warp
 constexpr int kRing = 3;            // row slots per CTA
-constexpr int kMaxItems = 32;       // item descriptors held at once (one batch)
+constexpr int kMaxItems = 22;       // item descriptors held at once (one batch)
 constexpr int kRoffMax = 520;       // row offsets staged in shared memory (B <= 519)
 constexpr int kMaxCluster = 16;
 constexpr int kMaxNvt = 5;          // 16-byte vectors per thread per row
-constexpr int kMaxChunks = kMaxNvt * kWarps;
+constexpr int kMaxStreamRows = 10;  // streaming kernel: 480-vector rows of chunks per row slice
+constexpr int kMaxChunks = (kMaxNvt > kMaxStreamRows ? kMaxNvt : kMaxStreamRows) * kWarps;
 constexpr uint32_t kSuspendNs = 1u << 20;  // one suspended wait: at most ~1 ms
 constexpr int kMaxWaitTries = 2048;        // ~2 s in all: a copy never takes this long
 // log2(e) as a float pair
@@ -72,13 +73,17 @@ enum : int32_t { REQ_TIMEOUT = 32 };  // internal: a bulk copy did not complete 
 // control warp decides item g, signals it, and only then finishes an earlier item (its results
 // and draw). Ring depths of the per-item buffers follow from how far apart the roles may run:
 constexpr int kLag = 0;
-constexpr int kWS = kLag + 2;       // pass-1 statistics (read by the item's exchange)
-constexpr int kPM = 2 * kLag + 4;   // bonus-row chunk sums (read by the draw, kLag + 1 items later)
-constexpr int kRM = kLag + 3;       // pass-2 residual chunk sums and alpha partials
-constexpr int kND = kLag + 3;       // decisions (read by pass 2, the results and the draw)
-constexpr int kNMS = kLag + 3;      // exchange slots (a record is read again kLag + 1 exchanges later)
-constexpr int kSB = kLag + 2;       // barriers: pass-1 statistics ready
-constexpr int kPB = kLag + 3;       // barriers: pass 2 done (kLag > 0)
+// The streaming kernel (spec_stream_kernel.cuh) runs pass 2 one item late; the depths below
+// cover both kernels.
+constexpr int kStreamLag = 1;
+constexpr int kDepthLag = kLag > kStreamLag ? kLag : kStreamLag;
+constexpr int kWS = kDepthLag + 2;       // pass-1 statistics (read by the item's exchange)
+constexpr int kPM = 2 * kDepthLag + 4;   // bonus-row chunk sums (read by the draw, lag + 1 items later)
+constexpr int kRM = kDepthLag + 3;       // pass-2 residual chunk sums and alpha partials
+constexpr int kND = kDepthLag + 3;       // decisions (read by pass 2, the results and the draw)
+constexpr int kNMS = kDepthLag + 3;      // exchange slots (a record is read again lag + 1 exchanges later)
+constexpr int kSB = kDepthLag + 2;       // barriers: pass-1 statistics ready
+constexpr int kPB = kDepthLag + 3;       // barriers: pass 2 done (lagged pipelines)
 
 struct RowsParams {
     const void *target;

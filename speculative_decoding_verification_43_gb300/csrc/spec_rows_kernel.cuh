@@ -25,7 +25,7 @@ struct CtaShared {
     float wz[kRM][kWarps];                // per-warp residual mass (units 2^B_t), by item % kRM
     float rm[kRM][kMaxChunks];            // residual chunk sums (units 2^B_t), by item % kRM
     float pm[kPM][kMaxChunks];            // bonus-row chunk sums (units 2^pref), by item % kPM
-    float pref[kPM][kWarps];              // their integral reference exponents (one per warp)
+    float pref[kPM][kMaxChunks];          // their integral reference exponents (one per chunk)
     Decision dec[kND];                    // by item % kND
     uint4 draw_buf[2][kChunkVecs];        // target / draft chunk of the pending draw
     int32_t timed_out;
@@ -352,7 +352,9 @@ __device__ __forceinline__ void row_stats(const Row &row, CtaShared &sh, int wb,
         }
     }
     if (lane == 0) {
-        if (CHUNKS) sh.pref[pb][warp] = Bw;
+        if (CHUNKS)
+#pragma unroll
+            for (int v = 0; v < NVT; ++v) sh.pref[pb][v * kWarps + warp] = Bw;
         // a reference beyond 2^28 (logits far outside any float32 softmax) reads as invalid
         const bool inval = bad || (Sw > 0.0f && !(fabsf(Bw) < 0x1p28f));
         sh.ws[wb][warp].a[r] = (Sw > 0.0f && !inval) ? static_cast<int>(Bw) : kNoRef;
@@ -927,7 +929,7 @@ __device__ __noinline__ void draw_chunk(CtaShared &sh, const RowsParams &P, int 
                 mk = sh.rm[rb][k];  // p masses, from fb_chunk_masses
             } else {
                 const float pmk = sh.pm[pb][k];
-                mk = pmk > 0.0f ? pmk * pow2i(sh.pref[pb][k % kWarps] - D.B_t) : 0.0f;
+                mk = pmk > 0.0f ? pmk * pow2i(sh.pref[pb][k] - D.B_t) : 0.0f;
             }
         }
         const bool pos = k < nch && mk > 0.0f;
@@ -962,7 +964,7 @@ __device__ __noinline__ void draw_chunk(CtaShared &sh, const RowsParams &P, int 
             lt = rem.hi + rem.lo;
         } else if (ksel >= 0) {
             // p weights of the chunk are in units of 2^bg: 2^(bg - B_t) cluster units
-            bg = sh.pref[pb][ksel % kWarps];
+            bg = sh.pref[pb][ksel];
             unit = pow2i(bg - D.B_t);
             lt = (rem.hi + rem.lo) * pow2i(D.B_t - bg);
         }

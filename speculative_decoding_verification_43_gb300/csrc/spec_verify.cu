@@ -4,8 +4,9 @@
 // ("What to do", steps 3-4) and SDCP Rules 1 and 2 ("Acceptance Rules"); the C ABI and its
 // conventions are documented in include/spec_verify.h.
 //
-// Two kernels per call: the per-position kernel (spec_rows.cuh, spec_rows_kernel.cuh) verifies
-// every (request, position) on a persistent grid of thread-block clusters; the selection kernel walks
+// Two kernels per call: the per-position kernel verifies every (request, position) on a
+// persistent grid of thread-block clusters (spec_stream_kernel.cuh when a CTA's slice of a row
+// fits its tiles, else spec_rows_kernel.cuh; both on spec_rows.cuh); the selection kernel walks
 // each request's accept flags left to right (a warp ballot), picks the candidate of the first
 // rejection or the bonus, applies stop-token / max_new truncation and reduces alpha for the
 // gamma controller.
@@ -16,12 +17,15 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "spec_device.cuh"
 #include "spec_verify.h"
 
 #include "spec_rows_kernel.cuh"
+#include "spec_stream_kernel.cuh"
 #include "spec_trunc.cuh"
 
 namespace spec {
@@ -250,12 +254,35 @@ struct ClusterOption {
     int slice_vecs_max = 0;
     size_t smem = 0;
     int active = 0;
+    int per_sm = 1;  // CTAs resident per SM
 };
 
 struct ShapeTable {
     int dev = -1, nvec_row = -1;
-    ClusterOption opt[5];  // C = 1, 2, 4, 8, 16
+    ClusterOption opt[5];   // rows kernel, C = 1, 2, 4, 8, 16
+    ClusterOption sopt[5];  // streaming kernel, C = 1, 2, 4, 8, 16
 };
+
+// Resident clusters of C CTAs of kernel k (`block` threads, `smem` bytes of dynamic shared memory).
+static int clusters_resident(const void *k, int C, int block, size_t smem) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(C * 16, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(block), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, k, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return active;
+}
 
 template <int DT>
 static cudaError_t shape_table(int nvec_row, ShapeTable &out) {
@@ -300,53 +327,98 @@ static cudaError_t shape_table(int nvec_row, ShapeTable &out) {
             if (e != cudaSuccess) return e;
             attrs_set[ki] = true;
         }
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(C * 16, 1, 1);
-        cfg.blockDim = dim3(kBlock, 1, 1);
-        cfg.dynamicSmemBytes = smem;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, k, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            continue;
-        }
+        const int active = clusters_resident(reinterpret_cast<const void *>(k), C, kBlock, smem);
+        if (active <= 0) continue;
         o.C = C;
         o.nvt = nvt;
         o.slice_vecs_max = slice;
         o.smem = smem;
         o.active = active;
+        o.per_sm = 2;
+    }
+    // the streaming kernel: one CTA per SM, a slice of at most Geo<DT>::kMaxTiles tiles
+    static bool stream_attrs_set = false;
+    for (int ci = 0; ci < 5; ++ci) {
+        const int C = 1 << ci;
+        ClusterOption &o = t.sopt[ci];
+        if (C > nvec_row) continue;
+        const int slice = (nvec_row + C - 1) / C;
+        if (slice > Geo<DT>::kMaxTiles * Geo<DT>::kTileVecs) continue;
+        const RowsKernel k = spec_stream_kernel<DT>;
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, k);
+        if (e != cudaSuccess) return e;
+        const size_t smem = Geo<DT>::kDynSmem;
+        if (smem + fa.sharedSizeBytes > static_cast<size_t>(max_optin)) continue;
+        if (!stream_attrs_set) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     max_optin - static_cast<int>(fa.sharedSizeBytes));
+            if (e != cudaSuccess) return e;
+            stream_attrs_set = true;
+        }
+        const int active = clusters_resident(reinterpret_cast<const void *>(k), C, kStreamBlock, smem);
+        if (active <= 0) continue;
+        o.C = C;
+        o.nvt = 0;
+        o.slice_vecs_max = slice;
+        o.smem = smem;
+        o.active = active;
+        o.per_sm = 1;
     }
     cached = t;
     out = t;
     return cudaSuccess;
 }
 
-// The persistent grid: the cluster size that keeps the most SMs busy on this many target rows
-// (a cluster lives in one GPC, so large clusters strand SMs; too few rows leave clusters idle).
-// Ties go to the smaller cluster (fewer barriers per logit).
+// The persistent grid. The kernel: the streaming kernel whenever a CTA's slice fits its tiles
+// (pass 2 of an item overlaps the next item's pass 1; measured faster on all five workloads),
+// else the rows kernel. The cluster size: the one that keeps the most SMs busy on this many
+// target rows (a cluster lives in one GPC, so large clusters strand SMs; too few rows leave
+// clusters idle); ties go to the smaller cluster (fewer barriers per logit).
+// SPEC_VERIFY_KERNEL=rows or =stream in the environment restricts the choice to one kernel
+// (read on every call).
+struct Plan {
+    ClusterOption opt;
+    bool streaming = false;
+    bool ok = false;
+};
+
 template <int DT>
-static spec_status launch_rows(const RowsParams &P, cudaStream_t stream) {
+static Plan choose_plan(int nvec_row, int total_rows, int B) {
+    Plan plan;
     ShapeTable t;
-    if (shape_table<DT>(P.nvec_row, t) != cudaSuccess) return SPEC_ERR_UNSUPPORTED;
-    int best = -1;
-    long long best_score = 0;
-    for (int ci = 0; ci < 5; ++ci) {
-        const ClusterOption &o = t.opt[ci];
-        if (o.C == 0 || o.active <= 0) continue;
-        const long long score = static_cast<long long>(std::min(o.active, P.total_rows)) * o.C;
-        if (score > best_score) {
-            best_score = score;
-            best = ci;
+    if (shape_table<DT>(nvec_row, t) != cudaSuccess) return plan;
+    const char *force = std::getenv("SPEC_VERIFY_KERNEL");
+    const bool only_rows = force && std::strcmp(force, "rows") == 0;
+    const bool only_stream = force && std::strcmp(force, "stream") == 0;
+    (void)B;
+    for (int pass = 0; pass < 2 && !plan.ok; ++pass) {
+        const bool streaming = pass == 0;
+        if ((streaming && only_rows) || (!streaming && only_stream)) continue;
+        long long best_score = 0;
+        for (int ci = 0; ci < 5; ++ci) {
+            const ClusterOption &o = streaming ? t.sopt[ci] : t.opt[ci];
+            if (o.C == 0 || o.active <= 0) continue;
+            // SMs covered, in units of 1/2 SM
+            const long long score = static_cast<long long>(std::min(o.active, total_rows)) * o.C * 2 / o.per_sm;
+            if (score > best_score) {
+                best_score = score;
+                plan.opt = o;
+                plan.streaming = streaming;
+                plan.ok = true;
+            }
         }
     }
-    if (best < 0) return SPEC_ERR_UNSUPPORTED;
-    const ClusterOption &o = t.opt[best];
+    return plan;
+}
+
+template <int DT>
+static spec_status launch_rows(const RowsParams &P, cudaStream_t stream) {
+    const Plan plan = choose_plan<DT>(P.nvec_row, P.total_rows, P.B);
+    if (!plan.ok) return SPEC_ERR_UNSUPPORTED;
+    const ClusterOption &o = plan.opt;
     RowsParams Q = P;
     Q.slice_vecs_max = o.slice_vecs_max;
     Q.nclusters = std::min(o.active, P.total_rows);
@@ -357,12 +429,13 @@ static spec_status launch_rows(const RowsParams &P, cudaStream_t stream) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(Q.nclusters * o.C), 1, 1);
-    cfg.blockDim = dim3(kBlock, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(plan.streaming ? kStreamBlock : kBlock), 1, 1);
     cfg.dynamicSmemBytes = o.smem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, rows_kernel_for<DT>(o.nvt), Q) != cudaSuccess) return SPEC_ERR_CUDA;
+    const RowsKernel k = plan.streaming ? spec_stream_kernel<DT> : rows_kernel_for<DT>(o.nvt);
+    if (cudaLaunchKernelEx(&cfg, k, Q) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
 
@@ -528,4 +601,18 @@ extern "C" spec_status spec_verify_noalloc(const spec_verify_args *a, cudaStream
         ptr = noalloc_ptr[dev];
     }
     return spec_verify(a, ptr, kNoallocScratchBytes, stream);
+}
+
+extern "C" const char *spec_verify_plan(int32_t B, int32_t V, int32_t total_rows, spec_dtype dtype, int32_t *cluster,
+                                        int32_t *clusters) {
+    if (B <= 0 || V <= 0 || total_rows < B || (dtype != SPEC_BF16 && dtype != SPEC_F32)) return nullptr;
+    const int per_vec = (dtype == SPEC_BF16) ? 8 : 4;
+    if (V % per_vec != 0) return nullptr;
+    const int nvec_row = V / per_vec;
+    const Plan plan = (dtype == SPEC_BF16) ? choose_plan<SPEC_BF16>(nvec_row, total_rows, B)
+                                           : choose_plan<SPEC_F32>(nvec_row, total_rows, B);
+    if (!plan.ok) return nullptr;
+    if (cluster) *cluster = plan.opt.C;
+    if (clusters) *clusters = std::min(plan.opt.active, total_rows);
+    return plan.streaming ? "spec_stream_kernel" : "spec_rows_kernel";
 }

@@ -170,3 +170,12 @@ def test_zipf_rows_follow_the_recipe():
     assert np.abs(np.mean(srt[1000:3000] + 1.1 * np.log(ranks[1000:3000]))) < 0.5
     # draft noise 0 gives the same row
     assert torch.equal(rd.draft[0], rd.target[0])
+
+
+def test_plan_rejects_invalid_shapes_without_a_device(lib):
+    """spec_verify_plan checks the shape before it asks the device anything."""
+    f = lib.lib.spec_verify_plan
+    assert f(0, 1000, 10, lib.SPEC_F32, None, None) is None
+    assert f(4, 1001, 10, lib.SPEC_BF16, None, None) is None
+    assert f(8, 1024, 7, lib.SPEC_F32, None, None) is None
+    assert f(4, 1024, 10, 7, None, None) is None
