@@ -230,12 +230,10 @@ __device__ __forceinline__ void warp_greedy_stats(CtaShared &sh, int wb, int r, 
     }
 }
 
-// Bonus rows: the chunk (tile t, this warp) of p for a later draw, at the warp's reference of
-// this tile (kept per chunk: the reference may rise between tiles).
-__device__ __forceinline__ void chunk_of_tile(CtaShared &sh, int pb, int k, int lane, float b, float a) {
-    const bool ok = a > 0.0f && !isinf(a);
-    const float Bw = warp_max(ok ? b : -INFINITY);
-    const float c = warp_sum(ok ? a * pow2i(b - Bw) : 0.0f);
+// Bonus rows: chunk k (this warp's vectors of one chunk row) of p for a later draw, in units of
+// 2^Bw, Bw the warp's largest reference (one per tile: the reference may rise between tiles).
+__device__ __forceinline__ void chunk_of_tile(CtaShared &sh, int pb, int k, int lane, float b, float Bw, float a) {
+    const float c = warp_sum(a > 0.0f ? a * pow2i(b - Bw) : 0.0f);
     if (lane == 0) {
         sh.pm[pb][k] = c;
         sh.pref[pb][k] = Bw;
@@ -305,14 +303,19 @@ __device__ __forceinline__ bool stream_pass1(StreamShared &ss, const uint4 *trin
                 Ad.b = floorf(Elt<DT>::vmax(wd[0]) * s_hi);
             }
             float a[G::kVPT], q[G::kVPT];
-            bool slow = false;
 #pragma unroll
             for (int u = 0; u < G::kVPT; ++u) {
                 a[u] = vec_share<DT>(wt[u], At.b, shi2, slo2);
                 q[u] = (nr == 2) ? vec_share<DT>(wd[u], Ad.b, shi2, slo2) : 0.0f;
-                slow |= !(a[u] <= 0x1p64f) || !(q[u] <= 0x1p64f);
             }
-            if (__any_sync(0xffffffffu, slow)) {
+            // one test on the tile's total: a NaN, an infinity or a share above 2^64 carries into it
+            float ta = a[0], tq = q[0];
+#pragma unroll
+            for (int u = 1; u < G::kVPT; ++u) {
+                ta += a[u];
+                tq += q[u];
+            }
+            if (__any_sync(0xffffffffu, !(ta + tq <= 0x1p66f))) {
 #pragma unroll
                 for (int u = 0; u < G::kVPT; ++u) {
                     // a later vector's slow path may raise the reference: earlier shares rescale
@@ -324,18 +327,23 @@ __device__ __forceinline__ bool stream_pass1(StreamShared &ss, const uint4 *trin
                         q[w] *= (Ad.b == d0) ? 1.0f : pow2i(d0 - Ad.b);
                     }
                 }
-            }
+                ta = a[0];
+                tq = q[0];
 #pragma unroll
-            for (int u = 0; u < G::kVPT; ++u) {
-                At.s += a[u];
-                Ad.s += q[u];
+                for (int u = 1; u < G::kVPT; ++u) {
+                    ta += a[u];
+                    tq += q[u];
+                }
             }
+            At.s += ta;
+            Ad.s += tq;
             if (nr == 1) {
+                const float Bw = warp_max(At.b);
 #pragma unroll
                 for (int u = 0; u < G::kVPT; ++u) {
                     const int r = t * G::kVPT + u;
                     if (r * kThreads + warp * kWarp < nvec)  // warp-uniform
-                        chunk_of_tile(sh, pb, r * kWarps + warp, lane, At.b, a[u]);
+                        chunk_of_tile(sh, pb, r * kWarps + warp, lane, At.b, Bw, a[u]);
                     else if (lane == 0) {
                         sh.pm[pb][r * kWarps + warp] = 0.0f;
                         sh.pref[pb][r * kWarps + warp] = -INFINITY;
@@ -343,12 +351,20 @@ __device__ __forceinline__ bool stream_pass1(StreamShared &ss, const uint4 *trin
                 }
             }
         }
+        const int rel = xv - t * G::kTileVecs - tid;  // the draft token's vector, relative to this thread
+        if (rel >= 0 && rel < G::kTileVecs && rel % kThreads == 0) {
+            // the thread holding the draft token: (y_t - y_d) s there, as a float pair
+            const int u = rel / kThreads;
+            uint4 xt = wt[0], xd = wd[0];
 #pragma unroll
-        for (int u = 0; u < G::kVPT; ++u) {
-            if (xv == t * G::kTileVecs + u * kThreads + tid) {
-                // the thread holding the draft token: (y_t - y_d) s there, as a float pair
+            for (int v = 1; v < G::kVPT; ++v)
+                if (u == v) {
+                    xt = wt[v];
+                    xd = wd[v];
+                }
+            {
                 const int e = x % E;
-                const float yt = vec_elem<DT>(wt[u], e), yd = vec_elem<DT>(wd[u], e);
+                const float yt = vec_elem<DT>(xt, e), yd = vec_elem<DT>(xd, e);
                 const F2 Ex = f2_mul(f2_add({yt, 0.0f}, {-yd, 0.0f}), {s_hi, s_lo});
                 sh.xE[wb][0] = Ex.hi;
                 sh.xE[wb][1] = Ex.lo;
@@ -419,8 +435,11 @@ __device__ __forceinline__ bool stream_pass2(StreamShared &ss, const uint4 *trin
                 wd[u] = in ? dsrc[u * kThreads] : kNegInfVec<DT>();
             }
         }
-        slot_done(&ss.tempty[slot], lane);
-        slot_done(&ss.dempty[ds], lane);
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&ss.tempty[slot]);
+            mbar_arrive(&ss.dempty[ds]);
+        }
         if (work) {
 #pragma unroll
             for (int u = 0; u < G::kVPT; ++u) {
