@@ -258,6 +258,11 @@ __device__ __forceinline__ bool stream_pass1(StreamShared &ss, const uint4 *trin
     const float2 shi2 = f2splat(s_hi), slo2 = f2splat(s_lo);
     int xv = (nr == 2 && x >= 0 && x < V) ? x / E - lo : -1;
     if (xv >= nvec) xv = -1;  // another CTA's slice
+    // the tile, the thread and the vector of the tile that hold the draft token (none: tile -1)
+    const int x_tile = xv >= 0 ? xv / G::kTileVecs : -1;
+    const bool x_here = xv >= 0 && (xv % kThreads) == tid;
+    const int x_u = xv >= 0 ? (xv % G::kTileVecs) / kThreads : 0;
+    const int full_tiles = nvec / G::kTileVecs;  // tiles with no vector past the slice end
     RowAcc At = {-INFINITY, 0.0f}, Ad = {-INFINITY, 0.0f};
     float bt = -INFINITY, bd = -INFINITY;
     int it = INT_MAX, id = INT_MAX, badt = 0, badd = 0;
@@ -270,7 +275,7 @@ __device__ __forceinline__ bool stream_pass1(StreamShared &ss, const uint4 *trin
         uint4 wt[G::kVPT], wd[G::kVPT];
         const uint4 *ts = tring + static_cast<size_t>(slot) * G::kTileVecs + tid;
         const uint4 *dsrc = dring + static_cast<size_t>(ds) * G::kTileVecs + tid;
-        if ((t + 1) * G::kTileVecs <= nvec) {  // a whole tile (warp-uniform)
+        if (t < full_tiles) {  // a whole tile (warp-uniform)
 #pragma unroll
             for (int u = 0; u < G::kVPT; ++u) {
                 wt[u] = ts[u * kThreads];
@@ -351,10 +356,9 @@ __device__ __forceinline__ bool stream_pass1(StreamShared &ss, const uint4 *trin
                 }
             }
         }
-        const int rel = xv - t * G::kTileVecs - tid;  // the draft token's vector, relative to this thread
-        if (rel >= 0 && rel < G::kTileVecs && rel % kThreads == 0) {
+        if (t == x_tile && x_here) {
             // the thread holding the draft token: (y_t - y_d) s there, as a float pair
-            const int u = rel / kThreads;
+            const int u = x_u;
             uint4 xt = wt[0], xd = wd[0];
 #pragma unroll
             for (int v = 1; v < G::kVPT; ++v)
@@ -414,6 +418,25 @@ __device__ __forceinline__ bool stream_pass2(StreamShared &ss, const uint4 *trin
     float2 acc_a = make_float2(0.0f, 0.0f);
     float my_z = 0.0f;
     bool ok = true;
+    if (!work) {
+        // the greedy rule or a failed item: nothing to compute, the slots only go back to the rings
+        for (int t = 0; t < ntiles; ++t) {
+            ok &= stream_wait(sh, &ss.tfull[TP.slot], TP.par);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&ss.tempty[TP.slot]);
+                mbar_arrive(&ss.dempty[DB.slot]);
+            }
+            ring_next<G::kTRing>(TP);
+            ring_next<G::kDRing>(DB);
+        }
+        if (lane == 0) {
+            sh.wal[rb][warp] = 0.0f;
+            sh.wz[rb][warp] = 0.0f;
+        }
+        return ok;
+    }
+    const int full_tiles = nvec / G::kTileVecs;  // tiles with no vector past the slice end
     for (int t = 0; t < ntiles; ++t) {
         const int slot = TP.slot;
         const int ds = DB.slot;  // landed in pass 1, where this warp waited for it
@@ -421,7 +444,7 @@ __device__ __forceinline__ bool stream_pass2(StreamShared &ss, const uint4 *trin
         uint4 wt[G::kVPT], wd[G::kVPT];
         const uint4 *ts = tring + static_cast<size_t>(slot) * G::kTileVecs + tid;
         const uint4 *dsrc = dring + static_cast<size_t>(ds) * G::kTileVecs + tid;
-        if (work && (t + 1) * G::kTileVecs <= nvec) {  // a whole tile (warp-uniform)
+        if (t < full_tiles) {  // a whole tile (warp-uniform)
 #pragma unroll
             for (int u = 0; u < G::kVPT; ++u) {
                 wt[u] = ts[u * kThreads];
@@ -430,7 +453,7 @@ __device__ __forceinline__ bool stream_pass2(StreamShared &ss, const uint4 *trin
         } else {
 #pragma unroll
             for (int u = 0; u < G::kVPT; ++u) {
-                const bool in = work && t * G::kTileVecs + u * kThreads + tid < nvec;
+                const bool in = t * G::kTileVecs + u * kThreads + tid < nvec;
                 wt[u] = in ? ts[u * kThreads] : kNegInfVec<DT>();
                 wd[u] = in ? dsrc[u * kThreads] : kNegInfVec<DT>();
             }
@@ -440,7 +463,7 @@ __device__ __forceinline__ bool stream_pass2(StreamShared &ss, const uint4 *trin
             mbar_arrive(&ss.tempty[slot]);
             mbar_arrive(&ss.dempty[ds]);
         }
-        if (work) {
+        {
 #pragma unroll
             for (int u = 0; u < G::kVPT; ++u) {
                 const int r = t * G::kVPT + u;
