@@ -140,6 +140,7 @@ __device__ __forceinline__ void produce_drafts(StreamShared &ss, uint4 *dring, c
     const size_t row_bytes = static_cast<size_t>(P.nvec_row) * 16;
     const uint64_t drop = policy_evict_first();
     long long pos = ss.d_issued;
+    bool launch = pos == 0;  // the kernel's first pair
     for (int i = 0; i < nbatch; ++i) {
         if (ss.rows[i] != 2) continue;
         const unsigned char *src = static_cast<const unsigned char *>(P.draft) +
@@ -148,6 +149,14 @@ __device__ __forceinline__ void produce_drafts(StreamShared &ss, uint4 *dring, c
         for (int t = 0; t < ntiles; ++t, ++pos)
             issue_tile<DT>(ss.c, ss.dfull, ss.dempty, dring, G::kDRing, pos, src + static_cast<size_t>(t) * G::kTileVecs * 16,
                        tile_bytes<DT>(t, nvec), drop);
+        if (launch) {
+            // at launch every CTA asks for its first tiles at once: the next pair's drafts wait until
+            // the first pair's have landed, so that they do not queue ahead of the first items' tiles
+            launch = false;
+            const long long last = pos - 1;
+            if (!stream_wait(ss.c, &ss.dfull[last % G::kDRing], static_cast<uint32_t>((last / G::kDRing) & 1)))
+                ss.c.timed_out = 1;
+        }
     }
     ss.d_issued = pos;
 }
