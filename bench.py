@@ -2,7 +2,9 @@
 """Throughput of the batched speculative-decoding verifier step on GB300.
 
 One step = one pass of the whole hot path over one batch: spec_verify (per-position kernel +
-per-request selection), spec_compact and spec_choose_gamma, on the workload
+per-request selection), spec_compact and spec_choose_gamma, enqueued as one spec_verify_round
+call (the per-position kernel, then one kernel for the selection, the compaction and the gamma
+choice), on the workload
 "B=64 ragged K_i ~ U{0..7}, V=128256, bf16 Zipf logits, T=0.7" (synthetic, seeded). Four
 input sets of ~131 MB each (larger than the 126 MB L2) rotate between steps.
 
@@ -209,7 +211,7 @@ def workload_config(wl, rows, logit_bytes):
         "workload": f"{wl.name}: {wl.note}",
         "B": wl.B, "V": wl.V, "input_dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
         "rows_per_step": rows, "logit_bytes_per_step": logit_bytes,
-        "step": "spec_verify + spec_compact (P=4096, page 16) + spec_choose_gamma",
+        "step": "spec_verify_round: spec_verify + spec_compact (P=4096, page 16) + spec_choose_gamma in one call",
         "l2": "inputs larger than L2: 4 rotating input sets of ~131 MB each (L2 126 MB)",
     }
 
@@ -309,9 +311,7 @@ def run_ours(args):
     def step(s):
         k = s % len(sets)
         v = verifiers[k]
-        v.run(stream)
-        compactors[k].run(stream)
-        api.choose_gamma(v.out.alpha_sum, v.out.alpha_count, 0.5, GAMMA_COST, 0, 8, out=gout, stream=stream)
+        api.run_round(v, compactors[k], 0.5, GAMMA_COST, 0, 8, out=gout, stream=stream)
 
     for s in range(args.warmup):
         step(s)
@@ -363,7 +363,7 @@ def run_ours(args):
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
                      "algorithmic_bytes_per_launch": logit_bytes},
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 2 * args.steps,  # the per-position kernel and the round's tail kernel
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -397,10 +397,7 @@ def run_e2e(args, sets, verifiers, compactors, gout, stream, dev, world):
         rd = sets[k]
         for name, t in host_in[k].items():
             getattr(rd, name).copy_(t, non_blocking=True)
-        verifiers[k].run(stream)
-        compactors[k].run(stream)
-        api.choose_gamma(verifiers[k].out.alpha_sum, verifiers[k].out.alpha_count, 0.5, GAMMA_COST, 0, 8,
-                         out=gout, stream=stream)
+        api.run_round(verifiers[k], compactors[k], 0.5, GAMMA_COST, 0, 8, out=gout, stream=stream)
         for d, h in outs[k]:
             h.copy_(d, non_blocking=True)
         g_host[0].copy_(gout[0], non_blocking=True)

@@ -199,7 +199,9 @@ typedef struct {
     int32_t *compact_status;     /* [B] req_status | SPEC_REQ_BAD_BLOCKS (may be NULL)           */
 } spec_compact_args;
 
-/* Enqueues one kernel on `stream`. Needs no workspace. */
+/* Enqueues one kernel on `stream`. Needs no workspace. The output arrays must not overlap the
+ * input arrays (the kernel reads each request's inputs before it writes its packed outputs, in
+ * any order across requests). */
 spec_status spec_compact(const spec_compact_args *args, cudaStream_t stream);
 
 /* ---- choosing gamma ---------------------------------------------------------------------
@@ -236,6 +238,24 @@ double spec_depth_objective(const int32_t *n_reached, const int32_t *n_accepted,
 spec_status spec_choose_gamma(const double *alpha_sum, const int32_t *alpha_count,
                               double alpha_prev, double c, int32_t gamma_min, int32_t gamma_max,
                               int32_t *gamma_out, double *alpha_out, cudaStream_t stream);
+
+/* ---- spec_verify_round ---------------------------------------------------------------------
+ * One verification round, enqueued as one call: the same results, bit for bit, as
+ *   spec_verify(args, workspace, workspace_bytes, stream);
+ *   spec_compact(compact, stream);
+ *   spec_choose_gamma(args->alpha_sum, args->alpha_count, alpha_prev, c, gamma_min, gamma_max,
+ *                     gamma_out, alpha_out, stream);
+ * with the selection, the compaction and the gamma choice run one after another in one kernel
+ * after the per-position kernel (the three launch and hand-off latencies of the separate calls
+ * become one). `compact` carries the compaction's own inputs and outputs as for spec_compact;
+ * its accept_len / n_emitted / out_tokens / req_status are normally args' outputs. Every
+ * argument is checked as by the three calls (plus compact->B == args->B and
+ * compact->total_rows == args->total_rows; args->alpha_sum and args->alpha_count are required)
+ * before anything is enqueued; errors are theirs. A convenience of this library: the pages
+ * define the three steps, not their grouping. */
+spec_status spec_verify_round(const spec_verify_args *args, void *workspace, size_t workspace_bytes,
+                              const spec_compact_args *compact, double alpha_prev, double c, int32_t gamma_min,
+                              int32_t gamma_max, int32_t *gamma_out, double *alpha_out, cudaStream_t stream);
 
 /* Version string of the library build. */
 const char *spec_version(void);

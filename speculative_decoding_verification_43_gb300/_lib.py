@@ -64,7 +64,8 @@ class SpecCompactArgs(ctypes.Structure):
 
 
 # every symbol include/spec_verify.h declares
-EXPORTS = ("spec_verify_workspace_size", "spec_verify", "spec_verify_noalloc", "spec_verify_plan", "spec_compact",
+EXPORTS = ("spec_verify_workspace_size", "spec_verify", "spec_verify_noalloc", "spec_verify_plan",
+           "spec_verify_round", "spec_compact",
            "spec_gamma_objective", "spec_choose_gamma", "spec_choose_gamma_depth", "spec_depth_objective",
            "spec_version")
 
@@ -83,6 +84,10 @@ def _load():
     lib.spec_verify_noalloc.restype = ctypes.c_int
     lib.spec_verify_plan.argtypes = [_i32, _i32, _i32, ctypes.c_int, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
     lib.spec_verify_plan.restype = ctypes.c_char_p
+    lib.spec_verify_round.argtypes = [ctypes.POINTER(SpecVerifyArgs), _p, ctypes.c_size_t,
+                                      ctypes.POINTER(SpecCompactArgs), ctypes.c_double, ctypes.c_double, _i32, _i32,
+                                      _p, _p, _p]
+    lib.spec_verify_round.restype = ctypes.c_int
     lib.spec_compact.argtypes = [ctypes.POINTER(SpecCompactArgs), _p]
     lib.spec_compact.restype = ctypes.c_int
     lib.spec_gamma_objective.argtypes = [ctypes.c_double, ctypes.c_double, _i32]

@@ -229,6 +229,22 @@ def compact(row_off, accept_len, n_emitted, out_tokens, req_status, prefix_len, 
     return c.run(stream)
 
 
+def run_round(verifier: "Verifier", compactor: "Compactor", alpha_prev: float, c: float, gamma_min: int = 0,
+              gamma_max: int = 8, *, out=None, stream=None):
+    """One round through spec_verify_round: the bound verifier, the bound compactor and the gamma
+    choice in one call (the same results as verifier.run(), compactor.run() and choose_gamma()).
+    Returns (verify outputs, compaction outputs, (gamma int32[1], alpha float64[1]))."""
+    dev = verifier.out.alpha_sum.device
+    if out is None:
+        out = (torch.empty(1, dtype=torch.int32, device=dev), torch.empty(1, dtype=torch.float64, device=dev))
+    g, a = out
+    rc = lib.spec_verify_round(ctypes.byref(verifier.args), ctypes.c_void_p(verifier.workspace.data_ptr()),
+                               verifier.ws_bytes, ctypes.byref(compactor.args), float(alpha_prev), float(c),
+                               int(gamma_min), int(gamma_max), _ptr(g), _ptr(a), _stream_handle(stream))
+    check(rc, "spec_verify_round")
+    return verifier.out, compactor.out, (g, a)
+
+
 def choose_gamma(alpha_sum, alpha_count, alpha_prev: float, c: float, gamma_min: int = 0,
                  gamma_max: int = 8, *, out=None, stream=None):
     """Device-side gamma choice; returns (gamma int32[1], alpha float64[1]) device tensors."""

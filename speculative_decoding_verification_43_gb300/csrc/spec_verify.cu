@@ -27,182 +27,14 @@
 #include "spec_rows_kernel.cuh"
 #include "spec_stream_kernel.cuh"
 #include "spec_trunc.cuh"
+#include "spec_tail.cuh"
 
 namespace spec {
 
 // ------------------------------------------------------------------------------------------
 // Per-request selection: the first rejection, the emitted tokens, stopping, alpha reduction.
 
-struct FinParams {
-    const int32_t *row_off;
-    const int32_t *draft_tokens;
-    const int32_t *stop_token;
-    const int32_t *max_new;
-    int32_t B, K_max, total_rows;
-    const int32_t *item_flag, *item_tok, *item_status, *item_fb;
-    const float *item_prob, *item_margin, *alpha_ws;
-    int32_t *accept_len, *n_emitted, *out_tokens, *req_status, *fallback, *alpha_count;
-    float *frontier_prob, *frontier_margin;
-    double *alpha_sum;
-    int32_t *depth_reached, *depth_accepted;  // [K_max] each, or NULL
-};
-
-constexpr int kFinThreads = 1024;
-
-__global__ void __launch_bounds__(kFinThreads) spec_select_kernel(const FinParams P) {
-    __shared__ float red_hi[kFinThreads / kWarp];
-    __shared__ float red_lo[kFinThreads / kWarp];
-    __shared__ int red_n[kFinThreads / kWarp];
-    // depth statistics ("M7.8 - Speculative Serving", 0x02D): requests that reached / accepted
-    // depth j = 1..K_max
-    __shared__ int hist_r[64], hist_a[64];
-    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    griddep_launch_dependents();
-    if (threadIdx.x < 64) hist_r[threadIdx.x] = hist_a[threadIdx.x] = 0;
-    // Inputs first (they do not depend on the per-position kernel): the offsets must start at 0,
-    // end at total_rows and grow by at least one row per request; otherwise every request is
-    // BAD_SHAPE and nothing is read through them.
-    int bad_off = (__ldg(P.row_off) != 0) || (__ldg(P.row_off + P.B) != P.total_rows);
-    for (int i = threadIdx.x; i < P.B && !bad_off; i += kFinThreads)
-        if (__ldg(P.row_off + i + 1) <= __ldg(P.row_off + i)) bad_off = 1;
-    const bool global_ok = !__syncthreads_or(bad_off);
-    griddep_wait();  // the per-position results are complete from here on
-    F2 asum = {0.0f, 0.0f};
-    int acnt = 0;
-    // one request per warp at a time, lane j taking position j (K_max <= 64: two rounds at most);
-    // every per-position value is fetched in one round of independent loads
-    for (int i = warp; i < P.B; i += kFinThreads / kWarp) {
-        const int r0 = __ldg(P.row_off + i), r1 = __ldg(P.row_off + i + 1);
-        const int K = r1 - r0 - 1;
-        const int d0 = r0 - i;
-        int status = 0;
-        if (!global_ok || K < 0 || K > P.K_max || r0 < 0 || r1 > P.total_rows || d0 < 0) status |= SPEC_REQ_BAD_SHAPE;
-        const int n_cap = P.max_new ? __ldg(P.max_new + i) : INT_MAX;
-        const int stop = P.stop_token ? __ldg(P.stop_token + i) : -1;
-        // positions j = lane and j = lane + 32
-        int st_items = 0;
-        unsigned rej_lo = 0u, rej_hi = 0u;
-        int tok0 = -1, tok1 = -1, fb0 = 0, fb1 = 0, x0 = -1, x1 = -1;
-        float pr0 = NAN, pr1 = NAN, mg0 = NAN, mg1 = NAN, al0 = 0.0f, al1 = 0.0f;
-        int tok2 = -1, fb2 = 0;  // position 64 (lane 0), when K = 64
-        float pr2 = NAN, mg2 = NAN;
-        if (!status) {
-            const int j0 = lane, j1 = lane + kWarp;
-            const bool in0 = j0 <= K, in1 = j1 <= K;
-            if (in0) {
-                st_items |= P.item_status[r0 + j0];
-                tok0 = P.item_tok[r0 + j0];
-                pr0 = P.item_prob[r0 + j0];
-                mg0 = P.item_margin[r0 + j0];
-                fb0 = P.item_fb[r0 + j0];
-                if (j0 < K) {
-                    x0 = __ldg(P.draft_tokens + d0 + j0);
-                    al0 = P.alpha_ws[d0 + j0];
-                }
-            }
-            if (in1) {
-                st_items |= P.item_status[r0 + j1];
-                tok1 = P.item_tok[r0 + j1];
-                pr1 = P.item_prob[r0 + j1];
-                mg1 = P.item_margin[r0 + j1];
-                fb1 = P.item_fb[r0 + j1];
-                if (j1 < K) {
-                    x1 = __ldg(P.draft_tokens + d0 + j1);
-                    al1 = P.alpha_ws[d0 + j1];
-                }
-            }
-            if (K == 2 * kWarp && lane == 0) {  // K_max <= 64: the frontier slot of K = 64
-                st_items |= P.item_status[r0 + K];
-                tok2 = P.item_tok[r0 + K];
-                pr2 = P.item_prob[r0 + K];
-                mg2 = P.item_margin[r0 + K];
-                fb2 = P.item_fb[r0 + K];
-            }
-            rej_lo = __ballot_sync(0xffffffffu, j0 < K && P.item_flag[r0 + j0] == 0);
-            rej_hi = __ballot_sync(0xffffffffu, j1 < K && P.item_flag[r0 + j1] == 0);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) st_items |= __shfl_xor_sync(0xffffffffu, st_items, o);
-        }
-        status |= st_items;
-        if (status) {
-            if (!(status & SPEC_REQ_BAD_SHAPE) || (K >= 0 && r1 <= P.total_rows && r0 >= 0))
-                for (int j = lane; j <= K; j += kWarp) P.out_tokens[r0 + j] = -1;
-            if (lane == 0) {
-                P.req_status[i] = status;
-                P.accept_len[i] = 0;
-                if (P.n_emitted) P.n_emitted[i] = 0;
-                if (P.frontier_prob) P.frontier_prob[i] = NAN;
-                if (P.frontier_margin) P.frontier_margin[i] = NAN;
-                if (P.fallback) P.fallback[i] = 0;
-            }
-            continue;
-        }
-        // A = index of the first rejected position (K when all are accepted)
-        const int A = rej_lo ? __ffs(rej_lo) - 1 : (rej_hi ? kWarp + __ffs(rej_hi) - 1 : K);
-        // the frontier's values, from the lane that holds position A
-        const int la = A & (kWarp - 1), half = A >> 5;  // 0, 1, or 2 (A = 64, lane 0)
-        const int frontier = __shfl_sync(0xffffffffu, half == 0 ? tok0 : half == 1 ? tok1 : tok2, la);
-        const float fprob = __shfl_sync(0xffffffffu, half == 0 ? pr0 : half == 1 ? pr1 : pr2, la);
-        const float fmarg = __shfl_sync(0xffffffffu, half == 0 ? mg0 : half == 1 ? mg1 : mg2, la);
-        const int ffb = __shfl_sync(0xffffffffu, half == 0 ? fb0 : half == 1 ? fb1 : fb2, la);
-        const int out0 = (lane < A) ? x0 : (lane == A ? frontier : -1);
-        const int out1 = (lane + kWarp < A) ? x1 : (lane + kWarp == A ? frontier : -1);
-        int n = min(A + 1, max(n_cap, 0));
-        if (stop >= 0) {
-            const unsigned h0 = __ballot_sync(0xffffffffu, lane < n && out0 == stop);
-            const unsigned h1 = __ballot_sync(0xffffffffu, lane + kWarp < n && out1 == stop);
-            if (h0)
-                n = __ffs(h0);
-            else if (h1)
-                n = kWarp + __ffs(h1);
-        }
-        if (lane <= K) P.out_tokens[r0 + lane] = lane < n ? out0 : -1;
-        if (lane + kWarp <= K) P.out_tokens[r0 + lane + kWarp] = lane + kWarp < n ? out1 : -1;
-        if (lane == 0 && K == 2 * kWarp) P.out_tokens[r0 + K] = (A == K && n > K) ? frontier : -1;
-        asum = f2_add(f2_add(asum, {al0, 0.0f}), {al1, 0.0f});
-        // depth j + 1 was reached when the first j drafts were accepted, accepted when j < A
-        if (P.depth_reached) {
-            if (lane < K && lane <= A) atomicAdd(&hist_r[lane], 1);
-            if (lane + kWarp < K && lane + kWarp <= A) atomicAdd(&hist_r[lane + kWarp], 1);
-        }
-        if (P.depth_accepted) {
-            if (lane < K && lane < A) atomicAdd(&hist_a[lane], 1);
-            if (lane + kWarp < K && lane + kWarp < A) atomicAdd(&hist_a[lane + kWarp], 1);
-        }
-        if (lane == 0) {
-            acnt += K;
-            P.req_status[i] = 0;
-            P.accept_len[i] = A;
-            if (P.n_emitted) P.n_emitted[i] = n;
-            if (P.frontier_prob) P.frontier_prob[i] = fprob;
-            if (P.frontier_margin) P.frontier_margin[i] = fmarg;
-            if (P.fallback) P.fallback[i] = ffb;
-        }
-    }
-    asum = warp_sum_f2(asum);
-    if (lane == 0) {
-        red_hi[warp] = asum.hi;
-        red_lo[warp] = asum.lo;
-        red_n[warp] = acnt;
-    }
-    __syncthreads();
-    for (int j = threadIdx.x; j < P.K_max; j += kFinThreads) {
-        if (P.depth_reached) P.depth_reached[j] = hist_r[j];
-        if (P.depth_accepted) P.depth_accepted[j] = hist_a[j];
-    }
-    if (warp == 0) {
-        F2 a = {red_hi[lane], red_lo[lane]};
-        int c = red_n[lane];
-        a = warp_sum_f2(a);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-        if (lane == 0) {
-            // the one float64 operation of the call: the pair becomes the output double
-            if (P.alpha_sum) *P.alpha_sum = static_cast<double>(a.hi) + static_cast<double>(a.lo);
-            if (P.alpha_count) *P.alpha_count = c;
-        }
-    }
-}
+__global__ void __launch_bounds__(kFinThreads) spec_select_kernel(const FinParams P) { select_body(P); }
 
 // ------------------------------------------------------------------------------------------
 // Host side
@@ -449,8 +281,21 @@ extern "C" size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t total
     return ws_layout(B, total_rows).total;
 }
 
-extern "C" spec_status spec_verify(const spec_verify_args *a, void *workspace, size_t workspace_bytes,
-                                   cudaStream_t stream) {
+// The round's tail in one kernel: the selection, then (its outputs visible to the whole CTA) the
+// compaction, then the gamma choice on one thread.
+__global__ void __launch_bounds__(kFinThreads) spec_round_tail_kernel(const FinParams F, const CompactParams C,
+                                                                      const GammaParams G) {
+    select_body(F);
+    __syncthreads();
+    compact_body(C, false);
+    __syncthreads();
+    if (threadIdx.x == 0) gamma_body(G);
+}
+
+// spec_verify's checks and launches; with C and G, the tail kernel of a round in place of the
+// selection kernel. Nothing is enqueued when a check fails.
+static spec_status verify_enqueue(const spec_verify_args *a, void *workspace, size_t workspace_bytes,
+                                  cudaStream_t stream, const CompactParams *C, const GammaParams *G) {
     if (!a) return SPEC_ERR_INVALID_ARG;
     if (a->B < 1 || a->V < 1 || a->K_max < 0 || a->K_max > 64 || a->total_rows < a->B) return SPEC_ERR_INVALID_ARG;
     if (static_cast<int64_t>(a->total_rows) > static_cast<int64_t>(a->B) * (a->K_max + 1)) return SPEC_ERR_INVALID_ARG;
@@ -549,8 +394,29 @@ extern "C" spec_status spec_verify(const spec_verify_args *a, void *workspace, s
     F.alpha_sum = a->alpha_sum;
     F.depth_reached = a->depth_reached;
     F.depth_accepted = a->depth_accepted;
-    if (launch_after(spec_select_kernel, dim3(1), dim3(kFinThreads), stream, F) != cudaSuccess) return SPEC_ERR_CUDA;
-    return SPEC_OK;
+    const cudaError_t e = (C && G) ? launch_after(spec_round_tail_kernel, dim3(1), dim3(kFinThreads), stream, F, *C, *G)
+                                   : launch_after(spec_select_kernel, dim3(1), dim3(kFinThreads), stream, F);
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+extern "C" spec_status spec_verify(const spec_verify_args *a, void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+    return verify_enqueue(a, workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+extern "C" spec_status spec_verify_round(const spec_verify_args *a, void *workspace, size_t workspace_bytes,
+                                         const spec_compact_args *compact, double alpha_prev, double c,
+                                         int32_t gamma_min, int32_t gamma_max, int32_t *gamma_out,
+                                         double *alpha_out, cudaStream_t stream) {
+    if (!a || !compact) return SPEC_ERR_INVALID_ARG;
+    CompactParams C;
+    GammaParams G;
+    spec_status st = compact_params(compact, C);
+    if (st != SPEC_OK) return st;
+    if (compact->B != a->B || compact->total_rows != a->total_rows) return SPEC_ERR_INVALID_ARG;
+    st = gamma_params(a->alpha_sum, a->alpha_count, alpha_prev, c, gamma_min, gamma_max, gamma_out, alpha_out, G);
+    if (st != SPEC_OK) return st;
+    return verify_enqueue(a, workspace, workspace_bytes, stream, &C, &G);
 }
 
 extern "C" const char *spec_version(void) { return "spec-verify-gb300 0.1 (sm_103a)"; }

@@ -179,3 +179,36 @@ def test_plan_rejects_invalid_shapes_without_a_device(lib):
     assert f(4, 1001, 10, lib.SPEC_BF16, None, None) is None
     assert f(8, 1024, 7, lib.SPEC_F32, None, None) is None
     assert f(4, 1024, 10, 7, None, None) is None
+
+
+def test_round_argument_checks(lib):
+    """spec_verify_round checks all three calls' arguments before it enqueues anything: each bad
+    one fails without touching a device (every pointer here is fake)."""
+    fake = ctypes.c_void_p(0x10000)
+    ws = ctypes.c_void_p(0x20000)
+    f = lib.lib.spec_verify_round
+
+    def compact(**kw):
+        c = lib.SpecCompactArgs()
+        c.B, c.page_size, c.max_blocks, c.total_rows = 4, 16, 8, 8
+        for n in ("row_off", "accept_len", "out_tokens", "prefix_len", "block_table", "out_off", "packed_tokens",
+                  "packed_pos", "kv_off", "new_seq_len", "new_kv_len", "cand_kv_rows", "kv_src", "kv_dst"):
+            setattr(c, n, fake)
+        for k, v in kw.items():
+            setattr(c, k, v)
+        return c
+
+    a = _args(lib, alpha_sum=fake, alpha_count=fake)
+    good = compact()
+    assert f(None, ws, 1 << 20, ctypes.byref(good), 0.5, 0.1, 0, 8, fake, fake, None) == -1
+    assert f(ctypes.byref(a), ws, 1 << 20, None, 0.5, 0.1, 0, 8, fake, fake, None) == -1
+    assert f(ctypes.byref(a), ws, 1 << 20, ctypes.byref(compact(page_size=0)), 0.5, 0.1, 0, 8, fake, fake, None) == -1
+    assert f(ctypes.byref(a), ws, 1 << 20, ctypes.byref(compact(B=5, total_rows=9)), 0.5, 0.1, 0, 8, fake, fake,
+             None) == -1
+    assert f(ctypes.byref(a), ws, 1 << 20, ctypes.byref(good), 0.5, -1.0, 0, 8, fake, fake, None) == -1
+    assert f(ctypes.byref(a), ws, 1 << 20, ctypes.byref(good), 0.5, 0.1, 5, 2, fake, fake, None) == -1
+    b = _args(lib)  # no alpha_sum / alpha_count for the gamma step
+    assert f(ctypes.byref(b), ws, 1 << 20, ctypes.byref(good), 0.5, 0.1, 0, 8, fake, fake, None) == -1
+    # a verify argument that spec_verify rejects is rejected here too
+    c = _args(lib, alpha_sum=fake, alpha_count=fake, V=1001)
+    assert f(ctypes.byref(c), ws, 1 << 20, ctypes.byref(good), 0.5, 0.1, 0, 8, fake, fake, None) == -4

@@ -5,6 +5,7 @@ streamed in tiles, pass 2 one item late) and spec_rows_kernel (row slices held w
 per SM). The library picks one per shape (spec_verify_plan); SPEC_VERIFY_KERNEL forces either,
 and every case below runs under both, against the float64 oracle.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -86,3 +87,56 @@ def test_top_k_top_p(kernel):
 
 def test_wide_logit_ranges(kernel):
     G.test_wide_logit_ranges(torch.bfloat16, 131072)
+
+
+def _round_case(wl, seed, **verify_kw):
+    rd = W.make_round(wl, seed=seed, rnd=0, device="cuda")
+    ci = W.make_compaction_inputs(rd, 37, 16)
+    outs = []
+    for fused in (False, True):
+        v = api.Verifier(rd.B, rd.target.shape[1], rd.T, rd.target.dtype)
+        v.bind(rd.target, rd.draft, rd.row_off, rd.draft_tokens, rd.uniforms, rd.temperature, **verify_kw)
+        c = api.Compactor(rd.B, rd.T)
+        c.bind(rd.row_off, v.out.accept_len, v.out.n_emitted, v.out.out_tokens, v.out.req_status,
+               ci["prefix_len"], ci["cand_kv_rows"], ci["block_table"], 16)
+        if fused:
+            vo, co, (g, a) = api.run_round(v, c, 0.4, 0.05, 1, 12)
+        else:
+            vo = v.run()
+            co = c.run()
+            g, a = api.choose_gamma(vo.alpha_sum, vo.alpha_count, 0.4, 0.05, 1, 12)
+        torch.cuda.synchronize()
+        d = {k: t.cpu().clone() for k, t in vars(vo).items() if isinstance(t, torch.Tensor)}
+        d.update({"c_" + k: t.cpu().clone() for k, t in vars(co).items() if isinstance(t, torch.Tensor)})
+        d["gamma"], d["alpha"] = g.cpu().clone(), a.cpu().clone()
+        outs.append(d)
+    return outs
+
+
+@pytest.mark.parametrize("name,B", [("c3", None), ("c2", None), ("multi", 2600)])
+def test_round_equals_the_three_calls(name, B):
+    """spec_verify_round gives bit for bit the results of spec_verify, spec_compact and
+    spec_choose_gamma called one after another (also with more requests than one compaction
+    pass and with stop tokens / budgets)."""
+    if B is None:
+        wl, kw = W.WORKLOADS[name], {}
+    else:
+        wl = W.Workload("t", B=B, V=64, dtype=torch.float32, temperature=1.0, logits="normal", sigma=1.0,
+                        draft_sigma=0.2, K="uniform:0:40")
+        rng = np.random.default_rng(4)
+        kw = {"stop_token": torch.as_tensor(rng.integers(-1, 64, B).astype(np.int32), device="cuda"),
+              "max_new": torch.as_tensor(rng.integers(0, 30, B).astype(np.int32), device="cuda")}
+    sep, fused = _round_case(wl, 5, **kw)
+    assert sep.keys() == fused.keys()
+    # the packed arrays hold out_off[B] tokens and kv_off[B] KV pairs; the rest is not written
+    n_out, n_kv = int(sep["c_out_off"][-1]), int(sep["c_kv_off"][-1])
+    assert n_out == int(fused["c_out_off"][-1]) and n_kv == int(fused["c_kv_off"][-1])
+    cut = {"c_packed_tokens": n_out, "c_packed_pos": n_out, "c_kv_src": n_kv, "c_kv_dst": n_kv}
+    for k in sep:
+        a, b = sep[k], fused[k]
+        if k in cut:
+            a, b = a[:cut[k]], b[:cut[k]]
+        if a.is_floating_point():
+            assert torch.equal(torch.nan_to_num(a, nan=-7.0), torch.nan_to_num(b, nan=-7.0)), k
+        else:
+            assert torch.equal(a, b), k

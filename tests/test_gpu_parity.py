@@ -313,6 +313,30 @@ def test_compaction_bit_exact_c4():
         np.testing.assert_array_equal(getattr(c, k).cpu().numpy()[:n], o[k], err_msg=k)
 
 
+def test_compaction_of_more_requests_than_one_pass():
+    """B = 2600 requests: the compaction kernel scans and copies them in three passes of 1024,
+    carrying the offsets across passes; K up to 40, so that some requests copy more tokens than
+    a warp has lanes."""
+    base = W.Workload("t", B=2600, V=64, dtype=torch.float32, temperature=1.0, logits="normal",
+                      sigma=1.0, draft_sigma=0.2, K="uniform:0:40")
+    rd = W.make_round(base, seed=21, device="cuda")
+    out = api.verify(rd.target, rd.draft, rd.row_off, rd.draft_tokens, rd.uniforms, rd.temperature)
+    ci = W.make_compaction_inputs(rd, 37, 16)
+    c = api.compact(rd.row_off, out.accept_len, out.n_emitted, out.out_tokens, out.req_status,
+                    ci["prefix_len"], ci["cand_kv_rows"], ci["block_table"], 16)
+    torch.cuda.synchronize()
+    o = oracle.compact(rd.row_off.cpu().numpy(), out.accept_len.cpu().numpy(), out.n_emitted.cpu().numpy(),
+                       out.out_tokens.cpu().numpy(), out.req_status.cpu().numpy(),
+                       ci["prefix_len"].cpu().numpy(), ci["cand_kv_rows"].cpu().numpy(),
+                       ci["block_table"].cpu().numpy(), 16)
+    assert int(o["kv_off"][-1]) > 0 and int(out.accept_len.max()) > 32
+    n_out, n_kv = int(o["out_off"][-1]), int(o["kv_off"][-1])
+    for k in ("out_off", "kv_off", "new_seq_len", "new_kv_len", "new_draft_len", "compact_status"):
+        np.testing.assert_array_equal(getattr(c, k).cpu().numpy(), o[k], err_msg=k)
+    for k, n in (("packed_tokens", n_out), ("packed_pos", n_out), ("kv_src", n_kv), ("kv_dst", n_kv)):
+        np.testing.assert_array_equal(getattr(c, k).cpu().numpy()[:n], o[k], err_msg=k)
+
+
 def test_compaction_with_stops_and_bad_blocks():
     base = W.Workload("t", B=300, V=1024, dtype=torch.float32, temperature=1.0, logits="normal",
                       sigma=1.0, draft_sigma=0.4, K="uniform:0:6")
