@@ -32,7 +32,7 @@ constexpr int kFinThreads = 1024;
 // The selection of every request (one CTA of kFinThreads threads): the first rejection, the emitted
 // tokens, stopping, the alpha reduction and the depth histogram. Waits for the kernel ahead of it
 // in the stream (the per-position kernel) after reading the offsets.
-__device__ __forceinline__ void select_body(const FinParams &P) {
+__device__ __forceinline__ bool select_body(const FinParams &P) {
     __shared__ float red_hi[kFinThreads / kWarp];
     __shared__ float red_lo[kFinThreads / kWarp];
     __shared__ int red_n[kFinThreads / kWarp];
@@ -49,19 +49,60 @@ __device__ __forceinline__ void select_body(const FinParams &P) {
     for (int i = threadIdx.x; i < P.B && !bad_off; i += kFinThreads)
         if (__ldg(P.row_off + i + 1) <= __ldg(P.row_off + i)) bad_off = 1;
     const bool global_ok = !__syncthreads_or(bad_off);
+    // The inputs of this warp's first kPre requests (offsets, budget, stop token, draft tokens)
+    // also load before the wait: after it, a request costs one round of loads, not two.
+    constexpr int kPre = 4;
+    int pr_r0[kPre], pr_r1[kPre], pr_cap[kPre], pr_stop[kPre], pr_x0[kPre], pr_x1[kPre];
+#pragma unroll
+    for (int q = 0; q < kPre; ++q) {
+        const int i = warp + q * (kFinThreads / kWarp);
+        pr_r0[q] = pr_r1[q] = 0;
+        pr_cap[q] = INT_MAX;
+        pr_stop[q] = pr_x0[q] = pr_x1[q] = -1;
+        if (i < P.B) {
+            pr_r0[q] = __ldg(P.row_off + i);
+            pr_r1[q] = __ldg(P.row_off + i + 1);
+            if (P.max_new) pr_cap[q] = __ldg(P.max_new + i);
+            if (P.stop_token) pr_stop[q] = __ldg(P.stop_token + i);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kPre; ++q) {
+        const int i = warp + q * (kFinThreads / kWarp);
+        const int K = pr_r1[q] - pr_r0[q] - 1, d0 = pr_r0[q] - i;
+        if (i < P.B && global_ok && K >= 0 && K <= P.K_max && pr_r0[q] >= 0 && pr_r1[q] <= P.total_rows && d0 >= 0) {
+            if (lane < K) pr_x0[q] = __ldg(P.draft_tokens + d0 + lane);
+            if (lane + kWarp < K) pr_x1[q] = __ldg(P.draft_tokens + d0 + lane + kWarp);
+        }
+    }
     griddep_wait();  // the per-position results are complete from here on
     F2 asum = {0.0f, 0.0f};
     int acnt = 0;
     // one request per warp at a time, lane j taking position j (K_max <= 64: two rounds at most);
     // every per-position value is fetched in one round of independent loads
-    for (int i = warp; i < P.B; i += kFinThreads / kWarp) {
-        const int r0 = __ldg(P.row_off + i), r1 = __ldg(P.row_off + i + 1);
+    for (int i = warp, q = 0; i < P.B; i += kFinThreads / kWarp, ++q) {
+        int r0 = 0, r1 = 0, n_cap = INT_MAX, stop = -1, px0 = -1, px1 = -1;
+        if (q < kPre) {
+#pragma unroll
+            for (int k = 0; k < kPre; ++k)
+                if (k == q) {
+                    r0 = pr_r0[k];
+                    r1 = pr_r1[k];
+                    n_cap = pr_cap[k];
+                    stop = pr_stop[k];
+                    px0 = pr_x0[k];
+                    px1 = pr_x1[k];
+                }
+        } else {
+            r0 = __ldg(P.row_off + i);
+            r1 = __ldg(P.row_off + i + 1);
+            if (P.max_new) n_cap = __ldg(P.max_new + i);
+            if (P.stop_token) stop = __ldg(P.stop_token + i);
+        }
         const int K = r1 - r0 - 1;
         const int d0 = r0 - i;
         int status = 0;
         if (!global_ok || K < 0 || K > P.K_max || r0 < 0 || r1 > P.total_rows || d0 < 0) status |= SPEC_REQ_BAD_SHAPE;
-        const int n_cap = P.max_new ? __ldg(P.max_new + i) : INT_MAX;
-        const int stop = P.stop_token ? __ldg(P.stop_token + i) : -1;
         // positions j = lane and j = lane + 32
         int st_items = 0;
         unsigned rej_lo = 0u, rej_hi = 0u;
@@ -79,7 +120,7 @@ __device__ __forceinline__ void select_body(const FinParams &P) {
                 mg0 = P.item_margin[r0 + j0];
                 fb0 = P.item_fb[r0 + j0];
                 if (j0 < K) {
-                    x0 = __ldg(P.draft_tokens + d0 + j0);
+                    x0 = q < kPre ? px0 : __ldg(P.draft_tokens + d0 + j0);
                     al0 = P.alpha_ws[d0 + j0];
                 }
             }
@@ -90,7 +131,7 @@ __device__ __forceinline__ void select_body(const FinParams &P) {
                 mg1 = P.item_margin[r0 + j1];
                 fb1 = P.item_fb[r0 + j1];
                 if (j1 < K) {
-                    x1 = __ldg(P.draft_tokens + d0 + j1);
+                    x1 = q < kPre ? px1 : __ldg(P.draft_tokens + d0 + j1);
                     al1 = P.alpha_ws[d0 + j1];
                 }
             }
@@ -185,6 +226,7 @@ __device__ __forceinline__ void select_body(const FinParams &P) {
             if (P.alpha_count) *P.alpha_count = c;
         }
     }
+    return global_ok;  // the offsets passed their checks
 }
 
 
@@ -234,8 +276,9 @@ struct CopyJob {
 
 // The compaction of every request (one CTA of kCompactThreads threads). wait: call griddep_wait()
 // once the caller's offsets are checked (a kernel of its own waits for the kernel ahead of it;
-// the round's tail kernel has waited already).
-__device__ __forceinline__ void compact_body(const CompactParams &P, bool wait) {
+// the round's tail kernel has waited already). known_ok: 1 / 0 when the offsets were checked
+// already (the selection of the same round, same array), -1 to check them here.
+__device__ __forceinline__ void compact_body(const CompactParams &P, bool wait, int known_ok = -1) {
     __shared__ int tot_n[kWarp + 1];
     __shared__ int tot_e[kWarp + 1];
     __shared__ CopyJob job[kCompactThreads];
@@ -243,10 +286,13 @@ __device__ __forceinline__ void compact_body(const CompactParams &P, bool wait) 
     // offsets must start at 0, end at total_rows and grow by at least one row per request;
     // otherwise every request is BAD_SHAPE, so packed writes stay within their capacities. The
     // offsets are the caller's input, read while the kernel ahead of this one still runs.
-    int bad_off = (__ldg(P.row_off) != 0) || (__ldg(P.row_off + P.B) != P.total_rows);
-    for (int i = threadIdx.x; i < P.B && !bad_off; i += kCompactThreads)
-        if (__ldg(P.row_off + i + 1) <= __ldg(P.row_off + i)) bad_off = 1;
-    const bool offsets_ok = !__syncthreads_or(bad_off);
+    bool offsets_ok = known_ok == 1;
+    if (known_ok < 0) {
+        int bad_off = (__ldg(P.row_off) != 0) || (__ldg(P.row_off + P.B) != P.total_rows);
+        for (int i = threadIdx.x; i < P.B && !bad_off; i += kCompactThreads)
+            if (__ldg(P.row_off + i + 1) <= __ldg(P.row_off + i)) bad_off = 1;
+        offsets_ok = !__syncthreads_or(bad_off);
+    }
     if (wait) griddep_wait();  // the outputs of the kernel ahead are ready from here on
     for (int base = 0; base < P.B; base += kCompactThreads) {
         const int i = base + static_cast<int>(threadIdx.x);

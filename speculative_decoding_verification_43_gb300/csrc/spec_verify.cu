@@ -34,7 +34,7 @@ namespace spec {
 // ------------------------------------------------------------------------------------------
 // Per-request selection: the first rejection, the emitted tokens, stopping, alpha reduction.
 
-__global__ void __launch_bounds__(kFinThreads) spec_select_kernel(const FinParams P) { select_body(P); }
+__global__ void __launch_bounds__(kFinThreads) spec_select_kernel(const FinParams P) { (void)select_body(P); }
 
 // ------------------------------------------------------------------------------------------
 // Host side
@@ -285,9 +285,10 @@ extern "C" size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t total
 // compaction, then the gamma choice on one thread.
 __global__ void __launch_bounds__(kFinThreads) spec_round_tail_kernel(const FinParams F, const CompactParams C,
                                                                       const GammaParams G) {
-    select_body(F);
+    const bool offsets_ok = select_body(F);
     __syncthreads();
-    compact_body(C, false);
+    // the same offsets (same array, same B and total_rows) need no second check
+    compact_body(C, false, (C.row_off == F.row_off && C.B == F.B && C.total_rows == F.total_rows) ? (offsets_ok ? 1 : 0) : -1);
     __syncthreads();
     if (threadIdx.x == 0) gamma_body(G);
 }
