@@ -25,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -179,10 +180,20 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def kernel_hash():
+def code_of(src: str) -> str:
+    """A C++/CUDA source without its comments and blank lines: what the compiler sees."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
+def kernel_hash(read=None):
+    """Hash of the per-position kernel's code (comments excluded): a recorded ncu figure counts
+    only while the code it was taken on is unchanged."""
+    read = read or (lambda f: open(os.path.join(CSRC, f)).read())
     h = hashlib.sha256()
     for f in KERNEL_SRCS:
-        h.update(open(os.path.join(CSRC, f), "rb").read())
+        h.update(code_of(read(f)).encode())
     return h.hexdigest()[:16]
 
 

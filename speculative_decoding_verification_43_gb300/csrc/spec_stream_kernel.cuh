@@ -1,9 +1,10 @@
 // spec_stream_kernel: the per-position kernel of spec_verify for row slices of up to
-// kMaxStreamTiles tiles (included once, by spec_verify.cu; the rule and the exchange are those of
+// Geo<DT>::kMaxTiles tiles (included once, by spec_verify.cu; the rule and the exchange are those of
 // spec_rows.cuh and spec_rows_kernel.cuh).
 //
 // One CTA per SM (clusters of C CTAs; C = 4 for bf16 V = 128256), rows streamed through shared
-// memory in tiles of 1440 vectors (three 16-byte vectors per data thread):
+// memory in tiles of Geo<DT>::kVPT 16-byte vectors per data thread (three for bf16: 1440-vector
+// tiles; two for f32: 960):
 //   - a target ring of kTRing tiles carries, item after item, the target tiles of pass 1 of item
 //     i (from HBM) and then those of pass 2 of item i - 1 (read again, from L2);
 //   - a draft ring of kDRing tiles carries each pair's draft tiles; pass 1 reads them and leaves
@@ -14,9 +15,10 @@
 // Warp roles: the control warp (exchange, decision, draw), 15 data warps, and one producer warp
 // per ring. A producer walks its ring's sequence and refills a slot as soon as the 15 data warps
 // have arrived on the slot's "empty" barrier (bulk copy completing on its "full" barrier), so the
-// data warps never issue copies. Thread t takes vectors t, t + 480 and t + 960 of every tile, so
-// chunk (r, warp), r = 3 tile + u, covers vectors 480 r + 32 warp ..., the chunk numbering of the
-// rows kernel, and the control warp's exchange, decision and draw code is shared with it.
+// data warps never issue copies. Thread t takes vectors t, t + 480, ... of every tile (one per
+// vector of the thread), so chunk (r, warp), r = kVPT tile + u, covers vectors 480 r + 32 warp ...,
+// the chunk numbering of the rows kernel, and the control warp's exchange, decision and draw code
+// is shared with it.
 #pragma once
 
 #include "spec_rows_kernel.cuh"
