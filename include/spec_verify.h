@@ -60,7 +60,11 @@ enum {
     SPEC_REQ_BAD_LOGITS = 2,   /* a row of the request holds NaN or +inf, or no finite logit  */
     SPEC_REQ_BAD_SHAPE = 4,    /* K_i < 0, K_i > K_max, or row_off inconsistent               */
     SPEC_REQ_BAD_PARAM = 8,    /* temperature NaN, infinite or negative, or top_p NaN         */
-    SPEC_REQ_BAD_BLOCKS = 16   /* spec_compact: a committed position has no page             */
+    SPEC_REQ_BAD_BLOCKS = 16,  /* spec_compact: a committed position has no page             */
+    SPEC_REQ_TIMEOUT = 32      /* a bounded wait inside the kernel gave up (a copy or a peer
+                                  CTA's published result did not arrive within about a
+                                  second); the request's result is not computed. Not expected
+                                  on a healthy device: it stands in for a hang               */
 };
 
 /* ---- spec_verify ------------------------------------------------------------------------
@@ -106,7 +110,8 @@ typedef struct {
                                     token's CDF interval, over Z                                */
     int32_t *fallback;           /* [B] 1 when the residual had zero mass and p was used        */
     /* profiling (may be NULL): two cudaEvent_t recorded on `stream` immediately before and after
-       the per-position kernel, so a caller can time that kernel alone */
+       the verifier's kernel (after the truncation kernel, when there is one), so a caller can
+       time that kernel alone */
     cudaEvent_t rows_event_begin;
     cudaEvent_t rows_event_end;
     /* depth statistics ("M7.8 - Speculative Serving", sections 0x02D and 0x07B; each may be
@@ -118,7 +123,7 @@ typedef struct {
     /* top-k / top-p (SDCP "Session Model": p is the target's distribution after temperature,
        top-k and top-p, in that order; q is not truncated). Tokens rank by logit, ties by
        ascending id. Each may be NULL (no truncation); ignored under the greedy rule (T == 0).
-       The cut of each target row is computed by an extra kernel (one CTA per target row) and
+       The cut of each target row is computed by an extra kernel before the verifier's, and
        every other token is treated as probability zero: the accept ratio, alpha, the residual
        and both draws use the truncated, renormalised law. */
     const int32_t *top_k;        /* [B] keep the k highest-ranked tokens (k <= 0 or k >= V: all) */
@@ -127,12 +132,18 @@ typedef struct {
                                     token; NaN: SPEC_REQ_BAD_PARAM)                            */
 } spec_verify_args;
 
-/* Bytes of device workspace spec_verify needs for a batch of total_rows target rows.
- * The workspace must be 256-byte aligned. Its contents need no initialisation. */
+/* Bytes of device workspace spec_verify needs for a batch of total_rows target rows of V logits
+ * of type dtype. The workspace must be 256-byte aligned and zero-filled before its first use
+ * (cudaMemset): it holds counters and published records that the kernel's CTAs exchange. Every
+ * call leaves it ready for the next one (counters back at zero, a new epoch for the records), so
+ * it is filled once, not per call, and may serve calls of any shape that fits its size. Calls
+ * that share a workspace must not overlap on the GPU. */
 size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t total_rows, spec_dtype dtype);
 
-/* Verify one round. Enqueues two kernels on `stream` (three with top-k / top-p); returns
- * without waiting. */
+/* Verify one round. Enqueues one kernel on `stream` (two with top-k / top-p, whose cut of each
+ * target row runs first); returns without waiting. The kernel is a persistent grid of one CTA per
+ * SM, launched cooperatively (all CTAs resident at once); it fails with SPEC_ERR_CUDA when the
+ * device cannot host that grid (for example while another cooperative kernel holds its SMs). */
 spec_status spec_verify(const spec_verify_args *args, void *workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 
@@ -140,26 +151,23 @@ spec_status spec_verify(const spec_verify_args *args, void *workspace, size_t wo
  * memory where they verify (a memory planner that owns all device memory, a callback inside
  * another runtime, a path where cudaMalloc's synchronisation is not acceptable). The pages have
  * no counterpart to this entry point: it is an interface convenience of this library.
- * Scratch comes from one fixed array of 576 KiB in the library's device memory, present on
- * every GPU that loads the library until exit. Limit: total_rows <= 16384 target rows per
- * call; larger batches return SPEC_ERR_UNSUPPORTED before anything is enqueued. The array's
- * address is looked up on the first call on each device (make that call before any stream
- * capture). All calls share the array: calls that overlap on the GPU (other streams, other
- * threads) race on it and must be serialised by the caller. Arguments, outputs and errors are
- * otherwise those of spec_verify. */
+ * Scratch comes from one fixed array of 4 MiB in the library's device memory, present on every
+ * GPU that loads the library until exit; it starts zeroed and each call leaves it ready for the
+ * next. Limits: total_rows <= 16384 target rows per call, and spec_verify_workspace_size() of the
+ * call's shape at most 4 MiB (for example T = 16384 rows with V * sizeof(logit) <= 16 KB, or the
+ * B = 64, V = 128256 bf16 batch); larger calls return SPEC_ERR_UNSUPPORTED before anything is
+ * enqueued. The array's address is looked up on the first call on each device (make that call
+ * before any stream capture). All calls share the array: calls that overlap on the GPU (other
+ * streams, other threads) race on it and must be serialised by the caller. Arguments, outputs
+ * and errors are otherwise those of spec_verify. */
 spec_status spec_verify_noalloc(const spec_verify_args *args, cudaStream_t stream);
 
-/* Which per-position kernel spec_verify launches for a batch of this shape (B requests,
- * total_rows target rows, vocabulary V, dtype) on the current device, and its persistent grid:
- * *cluster CTAs per cluster and *clusters clusters (either pointer may be NULL). Returns a
- * static string naming the kernel, "spec_stream_kernel" (row slices streamed in tiles, one CTA
- * per SM) or "spec_rows_kernel" (row slices held whole, two CTAs per SM), or NULL when no
- * configuration fits this device (spec_verify then returns SPEC_ERR_UNSUPPORTED) or the shape is
- * invalid (B <= 0, V <= 0, total_rows < B, a row not a multiple of 16 bytes). A diagnostic of
- * this library: it enqueues nothing and only queries the device's occupancy. The kernel is the
- * streaming one whenever a CTA's row slice fits its tiles, else the rows one; the cluster size
- * keeps the most SMs busy on total_rows items. The environment variable SPEC_VERIFY_KERNEL=rows
- * or =stream (read on every call, here and in spec_verify) restricts the choice to one kernel. */
+/* Which kernel spec_verify launches for a batch of this shape (B requests, total_rows target
+ * rows, vocabulary V, dtype) on the current device, and its grid: *cluster CTAs per cluster (1)
+ * and *clusters CTAs (one per SM); either pointer may be NULL. Returns a static string naming
+ * the kernel ("spec_slice_kernel"), or NULL when the shape is invalid (B <= 0, V <= 0,
+ * total_rows < B, a row not a multiple of 16 bytes) or the device cannot host the kernel. A
+ * diagnostic: it enqueues nothing and only queries the device. */
 const char *spec_verify_plan(int32_t B, int32_t V, int32_t total_rows, spec_dtype dtype, int32_t *cluster,
                              int32_t *clusters);
 
@@ -245,11 +253,10 @@ spec_status spec_choose_gamma(const double *alpha_sum, const int32_t *alpha_coun
  *   spec_compact(compact, stream);
  *   spec_choose_gamma(args->alpha_sum, args->alpha_count, alpha_prev, c, gamma_min, gamma_max,
  *                     gamma_out, alpha_out, stream);
- * with the selection, the compaction and the gamma choice run one after another in one kernel
- * after the per-position kernel (the three launch and hand-off latencies of the separate calls
- * become one). `compact` carries the compaction's own inputs and outputs as for spec_compact;
- * its accept_len / n_emitted / out_tokens / req_status are normally args' outputs. Every
- * argument is checked as by the three calls (plus compact->B == args->B and
+ * with the compaction and the gamma choice run by the last CTA of spec_verify's kernel, so that
+ * the round is one launch. `compact` carries the compaction's own inputs and outputs as for
+ * spec_compact; its accept_len / n_emitted / out_tokens / req_status are normally args'
+ * outputs. Every argument is checked as by the three calls (plus compact->B == args->B and
  * compact->total_rows == args->total_rows; args->alpha_sum and args->alpha_count are required)
  * before anything is enqueued; errors are theirs. A convenience of this library: the pages
  * define the three steps, not their grouping. */

@@ -27,6 +27,7 @@ REQ_BAD_LOGITS = 2
 REQ_BAD_SHAPE = 4
 REQ_BAD_PARAM = 8
 REQ_BAD_BLOCKS = 16
+REQ_TIMEOUT = 32
 
 NOALLOC_MAX_ROWS = 16384
 

@@ -37,8 +37,8 @@ def workspace_size(B: int, V: int, total_rows: int, dtype: torch.dtype) -> int:
 
 
 def verify_plan(B: int, V: int, total_rows: int, dtype: torch.dtype):
-    """(kernel name, CTAs per cluster, clusters) that spec_verify launches for this shape on the
-    current device, or None when no configuration fits (or the shape is invalid)."""
+    """(kernel name, CTAs per cluster, CTAs) that spec_verify launches for this shape on the
+    current device, or None when the device cannot host it (or the shape is invalid)."""
     c, n = ctypes.c_int32(0), ctypes.c_int32(0)
     name = lib.spec_verify_plan(B, V, total_rows, _DTYPE[dtype], ctypes.byref(c), ctypes.byref(n))
     return None if name is None else (name.decode(), c.value, n.value)
@@ -67,7 +67,8 @@ class Verifier:
 
     Holds the C struct, the workspace and the output tensors, so that repeated rounds on the
     same buffers cost one ctypes call each. Inputs are bound with ``bind``; ``run`` enqueues
-    the two kernels on the given (or current) stream and returns without synchronising.
+    the verifier's kernel on the given (or current) stream and returns without synchronising.
+    The workspace is zero-filled once, here: every call leaves it ready for the next one.
     """
 
     def __init__(self, B: int, V: int, total_rows: int, dtype: torch.dtype, *, K_max: int = 64,
@@ -91,8 +92,8 @@ class Verifier:
             self.out.frontier_margin = torch.empty(B, **f32)
             self.out.fallback = torch.empty(B, **i32)
         self.ws_bytes = workspace_size(B, V, total_rows, dtype)
-        # 256-byte aligned: the caching allocator hands out 512-byte aligned blocks
-        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        # 256-byte aligned (the caching allocator hands out 512-byte aligned blocks) and zeroed
+        self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
         self.args = SpecVerifyArgs()
         a = self.args
         a.B, a.V, a.K_max, a.total_rows, a.dtype = B, V, K_max, total_rows, _DTYPE[dtype]

@@ -24,8 +24,9 @@
 namespace spec {
 
 __global__ void __launch_bounds__(kCompactThreads) spec_compact_kernel(const CompactParams P) {
+    __shared__ CompactScratch<kCompactThreads> scratch;
     griddep_launch_dependents();
-    compact_body(P, true);
+    compact_body<kCompactThreads>(P, true, -1, scratch);
 }
 
 __global__ void spec_gamma_kernel(const GammaParams G) {

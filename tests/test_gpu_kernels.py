@@ -1,9 +1,9 @@
-"""GPU: which per-position kernel spec_verify launches, and the parity of each one.
+"""GPU: the verifier's kernel and its grid, and spec_verify_round against the three calls.
 
-spec_verify has two per-position kernels with the same results: spec_stream_kernel (row slices
-streamed in tiles, pass 2 one item late) and spec_rows_kernel (row slices held whole, two CTAs
-per SM). The library picks one per shape (spec_verify_plan); SPEC_VERIFY_KERNEL forces either,
-and every case below runs under both, against the float64 oracle.
+spec_verify launches one kernel, spec_slice_kernel: a persistent grid of one CTA per SM whose
+CTAs exchange published statistics through the workspace. These tests check the plan the
+library reports, that a workspace serves many calls of different shapes in a row (its counters
+return to zero and its epoch advances), and that the one-launch round equals the three calls.
 """
 import numpy as np
 import pytest
@@ -17,34 +17,14 @@ import test_gpu_parity as G
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["rows", "stream"])
-def kernel(request, monkeypatch):
-    monkeypatch.setenv("SPEC_VERIFY_KERNEL", request.param)
-    return request.param
-
-
-def _rows(wl):
-    return W.make_round(wl, seed=0, rnd=0, device="cuda").T
-
-
-def test_plan_of_the_workloads(monkeypatch):
-    """Every workload's row slices fit the streaming kernel's tiles: it runs them all, on
-    clusters that keep at least 120 of the 152 SMs busy (c3: 4-CTA clusters)."""
-    monkeypatch.delenv("SPEC_VERIFY_KERNEL", raising=False)
+def test_plan_of_the_workloads():
+    """Every workload runs on the slice kernel, one CTA on every SM of the device."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     for name in ("c1", "c2", "c3", "c4", "c5"):
         wl = W.WORKLOADS[name]
-        kern, c, n = api.verify_plan(wl.B, wl.V, _rows(wl), wl.dtype)
-        assert kern == "spec_stream_kernel", (name, kern, c, n)
-        assert n * c >= min(120, _rows(wl) * c), (name, c, n)
-        if name == "c3":
-            assert c == 4
-
-
-def test_forced_plan(kernel):
-    c3 = W.WORKLOADS["c3"]
-    name, c, n = api.verify_plan(c3.B, c3.V, _rows(c3), c3.dtype)
-    assert name == f"spec_{kernel}_kernel"
-    assert n >= 1 and c in (1, 2, 4, 8, 16)
+        rows = W.make_round(wl, seed=0, rnd=0, device="cuda").T
+        kern, c, n = api.verify_plan(wl.B, wl.V, rows, wl.dtype)
+        assert (kern, c, n) == ("spec_slice_kernel", 1, sms), (name, kern, c, n)
 
 
 def test_invalid_shapes_have_no_plan():
@@ -53,40 +33,31 @@ def test_invalid_shapes_have_no_plan():
     assert api.verify_plan(8, 1024, 7, torch.float32) is None    # fewer rows than requests
 
 
-def test_c3_full_batch(kernel):
-    G.test_c3_full_batch()
-
-
-def test_c5_sampled(kernel):
-    G.test_full_size_sampled("c5", 32)
-
-
-@pytest.mark.parametrize("dtype,V,B,Kspec,T", [
-    (torch.bfloat16, 50264, 40, "uniform:0:8", 0.8),
-    (torch.float32, 12348, 24, "uniform:0:6", 1.3),
-    (torch.float32, 8, 9, "uniform:0:3", 0.9),
-    (torch.bfloat16, 262144, 6, "uniform:1:3", 1.0),
-])
-def test_shapes(kernel, dtype, V, B, Kspec, T):
-    G.test_shapes(dtype, V, B, Kspec, T)
-
-
-def test_greedy_and_mixed_temperatures(kernel):
-    G.test_greedy_and_mixed_temperatures()
-
-
-def test_bad_requests(kernel):
-    G.test_bad_requests()
-    G.test_k_max_exceeded_is_bad_shape()
-
-
-def test_top_k_top_p(kernel):
-    G.test_top_k_top_p(torch.bfloat16, 32000, "zipf")
-    G.test_top_k_cuts_inside_ties()
-
-
-def test_wide_logit_ranges(kernel):
-    G.test_wide_logit_ranges(torch.bfloat16, 131072)
+def test_one_workspace_serves_many_calls():
+    """Rounds of different shapes through one workspace, sized for the largest: each call
+    leaves the counters at zero for the next, and the per-call tag keeps the previous call's
+    published words from being read as this call's."""
+    big = W.scaled(W.WORKLOADS["c3"], B=24, V=32768)
+    rd0 = W.make_round(big, seed=4, rnd=0, device="cuda")
+    v = api.Verifier(rd0.B, rd0.target.shape[1], rd0.T, rd0.target.dtype, diagnostics=True)
+    ws = v.workspace
+    for rnd in range(6):
+        rd = W.make_round(big, seed=4, rnd=rnd, device="cuda")
+        if rd.T > rd0.T:
+            continue
+        w = api.Verifier(rd.B, rd.target.shape[1], rd.T, rd.target.dtype, diagnostics=True)
+        assert w.ws_bytes <= ws.numel()
+        w.workspace = ws
+        w.ws_bytes = ws.numel()
+        w.bind(rd.target, rd.draft, rd.row_off, rd.draft_tokens, rd.uniforms, rd.temperature)
+        w.run()
+        fresh = api.verify(rd.target, rd.draft, rd.row_off, rd.draft_tokens, rd.uniforms, rd.temperature,
+                           diagnostics=True)
+        torch.cuda.synchronize()
+        for k in ("accept_len", "n_emitted", "out_tokens", "req_status"):
+            assert torch.equal(getattr(w.out, k), getattr(fresh, k)), (rnd, k)
+        assert torch.equal(w.out.alpha_rows, fresh.alpha_rows), rnd
+        G.assert_report(G.check_round(rd))
 
 
 def _round_case(wl, seed, **verify_kw):
