@@ -66,45 +66,43 @@
 namespace spec {
 namespace slice {
 
-constexpr int kDW = 8;                              // data warps
-constexpr int kDataThreads = kDW * kWarp;           // 256
-constexpr int kVPT = 4;                             // 16-byte vectors per data thread, row and slice
+constexpr int kDW = 16;                             // data warps
+constexpr int kDataThreads = kDW * kWarp;           // 512
+constexpr int kVPT = 2;                             // 16-byte vectors per data thread, row and slice
 constexpr int kSliceVecs = kDataThreads * kVPT;     // 1024 vectors: 16 KB of one row
-constexpr int kChunkVecs = kWarp * kVPT;            // 128 vectors: a data warp's share, a draw chunk
-constexpr int kChunksPerSlice = kDW;                // 8
+constexpr int kChunkVecs = kWarp * kVPT;            // 64 vectors: a data warp's share, a draw chunk
 constexpr int kJobs = 6;                            // job ring: a job (pass 1 or pass 2 of a unit)
-                                                    // lands its slices in slots 2j and 2j + 1
+                                                    // owns two 16 KB slots
 constexpr int kSlots = 2 * kJobs;                   // 16 KB slots
 constexpr int kLag = 10;                            // pass 2 of unit n - kLag follows pass 1 of unit n
-constexpr int kR = 16;                              // unit ring: descriptors and decisions
-constexpr int kSR = 3;                              // pass-1 partial buffers
-constexpr int kPR = 3;                              // pass-2 partial buffers
-constexpr int kFQ = 8;                              // finalisation queue
+constexpr int kR = 16;                              // unit ring: descriptors
+constexpr int kFQ = 16;                             // the final warp's queue
 constexpr int kStage = 520;                         // row offsets staged in shared memory (B < kStage)
-constexpr int kPartPitch = kDataThreads + kDataThreads / 8;  // partial of thread t at t + t / 8
 constexpr int kPrep = 8;                            // producer: descriptors prepared at once
-constexpr int kGroups = 4;                          // decide warp: lane groups, one unit each
-constexpr int kGroupLanes = kWarp / kGroups;        // 8
-static_assert(kR >= kLag + kJobs, "a unit's descriptor must outlive its pass-2 job");
+static_assert(kR >= kLag + kJobs, "a unit's descriptor must outlive its last job");
 
-enum : int { W_PROD = kDW, W_STATS, W_DECIDE, W_FINISH, W_FINAL, kNumWarps };
-constexpr int kBlock = kNumWarps * kWarp;  // 416 threads (at most 128 registers a thread: four
-                                           // warps on one of the SM's four sub-partitions)
+// Warps: the data warps, the producer, the final warp. Eighteen warps put at most five on each of
+// the four schedulers, whose register files (16384 each) then leave 96 registers to a thread.
+enum : int { W_PROD = kDW, W_FINAL, kNumWarps };
+constexpr int kBlock = kNumWarps * kWarp;  // 576 threads
+constexpr int kMaxRegs = 96;
 
-// Words of a unit's published pass-1 record: the unit's statistics of both rows, the shares of
-// its target row's eight chunks (units 2^ref_t), and, from the unit holding the draft token,
-// (y_t - y_d) s there as a float pair and its flags.
-enum : int { SR_AT = 0, SR_ST = 1, SR_AD = 2, SR_SD = 3, SR_CHUNK = 4, SR_XHI = 12, SR_XLO = 13, SR_XF = 14,
-             kStatWords = 16 };
-// Words of a unit's published pass-2 record: alpha share, residual mass (a probability), then the
-// residual mass of each chunk.
-enum : int { PR_ALPHA = 0, PR_Z = 1, PR_CHUNK = 2, kP2Words = 10 };
-// Control words of the workspace.
+// Published records (64-bit tagged words), per data warp of a unit (one 128-vector chunk of each
+// slice), contiguous per item: pass 1, the reference exponent and sum of its target and its draft
+// chunk (greedy: argmax and max); pass 2, its alpha share and residual mass. Per item: the draft
+// token's words (from the thread holding them) and the item's decision.
+enum : int { W1_AT = 0, W1_ST = 1, W1_AD = 2, W1_SD = 3, kW1Words = 4 };
+enum : int { W2_ALPHA = 0, W2_Z = 1, kW2Words = 2 };
+enum : int { X_HI = 0, X_LO = 1, X_F = 2, kXWords = 4 };
+// the decision: UnitDec's sixteen 32-bit fields in order
+constexpr int kDecWords = 16;
+// control words of the workspace
 enum : int { CTL_DONE = 0, CTL_EPOCH = 1, kCtlWords = 4 };
-// Flags of the draft token's logits: q(x) = 0, p(x) = 0 (target logit -inf or outside the cut).
 enum : int32_t { XF_QZERO = 1, XF_PZERO = 2 };
 
 enum : int32_t { U_END = 0, U_PAIR = 1, U_ROW = 2, U_SKIP = 3 };
+// jobs: pass 1 of a unit; its pass 2 (slices again, with the item's decision); a unit without rows;
+// the end
 enum : int32_t { J_END = 0, J_P1 = 1, J_P2 = 2, J_SKIP = 3 };
 enum : int32_t { SAMPLE_NONE = 0, SAMPLE_RESIDUAL = 1, SAMPLE_P = 2 };
 enum : int32_t { REQ_TIMEOUT = SPEC_REQ_TIMEOUT };
@@ -135,8 +133,10 @@ struct SliceParams {
     int32_t ns;              // slices per row
     int32_t nunits;          // total_rows * ns
     // workspace
-    unsigned long long *stat_rec;  // [nunits][kStatWords]
-    unsigned long long *p2_rec;    // [nunits][kP2Words]
+    unsigned long long *p1w;       // [nunits][kDW][kW1Words]
+    unsigned long long *p2w;       // [nunits][kDW][kW2Words]
+    unsigned long long *xrec;      // [T][kXWords]
+    unsigned long long *drec;      // [T][kDecWords]
     uint32_t *req_cnt;             // [B] items of the request finalised
     uint32_t *ctl;                 // [kCtlWords]
     int32_t *item_flag, *item_tok, *item_status, *item_fb;
@@ -179,36 +179,37 @@ struct UnitDec {
     F2 u_s;
 };
 
+static_assert(sizeof(UnitDec) == kDecWords * 4, "the decision record holds UnitDec's fields");
+
+// A job of the final warp: decide an item (its last unit has been through pass 1 in this CTA),
+// or finalise it (results and draw) with its decision; or the end of the queue.
+enum : int32_t { F_END = 0, F_DECIDE = 1, F_FINAL = 2 };
 struct FinJob {
+    int32_t op;
     UnitDesc d;
     UnitDec D;
 };
 
-// A job of the data warps: pass 1 or pass 2 of a unit, its slices in the job's two slots.
+// A job of the data warps, in the job's slots: pass 1 (the unit's slices), or pass 2 (the slices
+// again and the item's decision record).
 struct Job {
     int32_t type, unit;
 };
 
 struct Shared {
-    float4 p1part[kSR][kPartPitch];  // pass-1 partials: (b_t, s_t, b_d, s_d) per data thread
-    float2 p2part[kPR][kPartPitch];  // pass-2 partials: (alpha, residual) per data thread
-    float4 xval[kSR];                // (E_hi, E_lo, flags, -) from the thread holding the draft token
+    unsigned long long drec[kJobs][kDecWords];  // a pass-2 job's copy of the item's decision
     UnitDesc desc[kR];
-    UnitDec dec[kR];
     FinJob fq[kFQ];
     Job jobs[kJobs];
     UnitDesc prep[kPrep];     // producer: the next batch of descriptors, prepared one per lane
     int32_t roff[kStage + 1];
     uint64_t desc_full[kR];   // producer: descriptor written
-    uint64_t desc_empty[kR];  // every consumer (data, stats, decide, finish warps) is done with it
-    uint64_t dec_ready[kR];   // decide: the unit's decision is written
-    uint64_t p1_done[kSR];    // data warps: pass-1 partials written
-    uint64_t p1_free[kSR];    // stats: partial buffer read
-    uint64_t p2_done[kPR];    // data warps: pass-2 partials written
-    uint64_t p2_free[kPR];    // finish: partial buffer read
-    uint64_t job_full[kJobs];     // producer: the job written, its slices landed
+    uint64_t desc_empty[kR];  // every data warp is done with it
+    uint64_t job_full[kJobs];     // producer: the job written, its copies landed
     uint64_t job_empty[kJobs];    // data warps: done with the job's slots
     uint64_t fq_full[kFQ], fq_empty[kFQ];
+    int32_t fq_tail;          // tickets of the final warp's queue (several data warps push)
+    int32_t end_cnt;          // data warps that reached the end
     int32_t timed_out;
     int32_t bad_offsets;      // row_off fails its checks: every request is BAD_SHAPE
     int32_t staged;           // row_off is in roff
@@ -233,6 +234,11 @@ __device__ __forceinline__ void st_word(unsigned long long *p, uint32_t value, u
 __device__ __forceinline__ unsigned long long ld_word(const unsigned long long *p) {
     unsigned long long w;
     asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+__device__ __forceinline__ ulonglong2 ld_word2(const unsigned long long *p) {
+    ulonglong2 w;
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(w.x), "=l"(w.y) : "l"(p) : "memory");
     return w;
 }
 __device__ __forceinline__ uint32_t ld_u32_relaxed(const uint32_t *p) {
@@ -358,30 +364,33 @@ __device__ __forceinline__ float vec_sum(const uint4 &w, float2 shi2, float2 slo
     return e[0].x + e[0].y;
 }
 
-// A thread's sum of 2^(y s - b) over its kVPT vectors of one row, b an integral reference.
-// Fast path: b from the thread's first vector, so no exponential waits on a running max. When a
-// thread of the warp overflows (a sum above 2^64: a later vector much larger than the first one,
-// an all -inf first vector, a NaN or +inf), the whole warp takes the exact path: b from the
-// thread's max over all its vectors (0 for an all -inf thread, whose sum is then 0).
+// Vector vi of a slice in its slot, or -inf past the slice's end (no mass, never a maximum).
 template <int DT>
-__device__ __forceinline__ float row_sum_exact(uint4 v0, uint4 v1, uint4 v2, uint4 v3, float s_hi, float2 shi2,
-                                               float2 slo2, float &b) {
-    static_assert(kVPT == 4, "the exact path takes the thread's four vectors by value");
-    const float m = fmaxf(fmaxf(Elt<DT>::vmax(v0), Elt<DT>::vmax(v1)), fmaxf(Elt<DT>::vmax(v2), Elt<DT>::vmax(v3)));
-    b = (m == -INFINITY) ? 0.0f : floorf(m * s_hi);
-    return vec_sum<DT>(v0, shi2, slo2, b) + vec_sum<DT>(v1, shi2, slo2, b) + vec_sum<DT>(v2, shi2, slo2, b) +
-           vec_sum<DT>(v3, shi2, slo2, b);
+__device__ __forceinline__ uint4 slice_vec(const uint4 *slot, int vi, int nvec) {
+    return vi < nvec ? slot[vi] : kNegInfVec<DT>();
 }
 
+// A thread's sum of 2^(y s - b) over its kVPT vectors of one row in the exact form, for a warp in
+// which some thread's fast sum overflowed (above 2^64: a later vector much larger than the first,
+// an all -inf first vector, a NaN or +inf): b from the thread's max over all its vectors (0 for an
+// all -inf thread, whose sum is then 0). Rare: out of line, the vectors read again from the slot.
 template <int DT>
-__device__ __forceinline__ float row_sum(const uint4 (&v)[kVPT], float s_hi, float2 shi2, float2 slo2, float &b) {
-    b = floorf(Elt<DT>::vmax(v[0]) * s_hi);
+__device__ __noinline__ float2 row_sum_exact(const UnitDesc &d, const uint4 *slot, int vbase, bool cut) {
+    const int vglob = d.slice * kSliceVecs + vbase;
+    const float2 shi2 = f2splat(d.s_hi), slo2 = f2splat(d.s_lo);
+    uint4 v[kVPT];
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kVPT; ++k) {
+        v[k] = slice_vec<DT>(slot, vbase + k * kWarp, d.nvec);
+        if (cut) mask_cut<DT>(v[k], vglob + k * kWarp, d.cut_tau, d.cut_id);
+        m = fmaxf(m, Elt<DT>::vmax(v[k]));
+    }
+    const float b = (m == -INFINITY) ? 0.0f : floorf(m * d.s_hi);
     float s = 0.0f;
 #pragma unroll
     for (int k = 0; k < kVPT; ++k) s += vec_sum<DT>(v[k], shi2, slo2, b);
-    // the exact path: rare (a warp-uniform branch)
-    if (__any_sync(0xffffffffu, !(s <= 0x1p64f))) s = row_sum_exact<DT>(v[0], v[1], v[2], v[3], s_hi, shi2, slo2, b);
-    return s;
+    return make_float2(b, s);
 }
 
 // Greedy rule, one thread's vectors of one row: the largest logit and the smallest index that
@@ -413,62 +422,88 @@ __device__ __forceinline__ void row_argmax(const uint4 (&v)[kVPT], int vbase, fl
     }
 }
 
-// Loads a thread's vectors of a slice from its slot (past the slice end: -inf).
-template <int DT, bool RAGGED>
-__device__ __forceinline__ void load_slice(const uint4 *slot, int vbase, int nvec, uint4 (&v)[kVPT]) {
+// Pass 1 of one unit under the greedy rule by one data thread: (max_t, argmax_t, max_d, argmax_d)
+// of its vectors (indices as int bits). Out of line (the greedy rule is the rare one).
+template <int DT>
+__device__ __noinline__ float4 pass1_greedy(const UnitDesc &d, const uint4 *tslot, const uint4 *dslot, int vbase) {
+    const bool pair = d.kind == U_PAIR;
+    const int vglob = d.slice * kSliceVecs + vbase;
+    uint4 vt[kVPT], vd[kVPT];
 #pragma unroll
     for (int k = 0; k < kVPT; ++k) {
-        const int vi = vbase + k * kWarp;
-        v[k] = (!RAGGED || vi < nvec) ? slot[vi] : kNegInfVec<DT>();
+        vt[k] = slice_vec<DT>(tslot, vbase + k * kWarp, d.nvec);
+        vd[k] = pair ? slice_vec<DT>(dslot, vbase + k * kWarp, d.nvec) : kNegInfVec<DT>();
     }
+    float bt, bd = -INFINITY;
+    int it, id = INT_MAX;
+    row_argmax<DT>(vt, vglob, bt, it);
+    if (pair) row_argmax<DT>(vd, vglob, bd, id);
+    return make_float4(bt, __int_as_float(it), bd, __int_as_float(id));
 }
 
-// Pass 1 of one unit by one data thread: the partial (b_t, s_t, b_d, s_d) of its vectors, or
-// under the greedy rule (max_t, argmax_t, max_d, argmax_d) (indices as int bits). The thread
-// whose vector holds the draft token also writes (y_t - y_d) s there (a float pair) and its flags.
-template <int DT, bool RAGGED, bool TRUNC>
-__device__ __forceinline__ float4 pass1(const UnitDesc &d, const uint4 *tslot, const uint4 *dslot, int vbase,
-                                        float4 *xval) {
+// The draft token's words of a pair, published by the thread whose vectors hold it: (y_t - y_d) s
+// at the token (a float pair) and the flags of a -inf logit. Out of line (one unit of a row holds
+// it).
+template <int DT>
+__device__ __noinline__ void extract_x(const UnitDesc &d, const uint4 *tslot, const uint4 *dslot, int vbase,
+                                       unsigned long long *xrec, uint32_t tag) {
     constexpr int E = Elt<DT>::kPerVec;
+    // x = E * (vglob + 32 k) + e for one thread and one k
+    const int xv = d.x / E - d.slice * kSliceVecs;  // its vector's index in the slice
+    if (xv < vbase || xv >= vbase + kVPT * kWarp || (xv - vbase) % kWarp != 0) return;
+    uint4 wt = tslot[xv];
+    const uint4 wd = dslot[xv];
+    if (d.trunc) mask_cut<DT>(wt, d.slice * kSliceVecs + xv, d.cut_tau, d.cut_id);
+    const float yt = vec_elem<DT>(wt, d.x % E), yd = vec_elem<DT>(wd, d.x % E);
+    const F2 Ex = f2_mul(f2_add({yt, 0.0f}, {-yd, 0.0f}), {d.s_hi, d.s_lo});
+    const int flags = (yd == -INFINITY ? XF_QZERO : 0) | (yt == -INFINITY ? XF_PZERO : 0);
+    st_word(xrec + X_HI, f2u(Ex.hi), tag);
+    st_word(xrec + X_LO, f2u(Ex.lo), tag);
+    st_word(xrec + X_F, static_cast<uint32_t>(flags), tag);
+}
+
+// Pass 1 of one unit under Rule 2 by one data thread: (b_t, s_t, b_d, s_d), per row the sum of
+// 2^(y s - b) over its vectors with b an integral reference from its first vector (so that no
+// exponential waits on a running max); a warp in which a sum overflowed takes the exact form.
+// CUT: the target row's top-k / top-p cut (a separate, out-of-line instance).
+template <int DT, bool CUT>
+__device__ __forceinline__ float4 pass1_body(const UnitDesc &d, const uint4 *tslot, const uint4 *dslot, int vbase) {
     const bool pair = d.kind == U_PAIR;
-    uint4 vt[kVPT], vd[kVPT];
-    load_slice<DT, RAGGED>(tslot, vbase, d.nvec, vt);
-    if (pair) load_slice<DT, RAGGED>(dslot, vbase, d.nvec, vd);
-    const int vglob = d.slice * kSliceVecs + vbase;  // vector index in the row
-    if (TRUNC) {
-#pragma unroll
-        for (int k = 0; k < kVPT; ++k) mask_cut<DT>(vt[k], vglob + k * kWarp, d.cut_tau, d.cut_id);
-    }
-    if (pair && d.xslice == d.slice) {
-        // the draft token's vector: x = E * (vglob + 32 k) + e for one thread and one k
-        const int xv = d.x / E - d.slice * kSliceVecs;  // its index in the slice
-        if (xv >= vbase && xv < vbase + kVPT * kWarp && (xv - vbase) % kWarp == 0) {
-            const int k = (xv - vbase) / kWarp;
-            uint4 wt = vt[0], wd = vd[0];
-#pragma unroll
-            for (int q = 1; q < kVPT; ++q)
-                if (q == k) {
-                    wt = vt[q];
-                    wd = vd[q];
-                }
-            const float yt = vec_elem<DT>(wt, d.x % E), yd = vec_elem<DT>(wd, d.x % E);
-            const F2 Ex = f2_mul(f2_add({yt, 0.0f}, {-yd, 0.0f}), {d.s_hi, d.s_lo});
-            const int flags = (yd == -INFINITY ? XF_QZERO : 0) | (yt == -INFINITY ? XF_PZERO : 0);
-            *xval = make_float4(Ex.hi, Ex.lo, __int_as_float(flags), 0.0f);
-        }
-    }
-    if (d.greedy) {
-        float bt, bd = -INFINITY;
-        int it, id = INT_MAX;
-        row_argmax<DT>(vt, vglob, bt, it);
-        if (pair) row_argmax<DT>(vd, vglob, bd, id);
-        return make_float4(bt, __int_as_float(it), bd, __int_as_float(id));
-    }
+    const int nvec = d.nvec;
     const float2 shi2 = f2splat(d.s_hi), slo2 = f2splat(d.s_lo);
-    float bt, bd = 0.0f, sd = 0.0f;
-    const float st = row_sum<DT>(vt, d.s_hi, shi2, slo2, bt);
-    if (pair) sd = row_sum<DT>(vd, d.s_hi, shi2, slo2, bd);
+    uint4 vt[kVPT], vd[kVPT];
+#pragma unroll
+    for (int k = 0; k < kVPT; ++k) {
+        vt[k] = slice_vec<DT>(tslot, vbase + k * kWarp, nvec);
+        if (CUT) mask_cut<DT>(vt[k], d.slice * kSliceVecs + vbase + k * kWarp, d.cut_tau, d.cut_id);
+    }
+    float bt = floorf(Elt<DT>::vmax(vt[0]) * d.s_hi);
+    float st = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kVPT; ++k) st += vec_sum<DT>(vt[k], shi2, slo2, bt);
+    float bd = 0.0f, sd = 0.0f;
+    if (pair) {
+#pragma unroll
+        for (int k = 0; k < kVPT; ++k) vd[k] = slice_vec<DT>(dslot, vbase + k * kWarp, nvec);
+        bd = floorf(Elt<DT>::vmax(vd[0]) * d.s_hi);
+#pragma unroll
+        for (int k = 0; k < kVPT; ++k) sd += vec_sum<DT>(vd[k], shi2, slo2, bd);
+    }
+    if (__any_sync(0xffffffffu, !(st <= 0x1p64f))) {
+        const float2 e = row_sum_exact<DT>(d, tslot, vbase, CUT);
+        bt = e.x;
+        st = e.y;
+    }
+    if (__any_sync(0xffffffffu, !(sd <= 0x1p64f))) {
+        const float2 e = row_sum_exact<DT>(d, dslot, vbase, false);
+        bd = e.x;
+        sd = e.y;
+    }
     return make_float4(bt, st, bd, sd);
+}
+template <int DT>
+__device__ __noinline__ float4 pass1_cut(const UnitDesc &d, const uint4 *tslot, const uint4 *dslot, int vbase) {
+    return pass1_body<DT, true>(d, tslot, dslot, vbase);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -477,18 +512,17 @@ __device__ __forceinline__ float4 pass1(const UnitDesc &d, const uint4 *tslot, c
 // The partial (alpha share, residual mass) of one thread's vectors, both normalised. Where the
 // position rejects, max(p - q, 0) and min(p, q) by resid_weights; where it accepts, only alpha:
 // min(p, q) = 2^min(y_t s - c_t, y_d s - c_d), c the log2 of the normaliser.
-template <int DT, bool RAGGED, bool TRUNC>
-__device__ __forceinline__ float2 pass2(const UnitDesc &d, const UnitDec &D, const uint4 *tslot, const uint4 *dslot,
-                                        int vbase) {
+template <int DT, bool CUT>
+__device__ __forceinline__ float2 pass2_body(const UnitDesc &d, const UnitDec &D, const uint4 *tslot,
+                                             const uint4 *dslot, int vbase) {
     constexpr int H = Elt<DT>::kPerVec / 2;
     if (D.status != 0) return make_float2(0.0f, 0.0f);
     uint4 vt[kVPT], vd[kVPT];
-    load_slice<DT, RAGGED>(tslot, vbase, d.nvec, vt);
-    load_slice<DT, RAGGED>(dslot, vbase, d.nvec, vd);
-    if (TRUNC) {
-        const int vglob = d.slice * kSliceVecs + vbase;
 #pragma unroll
-        for (int k = 0; k < kVPT; ++k) mask_cut<DT>(vt[k], vglob + k * kWarp, d.cut_tau, d.cut_id);
+    for (int k = 0; k < kVPT; ++k) {
+        vt[k] = slice_vec<DT>(tslot, vbase + k * kWarp, d.nvec);
+        vd[k] = slice_vec<DT>(dslot, vbase + k * kWarp, d.nvec);
+        if (CUT) mask_cut<DT>(vt[k], d.slice * kSliceVecs + vbase + k * kWarp, d.cut_tau, d.cut_id);
     }
     const float2 shi2 = f2splat(d.s_hi);
     const float2 nct = f2splat(-D.c_t), nctf = f2splat(-D.c_tf);
@@ -524,102 +558,85 @@ __device__ __forceinline__ float2 pass2(const UnitDesc &d, const UnitDec &D, con
     }
     return make_float2(acc.x + acc.y, 0.0f);
 }
-
-// The rarer forms of the passes: a short last slice, top-k / top-p, the greedy rule (the common one
-// is Rule 2 on a whole slice without truncation). Inline: a call from the data warps' loop would
-// make the compiler keep the loop's values in local memory around it.
 template <int DT>
-__device__ __forceinline__ float4 pass1_rare(const UnitDesc &d, const uint4 *tslot, const uint4 *dslot, int vbase,
-                                          float4 *xval) {
-    const bool ragged = d.nvec < kSliceVecs;
-    if (d.trunc)
-        return ragged ? pass1<DT, true, true>(d, tslot, dslot, vbase, xval) : pass1<DT, false, true>(d, tslot, dslot, vbase, xval);
-    return ragged ? pass1<DT, true, false>(d, tslot, dslot, vbase, xval) : pass1<DT, false, false>(d, tslot, dslot, vbase, xval);
-}
-template <int DT>
-__device__ __forceinline__ float2 pass2_rare(const UnitDesc &d, const UnitDec &D, const uint4 *tslot, const uint4 *dslot,
-                                          int vbase) {
-    const bool ragged = d.nvec < kSliceVecs;
-    if (d.trunc)
-        return ragged ? pass2<DT, true, true>(d, D, tslot, dslot, vbase) : pass2<DT, false, true>(d, D, tslot, dslot, vbase);
-    return pass2<DT, true, false>(d, D, tslot, dslot, vbase);
+__device__ __noinline__ float2 pass2_cut(const UnitDesc &d, const UnitDec &D, const uint4 *tslot, const uint4 *dslot,
+                                         int vbase) {
+    return pass2_body<DT, true>(d, D, tslot, dslot, vbase);
 }
 
 // ------------------------------------------------------------------------------------------------
-// stats warp: pass-1 partials -> the unit's record
+// reductions: a data warp's partial (its chunk), then the unit's (the eight warps, by the last data
+// warp to finish the job)
 
-// Rule 2, one row: lane j holds the partials of data threads 8j .. 8j + 7 (data warp j / 4). The
-// references combine by exact powers of two: per lane, per chunk (four lanes), per unit (eight
-// chunks). Returns the unit's (ref, sum) in every lane and the chunk's share (units 2^ref) in
-// lanes 4w.
-__device__ __forceinline__ void combine_row(const float (&b)[8], const float (&s)[8], int &ref, float &sum,
-                                            float &chunk) {
-    float Bj = -INFINITY;
-    int bad = 0;
+// Rule 2, one row, one (reference, sum) per lane over `width` lanes: the largest reference among
+// lanes with mass and the sum scaled to it by exact powers of two. A sum that is NaN, +inf or
+// negative in any lane (of the whole warp) makes the result's sum NaN; no mass gives (-inf, 0).
+template <int W>
+__device__ __forceinline__ float2 ref_sum(float b, float s) {
+    const bool ok = s > 0.0f && !isinf(s);
+    const int bad = __any_sync(0xffffffffu, !(s >= 0.0f) || isinf(s));
+    float B = ok ? b : -INFINITY;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const bool ok = s[k] > 0.0f && !isinf(s[k]);
-        bad |= !(s[k] >= 0.0f) || isinf(s[k]);
-        if (ok) Bj = fmaxf(Bj, b[k]);
-    }
-    float Sj = 0.0f;
+    for (int o = 1; o < W; o <<= 1) B = fmaxf(B, __shfl_xor_sync(0xffffffffu, B, o));
+    float S = ok ? s * pow2i(b - B) : 0.0f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const bool ok = s[k] > 0.0f && !isinf(s[k]);
-        if (ok) Sj += s[k] * pow2i(b[k] - Bj);
-    }
-    // chunk: four lanes
-    float Bw = Bj;
-#pragma unroll
-    for (int o = 1; o < 4; o <<= 1) Bw = fmaxf(Bw, __shfl_xor_sync(0xffffffffu, Bw, o));
-    float Sw = (Bj == -INFINITY) ? 0.0f : Sj * pow2i(Bj - Bw);
-#pragma unroll
-    for (int o = 1; o < 4; o <<= 1) Sw += __shfl_xor_sync(0xffffffffu, Sw, o);
-    // unit: eight chunks
-    float Bu = Bw;
-#pragma unroll
-    for (int o = 4; o < kWarp; o <<= 1) Bu = fmaxf(Bu, __shfl_xor_sync(0xffffffffu, Bu, o));
-    const float cw = (Bw == -INFINITY) ? 0.0f : Sw * pow2i(Bw - Bu);
-    float Su = cw;
-#pragma unroll
-    for (int o = 4; o < kWarp; o <<= 1) Su += __shfl_xor_sync(0xffffffffu, Su, o);
-    bad = __any_sync(0xffffffffu, bad);
-    // a reference beyond 2^28 (logits far outside any float32 softmax) reads as invalid
-    const bool inval = bad || (Su > 0.0f && !(fabsf(Bu) < 0x1p28f));
-    ref = (Su > 0.0f && !inval) ? static_cast<int>(Bu) : kNoRef;
-    sum = inval ? NAN : Su;
-    chunk = inval ? NAN : cw;
+    for (int o = 1; o < W; o <<= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    return make_float2(B, bad ? NAN : S);
 }
 
-// Greedy rule, one row: the max and the smallest index attaining it over the lane's eight threads,
-// then over the warp; an invalid thread (max +inf, index -1) wins every comparison.
-__device__ __forceinline__ void combine_argmax(const float (&m)[8], const int (&ix)[8], float &best, int &bidx) {
-    float bm = -INFINITY;
-    int bi = INT_MAX;
+// Greedy rule: the largest value and the smallest index attaining it over `width` lanes; an
+// invalid part (+inf, index -1) wins every comparison.
+template <int W>
+__device__ __forceinline__ void arg_max(float &m, int &ix) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-        if (m[k] > bm || (m[k] == bm && ix[k] < bi)) {
-            bm = m[k];
-            bi = ix[k];
-        }
-#pragma unroll
-    for (int o = 1; o < kWarp; o <<= 1) {
-        const float om = __shfl_xor_sync(0xffffffffu, bm, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (om > bm || (om == bm && oi < bi)) {
-            bm = om;
-            bi = oi;
+    for (int o = 1; o < W; o <<= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, m, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, ix, o);
+        if (om > m || (om == m && oi < ix)) {
+            m = om;
+            ix = oi;
         }
     }
-    best = bm;
-    bidx = bi;
+}
+
+// A data warp's pass-1 partial from its threads' (the warp's chunk of both slices).
+__device__ __forceinline__ float4 warp_p1(float4 r, bool greedy, bool pair) {
+    if (greedy) {
+        float m0 = r.x, m1 = r.z;
+        int i0 = __float_as_int(r.y), i1 = __float_as_int(r.w);
+        arg_max<kWarp>(m0, i0);
+        arg_max<kWarp>(m1, i1);
+        return make_float4(m0, __int_as_float(i0), m1, __int_as_float(i1));
+    }
+    const float2 t = ref_sum<kWarp>(r.x, r.y);
+    const float2 d = pair ? ref_sum<kWarp>(r.z, r.w) : make_float2(-INFINITY, 0.0f);
+    return make_float4(t.x, t.y, d.x, d.y);
+}
+
+// A data warp's pass-1 record (lanes 0..3, one word each; w is the same in every lane): per row
+// its reference (kNoRef: no mass) and sum (NaN: invalid logits; a reference beyond 2^28 reads as
+// invalid), or under the greedy rule its argmax and max.
+__device__ __forceinline__ void store_w1(unsigned long long *rec, float4 w, bool greedy, bool pair, uint32_t tag) {
+    const int lane = threadIdx.x % kWarp;
+    uint32_t v0, v1, v2, v3;
+    if (greedy) {
+        v0 = static_cast<uint32_t>(__float_as_int(w.y));
+        v1 = f2u(w.x);
+        v2 = static_cast<uint32_t>(__float_as_int(w.w));
+        v3 = f2u(w.z);
+    } else {
+        const bool inval_t = isnan(w.y) || (w.y > 0.0f && !(fabsf(w.x) < 0x1p28f));
+        const bool inval_d = isnan(w.w) || (w.w > 0.0f && !(fabsf(w.z) < 0x1p28f));
+        v0 = static_cast<uint32_t>((w.y > 0.0f && !inval_t) ? static_cast<int>(w.x) : kNoRef);
+        v1 = f2u(inval_t ? NAN : w.y);
+        v2 = static_cast<uint32_t>((pair && w.w > 0.0f && !inval_d) ? static_cast<int>(w.z) : kNoRef);
+        v3 = f2u(pair ? (inval_d ? NAN : w.w) : 0.0f);
+    }
+    if (lane < kW1Words) st_word(rec + lane, lane == 0 ? v0 : lane == 1 ? v1 : lane == 2 ? v2 : v3, tag);
 }
 
 // ------------------------------------------------------------------------------------------------
-// decide warp
-
-// The lanes of lane group g: 8g .. 8g + 7.
-__device__ __forceinline__ unsigned group_mask(int g) { return 0xffu << (kGroupLanes * g); }
+// the decision of an item
 
 // The decision of unit d's item from its units' combined statistics (every lane of the group
 // computes it; the same inputs give the same result in every CTA). Rule 2: (a0, s0) / (a1, s1)
@@ -698,6 +715,214 @@ __device__ __forceinline__ UnitDec decide_item(const SliceParams &P, const UnitD
     return D;
 }
 
+// The decision of item d (whole warp) from the pass-1 records of every data warp of every unit of
+// the item, and the draft token's words, polled until they carry the call's tag (every CTA that
+// reads the item's records obtains the same values). Lane l combines records l, l + 32, ...; the
+// parts combine like a unit's: references by exact powers of two (argmax pairs under the greedy
+// rule).
+__device__ __noinline__ UnitDec decide_records(const SliceParams &P, const UnitDesc &d, uint32_t tag, Shared &sh) {
+    const int lane = threadIdx.x % kWarp;
+    const bool greedy = d.greedy != 0;
+    const int nrec = P.ns * kDW;
+    const unsigned long long *g = P.p1w + static_cast<size_t>(d.item) * nrec * kW1Words;
+    const uint64_t limit = *reinterpret_cast<volatile int32_t *>(&sh.timed_out) ? 1000000ull : kPollNs;
+    uint64_t t0 = 0;
+    bool gave_up = false;
+    int la0 = greedy ? INT_MAX : kNoRef, la1 = la0;
+    float ls0 = greedy ? -INFINITY : 0.0f, ls1 = ls0;
+    // rounds of up to kRound records per lane, every load of a round in flight at once
+    constexpr int kRound = 4;
+    for (int base = 0; base < nrec; base += kRound * kWarp) {
+        ulonglong2 w01[kRound], w23[kRound];
+        for (bool first = true;; first = false) {
+            bool ok = true;
+#pragma unroll
+            for (int k = 0; k < kRound; ++k) {
+                const int u = base + k * kWarp + lane;
+                if (u < nrec) {
+                    w01[k] = ld_word2(g + static_cast<size_t>(u) * kW1Words + W1_AT);
+                    w23[k] = ld_word2(g + static_cast<size_t>(u) * kW1Words + W1_AD);
+                    ok &= (word_tag(w01[k].x) == tag) & (word_tag(w01[k].y) == tag) & (word_tag(w23[k].x) == tag) &
+                          (word_tag(w23[k].y) == tag);
+                }
+            }
+            if (__all_sync(0xffffffffu, ok) || gave_up) break;
+            const uint64_t now = globaltimer_ns();
+            if (first) t0 = now;
+            gave_up = __shfl_sync(0xffffffffu, static_cast<int>(now - t0 > limit), 0) != 0;
+            if (!gave_up) __nanosleep(64);
+        }
+#pragma unroll
+        for (int k = 0; k < kRound; ++k) {
+            if (base + k * kWarp + lane >= nrec) continue;
+            const int ua0 = static_cast<int>(word_val(w01[k].x)), ua1 = static_cast<int>(word_val(w23[k].x));
+            const float us0 = u2f(word_val(w01[k].y)), us1 = u2f(word_val(w23[k].y));
+            if (greedy) {
+                if (us0 > ls0 || (us0 == ls0 && ua0 < la0)) {
+                    ls0 = us0;
+                    la0 = ua0;
+                }
+                if (us1 > ls1 || (us1 == ls1 && ua1 < la1)) {
+                    ls1 = us1;
+                    la1 = ua1;
+                }
+            } else {
+                // a NaN sum (an invalid part) stays NaN
+                const int n0 = max(la0, ua0), n1 = max(la1, ua1);
+                ls0 = ls0 * pow2_int(la0 - n0) + ((ua0 == kNoRef) ? us0 * 0.0f : us0 * pow2_int(ua0 - n0));
+                ls1 = ls1 * pow2_int(la1 - n1) + ((ua1 == kNoRef) ? us1 * 0.0f : us1 * pow2_int(ua1 - n1));
+                la0 = n0;
+                la1 = n1;
+            }
+        }
+    }
+    int a0, a1;
+    float s0, s1;
+    if (greedy) {
+        arg_max<kWarp>(ls0, la0);
+        arg_max<kWarp>(ls1, la1);
+        a0 = la0;
+        a1 = la1;
+        s0 = ls0;
+        s1 = ls1;
+    } else {
+        int B0 = la0, B1 = la1;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            B0 = max(B0, __shfl_xor_sync(0xffffffffu, B0, o));
+            B1 = max(B1, __shfl_xor_sync(0xffffffffu, B1, o));
+        }
+        float t0s = ls0 * pow2_int(la0 - B0), t1s = ls1 * pow2_int(la1 - B1);
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            t0s += __shfl_xor_sync(0xffffffffu, t0s, o);
+            t1s += __shfl_xor_sync(0xffffffffu, t1s, o);
+        }
+        a0 = B0;
+        a1 = B1;
+        s0 = t0s;
+        s1 = t1s;
+    }
+    // the draft token's words (Rule 2 pairs), by lane 0, then to every lane
+    F2 Ex = {0.0f, 0.0f};
+    int xf = 0;
+    if (d.kind == U_PAIR && !greedy && d.xslice >= 0) {
+        if (lane == 0) {
+            const unsigned long long *r = P.xrec + static_cast<size_t>(d.item) * kXWords;
+            unsigned long long x0 = 0, x1 = 0, x2 = 0;
+            uint64_t tx = 0;
+            for (bool first = true; !gave_up; first = false) {
+                x0 = ld_word(r + X_HI);
+                x1 = ld_word(r + X_LO);
+                x2 = ld_word(r + X_F);
+                if ((word_tag(x0) == tag) & (word_tag(x1) == tag) & (word_tag(x2) == tag)) break;
+                const uint64_t now = globaltimer_ns();
+                if (first) tx = now;
+                if (now - tx > limit)
+                    gave_up = true;
+                else
+                    __nanosleep(64);
+            }
+            Ex = {u2f(word_val(x0)), u2f(word_val(x1))};
+            xf = __float_as_int(u2f(word_val(x2)));
+        }
+        gave_up = __shfl_sync(0xffffffffu, gave_up ? 1 : 0, 0) != 0;
+        Ex.hi = __shfl_sync(0xffffffffu, Ex.hi, 0);
+        Ex.lo = __shfl_sync(0xffffffffu, Ex.lo, 0);
+        xf = __shfl_sync(0xffffffffu, xf, 0);
+    }
+    int status = d.status;
+    if (gave_up) {
+        status |= REQ_TIMEOUT;
+        if (lane == 0) sh.timed_out = 1;
+    }
+    if (*reinterpret_cast<volatile int32_t *>(&sh.timed_out)) status |= REQ_TIMEOUT;
+    return decide_item(P, d, status, a0, s0, a1, s1, Ex, xf);
+}
+
+// The decision as its record's words and back (the value of word k is UnitDec's field k).
+__device__ __forceinline__ uint32_t dec_word(const UnitDec &D, int k) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(&D);
+    uint32_t v = 0;
+#pragma unroll
+    for (int i = 0; i < kDecWords; ++i)
+        if (i == k) v = w[i];
+    return v;
+}
+
+// A pass-2 job's decision (whole warp): the job's copy of the item's decision record, or, where a
+// word of the copy is stale (the record was published after the copy), the record itself, polled.
+// A wait that gives up yields a decision with SPEC_REQ_TIMEOUT.
+__device__ __noinline__ UnitDec poll_decision(const SliceParams &P, const UnitDesc &d, uint32_t tag, Shared &sh) {
+    const int lane = threadIdx.x % kWarp;
+    const unsigned long long *r = P.drec + static_cast<size_t>(d.item) * kDecWords;
+    const uint64_t limit = *reinterpret_cast<volatile int32_t *>(&sh.timed_out) ? 1000000ull : kPollNs;
+    uint64_t t0 = 0;
+    unsigned long long w = 0;
+    for (bool first = true;; first = false) {
+        if (lane < kDecWords) w = ld_word(r + lane);
+        if (__all_sync(0xffffffffu, lane >= kDecWords || word_tag(w) == tag)) break;
+        const uint64_t now = globaltimer_ns();
+        if (first) t0 = now;
+        if (__shfl_sync(0xffffffffu, static_cast<int>(now - t0 > limit), 0)) {
+            if (lane == 0) sh.timed_out = 1;
+            UnitDec D = {};
+            D.status = d.status | REQ_TIMEOUT;
+            D.kind = SAMPLE_NONE;
+            D.argmax_t = -1;
+            return D;
+        }
+        __nanosleep(64);
+    }
+    UnitDec D;
+    uint32_t *dw = reinterpret_cast<uint32_t *>(&D);
+#pragma unroll
+    for (int k = 0; k < kDecWords; ++k) dw[k] = __shfl_sync(0xffffffffu, static_cast<uint32_t>(w >> 32), k);
+    return D;
+}
+__device__ __forceinline__ UnitDec read_decision(const SliceParams &P, const UnitDesc &d,
+                                                 const unsigned long long *copy, uint32_t tag, Shared &sh) {
+    UnitDec D;
+    uint32_t *dw = reinterpret_cast<uint32_t *>(&D);
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < kDecWords; k += 2) {
+        const ulonglong2 w = *reinterpret_cast<const ulonglong2 *>(copy + k);
+        ok &= (word_tag(w.x) == tag) & (word_tag(w.y) == tag);
+        dw[k] = word_val(w.x);
+        dw[k + 1] = word_val(w.y);
+    }
+    if (__all_sync(0xffffffffu, ok)) return D;
+    return poll_decision(P, d, tag, sh);
+}
+
+// The decision of a unit without rows (its request was rejected before any work).
+__device__ __forceinline__ UnitDec skip_decision(const UnitDesc &d) {
+    UnitDec D = {};
+    D.status = d.status;
+    D.kind = SAMPLE_NONE;
+    D.argmax_t = -1;
+    return D;
+}
+
+// Hands an item to the final warp (whole warp; several data warps push: the tickets keep the
+// queue in the order they were taken).
+__device__ __forceinline__ void fq_push(Shared &sh, int op, const UnitDesc &d, const UnitDec &D) {
+    const int lane = threadIdx.x % kWarp;
+    int t = 0;
+    if (lane == 0) t = atomicAdd(&sh.fq_tail, 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    const int q = t % kFQ;
+    if (t >= kFQ && !wait_bar(sh, &sh.fq_empty[q], static_cast<uint32_t>(((t / kFQ) - 1) & 1))) return;
+    if (lane == 0) {
+        sh.fq[q].op = op;
+        sh.fq[q].d = d;
+        sh.fq[q].D = D;
+        mbar_arrive(&sh.fq_full[q]);
+    }
+    __syncwarp();
+}
+
 // ------------------------------------------------------------------------------------------------
 // final warp: an item's results and draw, a request's selection
 
@@ -747,15 +972,13 @@ __device__ __forceinline__ void draw_weights(int kind, const uint4 &wt, const ui
     }
 }
 
-// The mass of chunk c (128 vectors of the row) in the law of the draw: the residual's
-// (normalised), or p's in units of 2^B_t.
+// The mass of chunk c (128 vectors of the row: data warp c mod kDW of unit c / kDW) in the law of
+// the draw: the residual's (normalised), or p's in units of 2^B_t.
 __device__ __forceinline__ float chunk_mass(const SliceParams &P, const UnitDesc &d, const UnitDec &D, int kind, int c) {
-    const int u = c / kChunksPerSlice, w = c % kChunksPerSlice;
-    const size_t unit = static_cast<size_t>(d.item) * P.ns + u;
-    if (kind == SAMPLE_RESIDUAL) return u2f(word_val(ld_word(P.p2_rec + unit * kP2Words + PR_CHUNK + w)));
-    const unsigned long long *r = P.stat_rec + unit * kStatWords;
-    const int ref = static_cast<int>(word_val(ld_word(r + SR_AT)));
-    const float cm = u2f(word_val(ld_word(r + SR_CHUNK + w)));
+    const size_t rec = static_cast<size_t>(d.item) * P.ns * kDW + c;
+    if (kind == SAMPLE_RESIDUAL) return u2f(word_val(ld_word(P.p2w + rec * kW2Words + W2_Z)));
+    const int ref = static_cast<int>(word_val(ld_word(P.p1w + rec * kW1Words + W1_AT)));
+    const float cm = u2f(word_val(ld_word(P.p1w + rec * kW1Words + W1_ST)));
     return (ref == kNoRef || !(cm > 0.0f)) ? 0.0f : cm * pow2_int(ref - static_cast<int>(D.B_t));
 }
 
@@ -1004,16 +1227,17 @@ __device__ __noinline__ void finalize_item(const SliceParams &P, const FinJob &j
     float alpha = 0.0f, Zres = 0.0f;
     const bool rule2_pair = pair && !d.greedy && st == 0;
     if (rule2_pair) {
-        const unsigned long long *rec = P.p2_rec + static_cast<size_t>(d.item) * P.ns * kP2Words;
-        if (!poll_units(sh, rec, P.ns, kP2Words, kP2Words, tag)) {
+        const int nrec = P.ns * kDW;
+        const unsigned long long *rec = P.p2w + static_cast<size_t>(d.item) * nrec * kW2Words;
+        if (!poll_units(sh, rec, nrec, kW2Words, kW2Words, tag)) {
             st |= REQ_TIMEOUT;
             sh.timed_out = 1;
         }
-        // sums in unit order over the lanes (the same in every lane)
+        // sums in record order over the lanes (the same in every lane)
         float a = 0.0f, z = 0.0f;
-        for (int u = lane; u < P.ns; u += kWarp) {
-            a += u2f(word_val(ld_word(rec + static_cast<size_t>(u) * kP2Words + PR_ALPHA)));
-            z += u2f(word_val(ld_word(rec + static_cast<size_t>(u) * kP2Words + PR_Z)));
+        for (int u = lane; u < nrec; u += kWarp) {
+            a += u2f(word_val(ld_word(rec + static_cast<size_t>(u) * kW2Words + W2_ALPHA)));
+            z += u2f(word_val(ld_word(rec + static_cast<size_t>(u) * kW2Words + W2_Z)));
         }
         alpha = warp_sum(a);
         Zres = warp_sum(z);
@@ -1025,9 +1249,9 @@ __device__ __noinline__ void finalize_item(const SliceParams &P, const FinJob &j
         fb = 1;
     }
     if (kind == SAMPLE_P) {
-        // the draw from p reads every unit's chunk shares of the target row
-        const unsigned long long *rec = P.stat_rec + static_cast<size_t>(d.item) * P.ns * kStatWords;
-        if (!poll_units(sh, rec, P.ns, kStatWords, SR_CHUNK + kChunksPerSlice, tag)) {
+        // the draw from p reads the chunk shares of the target row (every data warp's pass-1 record)
+        const int nrec = P.ns * kDW;
+        if (!poll_units(sh, P.p1w + static_cast<size_t>(d.item) * nrec * kW1Words, nrec, kW1Words, kW1Words, tag)) {
             st |= REQ_TIMEOUT;
             sh.timed_out = 1;
             kind = SAMPLE_NONE;
@@ -1153,6 +1377,7 @@ __device__ __noinline__ void batch_tail(const SliceParams &P, Shared &sh, unsign
     }
     // the workspace's counters back to zero and the next epoch, for the next call
     for (int i = tid; i < P.B; i += kBlock) P.req_cnt[i] = 0u;
+
     if (tid == 0) {
         P.ctl[CTL_DONE] = 0u;
         P.ctl[CTL_EPOCH] = sh.epoch + 1u;
@@ -1188,74 +1413,74 @@ __device__ __forceinline__ int find_request(const SliceParams &P, const Shared &
 extern __shared__ __align__(128) unsigned char s_dyn[];
 __shared__ Shared s_sh;
 
-// Data warps: the jobs in order (pass 1 of unit n, then pass 2 of unit n - kLag).
+// Whether unit d has pass 2: a pair under Rule 2 (alpha and the residual need the item's
+// normalisers, so its slices are read again once every unit of the item is through pass 1).
+__device__ __forceinline__ bool has_p2(const UnitDesc &d) { return d.kind == U_PAIR && !d.greedy; }
+
+// Data warps: the jobs in order (pass 1 of unit n; pass 2 of unit n - kLag), each warp its chunk
+// of the slices, its record published in global memory. The CTA holding an item's designated unit
+// (slice item mod ns) hands the item to its final warp: after pass 1 to be decided, after pass 2
+// to be finalised.
 template <int DT>
 __device__ __noinline__ void role_data(const SliceParams &P, uint32_t tag) {
     Shared &sh = s_sh;
-    uint4 *const slots = reinterpret_cast<uint4 *>(s_dyn);
-    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-    const int G = gridDim.x;
-    constexpr int E = Elt<DT>::kPerVec;
-    (void)slots;
-    (void)tid;
-    (void)warp;
-    (void)G;
-    (void)E;
-        // ================= data warps: the jobs in order ===========================================
-        const int vbase = warp * kChunkVecs + lane;  // this thread's first vector in a slice
-        const int pt = warp * kWarp + lane;
-        const int skew = pt + (pt >> 3);
-        int p1n = 0, p2q = 0;
-        for (int j = 0;; ++j) {
-            const int q = j % kJobs;
-            if (!wait_bar(sh, &sh.job_full[q], static_cast<uint32_t>((j / kJobs) & 1))) break;
-            const int type = sh.jobs[q].type, n = sh.jobs[q].unit;
-            if (type == J_END) break;
-            const int e = n % kR;
-            const UnitDesc &d = sh.desc[e];
-            const uint4 *ts = slots + static_cast<size_t>(2 * q) * kSliceVecs;
-            const uint4 *ds = ts + kSliceVecs;
-            const bool p2unit = d.kind == U_PAIR && !d.greedy;
-            if (type == J_P1) {
-                const int pb = p1n % kSR;
-                if (p1n >= kSR) wait_bar(sh, &sh.p1_free[pb], static_cast<uint32_t>(((p1n / kSR) - 1) & 1));
-                float4 r;
-                if (warp * kChunkVecs >= d.nvec) {
-                    // this warp's chunk is past the end of a short last slice
-                    r = d.greedy ? make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, __int_as_float(INT_MAX))
-                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                } else if (d.trunc || d.greedy || d.nvec < kSliceVecs) {
-                    r = pass1_rare<DT>(d, ts, ds, vbase, &sh.xval[pb]);
-                } else {
-                    r = pass1<DT, false, false>(d, ts, ds, vbase, &sh.xval[pb]);
-                }
-                sh.p1part[pb][skew] = r;
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&sh.p1_done[pb]);
-                    mbar_arrive(&sh.job_empty[q]);
-                }
-                ++p1n;
-            } else if (type == J_P2) {
-                wait_bar(sh, &sh.dec_ready[e], static_cast<uint32_t>((n / kR) & 1));
-                const UnitDec &D = sh.dec[e];
-                const int qb = p2q % kPR;
-                if (p2q >= kPR) wait_bar(sh, &sh.p2_free[qb], static_cast<uint32_t>(((p2q / kPR) - 1) & 1));
-                const float2 r2 = (d.trunc || d.nvec < kSliceVecs) ? pass2_rare<DT>(d, D, ts, ds, vbase)
-                                                                    : pass2<DT, false, false>(d, D, ts, ds, vbase);
-                sh.p2part[qb][skew] = r2;
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&sh.p2_done[qb]);
-                    mbar_arrive(&sh.job_empty[q]);
-                }
-                ++p2q;
+    const uint4 *const slots = reinterpret_cast<const uint4 *>(s_dyn);
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int vbase = warp * kChunkVecs + lane;  // this thread's first vector in a slice
+    for (int j = 0;; ++j) {
+        const int q = j % kJobs;
+        if (!wait_bar(sh, &sh.job_full[q], static_cast<uint32_t>((j / kJobs) & 1))) break;
+        const int type = sh.jobs[q].type, n = sh.jobs[q].unit;
+        if (type == J_END) break;
+        const int e = n % kR;
+        const UnitDesc &d = sh.desc[e];
+        const uint4 *ts = slots + static_cast<size_t>(2 * q) * kSliceVecs;
+        const uint4 *ds = ts + kSliceVecs;
+        const size_t wrec = (static_cast<size_t>(d.item) * P.ns + d.slice) * kDW + warp;  // this warp's record
+        const bool hand = d.designated && warp == n % kDW;  // this warp hands the item over
+        if (type == J_P1) {
+            float4 r;
+            if (warp * kChunkVecs >= d.nvec) {
+                // this warp's chunk is past the end of a short last slice
+                r = d.greedy ? make_float4(-INFINITY, __int_as_float(INT_MAX), -INFINITY, __int_as_float(INT_MAX))
+                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            } else if (d.greedy) {
+                r = pass1_greedy<DT>(d, ts, ds, vbase);
+            } else if (d.trunc) {
+                r = pass1_cut<DT>(d, ts, ds, vbase);
             } else {
-                warp_arrive(&sh.job_empty[q], lane);  // a unit without rows
+                r = pass1_body<DT, false>(d, ts, ds, vbase);
             }
-            // the unit's descriptor, after its last job
-            if (type != J_P1 || !p2unit) warp_arrive(&sh.desc_empty[e], lane);
+            if (d.kind == U_PAIR && !d.greedy && d.xslice == d.slice)
+                extract_x<DT>(d, ts, ds, vbase, P.xrec + static_cast<size_t>(d.item) * kXWords, tag);
+            const float4 w = warp_p1(r, d.greedy != 0, d.kind == U_PAIR);
+            store_w1(P.p1w + wrec * kW1Words, w, d.greedy != 0, d.kind == U_PAIR, tag);
+            warp_arrive(&sh.job_empty[q], lane);
+            if (hand) fq_push(sh, F_DECIDE, d, skip_decision(d));
+            if (!has_p2(d)) warp_arrive(&sh.desc_empty[e], lane);
+        } else if (type == J_P2) {
+            const UnitDec D = read_decision(P, d, sh.drec[q], tag, sh);
+            const float2 r2 = d.trunc ? pass2_cut<DT>(d, D, ts, ds, vbase) : pass2_body<DT, false>(d, D, ts, ds, vbase);
+            const float a = warp_sum(r2.x), z = warp_sum(r2.y);
+            if (lane < kW2Words) st_word(P.p2w + wrec * kW2Words + lane, f2u(lane == W2_ALPHA ? a : z), tag);
+            warp_arrive(&sh.job_empty[q], lane);
+            if (hand) fq_push(sh, F_FINAL, d, D);
+            warp_arrive(&sh.desc_empty[e], lane);
+        } else {
+            // a unit without rows
+            warp_arrive(&sh.job_empty[q], lane);
+            if (hand) fq_push(sh, F_FINAL, d, skip_decision(d));
+            warp_arrive(&sh.desc_empty[e], lane);
         }
+    }
+    // the last data warp to finish closes the final warp's queue (after every push of the others)
+    int last = 0;
+    if (lane == 0) last = atomicAdd(&sh.end_cnt, 1) == kDW - 1;
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+        UnitDesc d = {};
+        d.kind = U_END;
+        fq_push(sh, F_END, d, skip_decision(d));
+    }
 }
 
 // Producer warp: descriptors, and the jobs' bulk copies.
@@ -1263,492 +1488,165 @@ template <int DT>
 __device__ __noinline__ void role_producer(const SliceParams &P, uint32_t tag) {
     Shared &sh = s_sh;
     uint4 *const slots = reinterpret_cast<uint4 *>(s_dyn);
-    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+    const int lane = threadIdx.x % kWarp;
     const int G = gridDim.x;
     constexpr int E = Elt<DT>::kPerVec;
-    (void)slots;
-    (void)tid;
-    (void)warp;
-    (void)G;
-    (void)E;
-        // ================= producer =================================================================
-        const size_t row_bytes = static_cast<size_t>(P.nvec_row) * 16;
-        const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
-        int n = 0, j = 0;  // units described, jobs issued (lane 0)
-        // the next job's pair of slots (once the data warps have left it), its bulk copies
-        // (nrows slices) completing on the job's barrier
-        auto issue = [&](int type, int unit, const UnitDesc &d, int nrows, uint64_t pol) {
-            const int q = j % kJobs;
-            if (j >= kJobs && !wait_bar(sh, &sh.job_empty[q], static_cast<uint32_t>(((j / kJobs) - 1) & 1)))
-                nrows = 0, type = (type == J_END) ? J_END : J_SKIP;
-            sh.jobs[q].type = type;
-            sh.jobs[q].unit = unit;
-            if (nrows > 0) {
-                const uint32_t bytes = static_cast<uint32_t>(d.nvec) * 16u;
-                mbar_expect_tx(&sh.job_full[q], bytes * nrows);
-                const size_t off = static_cast<size_t>(d.slice) * kSliceVecs * 16;
-                uint4 *dst = slots + static_cast<size_t>(2 * q) * kSliceVecs;
-                bulk_g2s(dst, static_cast<const unsigned char *>(P.target) + static_cast<size_t>(d.item) * row_bytes + off,
-                         bytes, &sh.job_full[q], pol);
-                if (nrows == 2)
-                    bulk_g2s(dst + kSliceVecs,
-                             static_cast<const unsigned char *>(P.draft) + static_cast<size_t>(d.drow) * row_bytes + off,
-                             bytes, &sh.job_full[q], pol);
-            }
-            mbar_arrive(&sh.job_full[q]);
-            ++j;
-        };
-        // pass 2 of unit m: its slices again (from L2), for a pair under Rule 2
-        auto issue_p2 = [&](int m) {
-            const UnitDesc &dm = sh.desc[m % kR];
-            if (dm.kind == U_PAIR && !dm.greedy) issue(J_P2, m, dm, 2, drop);
-        };
-        for (bool end = false; !end;) {
-            // lanes 0 .. kPrep-1 prepare the descriptors of units n .. n + kPrep - 1 at once, so that
-            // their loads overlap
-            if (lane < kPrep) {
-                const long long u = sh.bad_offsets ? P.nunits : static_cast<long long>(blockIdx.x) + static_cast<long long>(n + lane) * G;
-                UnitDesc d = {};
-                if (u >= P.nunits) {
-                    d.kind = U_END;
-                } else {
-                    const int g = static_cast<int>(u / P.ns), s = static_cast<int>(u % P.ns);
-                    int r0, r1;
-                    const int i = find_request(P, sh, g, r0, r1);
-                    const int K = r1 - r0 - 1, pos = g - r0;
-                    const int drow = r0 - i + pos;
-                    // the item's values, every load issued before any is used
-                    const float T = P.temperature ? __ldg(P.temperature + i) : P.temperature_scalar;
-                    const float tp = P.top_p ? __ldg(P.top_p + i) : 1.0f;
-                    const bool shaped = K <= P.K_max;
-                    const double ua = (shaped && pos < K) ? __ldg(P.uniforms + g) : 0.0;
-                    const double us = shaped ? __ldg(P.uniforms + r0 + K) : 0.0;
-                    const int x = (shaped && pos < K) ? __ldg(P.draft_tokens + drow) : -1;
-                    const int2 cut = (P.trunc && shaped) ? __ldg(P.trunc + g) : make_int2(0, INT_MAX);
-                    int status = shaped ? 0 : SPEC_REQ_BAD_SHAPE;
-                    if (!(T >= 0.0f) || isinf(T) || isnan(tp)) status |= SPEC_REQ_BAD_PARAM;
-                    d.kind = status ? U_SKIP : (pos < K ? U_PAIR : U_ROW);
-                    d.item = g;
-                    d.slice = s;
-                    d.req = i;
-                    d.pos = pos;
-                    d.K = K;
-                    d.drow = drow;
-                    d.nvec = min(kSliceVecs, P.nvec_row - s * kSliceVecs);
-                    d.status = status;
-                    d.greedy = (T == 0.0f) ? 1 : 0;
-                    d.designated = (s == g % P.ns) ? 1 : 0;
-                    d.ua = ua;
-                    d.us = us;
-                    d.x = x;
-                    d.xslice = (x >= 0 && x < P.V) ? (x / E) / kSliceVecs : -1;
-                    F2 sv = {0.0f, 0.0f};
-                    if (T > 0.0f && !isinf(T)) sv = f2_div({kLog2eHi, kLog2eLo}, {T, 0.0f});
-                    if (sv.hi > 0.0f && sv.lo < 0.0f) {
-                        // s_hi moved toward zero so that s_lo > 0: a -inf logit then gives -inf in
-                        // both terms of the exponent's argument (a negative s_lo would make it NaN)
-                        const float down = __uint_as_float(__float_as_uint(sv.hi) - 1u);
-                        sv.lo += sv.hi - down;
-                        sv.hi = down;
-                    }
-                    d.s_hi = sv.hi;
-                    d.s_lo = fmaxf(sv.lo, 1.401298464e-45f);
-                    d.cut_tau = static_cast<uint32_t>(cut.x);
-                    d.cut_id = cut.y;
-                    d.trunc = (!d.greedy && (cut.x != 0 || cut.y != INT_MAX)) ? 1 : 0;
-                }
-                sh.prep[lane] = d;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                for (int l = 0; l < kPrep; ++l, ++n) {
-                    const int e = n % kR;
-                    const bool ok = n < kR || wait_bar(sh, &sh.desc_empty[e], static_cast<uint32_t>(((n / kR) - 1) & 1));
-                    UnitDesc &d = sh.desc[e];
-                    d = sh.prep[l];
-                    if (!ok || sh.timed_out) d.kind = U_END;
-                    mbar_arrive(&sh.desc_full[e]);
-                    if (d.kind == U_END) {
-                        end = true;
-                        break;
-                    }
-                    // pass 1 of unit n: a pair's slices stay in L2 for its pass 2 (evict last)
-                    if (d.kind == U_SKIP)
-                        issue(J_SKIP, n, d, 0, drop);
-                    else
-                        issue(J_P1, n, d, d.kind == U_PAIR ? 2 : 1, (d.kind == U_PAIR && !d.greedy) ? keep : drop);
-                    if (n >= kLag) issue_p2(n - kLag);
-                }
-                if (end) {
-                    // the last units' pass 2, then the end
-                    for (int m = max(0, n - kLag); m < n; ++m) issue_p2(m);
-                    issue(J_END, n, sh.desc[n % kR], 0, drop);
-                    // copies still in flight (a wait gave up): wait for them, bounded, before leaving
-                    if (sh.timed_out)
-                        for (int m = max(0, j - kJobs); m < j; ++m)
-                            mbar_wait_sleep_bounded(&sh.job_full[m % kJobs], static_cast<uint32_t>((m / kJobs) & 1), kSuspendNs,
-                                                    4);
-                }
-            }
-            n = __shfl_sync(0xffffffffu, n, 0);
-            end = __shfl_sync(0xffffffffu, end ? 1 : 0, 0) != 0;
-            __syncwarp();
+    const size_t row_bytes = static_cast<size_t>(P.nvec_row) * 16;
+    const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
+    int n = 0, j = 0;  // units described, jobs issued (lane 0)
+    // the next job in the ring (once the data warps have left the slot): its slices (nrows rows)
+    // and, for pass 2, the item's decision record, all completing on the job's barrier
+    auto issue = [&](int type, int unit, const UnitDesc &d, int nrows, uint64_t pol) {
+        const int q = j % kJobs;
+        if (j >= kJobs && !wait_bar(sh, &sh.job_empty[q], static_cast<uint32_t>(((j / kJobs) - 1) & 1)))
+            nrows = 0, type = (type == J_END) ? J_END : J_SKIP;
+        const bool drec = type == J_P2;
+        sh.jobs[q].type = type;
+        sh.jobs[q].unit = unit;
+        const uint32_t sbytes = static_cast<uint32_t>(d.nvec) * 16u;
+        const uint32_t total = (nrows > 0 ? sbytes * nrows : 0u) + (drec ? kDecWords * 8u : 0u);
+        if (total) mbar_expect_tx(&sh.job_full[q], total);
+        if (nrows > 0) {
+            const size_t off = static_cast<size_t>(d.slice) * kSliceVecs * 16;
+            uint4 *dst = slots + static_cast<size_t>(2 * q) * kSliceVecs;
+            bulk_g2s(dst, static_cast<const unsigned char *>(P.target) + static_cast<size_t>(d.item) * row_bytes + off,
+                     sbytes, &sh.job_full[q], pol);
+            if (nrows == 2)
+                bulk_g2s(dst + kSliceVecs,
+                         static_cast<const unsigned char *>(P.draft) + static_cast<size_t>(d.drow) * row_bytes + off,
+                         sbytes, &sh.job_full[q], pol);
         }
-}
-
-// Stats warp: unit n's pass-1 partials -> its published statistics.
-template <int DT>
-__device__ __noinline__ void role_stats(const SliceParams &P, uint32_t tag) {
-    Shared &sh = s_sh;
-    uint4 *const slots = reinterpret_cast<uint4 *>(s_dyn);
-    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-    const int G = gridDim.x;
-    constexpr int E = Elt<DT>::kPerVec;
-    (void)slots;
-    (void)tid;
-    (void)warp;
-    (void)G;
-    (void)E;
-        // ================= stats: unit n's pass-1 partials -> its published statistics ============
-        int p1n = 0;
-        for (int n = 0;; ++n) {
-            const int e = n % kR;
-            if (!wait_bar(sh, &sh.desc_full[e], static_cast<uint32_t>((n / kR) & 1))) break;
-            const UnitDesc &d = sh.desc[e];
-            const int kind = d.kind;
-            if (kind == U_END) break;
-            if (kind == U_PAIR || kind == U_ROW) {
-                const int pb = p1n % kSR;
-                wait_bar(sh, &sh.p1_done[pb], static_cast<uint32_t>((p1n / kSR) & 1));
-                float b0[8], s0[8], b1[8], s1[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int t = lane * 8 + k;
-                    const float4 v = sh.p1part[pb][t + (t >> 3)];
-                    b0[k] = v.x;
-                    s0[k] = v.y;
-                    b1[k] = v.z;
-                    s1[k] = v.w;
-                }
-                const float4 xv = sh.xval[pb];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.p1_free[pb]);
-                ++p1n;
-                unsigned long long *rec = P.stat_rec + (static_cast<size_t>(d.item) * P.ns + d.slice) * kStatWords;
-                if (d.greedy) {
-                    int i0[8], i1[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        i0[k] = __float_as_int(s0[k]);
-                        i1[k] = __float_as_int(s1[k]);
-                    }
-                    float m0, m1;
-                    int a0, a1;
-                    combine_argmax(b0, i0, m0, a0);
-                    combine_argmax(b1, i1, m1, a1);
-                    if (lane == 0) {
-                        st_word(rec + SR_AT, static_cast<uint32_t>(a0), tag);
-                        st_word(rec + SR_ST, f2u(m0), tag);
-                        st_word(rec + SR_AD, static_cast<uint32_t>(a1), tag);
-                        st_word(rec + SR_SD, f2u(m1), tag);
-                    }
-                    if (lane < kChunksPerSlice) st_word(rec + SR_CHUNK + lane, 0u, tag);
-                } else {
-                    int ra0, ra1;
-                    float rs0, rs1, c0, c1;
-                    combine_row(b0, s0, ra0, rs0, c0);
-                    combine_row(b1, s1, ra1, rs1, c1);
-                    if (lane == 0) {
-                        st_word(rec + SR_AT, static_cast<uint32_t>(ra0), tag);
-                        st_word(rec + SR_ST, f2u(rs0), tag);
-                        st_word(rec + SR_AD, static_cast<uint32_t>(kind == U_PAIR ? ra1 : kNoRef), tag);
-                        st_word(rec + SR_SD, f2u(kind == U_PAIR ? rs1 : 0.0f), tag);
-                    }
-                    if ((lane & 3) == 0) st_word(rec + SR_CHUNK + (lane >> 2), f2u(c0), tag);
-                    if (kind == U_PAIR && d.xslice == d.slice && lane < 3) {
-                        // the draft token's logits, from the thread that held them
-                        const uint32_t v = lane == 0 ? f2u(xv.x) : lane == 1 ? f2u(xv.y) : f2u(xv.z);
-                        st_word(rec + SR_XHI + lane, v, tag);
-                    }
-                }
-            }
-            warp_arrive(&sh.desc_empty[e], lane);
-        }
-}
-
-// Decide warp: four lane groups, each deciding its own unit.
-template <int DT>
-__device__ __noinline__ void role_decide(const SliceParams &P, uint32_t tag) {
-    Shared &sh = s_sh;
-    uint4 *const slots = reinterpret_cast<uint4 *>(s_dyn);
-    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-    const int G = gridDim.x;
-    constexpr int E = Elt<DT>::kPerVec;
-    (void)slots;
-    (void)tid;
-    (void)warp;
-    (void)G;
-    (void)E;
-        // ================= decide: four lane groups, each deciding its own unit =====================
-        // Each round every group with a unit polls its item's records once; a group whose records are
-        // all published combines them, decides and releases the unit, then takes the next unit.
-        const int grp = lane / kGroupLanes, gl = lane % kGroupLanes;
-        const unsigned gmask = group_mask(grp);
-        int next = 0;          // the next unit to hand out
-        int mine = -1;         // this group's unit (-1: none)
-        bool done = false;     // the END descriptor has been reached
-        uint64_t t_wait = 0;   // since when no group has made progress (0: progress this round)
-        for (;;) {
-            // hand out units, in order, to the groups without one, while descriptors are ready
-            const unsigned idle = __ballot_sync(0xffffffffu, mine < 0) & 0x01010101u;
-            if (!done && idle) {
-                for (int g2 = 0; g2 < kGroups; ++g2) {
-                    if (!(idle >> (kGroupLanes * g2) & 1u)) continue;
-                    const int e = next % kR;
-                    int ready = 0;
-                    if (lane == 0) ready = mbar_try_wait(&sh.desc_full[e], static_cast<uint32_t>((next / kR) & 1)) ? 1 : 0;
-                    ready = __shfl_sync(0xffffffffu, ready, 0);
-                    if (!ready) break;
-                    if (sh.desc[e].kind == U_END) {
-                        done = true;
-                        break;
-                    }
-                    if (grp == g2) mine = next;
-                    ++next;
-                }
-            }
-            const unsigned busy = __ballot_sync(0xffffffffu, mine >= 0);
-            if (!busy && done) break;
-            // every group with a unit polls its item's records once
-            int ready = 0, a0 = kNoRef, a1 = kNoRef, xf = 0;
-            float s0 = 0.0f, s1 = 0.0f;
-            F2 Ex = {0.0f, 0.0f};
-            const int e = mine >= 0 ? mine % kR : 0;
-            const UnitDesc &d = sh.desc[e];
-            const bool live = mine >= 0 && d.kind != U_SKIP;
-            const bool greedy = live && d.greedy != 0;
-            {
-                int ok = 1;
-                int la0 = greedy ? INT_MAX : kNoRef, la1 = la0;
-                float ls0 = greedy ? -INFINITY : 0.0f, ls1 = ls0;
-                if (live) {
-                    const unsigned long long *rec = P.stat_rec + static_cast<size_t>(d.item) * P.ns * kStatWords;
-                    for (int u = gl; u < P.ns; u += kGroupLanes) {
-                        const unsigned long long *r = rec + static_cast<size_t>(u) * kStatWords;
-                        const unsigned long long w0 = ld_word(r + SR_AT), w1 = ld_word(r + SR_ST);
-                        const unsigned long long w2 = ld_word(r + SR_AD), w3 = ld_word(r + SR_SD);
-                        ok &= (word_tag(w0) == tag) & (word_tag(w1) == tag) & (word_tag(w2) == tag) & (word_tag(w3) == tag);
-                        const int ua0 = static_cast<int>(word_val(w0)), ua1 = static_cast<int>(word_val(w2));
-                        const float us0 = u2f(word_val(w1)), us1 = u2f(word_val(w3));
-                        if (greedy) {
-                            if (us0 > ls0 || (us0 == ls0 && ua0 < la0)) {
-                                ls0 = us0;
-                                la0 = ua0;
-                            }
-                            if (us1 > ls1 || (us1 == ls1 && ua1 < la1)) {
-                                ls1 = us1;
-                                la1 = ua1;
-                            }
-                        } else {
-                            // a NaN sum (an invalid part) stays NaN
-                            const int n0 = max(la0, ua0), n1 = max(la1, ua1);
-                            ls0 = ls0 * pow2_int(la0 - n0) + ((ua0 == kNoRef) ? us0 * 0.0f : us0 * pow2_int(ua0 - n0));
-                            ls1 = ls1 * pow2_int(la1 - n1) + ((ua1 == kNoRef) ? us1 * 0.0f : us1 * pow2_int(ua1 - n1));
-                            la0 = n0;
-                            la1 = n1;
-                        }
-                    }
-                    // the draft token's logits, from the unit holding them (lane 0 of the group)
-                    if (d.kind == U_PAIR && !greedy && d.xslice >= 0 && gl == 0) {
-                        const unsigned long long *r = rec + static_cast<size_t>(d.xslice) * kStatWords;
-                        const unsigned long long x0 = ld_word(r + SR_XHI), x1 = ld_word(r + SR_XLO), x2 = ld_word(r + SR_XF);
-                        ok &= (word_tag(x0) == tag) & (word_tag(x1) == tag) & (word_tag(x2) == tag);
-                        Ex = {u2f(word_val(x0)), u2f(word_val(x1))};
-                        xf = __float_as_int(u2f(word_val(x2)));
-                    }
-                }
-                // each group's reduction (lanes xor 1, 2, 4 stay in the group); the same for every group
-                if (greedy) {
-#pragma unroll
-                    for (int o = 1; o < kGroupLanes; o <<= 1) {
-                        const float om0 = __shfl_xor_sync(0xffffffffu, ls0, o), om1 = __shfl_xor_sync(0xffffffffu, ls1, o);
-                        const int oi0 = __shfl_xor_sync(0xffffffffu, la0, o), oi1 = __shfl_xor_sync(0xffffffffu, la1, o);
-                        if (om0 > ls0 || (om0 == ls0 && oi0 < la0)) {
-                            ls0 = om0;
-                            la0 = oi0;
-                        }
-                        if (om1 > ls1 || (om1 == ls1 && oi1 < la1)) {
-                            ls1 = om1;
-                            la1 = oi1;
-                        }
-                    }
-                    a0 = la0;
-                    a1 = la1;
-                    s0 = ls0;
-                    s1 = ls1;
-                } else {
-                    int Bm0 = la0, Bm1 = la1;
-#pragma unroll
-                    for (int o = 1; o < kGroupLanes; o <<= 1) {
-                        Bm0 = max(Bm0, __shfl_xor_sync(0xffffffffu, Bm0, o));
-                        Bm1 = max(Bm1, __shfl_xor_sync(0xffffffffu, Bm1, o));
-                    }
-                    float t0 = ls0 * pow2_int(la0 - Bm0), t1 = ls1 * pow2_int(la1 - Bm1);
-#pragma unroll
-                    for (int o = 1; o < kGroupLanes; o <<= 1) {
-                        t0 += __shfl_xor_sync(0xffffffffu, t0, o);
-                        t1 += __shfl_xor_sync(0xffffffffu, t1, o);
-                    }
-                    a0 = Bm0;
-                    a1 = Bm1;
-                    s0 = t0;
-                    s1 = t1;
-                }
-                // the x values to every lane of the group, and the group's readiness
-                const int src = kGroupLanes * grp;
-                Ex.hi = __shfl_sync(0xffffffffu, Ex.hi, src);
-                Ex.lo = __shfl_sync(0xffffffffu, Ex.lo, src);
-                xf = __shfl_sync(0xffffffffu, xf, src);
-                const unsigned okm = __ballot_sync(0xffffffffu, ok);
-                ready = mine >= 0 && ((okm & gmask) == gmask);
-            }
-            // no group ready for too long: every waiting group gives up (its unit times out)
-            const unsigned rmask = __ballot_sync(0xffffffffu, ready);
-            bool force = false;
-            if (!rmask && busy) {
-                const uint64_t now = globaltimer_ns();
-                if (t_wait == 0) t_wait = now;
-                const uint64_t limit = *reinterpret_cast<volatile int32_t *>(&sh.timed_out) ? 1000000ull : kPollNs;
-                force = __shfl_sync(0xffffffffu, static_cast<int>(now - t_wait > limit), 0) != 0;
-                if (force && lane == 0) sh.timed_out = 1;
+        if (drec)
+            bulk_g2s(sh.drec[q], P.drec + static_cast<size_t>(d.item) * kDecWords, kDecWords * 8u, &sh.job_full[q], drop);
+        mbar_arrive(&sh.job_full[q]);
+        ++j;
+    };
+    // pass 2 of unit m: its slices again (from L2) and the item's decision
+    auto issue_second = [&](int m) {
+        const UnitDesc &dm = sh.desc[m % kR];
+        if (has_p2(dm)) issue(J_P2, m, dm, 2, drop);
+    };
+    for (bool end = false; !end;) {
+        // lanes 0 .. kPrep-1 prepare the descriptors of units n .. n + kPrep - 1 at once, so that
+        // their loads overlap
+        if (lane < kPrep) {
+            const long long u = sh.bad_offsets ? P.nunits : static_cast<long long>(blockIdx.x) + static_cast<long long>(n + lane) * G;
+            UnitDesc d = {};
+            if (u >= P.nunits) {
+                d.kind = U_END;
             } else {
-                t_wait = 0;
+                const int g = static_cast<int>(u / P.ns), s = static_cast<int>(u % P.ns);
+                int r0, r1;
+                const int i = find_request(P, sh, g, r0, r1);
+                const int K = r1 - r0 - 1, pos = g - r0;
+                const int drow = r0 - i + pos;
+                // the item's values, every load issued before any is used
+                const float T = P.temperature ? __ldg(P.temperature + i) : P.temperature_scalar;
+                const float tp = P.top_p ? __ldg(P.top_p + i) : 1.0f;
+                const bool shaped = K <= P.K_max;
+                const double ua = (shaped && pos < K) ? __ldg(P.uniforms + g) : 0.0;
+                const double us = shaped ? __ldg(P.uniforms + r0 + K) : 0.0;
+                const int x = (shaped && pos < K) ? __ldg(P.draft_tokens + drow) : -1;
+                const int2 cut = (P.trunc && shaped) ? __ldg(P.trunc + g) : make_int2(0, INT_MAX);
+                int status = shaped ? 0 : SPEC_REQ_BAD_SHAPE;
+                if (!(T >= 0.0f) || isinf(T) || isnan(tp)) status |= SPEC_REQ_BAD_PARAM;
+                d.kind = status ? U_SKIP : (pos < K ? U_PAIR : U_ROW);
+                d.item = g;
+                d.slice = s;
+                d.req = i;
+                d.pos = pos;
+                d.K = K;
+                d.drow = drow;
+                d.nvec = min(kSliceVecs, P.nvec_row - s * kSliceVecs);
+                d.status = status;
+                d.greedy = (T == 0.0f) ? 1 : 0;
+                d.designated = (s == g % P.ns) ? 1 : 0;
+                d.ua = ua;
+                d.us = us;
+                d.x = x;
+                d.xslice = (x >= 0 && x < P.V) ? (x / E) / kSliceVecs : -1;
+                F2 sv = {0.0f, 0.0f};
+                if (T > 0.0f && !isinf(T)) sv = f2_div({kLog2eHi, kLog2eLo}, {T, 0.0f});
+                if (sv.hi > 0.0f && sv.lo < 0.0f) {
+                    // s_hi moved toward zero so that s_lo > 0: a -inf logit then gives -inf in
+                    // both terms of the exponent's argument (a negative s_lo would make it NaN)
+                    const float down = __uint_as_float(__float_as_uint(sv.hi) - 1u);
+                    sv.lo += sv.hi - down;
+                    sv.hi = down;
+                }
+                d.s_hi = sv.hi;
+                d.s_lo = fmaxf(sv.lo, 1.401298464e-45f);
+                d.cut_tau = static_cast<uint32_t>(cut.x);
+                d.cut_id = cut.y;
+                d.trunc = (!d.greedy && (cut.x != 0 || cut.y != INT_MAX)) ? 1 : 0;
             }
-            const bool fin = mine >= 0 && (ready || force);
-            if (!rmask && !force) {
-                __nanosleep(200);  // nothing to decide yet
-                continue;
-            }
-            // every lane evaluates the decision (idle groups on a dummy): no divergent shuffles
-            int status = d.status;
-            if (!ready || *reinterpret_cast<volatile int32_t *>(&sh.timed_out)) status |= REQ_TIMEOUT;
-            UnitDec D = decide_item(P, d, status, a0, s0, a1, s1, Ex, xf);
-            if (fin && d.kind == U_SKIP) {
-                D = UnitDec{};
-                D.status = d.status;
-                D.kind = SAMPLE_NONE;
-                D.argmax_t = -1;
-            }
-            if (fin && gl == 0) {
-                sh.dec[e] = D;
-                mbar_arrive(&sh.dec_ready[e]);
-                mbar_arrive(&sh.desc_empty[e]);
-            }
-            if (fin) mine = -1;
-            __syncwarp();
+            sh.prep[lane] = d;
         }
-}
-
-// Finish warp: in order, unit m's pass-2 partials -> its published record; items to the final warp.
-template <int DT>
-__device__ __noinline__ void role_finish(const SliceParams &P, uint32_t tag) {
-    Shared &sh = s_sh;
-    uint4 *const slots = reinterpret_cast<uint4 *>(s_dyn);
-    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-    const int G = gridDim.x;
-    constexpr int E = Elt<DT>::kPerVec;
-    (void)slots;
-    (void)tid;
-    (void)warp;
-    (void)G;
-    (void)E;
-        // ================= finish: in order, unit m's pass-2 partials -> its published record ======
-        int p2q = 0, j = 0;
-        for (int m = 0;; ++m) {
-            const int e = m % kR;
-            if (!wait_bar(sh, &sh.desc_full[e], static_cast<uint32_t>((m / kR) & 1))) break;
-            const UnitDesc &d = sh.desc[e];
-            if (d.kind == U_END) break;
-            wait_bar(sh, &sh.dec_ready[e], static_cast<uint32_t>((m / kR) & 1));
-            if (d.kind == U_PAIR && !d.greedy) {
-                const int pb = p2q % kPR;
-                wait_bar(sh, &sh.p2_done[pb], static_cast<uint32_t>((p2q / kPR) & 1));
-                float a = 0.0f, z = 0.0f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int t = lane * 8 + k;
-                    const float2 v = sh.p2part[pb][t + (t >> 3)];
-                    a += v.x;
-                    z += v.y;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.p2_free[pb]);
-                ++p2q;
-                // chunk w: lanes 4w .. 4w + 3; alpha and Z over all lanes
-#pragma unroll
-                for (int o = 1; o < 4; o <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-                float zt = (lane & 3) == 0 ? z : 0.0f;
-                zt = warp_sum(zt);
-                a = warp_sum(a);
-                unsigned long long *rec = P.p2_rec + (static_cast<size_t>(d.item) * P.ns + d.slice) * kP2Words;
-                if ((lane & 3) == 0) st_word(rec + PR_CHUNK + (lane >> 2), f2u(z), tag);
-                if (lane == 0) {
-                    st_word(rec + PR_ALPHA, f2u(a), tag);
-                    st_word(rec + PR_Z, f2u(zt), tag);
-                }
-            }
-            if (d.designated) {
-                // the item's designated unit: hand the item to the final warp
-                const int q = j % kFQ;
-                if (j >= kFQ) wait_bar(sh, &sh.fq_empty[q], static_cast<uint32_t>(((j / kFQ) - 1) & 1));
-                if (lane == 0) {
-                    sh.fq[q].d = d;
-                    sh.fq[q].D = sh.dec[e];
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.fq_full[q]);
-                ++j;
-            }
-            warp_arrive(&sh.desc_empty[e], lane);
-        }
-        // the end of the queue
-        const int q = j % kFQ;
-        if (j >= kFQ) wait_bar(sh, &sh.fq_empty[q], static_cast<uint32_t>(((j / kFQ) - 1) & 1));
+        __syncwarp();
         if (lane == 0) {
-            sh.fq[q].d.kind = U_END;
-            mbar_arrive(&sh.fq_full[q]);
+            for (int l = 0; l < kPrep; ++l, ++n) {
+                const int e = n % kR;
+                const bool ok = n < kR || wait_bar(sh, &sh.desc_empty[e], static_cast<uint32_t>(((n / kR) - 1) & 1));
+                UnitDesc &d = sh.desc[e];
+                d = sh.prep[l];
+                if (!ok || sh.timed_out) d.kind = U_END;
+                mbar_arrive(&sh.desc_full[e]);
+                if (d.kind == U_END) {
+                    end = true;
+                    break;
+                }
+                // pass 1 of unit n: a pair's slices stay in L2 for its pass 2 (evict last)
+                if (d.kind == U_SKIP)
+                    issue(J_SKIP, n, d, 0, drop);
+                else
+                    issue(J_P1, n, d, d.kind == U_PAIR ? 2 : 1, (d.kind == U_PAIR && !d.greedy) ? keep : drop);
+                if (n >= kLag) issue_second(n - kLag);
+            }
+            if (end) {
+                // the last units' second jobs, then the end
+                for (int m = max(0, n - kLag); m < n; ++m) issue_second(m);
+                issue(J_END, n, sh.desc[n % kR], 0, drop);
+                // copies still in flight (a wait gave up): wait for them, bounded, before leaving
+                if (sh.timed_out)
+                    for (int m = max(0, j - kJobs); m < j; ++m)
+                        mbar_wait_sleep_bounded(&sh.job_full[m % kJobs], static_cast<uint32_t>((m / kJobs) & 1), kSuspendNs,
+                                                4);
+            }
         }
+        n = __shfl_sync(0xffffffffu, n, 0);
+        end = __shfl_sync(0xffffffffu, end ? 1 : 0, 0) != 0;
+        __syncwarp();
+    }
+    (void)tag;
 }
 
-// Final warp: items' results and draws, requests' selections.
+// Final warp: items' decisions (each item once in the whole grid, by the CTA that counted its
+// last unit through pass 1), results and draws, requests' selections.
 template <int DT>
 __device__ __noinline__ void role_final(const SliceParams &P, uint32_t tag) {
     Shared &sh = s_sh;
-    uint4 *const slots = reinterpret_cast<uint4 *>(s_dyn);
-    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-    const int G = gridDim.x;
-    constexpr int E = Elt<DT>::kPerVec;
-    (void)slots;
-    (void)tid;
-    (void)warp;
-    (void)G;
-    (void)E;
-        // ================= final: items' results and draws, requests' selections ====================
-        for (int j = 0;; ++j) {
-            const int q = j % kFQ;
-            if (!wait_bar(sh, &sh.fq_full[q], static_cast<uint32_t>((j / kFQ) & 1))) break;
-            const FinJob job = sh.fq[q];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.fq_empty[q]);
-            if (job.d.kind == U_END) break;
-            finalize_item<DT>(P, job, tag, sh);
+    const int lane = threadIdx.x % kWarp;
+    for (int j = 0;; ++j) {
+        const int q = j % kFQ;
+        if (!wait_bar(sh, &sh.fq_full[q], static_cast<uint32_t>((j / kFQ) & 1))) break;
+        FinJob job = sh.fq[q];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.fq_empty[q]);
+        if (job.op == F_END) break;
+        if (job.op == F_DECIDE) {
+            job.D = decide_records(P, job.d, tag, sh);
+            // the decision record, for every CTA holding a unit of the item
+            unsigned long long *r = P.drec + static_cast<size_t>(job.d.item) * kDecWords;
+            if (lane < kDecWords) st_word(r + lane, dec_word(job.D, lane), tag);
+            if (has_p2(job.d)) continue;  // finalised after pass 2
         }
-        __threadfence();
-    
+        finalize_item<DT>(P, job, tag, sh);
+    }
+    __threadfence();
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kBlock, 1) spec_slice_kernel(const __grid_constant__ SliceParams P) {
+__global__ void __maxnreg__(kMaxRegs) spec_slice_kernel(const __grid_constant__ SliceParams P) {
     Shared &sh = s_sh;
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
     const int G = gridDim.x;
@@ -1756,16 +1654,7 @@ __global__ void __launch_bounds__(kBlock, 1) spec_slice_kernel(const __grid_cons
     if (tid == 0) {
         for (int k = 0; k < kR; ++k) {
             mbar_init(&sh.desc_full[k], 1);
-            mbar_init(&sh.desc_empty[k], kDW + 3);
-            mbar_init(&sh.dec_ready[k], 1);
-        }
-        for (int k = 0; k < kSR; ++k) {
-            mbar_init(&sh.p1_done[k], kDW);
-            mbar_init(&sh.p1_free[k], 1);
-        }
-        for (int k = 0; k < kPR; ++k) {
-            mbar_init(&sh.p2_done[k], kDW);
-            mbar_init(&sh.p2_free[k], 1);
+            mbar_init(&sh.desc_empty[k], kDW);
         }
         for (int k = 0; k < kJobs; ++k) {
             mbar_init(&sh.job_full[k], 1);
@@ -1775,6 +1664,8 @@ __global__ void __launch_bounds__(kBlock, 1) spec_slice_kernel(const __grid_cons
             mbar_init(&sh.fq_full[k], 1);
             mbar_init(&sh.fq_empty[k], 1);
         }
+        sh.fq_tail = 0;
+        sh.end_cnt = 0;
         fence_mbar_init();
         sh.timed_out = 0;
         sh.last_cta = 0;
@@ -1801,19 +1692,12 @@ __global__ void __launch_bounds__(kBlock, 1) spec_slice_kernel(const __grid_cons
     __syncthreads();
     const uint32_t tag = sh.tag;
 
-    // each role in a function of its own, so that each gets its own register allocation (one
-    // function for all roles kept the data warps' loop state in local memory)
+    // each role in a function of its own (its own register allocation)
     if (warp < kDW)
         role_data<DT>(P, tag);
     else if (warp == W_PROD)
         role_producer<DT>(P, tag);
-    else if (warp == W_STATS)
-        role_stats<DT>(P, tag);
-    else if (warp == W_DECIDE)
-        role_decide<DT>(P, tag);
-    else if (warp == W_FINISH)
-        role_finish<DT>(P, tag);
-    else
+    else if (warp == W_FINAL)
         role_final<DT>(P, tag);
 
     // ================= the last CTA: batch-level results, compaction, gamma, reset ===================

@@ -34,7 +34,8 @@ namespace spec {
 // workspace once); every call leaves its counters at zero and advances the epoch, so the next
 // call needs nothing.
 struct WsLayout {
-    size_t flag, tok, status, fb, prob, margin, alpha, cut, stat_rec, p2_rec, req_cnt, req_alpha, ctl, total;
+    size_t flag, tok, status, fb, prob, margin, alpha, cut, p1w, p2w, xrec, drec, req_cnt, req_alpha, ctl,
+        total;
     int32_t ns, nunits, nvec_row;
 };
 
@@ -59,8 +60,10 @@ static WsLayout ws_layout(int32_t B, int32_t V, int32_t total_rows, spec_dtype d
     };
     L.ctl = take(slice::kCtlWords * 4);
     L.req_cnt = take(nb * 4);
-    L.stat_rec = take(units * slice::kStatWords * 8);
-    L.p2_rec = take(units * slice::kP2Words * 8);
+    L.p1w = take(units * slice::kDW * slice::kW1Words * 8);
+    L.p2w = take(units * slice::kDW * slice::kW2Words * 8);
+    L.xrec = take(T * slice::kXWords * 8);
+    L.drec = take(T * slice::kDecWords * 8);
     L.flag = take(T * 4);
     L.tok = take(T * 4);
     L.status = take(T * 4);
@@ -185,8 +188,10 @@ static spec_status verify_enqueue(const spec_verify_args *a, void *workspace, si
     P.nvec_row = L.nvec_row;
     P.ns = L.ns;
     P.nunits = L.nunits;
-    P.stat_rec = reinterpret_cast<unsigned long long *>(ws + L.stat_rec);
-    P.p2_rec = reinterpret_cast<unsigned long long *>(ws + L.p2_rec);
+    P.p1w = reinterpret_cast<unsigned long long *>(ws + L.p1w);
+    P.p2w = reinterpret_cast<unsigned long long *>(ws + L.p2w);
+    P.xrec = reinterpret_cast<unsigned long long *>(ws + L.xrec);
+    P.drec = reinterpret_cast<unsigned long long *>(ws + L.drec);
     P.req_cnt = reinterpret_cast<uint32_t *>(ws + L.req_cnt);
     P.ctl = reinterpret_cast<uint32_t *>(ws + L.ctl);
     P.item_flag = reinterpret_cast<int32_t *>(ws + L.flag);
@@ -285,7 +290,7 @@ extern "C" const char *spec_version(void) { return "spec-verify-gb300 0.1 (sm_10
 
 namespace spec {
 constexpr int32_t kNoallocMaxRows = 16384;             // target rows per call: T = sum_i (K_i + 1)
-constexpr size_t kNoallocScratchBytes = 4u << 20;      // 4 MiB of device memory per GPU
+constexpr size_t kNoallocScratchBytes = 16u << 20;     // 16 MiB of device memory per GPU
 static __device__ __align__(256) unsigned char noalloc_scratch[kNoallocScratchBytes];
 
 static std::mutex noalloc_mu;
