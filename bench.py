@@ -48,7 +48,7 @@ KERNEL_SAMPLE = 8  # the per-position kernel is bracketed by CUDA events on ever
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "stream_kernel_c3_traffic.json")
 CSRC = os.path.join(ROOT, "speculative_decoding_verification_43_gb300", "csrc")
 # the per-position kernel's sources: a committed ncu traffic figure counts only while they match
-KERNEL_SRCS = ("spec_verify.cu", "spec_slice_kernel.cuh", "spec_math.cuh",
+KERNEL_SRCS = ("spec_verify.cu", "spec_kernels.cuh", "spec_math.cuh",
                "spec_device.cuh")
 
 

@@ -61,10 +61,8 @@ enum {
     SPEC_REQ_BAD_SHAPE = 4,    /* K_i < 0, K_i > K_max, or row_off inconsistent               */
     SPEC_REQ_BAD_PARAM = 8,    /* temperature NaN, infinite or negative, or top_p NaN         */
     SPEC_REQ_BAD_BLOCKS = 16,  /* spec_compact: a committed position has no page             */
-    SPEC_REQ_TIMEOUT = 32      /* a bounded wait inside the kernel gave up (a copy or a peer
-                                  CTA's published result did not arrive within about a
-                                  second); the request's result is not computed. Not expected
-                                  on a healthy device: it stands in for a hang               */
+    SPEC_REQ_TIMEOUT = 32      /* the request's positions were not all finished when the batch
+                                  was (an internal fault; not produced on a healthy device) */
 };
 
 /* ---- spec_verify ------------------------------------------------------------------------
@@ -103,7 +101,8 @@ typedef struct {
     /* diagnostics (each may be NULL) */
     float *rho_rows;             /* [T-B] p_j(x_j)/q_j(x_j) (greedy: 1 accepted / 0 rejected)   */
     float *resid_rows;           /* [T-B] sum_v max(p_j - q_j, 0) where the kernel formed the
-                                    residual (rejected positions), else -1                     */
+                                    residual (a request's first rejected position, the only
+                                    one drawn from), else -1                                   */
     float *frontier_prob;        /* [B] probability of the frontier token in the law it was
                                     drawn from                                                 */
     float *frontier_margin;      /* [B] distance of u*Z to the nearer end of the frontier
@@ -133,17 +132,17 @@ typedef struct {
 } spec_verify_args;
 
 /* Bytes of device workspace spec_verify needs for a batch of total_rows target rows of V logits
- * of type dtype. The workspace must be 256-byte aligned and zero-filled before its first use
- * (cudaMemset): it holds counters and published records that the kernel's CTAs exchange. Every
- * call leaves it ready for the next one (counters back at zero, a new epoch for the records), so
- * it is filled once, not per call, and may serve calls of any shape that fits its size. Calls
- * that share a workspace must not overlap on the GPU. */
+ * of type dtype. The workspace must be 256-byte aligned; its contents need no preparation (the
+ * first kernel of each call zeroes the counters the second uses), so one workspace may serve
+ * calls of any shape that fits its size. Calls that share a workspace must not overlap on the
+ * GPU. */
 size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t total_rows, spec_dtype dtype);
 
-/* Verify one round. Enqueues one kernel on `stream` (two with top-k / top-p, whose cut of each
- * target row runs first); returns without waiting. The kernel is a persistent grid of one CTA per
- * SM, launched cooperatively (all CTAs resident at once); it fails with SPEC_ERR_CUDA when the
- * device cannot host that grid (for example while another cooperative kernel holds its SMs). */
+/* Verify one round. Enqueues three kernels on `stream` (four with top-k / top-p, whose cut of each
+ * target row runs first) and returns without waiting: spec_stats_kernel reads every logit once
+ * (a persistent grid), spec_decide_kernel decides every position, and spec_finish_kernel reads the
+ * pairs' rows again for alpha and the frontier's residual, draws, and selects each request's
+ * result; each is launched so that its CTAs may start as the one before drains. */
 spec_status spec_verify(const spec_verify_args *args, void *workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 
@@ -151,21 +150,21 @@ spec_status spec_verify(const spec_verify_args *args, void *workspace, size_t wo
  * memory where they verify (a memory planner that owns all device memory, a callback inside
  * another runtime, a path where cudaMalloc's synchronisation is not acceptable). The pages have
  * no counterpart to this entry point: it is an interface convenience of this library.
- * Scratch comes from one fixed array of 4 MiB in the library's device memory, present on every
- * GPU that loads the library until exit; it starts zeroed and each call leaves it ready for the
- * next. Limits: total_rows <= 16384 target rows per call, and spec_verify_workspace_size() of the
- * call's shape at most 4 MiB (for example T = 16384 rows with V * sizeof(logit) <= 16 KB, or the
- * B = 64, V = 128256 bf16 batch); larger calls return SPEC_ERR_UNSUPPORTED before anything is
+ * Scratch comes from one fixed array of 16 MiB in the library's device memory, present on every
+ * GPU that loads the library until exit (a workspace needs no preparation between calls).
+ * Limits: total_rows <= 16384 target rows per call, and spec_verify_workspace_size() of the
+ * call's shape at most 16 MiB (for example T = 16384 rows with V * sizeof(logit) <= 64 KB, or the
+ * B = 512, V = 256000 bf16 batch); larger calls return SPEC_ERR_UNSUPPORTED before anything is
  * enqueued. The array's address is looked up on the first call on each device (make that call
  * before any stream capture). All calls share the array: calls that overlap on the GPU (other
  * streams, other threads) race on it and must be serialised by the caller. Arguments, outputs
  * and errors are otherwise those of spec_verify. */
 spec_status spec_verify_noalloc(const spec_verify_args *args, cudaStream_t stream);
 
-/* Which kernel spec_verify launches for a batch of this shape (B requests, total_rows target
- * rows, vocabulary V, dtype) on the current device, and its grid: *cluster CTAs per cluster (1)
- * and *clusters CTAs (one per SM); either pointer may be NULL. Returns a static string naming
- * the kernel ("spec_slice_kernel"), or NULL when the shape is invalid (B <= 0, V <= 0,
+/* Which kernel reads the logits for a batch of this shape (B requests, total_rows target rows,
+ * vocabulary V, dtype) on the current device, and its grid: *cluster CTAs per cluster (1) and
+ * *clusters CTAs (the same number on every SM); either pointer may be NULL. Returns a static
+ * string naming the kernel ("spec_stats_kernel"), or NULL when the shape is invalid (B <= 0, V <= 0,
  * total_rows < B, a row not a multiple of 16 bytes) or the device cannot host the kernel. A
  * diagnostic: it enqueues nothing and only queries the device. */
 const char *spec_verify_plan(int32_t B, int32_t V, int32_t total_rows, spec_dtype dtype, int32_t *cluster,
@@ -253,8 +252,8 @@ spec_status spec_choose_gamma(const double *alpha_sum, const int32_t *alpha_coun
  *   spec_compact(compact, stream);
  *   spec_choose_gamma(args->alpha_sum, args->alpha_count, alpha_prev, c, gamma_min, gamma_max,
  *                     gamma_out, alpha_out, stream);
- * with the compaction and the gamma choice run by the last CTA of spec_verify's kernel, so that
- * the round is one launch. `compact` carries the compaction's own inputs and outputs as for
+ * with the compaction and the gamma choice run by the CTA of spec_verify's finishing kernel that
+ * completes the batch, so that the round adds no launch. `compact` carries the compaction's own inputs and outputs as for
  * spec_compact; its accept_len / n_emitted / out_tokens / req_status are normally args'
  * outputs. Every argument is checked as by the three calls (plus compact->B == args->B and
  * compact->total_rows == args->total_rows; args->alpha_sum and args->alpha_count are required)

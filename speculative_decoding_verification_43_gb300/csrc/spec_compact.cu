@@ -146,7 +146,7 @@ extern "C" spec_status spec_compact(const spec_compact_args *a, cudaStream_t str
     CompactParams P;
     const spec_status st = compact_params(a, P);
     if (st != SPEC_OK) return st;
-    return launch_after(spec_compact_kernel, dim3(1), dim3(kCompactThreads), stream, P) == cudaSuccess ? SPEC_OK
+    return launch_after(spec_compact_kernel, dim3(1), dim3(kCompactThreads), 0, stream, P) == cudaSuccess ? SPEC_OK
                                                                                                      : SPEC_ERR_CUDA;
 }
 
@@ -165,7 +165,7 @@ extern "C" spec_status spec_choose_gamma(const double *alpha_sum, const int32_t 
     const spec_status st = gamma_params(alpha_sum, alpha_count, alpha_prev, c, gamma_min, gamma_max, gamma_out,
                                         alpha_out, G);
     if (st != SPEC_OK) return st;
-    return launch_after(spec_gamma_kernel, dim3(1), dim3(32), stream, G) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    return launch_after(spec_gamma_kernel, dim3(1), dim3(32), 0, stream, G) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 // Host evaluation in double precision of the depth-aware objective (for tests and callers that
@@ -196,7 +196,7 @@ extern "C" spec_status spec_choose_gamma_depth(const int32_t *n_reached, const i
     if (!(c >= 0.0) || !std::isfinite(c) || !(alpha_prev >= 0.0 && alpha_prev <= 1.0)) return SPEC_ERR_INVALID_ARG;
     const float ph = static_cast<float>(alpha_prev), pl = static_cast<float>(alpha_prev - static_cast<double>(ph));
     const float ch = static_cast<float>(c), cl = static_cast<float>(c - static_cast<double>(ch));
-    return launch_after(spec_gamma_depth_kernel, dim3(1), dim3(32), stream, n_reached, n_accepted,
+    return launch_after(spec_gamma_depth_kernel, dim3(1), dim3(32), 0, stream, n_reached, n_accepted,
                         static_cast<int>(depth_max), ph, pl, ch, cl, static_cast<int>(gamma_min),
                         static_cast<int>(gamma_max), gamma_out, ea_out) == cudaSuccess
                ? SPEC_OK

@@ -289,7 +289,7 @@ __device__ __forceinline__ float ex2(float x) {
 // running (programmatic stream serialisation); the kernel must call griddep_wait() first thing
 // before touching that kernel's outputs.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+inline cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                                 Args... args) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -297,7 +297,7 @@ inline cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;

@@ -4,11 +4,12 @@
 // ("What to do", steps 3-4) and SDCP Rules 1 and 2 ("Acceptance Rules"); the C ABI and its
 // conventions are documented in include/spec_verify.h.
 //
-// One kernel per call (two with top-k / top-p, whose cut of each target row comes first): the
-// slice kernel (spec_slice_kernel.cuh) verifies every (request, position) on a persistent grid of
-// one CTA per SM, selects each request's result (first rejection, emitted tokens, stopping),
-// reduces alpha for the gamma controller and, for spec_verify_round, compacts the round and
-// chooses gamma.
+// Two kernels per call (three with top-k / top-p, whose cut of each target row comes first), both in
+// spec_kernels.cuh: the statistics kernel reads every logit once (pass 1) on a persistent grid; the
+// finishing kernel, launched to start as the first drains, decides every (request, position), runs
+// pass 2 of the pairs from L2, draws the tokens, selects each request's result (first rejection,
+// emitted tokens, stopping), reduces alpha for the gamma controller and, for spec_verify_round,
+// compacts the round and chooses gamma.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,7 +22,7 @@
 #include "spec_device.cuh"
 #include "spec_verify.h"
 
-#include "spec_slice_kernel.cuh"
+#include "spec_kernels.cuh"
 #include "spec_trunc.cuh"
 #include "spec_tail.cuh"
 
@@ -30,13 +31,12 @@ namespace spec {
 // ------------------------------------------------------------------------------------------
 // Host side
 
-// Workspace of one call. The records and counters must start zeroed (the caller zero-fills the
-// workspace once); every call leaves its counters at zero and advances the epoch, so the next
-// call needs nothing.
+// Workspace of one call. It needs no preparation: the statistics kernel zeroes the counters the
+// finishing kernel uses, and every record is written before it is read within the call.
 struct WsLayout {
-    size_t flag, tok, status, fb, prob, margin, alpha, cut, p1w, p2w, xrec, drec, req_cnt, req_alpha, ctl,
+    size_t rec, xrec, desc, dec, alpha_c, zc, req_cnt, ctl, agg, flag, tok, status, fb, prob, margin, alpha, cut, req_alpha,
         total;
-    int32_t ns, nunits, nvec_row;
+    int32_t nvec_row, nchunk;
 };
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -49,21 +49,23 @@ static WsLayout ws_layout(int32_t B, int32_t V, int32_t total_rows, spec_dtype d
     const size_t eb = (dtype == SPEC_BF16) ? 2 : 4;
     const size_t nvec = V > 0 ? (static_cast<size_t>(V) * eb) / 16 : 0;
     L.nvec_row = static_cast<int32_t>(nvec);
-    L.ns = static_cast<int32_t>((nvec + slice::kSliceVecs - 1) / slice::kSliceVecs);
-    const size_t units = T * static_cast<size_t>(L.ns);
-    L.nunits = units > static_cast<size_t>(INT_MAX) ? INT_MAX : static_cast<int32_t>(units);
+    L.nchunk = static_cast<int32_t>((nvec + vk::kChunkVecs - 1) / vk::kChunkVecs);
+    const size_t chunks = T * static_cast<size_t>(L.nchunk);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;
         off = align_up(off + bytes, 256);
         return o;
     };
-    L.ctl = take(slice::kCtlWords * 4);
+    L.ctl = take(vk::kCtlWords * 4);
+    L.agg = take(vk::kAggWords * 4);
     L.req_cnt = take(nb * 4);
-    L.p1w = take(units * slice::kDW * slice::kW1Words * 8);
-    L.p2w = take(units * slice::kDW * slice::kW2Words * 8);
-    L.xrec = take(T * slice::kXWords * 8);
-    L.drec = take(T * slice::kDecWords * 8);
+    L.rec = take(chunks * 16);
+    L.alpha_c = take(chunks * 4);
+    L.zc = take(chunks * 4);
+    L.xrec = take(T * 16);
+    L.desc = take(T * sizeof(vk::ItemDesc));
+    L.dec = take(T * sizeof(vk::ItemDec));
     L.flag = take(T * 4);
     L.tok = take(T * 4);
     L.status = take(T * 4);
@@ -77,61 +79,49 @@ static WsLayout ws_layout(int32_t B, int32_t V, int32_t total_rows, spec_dtype d
     return L;
 }
 
-// The persistent grid of the slice kernel on the current device: one CTA per SM (its shared
-// memory allows no more), all resident at once.
-struct Grid {
-    int ctas = 0;
-    size_t smem = 0;
-};
-
+// The persistent grid of the statistics kernel on the current device: every SM filled with as many
+// CTAs as fit.
 template <int DT>
-static cudaError_t slice_grid(Grid &g) {
+static cudaError_t stats_grid(int &ctas, int *p2 = nullptr) {
     static std::mutex mu;
-    static uint64_t attrs_set = 0;  // one bit per device
-    static int ctas_of[64] = {0};
+    static int ctas_of[64] = {0}, p2_of[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const size_t smem = static_cast<size_t>(slice::kSlots) * slice::kSliceVecs * 16;
     std::lock_guard<std::mutex> lock(mu);
-    if (!(attrs_set >> dev & 1ull)) {
-        e = cudaFuncSetAttribute(slice::spec_slice_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        // the CTA needs nearly all of the SM's shared memory: ask for the largest carveout
-        e = cudaFuncSetAttribute(slice::spec_slice_kernel<DT>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
+    if (!ctas_of[dev]) {
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, slice::spec_slice_kernel<DT>, slice::kBlock, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vk::spec_stats_kernel<DT>, vk::kStatsBlock, 0);
         if (e != cudaSuccess) return e;
         ctas_of[dev] = sms * per_sm;
-        attrs_set |= 1ull << dev;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vk::spec_pass2_kernel<DT>, vk::kFinBlock, 0);
+        if (e != cudaSuccess) return e;
+        p2_of[dev] = sms * per_sm;
     }
-    g.ctas = ctas_of[dev];
-    g.smem = smem;
+    ctas = ctas_of[dev];
+    if (p2) *p2 = p2_of[dev];
     return cudaSuccess;
 }
 
 template <int DT>
-static spec_status launch_slice(const slice::SliceParams &P, cudaStream_t stream) {
-    Grid g;
-    if (slice_grid<DT>(g) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (g.ctas <= 0) return SPEC_ERR_UNSUPPORTED;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: they wait on one another
-    attr[0].val.cooperative = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(g.ctas), 1, 1);
-    cfg.blockDim = dim3(slice::kBlock, 1, 1);
-    cfg.dynamicSmemBytes = g.smem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, slice::spec_slice_kernel<DT>, P) != cudaSuccess) return SPEC_ERR_CUDA;
+static spec_status launch_verify(const vk::VerifyParams &P, cudaStream_t stream) {
+    int ctas = 0, p2_ctas = 0;
+    if (stats_grid<DT>(ctas, &p2_ctas) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (ctas <= 0 || p2_ctas <= 0) return SPEC_ERR_UNSUPPORTED;
+    vk::spec_stats_kernel<DT><<<ctas, vk::kStatsBlock, 0, stream>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+    if (launch_after(vk::spec_decide_kernel<DT>, dim3(static_cast<unsigned>(P.B)), dim3(vk::kDecWarps * kWarp), 0,
+                     stream, P) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (launch_after(vk::spec_pass2_kernel<DT>, dim3(static_cast<unsigned>(p2_ctas)), dim3(vk::kFinBlock), 0, stream,
+                     P) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    const unsigned fin_ctas = static_cast<unsigned>((P.total_rows + vk::kFinWarps - 1) / vk::kFinWarps);
+    if (launch_after(vk::spec_finish_kernel<DT>, dim3(fin_ctas), dim3(vk::kFinBlock), 0, stream, P) != cudaSuccess)
+        return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
 
@@ -144,7 +134,8 @@ extern "C" size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t total
 }
 
 // spec_verify's checks and launches (the truncation kernel when top-k / top-p is given, then the
-// slice kernel); with C and G the slice kernel also runs the round's compaction and gamma choice.
+// statistics and the finishing kernel); with C and G the finishing kernel also runs the round's
+// compaction and gamma choice.
 // Nothing is enqueued when a check fails.
 static spec_status verify_enqueue(const spec_verify_args *a, void *workspace, size_t workspace_bytes,
                                   cudaStream_t stream, const CompactParams *C, const GammaParams *G) {
@@ -165,12 +156,12 @@ static spec_status verify_enqueue(const spec_verify_args *a, void *workspace, si
     if (!a->temperature && !(a->temperature_scalar >= 0.0f && std::isfinite(a->temperature_scalar)))
         return SPEC_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(a->B, a->V, a->total_rows, a->dtype);
-    if (static_cast<int64_t>(a->total_rows) * L.ns > INT_MAX / 2) return SPEC_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(a->total_rows) * L.nchunk > INT_MAX / 2) return SPEC_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < L.total || reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
         return SPEC_ERR_WORKSPACE;
 
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    slice::SliceParams P = {};
+    vk::VerifyParams P = {};
     P.target = a->target_logits;
     P.draft = a->draft_logits;
     P.row_off = a->row_off;
@@ -186,14 +177,16 @@ static spec_status verify_enqueue(const spec_verify_args *a, void *workspace, si
     P.K_max = a->K_max;
     P.total_rows = a->total_rows;
     P.nvec_row = L.nvec_row;
-    P.ns = L.ns;
-    P.nunits = L.nunits;
-    P.p1w = reinterpret_cast<unsigned long long *>(ws + L.p1w);
-    P.p2w = reinterpret_cast<unsigned long long *>(ws + L.p2w);
-    P.xrec = reinterpret_cast<unsigned long long *>(ws + L.xrec);
-    P.drec = reinterpret_cast<unsigned long long *>(ws + L.drec);
+    P.nchunk = L.nchunk;
+    P.rec = reinterpret_cast<int4 *>(ws + L.rec);
+    P.xrec = reinterpret_cast<float4 *>(ws + L.xrec);
+    P.desc = reinterpret_cast<vk::ItemDesc *>(ws + L.desc);
+    P.dec = reinterpret_cast<vk::ItemDec *>(ws + L.dec);
+    P.alpha_c = reinterpret_cast<float *>(ws + L.alpha_c);
+    P.zc = reinterpret_cast<float *>(ws + L.zc);
     P.req_cnt = reinterpret_cast<uint32_t *>(ws + L.req_cnt);
     P.ctl = reinterpret_cast<uint32_t *>(ws + L.ctl);
+    P.agg = reinterpret_cast<uint32_t *>(ws + L.agg);
     P.item_flag = reinterpret_cast<int32_t *>(ws + L.flag);
     P.item_tok = reinterpret_cast<int32_t *>(ws + L.tok);
     P.item_status = reinterpret_cast<int32_t *>(ws + L.status);
@@ -221,7 +214,7 @@ static spec_status verify_enqueue(const spec_verify_args *a, void *workspace, si
     if (G) P.G = *G;
     P.trunc = nullptr;
     if (a->top_k || a->top_p) {
-        // top-k / top-p: the cut of every target row, before the slice kernel reads it
+        // top-k / top-p: the cut of every target row, before the statistics kernel reads it
         TruncParams Tp = {};
         Tp.target = a->target_logits;
         Tp.row_off = a->row_off;
@@ -242,7 +235,7 @@ static spec_status verify_enqueue(const spec_verify_args *a, void *workspace, si
     }
 
     if (a->rows_event_begin && cudaEventRecord(a->rows_event_begin, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-    const spec_status st = (a->dtype == SPEC_BF16) ? launch_slice<SPEC_BF16>(P, stream) : launch_slice<SPEC_F32>(P, stream);
+    const spec_status st = (a->dtype == SPEC_BF16) ? launch_verify<SPEC_BF16>(P, stream) : launch_verify<SPEC_F32>(P, stream);
     if (st != SPEC_OK) return st;
     if (a->rows_event_end && cudaEventRecord(a->rows_event_end, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
@@ -280,9 +273,8 @@ extern "C" const char *spec_version(void) { return "spec-verify-gb300 0.1 (sm_10
 // For them this entry point takes its workspace from a fixed array in the library's own
 // device memory instead of from the caller.
 //
-// The array lives in every GPU that loads the library until the process exits. It starts
-// zeroed (static device memory), as spec_verify's workspace must, and every call leaves it ready
-// for the next one (its counters back at zero, its epoch advanced). Its address is looked up once
+// The array lives in every GPU that loads the library until the process exits; a workspace needs
+// no preparation between calls, so every call finds it ready. Its address is looked up once
 // per device, on the first call made with that device current; make that first call before any
 // stream capture. All calls share the one array and it keeps the last call's contents; calls
 // that overlap on the GPU, on two streams or from two threads, race on it and must be
@@ -324,14 +316,14 @@ extern "C" const char *spec_verify_plan(int32_t B, int32_t V, int32_t total_rows
     if (B <= 0 || V <= 0 || total_rows < B || (dtype != SPEC_BF16 && dtype != SPEC_F32)) return nullptr;
     const int per_vec = (dtype == SPEC_BF16) ? 8 : 4;
     if (V % per_vec != 0) return nullptr;
-    Grid g;
-    const cudaError_t e = (dtype == SPEC_BF16) ? slice_grid<SPEC_BF16>(g) : slice_grid<SPEC_F32>(g);
+    int ctas = 0;
+    const cudaError_t e = (dtype == SPEC_BF16) ? stats_grid<SPEC_BF16>(ctas) : stats_grid<SPEC_F32>(ctas);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return nullptr;
     }
-    if (g.ctas <= 0) return nullptr;
+    if (ctas <= 0) return nullptr;
     if (cluster) *cluster = 1;
-    if (clusters) *clusters = g.ctas;
-    return "spec_slice_kernel";
+    if (clusters) *clusters = ctas;
+    return "spec_stats_kernel";
 }

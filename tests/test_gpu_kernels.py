@@ -1,9 +1,9 @@
 """GPU: the verifier's kernel and its grid, and spec_verify_round against the three calls.
 
-spec_verify launches one kernel, spec_slice_kernel: a persistent grid of one CTA per SM whose
-CTAs exchange published statistics through the workspace. These tests check the plan the
-library reports, that a workspace serves many calls of different shapes in a row (its counters
-return to zero and its epoch advances), and that the one-launch round equals the three calls.
+spec_verify launches two kernels: spec_stats_kernel (pass 1, a persistent grid that fills every
+SM) and spec_finish_kernel (decisions, pass 2, draws, selection). These tests check the plan the
+library reports, that a workspace serves many calls of different shapes in a row (the statistics
+kernel zeroes the finishing kernel's counters), and that the fused round equals the three calls.
 """
 import numpy as np
 import pytest
@@ -18,13 +18,15 @@ pytestmark = pytest.mark.gpu
 
 
 def test_plan_of_the_workloads():
-    """Every workload runs on the slice kernel, one CTA on every SM of the device."""
+    """Every workload's statistics kernel runs a persistent grid with the same number of CTAs on
+    every SM of the device."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for name in ("c1", "c2", "c3", "c4", "c5"):
         wl = W.WORKLOADS[name]
         rows = W.make_round(wl, seed=0, rnd=0, device="cuda").T
         kern, c, n = api.verify_plan(wl.B, wl.V, rows, wl.dtype)
-        assert (kern, c, n) == ("spec_slice_kernel", 1, sms), (name, kern, c, n)
+        assert kern == "spec_stats_kernel" and c == 1, (name, kern, c, n)
+        assert n >= sms and n % sms == 0, (name, n, sms)
 
 
 def test_invalid_shapes_have_no_plan():
@@ -34,9 +36,8 @@ def test_invalid_shapes_have_no_plan():
 
 
 def test_one_workspace_serves_many_calls():
-    """Rounds of different shapes through one workspace, sized for the largest: each call
-    leaves the counters at zero for the next, and the per-call tag keeps the previous call's
-    published words from being read as this call's."""
+    """Rounds of different shapes through one workspace, sized for the largest: the layout of
+    each call differs from the previous one's, and no call reads what an earlier one left."""
     big = W.scaled(W.WORKLOADS["c3"], B=24, V=32768)
     rd0 = W.make_round(big, seed=4, rnd=0, device="cuda")
     v = api.Verifier(rd0.B, rd0.target.shape[1], rd0.T, rd0.target.dtype, diagnostics=True)
