@@ -541,8 +541,15 @@ __global__ void __launch_bounds__(kStatsBlock) spec_stats_kernel(const __grid_co
     const long long u1 = min(total, (gw + 1) * per);
     int cur = -1;
     ItemDesc d = {};
-    for (long long u = gw * per; u < u1; ++u) {
-        const int item = static_cast<int>(u / P.nchunk), c = static_cast<int>(u % P.nchunk);
+    const long long ub = gw * per;
+    if (ub >= u1) return;
+    // (item, chunk) stepped without divisions
+    int item = static_cast<int>(ub / P.nchunk), c = static_cast<int>(ub % P.nchunk) - 1;
+    for (long long u = ub; u < u1; ++u) {
+        if (++c == P.nchunk) {
+            c = 0;
+            ++item;
+        }
         if (item != cur) {
             d = item_desc<DT>(P, item);
             cur = item;
@@ -1279,7 +1286,7 @@ __global__ void __launch_bounds__(kDecWarps * kWarp) spec_decide_kernel(const __
 // pieces (the item's values and decision read once per item). A chunk's alpha share goes to
 // alpha_c; at the request's frontier (its first rejection) its residual mass goes to zc.
 template <int DT>
-__global__ void __launch_bounds__(kFinBlock, 3) spec_pass2_kernel(const __grid_constant__ VerifyParams P) {
+__global__ void __launch_bounds__(kFinBlock, 4) spec_pass2_kernel(const __grid_constant__ VerifyParams P) {
     const int lane = static_cast<int>(threadIdx.x) % kWarp;
     griddep_wait();  // the statistics and decision kernels' output
     griddep_launch_dependents();
@@ -1294,8 +1301,15 @@ __global__ void __launch_bounds__(kFinBlock, 3) spec_pass2_kernel(const __grid_c
     bool work = false, frontier = false;
     ItemDesc d = {};
     ItemDec D = {};
-    for (long long u = gw * per; u < u1; ++u) {
-        const int item = static_cast<int>(u / P.nchunk), c = static_cast<int>(u % P.nchunk);
+    const long long ub = gw * per;
+    if (ub >= u1) return;
+    // (item, chunk) stepped without divisions
+    int item = static_cast<int>(ub / P.nchunk), c = static_cast<int>(ub % P.nchunk) - 1;
+    for (long long u = ub; u < u1; ++u) {
+        if (++c == P.nchunk) {
+            c = 0;
+            ++item;
+        }
         if (item != cur) {
             cur = item;
             d = P.desc[item];
