@@ -108,11 +108,15 @@ typedef struct {
     float *frontier_margin;      /* [B] distance of u*Z to the nearer end of the frontier
                                     token's CDF interval, over Z                                */
     int32_t *fallback;           /* [B] 1 when the residual had zero mass and p was used        */
-    /* profiling (may be NULL): two cudaEvent_t recorded on `stream` immediately before and after
-       the verifier's kernel (after the truncation kernel, when there is one), so a caller can
-       time that kernel alone */
+    /* profiling (each may be NULL): cudaEvent_t recorded on `stream` immediately before the
+       verifier's first kernel (after the truncation kernel, when there is one) and after its
+       last, so that a caller can time the verifier's kernels alone; stats_event_end is recorded
+       right after the first (per-chunk statistics) kernel, so that with rows_event_begin it
+       brackets that kernel alone. Recording it holds the next kernel back until the statistics
+       kernel has finished (no early launch), which costs the call a few microseconds. */
     cudaEvent_t rows_event_begin;
     cudaEvent_t rows_event_end;
+    cudaEvent_t stats_event_end;
     /* depth statistics ("M7.8 - Speculative Serving", sections 0x02D and 0x07B; each may be
        NULL): over the requests without status bits, depth j = 1..K_max (index j-1) was reached
        when K_i >= j and the first j-1 drafts were accepted, and accepted when A_i >= j. Written

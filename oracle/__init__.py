@@ -51,7 +51,7 @@ class _Result(ctypes.Structure):
         ("accept_len", _p), ("out_tokens", _p), ("n_emitted", _p), ("req_status", _p),
         ("alpha", _p), ("rho", _p), ("resid_mass", _p), ("accept_margin", _p),
         ("sample_margin", _p), ("sample_prob", _p), ("fallback", _p),
-        ("trunc_margin", _p), ("trunc_keep", _p),
+        ("trunc_margin", _p), ("trunc_keep", _p), ("resid_scale", _p), ("sample_cond", _p),
     ]
 
 
@@ -67,7 +67,8 @@ class _Compact(ctypes.Structure):
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (plain C11, -O2, no target-specific flags)."""
+    """Compile the oracle with gcc (plain C11, -O2, no target-specific flags), with OpenMP for
+    ``oracle_verify_threads`` where the compiler has it (else that entry runs serially)."""
     with _lock:
         stale = (not os.path.exists(_LIB_PATH)
                  or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC),
@@ -75,8 +76,11 @@ def build(force: bool = False) -> str:
         if force or stale:
             os.makedirs(_BUILD, exist_ok=True)
             tmp = _LIB_PATH + f".tmp{os.getpid()}"
-            subprocess.check_call(["gcc", "-std=c11", "-O2", "-Wall", "-fPIC", "-shared",
-                                   "-o", tmp, _SRC, "-lm"])
+            cmd = ["gcc", "-std=c11", "-O2", "-Wall", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+            try:
+                subprocess.check_call(cmd[:1] + ["-fopenmp"] + cmd[1:], stderr=subprocess.DEVNULL)
+            except subprocess.CalledProcessError:
+                subprocess.check_call(cmd)
             os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -87,6 +91,8 @@ def _load():
         lib = ctypes.CDLL(build())
         lib.oracle_verify.argtypes = [ctypes.POINTER(_Batch), ctypes.POINTER(_Result)]
         lib.oracle_verify.restype = ctypes.c_int
+        lib.oracle_verify_threads.argtypes = [ctypes.POINTER(_Batch), ctypes.POINTER(_Result), _i32]
+        lib.oracle_verify_threads.restype = ctypes.c_int
         lib.oracle_compact.argtypes = [ctypes.POINTER(_Compact)]
         lib.oracle_compact.restype = ctypes.c_int
         lib.oracle_gamma_objective.argtypes = [ctypes.c_double, ctypes.c_double, _i32]
@@ -120,11 +126,13 @@ def _c(a, dtype):
 
 
 def verify(target, draft, row_off, draft_tokens, uniforms, temperature, *, V=None,
-           K_max=64, stop_token=None, max_new=None, top_k=None, top_p=None):
+           K_max=64, stop_token=None, max_new=None, top_k=None, top_p=None, threads=None):
     """Run the verifier on host arrays.
 
     ``target``/``draft`` are 2-D float32 arrays, or uint16 arrays holding bfloat16 bits.
-    Returns a dict of numpy arrays named like the fields of ``oracle_result``.
+    Returns a dict of numpy arrays named like the fields of ``oracle_result``. With
+    ``threads=n`` the requests are split over up to n OpenMP threads (same results); the dict
+    then also holds ``threads_used``.
     """
     lib = _load()
     bf16 = target.dtype == np.uint16
@@ -155,14 +163,21 @@ def verify(target, draft, row_off, draft_tokens, uniforms, temperature, *, V=Non
         "sample_margin": np.zeros(B, np.float64), "sample_prob": np.zeros(B, np.float64),
         "fallback": np.zeros(B, np.int32),
         "trunc_margin": np.full(T, np.nan, np.float64), "trunc_keep": np.full(T, V, np.int32),
+        "resid_scale": np.zeros(nd, np.float64), "sample_cond": np.zeros(B, np.float64),
     }
     b = _Batch(B, V, K_max, 1 if bf16 else 0, _ptr(target), _ptr(draft), _ptr(row_off),
                _ptr(draft_tokens), _ptr(uniforms), _ptr(temperature), _ptr(stop_token),
                _ptr(max_new), _ptr(top_k), _ptr(top_p))
     r = _Result(*[_ptr(out[f]) for f, _ in _Result._fields_])
-    rc = lib.oracle_verify(ctypes.byref(b), ctypes.byref(r))
-    if rc != 0:
-        raise RuntimeError(f"oracle_verify failed: {rc}")
+    if threads is None:
+        rc = lib.oracle_verify(ctypes.byref(b), ctypes.byref(r))
+        if rc != 0:
+            raise RuntimeError(f"oracle_verify failed: {rc}")
+    else:
+        rc = lib.oracle_verify_threads(ctypes.byref(b), ctypes.byref(r), int(threads))
+        if rc < 1:
+            raise RuntimeError(f"oracle_verify_threads failed: {rc}")
+        out["threads_used"] = rc
     return out
 
 

@@ -11,6 +11,9 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* ---- reading logits --------------------------------------------------------------- */
 
@@ -208,9 +211,9 @@ static int32_t inverse_cdf(const double *w, int32_t V, double u, double *margin,
 
 /* ---- the verifier ---------------------------------------------------------------------- */
 
-int oracle_verify(const oracle_batch *in, oracle_result *out) {
-    const int32_t B = in->B, V = in->V;
-    if (B < 0 || V <= 0) return -1;
+/* Requests i0 .. i1-1 of the batch (each request is independent of the others). */
+static int verify_requests(const oracle_batch *in, oracle_result *out, int32_t i0, int32_t i1) {
+    const int32_t V = in->V;
     double *w = (double *)malloc(sizeof(double) * (size_t)V);
     row_law *Plaw = (row_law *)malloc(sizeof(row_law) * (size_t)(in->K_max + 1));
     row_law *Qlaw = (row_law *)malloc(sizeof(row_law) * (size_t)(in->K_max + 1));
@@ -221,7 +224,7 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
         return -2;
     }
 
-    for (int32_t i = 0; i < B; ++i) {
+    for (int32_t i = i0; i < i1; ++i) {
         const int32_t r0 = in->row_off[i];
         const int32_t K = in->row_off[i + 1] - r0 - 1;
         const int32_t d0 = r0 - i; /* first draft row of request i */
@@ -242,6 +245,7 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
         out->sample_margin[i] = NAN;
         out->sample_prob[i] = NAN;
         out->fallback[i] = 0;
+        if (out->sample_cond) out->sample_cond[i] = NAN;
         if (status) {
             for (int32_t j = 0; j < in->row_off[i + 1] - r0; ++j) out->out_tokens[r0 + j] = -1;
             for (int32_t j = 0; j < K; ++j) {
@@ -249,6 +253,7 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
                 out->rho[d0 + j] = NAN;
                 out->resid_mass[d0 + j] = NAN;
                 out->accept_margin[d0 + j] = NAN;
+                if (out->resid_scale) out->resid_scale[d0 + j] = NAN;
             }
             out->req_status[i] = status;
             continue;
@@ -285,6 +290,7 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
                 out->rho[d0 + j] = NAN;
                 out->resid_mass[d0 + j] = NAN;
                 out->accept_margin[d0 + j] = NAN;
+                if (out->resid_scale) out->resid_scale[d0 + j] = NAN;
             }
             continue;
         }
@@ -294,14 +300,16 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
         for (int32_t j = 0; j < K; ++j) {
             const row_law P = Plaw[j], Q = Qlaw[j];
             int32_t x = in->draft_tokens[d0 + j];
-            double a = 0.0, z = 0.0;
+            double a = 0.0, z = 0.0, zs = 0.0;
             for (int32_t v = 0; v < V; ++v) {
                 double p = row_prob(&P, v), q = row_prob(&Q, v);
                 a += (p < q ? p : q);
                 z += (p - q > 0.0 ? p - q : 0.0);
+                if (p > q) zs += p + q;
             }
             out->alpha[d0 + j] = a;
             out->resid_mass[d0 + j] = z;
+            if (out->resid_scale) out->resid_scale[d0 + j] = zs;
             if (P.greedy) {
                 /* Rule 1 has no ratio; report the accept test as 1/0. */
                 out->rho[d0 + j] = (x == P.argmax) ? 1.0 : 0.0;
@@ -341,6 +349,7 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
             if (T == 0.0) {
                 frontier = P.argmax; /* Rule 1: the correction is argmax p at the rejection */
                 out->sample_prob[i] = 1.0;
+                if (out->sample_cond) out->sample_cond[i] = 1.0;
                 break;
             }
             /* Rule 2 / step 3: resample from max(0, p - q), normalised. */
@@ -357,6 +366,18 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
                 for (int32_t v = 0; v < V; ++v) w[v] = row_prob(&P, v);
                 frontier = inverse_cdf(w, V, u_extra, &out->sample_margin[i],
                                        &out->sample_prob[i]);
+                if (out->sample_cond) out->sample_cond[i] = 1.0;
+            } else if (out->sample_cond) {
+                const double px = row_prob(&P, frontier), qx = row_prob(&Q, frontier);
+                double zs = 0.0, z = 0.0;
+                for (int32_t v = 0; v < V; ++v) {
+                    double p = row_prob(&P, v), q = row_prob(&Q, v);
+                    if (p > q) {
+                        zs += p + q;
+                        z += p - q;
+                    }
+                }
+                out->sample_cond[i] = (px + qx) / (px - qx) + zs / z;
             }
             break;
         }
@@ -371,6 +392,7 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
                 frontier = inverse_cdf(w, V, u_extra, &out->sample_margin[i],
                                        &out->sample_prob[i]);
             }
+            if (out->sample_cond) out->sample_cond[i] = 1.0;
         }
         out->out_tokens[r0 + A] = frontier;
         for (int32_t j = A + 1; j <= K; ++j) out->out_tokens[r0 + j] = -1;
@@ -396,6 +418,28 @@ int oracle_verify(const oracle_batch *in, oracle_result *out) {
     free(Plaw);
     free(Qlaw);
     return 0;
+}
+
+int oracle_verify(const oracle_batch *in, oracle_result *out) {
+    if (in->B < 0 || in->V <= 0) return -1;
+    return verify_requests(in, out, 0, in->B);
+}
+
+int oracle_verify_threads(const oracle_batch *in, oracle_result *out, int32_t n_threads) {
+    if (in->B < 0 || in->V <= 0 || n_threads < 1) return -1;
+#ifdef _OPENMP
+    int err = 0, used = 1;
+#pragma omp parallel num_threads(n_threads) reduction(| : err)
+    {
+#pragma omp single
+        used = omp_get_num_threads();
+#pragma omp for schedule(dynamic, 1)
+        for (int32_t i = 0; i < in->B; ++i) err |= (verify_requests(in, out, i, i + 1) != 0);
+    }
+    return err ? -2 : used;
+#else
+    return verify_requests(in, out, 0, in->B) == 0 ? 1 : -2;
+#endif
 }
 
 /* ---- compaction ---------------------------------------------------------------------- */

@@ -78,9 +78,25 @@ typedef struct {
                                    cumulative masses of the kept head and of the head one token
                                    shorter (when that has a token; NaN: no top-p cut)           */
     int32_t *trunc_keep;        /* [T] or NULL: tokens kept by top-k / top-p (V: all)          */
+    /* Conditioning of the residual quantities (diagnostics for comparing a float32 kernel; they
+     * take no part in any decision). A float32 p or q carries a relative error e, so
+     * p(v) - q(v) carries up to e (p(v) + q(v)): */
+    double *resid_scale;        /* [T-B] or NULL: sum over {v : p_j(v) > q_j(v)} of
+                                   p_j(v) + q_j(v); resid_scale / resid_mass is the relative
+                                   error bound of the residual mass per unit of e             */
+    double *sample_cond;        /* [B] or NULL: the same bound for sample_prob. A residual draw
+                                   of token x: (p(x) + q(x)) / (p(x) - q(x)) + resid_scale /
+                                   resid_mass of its row; a draw from p, or a greedy pick: 1;
+                                   NaN when no token was drawn                                 */
 } oracle_result;
 
 int oracle_verify(const oracle_batch *in, oracle_result *out);
+
+/* The same result computed with up to n_threads threads (OpenMP, requests split across them;
+ * each request is still computed by oracle_verify's own code, serially). Returns the number of
+ * threads used (1 when the library was built without OpenMP), or a negative error code. For
+ * timing the oracle on all of a host's cores. */
+int oracle_verify_threads(const oracle_batch *in, oracle_result *out, int32_t n_threads);
 
 typedef struct {
     int32_t B, page_size, max_blocks;

@@ -47,7 +47,7 @@ class SpecVerifyArgs(ctypes.Structure):
         ("accept_len", _p), ("n_emitted", _p), ("out_tokens", _p), ("req_status", _p),
         ("alpha_rows", _p), ("alpha_sum", _p), ("alpha_count", _p),
         ("rho_rows", _p), ("resid_rows", _p), ("frontier_prob", _p), ("frontier_margin", _p),
-        ("fallback", _p), ("rows_event_begin", _p), ("rows_event_end", _p),
+        ("fallback", _p), ("rows_event_begin", _p), ("rows_event_end", _p), ("stats_event_end", _p),
         ("depth_reached", _p), ("depth_accepted", _p),
         ("top_k", _p), ("top_p", _p),
     ]

@@ -140,12 +140,15 @@ class Verifier:
                       top_k, top_p)
         return self
 
-    def time_rows_with(self, begin, end):
-        """Record torch.cuda.Event pair `begin`/`end` around the per-position kernel on each
-        following run (None, None: stop)."""
-        self.args.rows_event_begin = ctypes.c_void_p(begin.cuda_event) if begin is not None else None
-        self.args.rows_event_end = ctypes.c_void_p(end.cuda_event) if end is not None else None
-        self._events = (begin, end)
+    def time_rows_with(self, begin, end, stats_end=None):
+        """On each following run, record torch.cuda.Event `begin` before the verifier's first
+        kernel, `end` after its last and `stats_end` after the statistics kernel (each may be
+        None; all None: stop)."""
+        ev = lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else None  # noqa: E731
+        self.args.rows_event_begin = ev(begin)
+        self.args.rows_event_end = ev(end)
+        self.args.stats_event_end = ev(stats_end)
+        self._events = (begin, end, stats_end)
 
     def run(self, stream=None) -> VerifyOutputs:
         rc = lib.spec_verify(ctypes.byref(self.args), ctypes.c_void_p(self.workspace.data_ptr()),

@@ -1,7 +1,8 @@
 // The verifier's kernels, launched back to back on one stream (included once, by spec_verify.cu):
-// spec_stats_kernel (pass 1 over every logit), spec_decide_kernel (every position's accept test),
-// spec_finish_kernel (pass 2, the frontier draws, the round's selection, and for spec_verify_round
-// its compaction and gamma choice).
+// spec_stats_kernel (pass 1 over every logit), spec_decide_kernel (every position's accept test and
+// each request's frontier), spec_pass2_kernel (pass 2 over the pairs: alpha, and the frontier's
+// residual), spec_finish_kernel (the frontier draws, the requests' selections, and in the CTA that
+// completes the batch its sums and, for spec_verify_round, the compaction and the gamma choice).
 //
 // The rule is that of "SOTA-227: Decode with a draft model and an accept-reject rule" ("What to
 // do", steps 3-4) and SDCP Rules 1 and 2 ("Acceptance Rules"): accept x_j when u_j <= p_j(x_j) /
@@ -18,23 +19,26 @@
 // lane, and reduces it to the chunk's statistics: per row an integral reference exponent and the
 // sum of 2^(y s - ref) (s = log2(e) / T), or under the greedy rule the max and its smallest index.
 // The lane whose vector holds the draft token also records (y_t - y_d) s there. A pair's rows are
-// loaded with an L2 evict-last hint: they are read again.
+// loaded with an L2 evict-last hint: pass 2 reads them again.
 //
-// spec_decide_kernel has one warp per item: it combines the item's chunk statistics (references
-// by exact powers of two) and decides the accept test.
+// spec_decide_kernel has one CTA per request and a warp per position: the warp combines the item's
+// chunk statistics (references by exact powers of two) and decides the accept test; the CTA then
+// marks the request's frontier, its first rejection or, with every draft accepted, its bonus row.
 //
-// spec_finish_kernel has one CTA per (item, part), a part being kPartChunks chunks of a row. For
-// a pair under Rule 2 each part reads its chunks of both rows again (from L2) for alpha = sum
-// min(p, q) and, at the request's frontier (its first rejection), the residual max(p - q, 0) per
-// chunk. The item's last part (a counter) draws the frontier's token: the chunk that holds u*Z by
-// a scan over the chunk masses, then the token within it. Later rejections need no residual and
-// no draw: nothing after the first rejection is emitted. The last item of a request runs the
-// request's selection (first rejection, emitted tokens, stopping); the last item of the batch the
-// batch-level results, and for a round the compaction and the gamma choice.
+// spec_pass2_kernel walks the pairs' chunks again like the statistics kernel (contiguous runs per
+// warp, from L2 where the rows stayed there): per chunk alpha = sum min(p, q) and, at the frontier,
+// the residual mass sum max(p - q, 0). Rejections after the first need no residual: nothing after
+// the first rejection is emitted.
+//
+// spec_finish_kernel has one warp per item: it sums the item's chunk shares, draws the frontier's
+// token (the chunk that holds u*Z by a scan over the chunk masses, then the token within it),
+// writes the item's results and counts the item for its request; the request's last item runs the
+// request's selection (first rejection, emitted tokens, stopping, its alpha into the batch's
+// fixed-point sums), and the CTA holding the batch's last item runs the batch's tail.
 //
 // Each kernel after the first is launched with programmatic stream serialisation: its CTAs may
 // start while the one before drains, and wait for it (griddepcontrol.wait) before reading anything
-// it wrote. The statistics kernel zeroes the finishing kernel's counters, so a workspace needs no
+// it wrote. The statistics kernel zeroes the later kernels' counters, so a workspace needs no
 // preparation between calls, whatever their shapes.
 //
 // The residual max(p - q, 0) is formed without cancellation: p (1 - 2^d) with d = log2(q/p) from

@@ -107,12 +107,13 @@ static cudaError_t stats_grid(int &ctas, int *p2 = nullptr) {
 }
 
 template <int DT>
-static spec_status launch_verify(const vk::VerifyParams &P, cudaStream_t stream) {
+static spec_status launch_verify(const vk::VerifyParams &P, cudaStream_t stream, cudaEvent_t stats_end) {
     int ctas = 0, p2_ctas = 0;
     if (stats_grid<DT>(ctas, &p2_ctas) != cudaSuccess) return SPEC_ERR_CUDA;
     if (ctas <= 0 || p2_ctas <= 0) return SPEC_ERR_UNSUPPORTED;
     vk::spec_stats_kernel<DT><<<ctas, vk::kStatsBlock, 0, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+    if (stats_end && cudaEventRecord(stats_end, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     if (launch_after(vk::spec_decide_kernel<DT>, dim3(static_cast<unsigned>(P.B)), dim3(vk::kDecWarps * kWarp), 0,
                      stream, P) != cudaSuccess)
         return SPEC_ERR_CUDA;
@@ -235,7 +236,8 @@ static spec_status verify_enqueue(const spec_verify_args *a, void *workspace, si
     }
 
     if (a->rows_event_begin && cudaEventRecord(a->rows_event_begin, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-    const spec_status st = (a->dtype == SPEC_BF16) ? launch_verify<SPEC_BF16>(P, stream) : launch_verify<SPEC_F32>(P, stream);
+    const spec_status st = (a->dtype == SPEC_BF16) ? launch_verify<SPEC_BF16>(P, stream, a->stats_event_end)
+                                                   : launch_verify<SPEC_F32>(P, stream, a->stats_event_end);
     if (st != SPEC_OK) return st;
     if (a->rows_event_end && cudaEventRecord(a->rows_event_end, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;

@@ -212,3 +212,34 @@ def test_round_argument_checks(lib):
     # a verify argument that spec_verify rejects is rejected here too
     c = _args(lib, alpha_sum=fake, alpha_count=fake, V=1001)
     assert f(ctypes.byref(c), ws, 1 << 20, ctypes.byref(good), 0.5, 0.1, 0, 8, fake, fake, None) == -4
+
+
+def test_ctypes_structs_match_the_header_layout():
+    """The binding's ctypes structs against the C compiler's layout of include/spec_verify.h:
+    every field at the same offset, and the same total size."""
+    import shutil
+    import subprocess
+    import tempfile
+
+    from speculative_decoding_verification_43_gb300 import _lib
+
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    if not shutil.which("gcc") or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers are missing")
+    inc = os.path.join(ROOT, "include")
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "spec_verify.h"', "int main(void) {"]
+    for cname, cls in (("spec_verify_args", _lib.SpecVerifyArgs), ("spec_compact_args", _lib.SpecCompactArgs)):
+        lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["return 0;", "}"]
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        open(src, "w").write("\n".join(lines))
+        subprocess.check_call(["gcc", "-std=c11", "-I", inc, "-I", cuda_inc, src, "-o", exe])
+        out = subprocess.check_output([exe], text=True)
+    got = {(a, b): int(c) for a, b, c in (ln.split() for ln in out.splitlines())}
+    for cname, cls in (("spec_verify_args", _lib.SpecVerifyArgs), ("spec_compact_args", _lib.SpecCompactArgs)):
+        assert got[(cname, "sizeof")] == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert got[(cname, f)] == getattr(cls, f).offset, (cname, f)

@@ -4,6 +4,9 @@ Sizes: the five workloads (c1 and c2 over many rounds; c3 in full; c4 and c5 at 
 the oracle run on a seeded sample of requests), plus smaller batches that still span several
 1024-token groups, several CTAs of a cluster and a ragged tail, and the edge cases of the rule.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -12,91 +15,112 @@ import oracle
 from speculative_decoding_verification_43_gb300 import api
 from speculative_decoding_verification_43_gb300 import workloads as W
 
-from parity import check_round, compare, run_gpu, run_oracle
+from parity import Report, check_round, compare, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
 
-def assert_report(rep, max_near_frac=0.5):
-    """No mismatch outside the band; the band itself is counted and printed. Every token of
-    probability below 2e-6 lies wholly inside the band, so flat distributions over large
-    vocabularies put a sizeable share of frontier draws there by construction."""
+def record(name, rep):
+    """Append the report's counts as one JSON line to the file named by SPEC_PARITY_COUNTS (when
+    set): the per-configuration table of requests, compared and band counts."""
+    path = os.environ.get("SPEC_PARITY_COUNTS")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(case=name, **rep.counts(), alpha_max_rel=rep.alpha_max_rel,
+                                    rho_max_rel=rep.rho_max_rel, resid_max_rel=rep.resid_max_rel,
+                                    prob_max_rel=rep.prob_max_rel)) + "\n")
+
+
+def assert_report(rep, max_near, name=None):
+    """No mismatch and no value failure outside the band. The band is the oracle's alone, so
+    its size is fixed by the seeded inputs: `max_near` bounds it per configuration at about
+    twice the oracle's own count on those inputs (plus one), so that a workload change that
+    pushes many draws into the band cannot pass unnoticed. A request that only the kernel's
+    margin would place in the band is compared all the same; at most one per case is expected
+    (its margin differs from the oracle's by rounding only)."""
     print(rep.summary())
+    if name:
+        record(name, rep)
     assert rep.ok(), (rep.mismatches[:5], rep.value_failures[:5])
-    assert rep.compared >= (1 - max_near_frac) * rep.requests, rep.summary()
+    assert rep.near_boundary <= max_near, rep.summary()
+    assert rep.gpu_near_only <= 1, rep.summary()
 
 
 def test_c1_all_rounds():
+    # the oracle's band count on these 100 rounds: 0
     wl = W.WORKLOADS["c1"]
-    near = 0
+    tot = Report()
     for rnd in range(wl.rounds):
         rd = W.make_round(wl, seed=0, rnd=rnd, device="cuda")
-        rep = check_round(rd)
-        assert rep.ok(), (rnd, rep.mismatches, rep.value_failures)
-        near += rep.near_boundary
-    print("c1 rounds", wl.rounds, "near", near)
-    assert near <= 0.1 * wl.rounds
+        tot.add(check_round(rd))
+    assert_report(tot, max_near=1, name="c1 (100 rounds)")
 
 
 def test_c2_rounds():
+    # the oracle's band count on these 60 rounds of 8 requests: 11
     wl = W.WORKLOADS["c2"]
-    near = compared = 0
+    tot = Report()
     for rnd in range(60):
         rd = W.make_round(wl, seed=0, rnd=rnd, device="cuda")
-        rep = check_round(rd)
-        assert rep.ok(), (rnd, rep.mismatches[:3], rep.value_failures[:3])
-        near += rep.near_boundary
-        compared += rep.compared
-    print("c2 compared", compared, "near", near)
-    assert near <= 0.1 * (compared + near)
+        tot.add(check_round(rd))
+    assert_report(tot, max_near=23, name="c2 (60 rounds)")
 
 
 def test_c3_full_batch():
+    # the oracle's band count on this round: 1 of 64
     wl = W.WORKLOADS["c3"]
     rd = W.make_round(wl, seed=0, rnd=0, device="cuda")
-    assert_report(check_round(rd))
+    assert_report(check_round(rd), max_near=3, name="c3")
 
 
-@pytest.mark.parametrize("name,n_sample", [("c4", 24), ("c5", 64)])
-def test_full_size_sampled(name, n_sample):
+# the oracle's band counts on these samples: 1 of 24 (c4) and 10 of 64 (c5: flat Zipf tails over
+# 256000 tokens)
+@pytest.mark.parametrize("name,n_sample,max_near", [("c4", 24, 3), ("c5", 64, 21)])
+def test_full_size_sampled(name, n_sample, max_near):
     wl = W.WORKLOADS[name]
     rd = W.make_round(wl, seed=0, rnd=0, device="cuda")
     rng = np.random.default_rng(7)
     reqs = sorted(rng.choice(rd.B, size=n_sample, replace=False).tolist())
-    assert_report(check_round(rd, reqs))
+    assert_report(check_round(rd, reqs), max_near=max_near, name=f"{name} (sample of {n_sample})")
 
 
-@pytest.mark.parametrize("dtype,V,B,Kspec,T", [
-    (torch.bfloat16, 50264, 40, "uniform:0:8", 0.8),    # several groups per CTA, ragged tail
-    (torch.float32, 12348, 24, "uniform:0:6", 1.3),     # fp32, ragged
-    (torch.bfloat16, 1032, 12, "uniform:0:4", 1.0),     # one CTA, partial group
-    (torch.float32, 8, 9, "uniform:0:3", 0.9),          # V smaller than one vector group
-    (torch.bfloat16, 262144, 6, "uniform:1:3", 1.0),    # large V, the largest cluster
+# the oracle's band counts over the three rounds of each shape: 6, 2, 0, 0, 2
+@pytest.mark.parametrize("dtype,V,B,Kspec,T,max_near", [
+    (torch.bfloat16, 50264, 40, "uniform:0:8", 0.8, 13),   # many chunks per row, ragged tail
+    (torch.float32, 12348, 24, "uniform:0:6", 1.3, 5),     # fp32, ragged
+    (torch.bfloat16, 1032, 12, "uniform:0:4", 1.0, 1),     # one partial chunk per row
+    (torch.float32, 8, 9, "uniform:0:3", 0.9, 1),          # V smaller than one vector per lane
+    (torch.bfloat16, 262144, 6, "uniform:1:3", 1.0, 5),    # large V: flat rows over 2^18 tokens
 ])
-def test_shapes(dtype, V, B, Kspec, T):
+def test_shapes(dtype, V, B, Kspec, T, max_near):
     base = W.Workload("t", B=B, V=V, dtype=dtype, temperature=T, logits="normal", sigma=2.0,
                       draft_sigma=0.7, K=Kspec)
+    tot = Report()
     for rnd in range(3):
         rd = W.make_round(base, seed=11, rnd=rnd, device="cuda")
-        assert_report(check_round(rd))
+        tot.add(check_round(rd))
+    assert_report(tot, max_near=max_near, name=f"shape {str(dtype)[6:]} V={V} B={B} K~{Kspec} T={T} (3 rounds)")
 
 
 def test_zipf_small_vocab_many_rounds():
+    # the oracle's band count over these 8 rounds of 32 requests: 1
     base = W.scaled(W.WORKLOADS["c3"], B=32, V=8192)
+    tot = Report()
     for rnd in range(8):
         rd = W.make_round(base, seed=3, rnd=rnd, device="cuda")
-        assert_report(check_round(rd), max_near_frac=0.2)
+        tot.add(check_round(rd))
+    assert_report(tot, max_near=3, name="c3 head at B=32 V=8192 (8 rounds)")
 
 
 def test_k0_only_and_max_k():
     base = W.Workload("t", B=16, V=4096, dtype=torch.bfloat16, temperature=1.0, logits="normal",
                       sigma=2.0, draft_sigma=0.5, K="fixed:0")
     rd = W.make_round(base, seed=5, device="cuda")
-    assert_report(check_round(rd))
+    assert_report(check_round(rd), max_near=3, name="k0_only_and_max_k#1")  # oracle: 1
     base = W.Workload("t", B=2, V=2048, dtype=torch.float32, temperature=1.0, logits="normal",
                       sigma=1.0, draft_sigma=0.2, K="fixed:64")
     rd = W.make_round(base, seed=6, device="cuda")
-    assert_report(check_round(rd))
+    assert_report(check_round(rd), max_near=1, name="k0_only_and_max_k#2")  # oracle: 0
 
 
 def test_forced_accept_all_and_reject_first():
@@ -112,7 +136,7 @@ def test_forced_accept_all_and_reject_first():
     gpu = run_gpu(rd)
     assert (gpu["accept_len"][0::2] == K).all()
     rep = check_round(rd)
-    assert_report(rep)
+    assert_report(rep, max_near=1, name="forced_accept_all_and_reject_first#1")  # oracle: 0
 
 
 def test_greedy_and_mixed_temperatures():
@@ -120,11 +144,11 @@ def test_greedy_and_mixed_temperatures():
                       sigma=2.0, draft_sigma=0.6, K="uniform:0:5")
     temps = np.array([0.0, 0.5, 1.0, 2.0] * 3, np.float32)
     rd = W.make_round(base, seed=9, device="cuda", temperature=temps)
-    assert_report(check_round(rd))
+    assert_report(check_round(rd), max_near=1, name="greedy_and_mixed_temperatures#1")  # oracle: 0
     # greedy rows with ties: the smallest index wins on both sides
     rd.target[:, 17] = 100.0
     rd.target[:, 3] = 100.0
-    assert_report(check_round(rd))
+    assert_report(check_round(rd), max_near=1, name="greedy_and_mixed_temperatures#2")  # oracle: 0
 
 
 def _resample_drafts(rd, seed):
@@ -172,7 +196,7 @@ def test_wide_logit_ranges(dtype, V):
     rd.target = tz.to(dtype).contiguous()
     rd.draft = dz.to(dtype).contiguous()
     _resample_drafts(rd, 17)
-    assert_report(check_round(rd))
+    assert_report(check_round(rd), max_near=1, name=f"wide_logit_ranges V={V}")  # oracle: 0 and 0
 
 
 def test_bad_requests():
@@ -188,7 +212,7 @@ def test_bad_requests():
     rd.draft[8 * 3 + 1, :] = float("-inf")                 # request 8: a draft row with no mass
     rd.temperature[9] = -1.0                               # request 9: bad temperature
     rep = check_round(rd)
-    assert_report(rep)
+    assert_report(rep, max_near=1, name="bad_requests#1")  # oracle: 0
     gpu = run_gpu(rd)
     assert gpu["req_status"][1] == api._lib.REQ_BAD_LOGITS
     assert gpu["req_status"][3] == api._lib.REQ_BAD_PROPOSAL
@@ -207,7 +231,7 @@ def test_k_max_exceeded_is_bad_shape():
     for i, k in enumerate(rd.K):
         assert (gpu["req_status"][i] == api._lib.REQ_BAD_SHAPE) == (k > 3)
     rep = check_round(rd, K_max=3)
-    assert_report(rep)
+    assert_report(rep, max_near=1, name="k_max_exceeded_is_bad_shape#1")  # oracle: 0
 
 
 def test_stop_token_and_budget():
@@ -227,7 +251,7 @@ def test_stop_token_and_budget():
     stop_t = torch.as_tensor(stop, device="cuda")
     budget_t = torch.as_tensor(budget, device="cuda")
     rep = check_round(rd, stop_token=stop_t, max_new=budget_t)
-    assert_report(rep)
+    assert_report(rep, max_near=1, name="stop_token_and_budget#1")  # oracle: 0
 
 
 def test_determinism():
@@ -374,9 +398,12 @@ def _trunc_params(B, V, seed):
     return top_k, top_p
 
 
-@pytest.mark.parametrize("dtype,V,logits", [(torch.bfloat16, 32000, "zipf"), (torch.float32, 20000, "normal"),
-                                            (torch.bfloat16, 128256, "zipf")])
-def test_top_k_top_p(dtype, V, logits):
+# the oracle's band counts: 10, 12 and 7 (a target row whose top-p cut lies within 1e-5 of top_p
+# counts as well as the draws)
+@pytest.mark.parametrize("dtype,V,logits,max_near", [(torch.bfloat16, 32000, "zipf", 21),
+                                                     (torch.float32, 20000, "normal", 25),
+                                                     (torch.bfloat16, 128256, "zipf", 15)])
+def test_top_k_top_p(dtype, V, logits, max_near):
     """Top-k then top-p of the target law (SDCP "Session Model"): the cut of each target row by
     the truncation kernel, the masked rows in the per-position kernel, every draw of the
     truncated law. Some requests use the greedy rule, which ignores truncation."""
@@ -387,7 +414,7 @@ def test_top_k_top_p(dtype, V, logits):
     temp[::11] = 0.0
     rd.temperature = temp
     top_k, top_p = _trunc_params(rd.B, V, 7)
-    assert_report(check_round(rd, top_k=top_k, top_p=top_p))
+    assert_report(check_round(rd, top_k=top_k, top_p=top_p), max_near=max_near, name=f"top_k_top_p V={V}")
 
 
 def test_top_k_cuts_inside_ties():
@@ -400,7 +427,7 @@ def test_top_k_cuts_inside_ties():
     top_k = torch.as_tensor(np.random.default_rng(2).integers(1, 400, rd.B).astype(np.int32), device="cuda")
     top_p = torch.full((rd.B,), 0.9, dtype=torch.float32, device="cuda")
     top_p[::2] = 1.0
-    assert_report(check_round(rd, top_k=top_k, top_p=top_p))
+    assert_report(check_round(rd, top_k=top_k, top_p=top_p), max_near=5, name="top_k_cuts_inside_ties#1")  # oracle: 2
 
 
 def test_nan_top_p_is_a_bad_parameter_on_device():
@@ -427,4 +454,4 @@ def test_all_64_drafts_accepted():
     gpu = run_gpu(rd)
     assert (gpu["accept_len"] == 64).all() and (gpu["n_emitted"] == 65).all()
     assert (gpu["out_tokens"].reshape(rd.B, 65) >= 0).all()
-    assert_report(check_round(rd), max_near_frac=0.7)
+    assert_report(check_round(rd), max_near=1, name="all_64_drafts_accepted")

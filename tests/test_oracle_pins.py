@@ -228,6 +228,56 @@ def test_residual_draw_switches_at_cdf_boundaries():
     np.testing.assert_allclose(o["resid_mass"][0], r.sum(), rtol=1e-12)
 
 
+def test_residual_conditioning_closed_forms():
+    """The conditioning diagnostics on rows whose residual is known in closed form."""
+    # p = (3/4, 1/4), q = (1/2, 1/2): draft token 1 has rho = 1/2, u = 0.9 rejects; the residual
+    # is (1/4, 0), Z = 1/4, its support {0} carries p + q = 5/4; the drawn token 0 has
+    # (p + q) / (p - q) = 5 and Z's own bound is (5/4) / (1/4) = 5.
+    o = single([[np.log(3.0), 0.0], [0.0, 0.0]], [[0.0, 0.0]], [1], [0.9, 0.3])
+    assert o["accept_len"][0] == 0 and o["out_tokens"][0] == 0
+    np.testing.assert_allclose(o["resid_mass"][0], 0.25, rtol=1e-6)
+    np.testing.assert_allclose(o["resid_scale"][0], 1.25, rtol=1e-6)
+    np.testing.assert_allclose(o["sample_cond"][0], 10.0, rtol=1e-5)
+    # disjoint supports: p = (1, 0), q = (0, 1); the residual is p itself, every bound is 1
+    o = single([[0.0, -np.inf], [0.0, 0.0]], [[-np.inf, 0.0]], [1], [0.5, 0.7])
+    assert o["accept_len"][0] == 0 and o["out_tokens"][0] == 0
+    assert o["resid_mass"][0] == 1.0 and o["resid_scale"][0] == 1.0 and o["sample_cond"][0] == 2.0
+    # identical rows: no residual at all (Z = 0, empty support); the bonus draw is from p
+    tz, _ = rows_example(V=6, K=1, seed=25)
+    o = single(tz, tz[:1], [2], [0.999, 0.4])
+    assert o["accept_len"][0] == 1
+    assert o["resid_mass"][0] == 0.0 and o["resid_scale"][0] == 0.0 and o["sample_cond"][0] == 1.0
+    # greedy picks and bad requests
+    o = single(tz, tz[:1] + 1.0, [int(np.argmax(tz[0])) ^ 1], [0.5, 0.5], T=0.0)
+    assert o["accept_len"][0] == 0 and o["sample_cond"][0] == 1.0
+    o = single(tz, tz[:1], [9], [0.5, 0.5])
+    assert o["req_status"][0] == oracle.REQ_BAD_PROPOSAL
+    assert np.isnan(o["sample_cond"][0]) and np.isnan(o["resid_scale"][0])
+
+
+def test_resid_scale_is_the_positive_part_support_mass():
+    tz, dz = rows_example(V=9, K=3, seed=26)
+    p, q = law(tz, 0.8), law(dz, 0.8)
+    o = single(tz, dz, [0, 1, 2], [0.1, 0.2, 0.3, 0.4], T=0.8)
+    want = np.where(p[:3] > q, p[:3] + q, 0.0).sum(axis=1)
+    np.testing.assert_allclose(o["resid_scale"], want, rtol=1e-12)
+    # the bound is never below 1: the support's p + q is at least its p - q
+    assert (o["resid_scale"] >= o["resid_mass"]).all()
+
+
+def test_threaded_oracle_equals_serial():
+    """The OpenMP split over requests changes nothing: every output, bit for bit."""
+    tz, dz, row_off, toks, u, K = ragged_batch(40, 30, 5, seed=57)
+    temp = np.linspace(0.0, 1.3, 40).astype(np.float32)
+    dz[row_off[3] - 3] = np.nan if K[3] > 0 else dz[row_off[3] - 3]
+    a = oracle.verify(tz, dz, row_off, toks, u, temp, top_k=7, top_p=0.8)
+    b = oracle.verify(tz, dz, row_off, toks, u, temp, top_k=7, top_p=0.8, threads=4)
+    assert b.pop("threads_used") >= 1
+    assert a.keys() == b.keys()
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
 def test_bonus_draw_uses_last_target_row_and_sample_slot():
     tz, dz = rows_example(V=6, K=3, seed=23)
     p = law(tz, 0.9)

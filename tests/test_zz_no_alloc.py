@@ -52,6 +52,33 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert int(nal.out.alpha_count.item()) == int(ref.out.alpha_count.item())
 
 
+def test_noalloc_at_its_row_limit():
+    """Exactly the largest batch the fixed scratch takes (16384 target rows, here 2048 requests of
+    seven drafts over a 2048-token vocabulary): accepted, and equal to the workspace entry point."""
+    from speculative_decoding_verification_43_gb300 import _lib, api
+    from speculative_decoding_verification_43_gb300 import workloads as W
+    wl = W.Workload("limit", B=2048, V=2048, dtype=torch.bfloat16, temperature=0.9, logits="normal",
+                    sigma=2.0, draft_sigma=0.6, K="fixed:7")
+    rd = W.make_round(wl, seed=5, rnd=0, device="cuda")
+    assert rd.T == _lib.NOALLOC_MAX_ROWS == 16384
+    stream = torch.cuda.current_stream()
+    ref = api.Verifier(rd.B, rd.target.shape[1], rd.T, rd.target.dtype, diagnostics=True)
+    ref.bind(rd.target, rd.draft, rd.row_off, rd.draft_tokens, rd.uniforms, rd.temperature)
+    ref.run(stream)
+    nal = api.Verifier(rd.B, rd.target.shape[1], rd.T, rd.target.dtype, diagnostics=True)
+    nal.bind(rd.target, rd.draft, rd.row_off, rd.draft_tokens, rd.uniforms, rd.temperature)
+    for name in ("accept_len", "out_tokens", "req_status", "n_emitted"):
+        getattr(nal.out, name).fill_(-7)
+    _run_noalloc(_lib, nal, stream)
+    torch.cuda.synchronize()
+    assert (ref.out.req_status == 0).all()
+    for name in ("accept_len", "n_emitted", "out_tokens", "req_status", "fallback"):
+        np.testing.assert_array_equal(getattr(nal.out, name).cpu().numpy(),
+                                      getattr(ref.out, name).cpu().numpy(), err_msg=name)
+    np.testing.assert_array_equal(nal.out.alpha_rows.cpu().numpy(), ref.out.alpha_rows.cpu().numpy())
+    assert int(nal.out.alpha_count.item()) == int(ref.out.alpha_count.item()) == rd.T - rd.B
+
+
 def test_noalloc_rejects_batches_beyond_its_scratch():
     from speculative_decoding_verification_43_gb300 import _lib, api
     T = _lib.NOALLOC_MAX_ROWS + 1
