@@ -61,8 +61,9 @@ enum {
     SPEC_REQ_BAD_SHAPE = 4,    /* K_i < 0, K_i > K_max, or row_off inconsistent               */
     SPEC_REQ_BAD_PARAM = 8,    /* temperature NaN, infinite or negative, or top_p NaN         */
     SPEC_REQ_BAD_BLOCKS = 16,  /* spec_compact: a committed position has no page             */
-    SPEC_REQ_TIMEOUT = 32      /* the request's positions were not all finished when the batch
-                                  was (an internal fault; not produced on a healthy device) */
+    SPEC_REQ_TIMEOUT = 32      /* a bounded wait inside the verifier gave up before the request's
+                                  data was ready; the request emits nothing (an internal fault,
+                                  never produced on a healthy device)                          */
 };
 
 /* ---- spec_verify ------------------------------------------------------------------------
