@@ -21,6 +21,8 @@ Prints one JSON line:
   e2e         the same step through the public API from pinned host memory and back, with the
               next step's input copy and the previous step's result copy on two copy streams
               overlapping the current step's kernels;
+  truncation  the cost of top-k 50 then top-p 0.9 on every request (SDCP "Session Model"):
+              spec_verify calls with and without, timed whole;
   cpu_baseline the float64 oracle on this host: one thread, and all cores (OpenMP over
               requests).
 
@@ -76,6 +78,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--truncation", type=int, default=1, help="also time top-k 50 / top-p 0.9 calls (1: yes)")
     return ap.parse_args()
 
 
@@ -394,6 +397,37 @@ def time_kernels(verifiers, stream, n):
     return loop(False), loop(True)
 
 
+def time_truncation(sets, stream, dev, n, top_k=50, top_p=0.9):
+    """spec_verify with top-k then top-p on every request, against the same calls without: CUDA
+    events around each whole call (the truncation kernel included), input sets rotating."""
+    from speculative_decoding_verification_43_gb300 import api
+    res = {}
+    for label, trunc in (("plain", False), ("truncated", True)):
+        vs = []
+        for rd in sets:
+            v = api.Verifier(rd.B, rd.target.shape[1], rd.T, rd.target.dtype, device=dev)
+            kw = {}
+            if trunc:
+                kw = dict(top_k=torch.full((rd.B,), top_k, dtype=torch.int32, device=dev),
+                          top_p=torch.full((rd.B,), top_p, dtype=torch.float32, device=dev))
+            v.bind(rd.target, rd.draft, rd.row_off, rd.draft_tokens, rd.uniforms, rd.temperature, **kw)
+            vs.append(v)
+        for v in vs:
+            v.run(stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize(dev)
+        for k, (b, e) in enumerate(evs):
+            b.record(stream)
+            vs[k % len(vs)].run(stream)
+            e.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = [b.elapsed_time(e) for b, e in evs]
+        res[label] = statistics.fmean(ms)
+    return {"top_k": top_k, "top_p": top_p, "calls": n, "call_ms_mean": res["truncated"],
+            "plain_call_ms_mean": res["plain"], "extra_us": 1e3 * (res["truncated"] - res["plain"]),
+            "timing": "CUDA events around each spec_verify call (truncation kernel included)"}
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -449,6 +483,7 @@ def run_ours(args):
 
     # the statistics (dominant) kernel and the verifier, launch by launch
     ver_ms, stats_ms = time_kernels(verifiers, stream, KERNEL_LAUNCHES)
+    trunc = time_truncation(sets, stream, dev, KERNEL_LAUNCHES) if args.truncation else None
 
     # acceptance of the timed inputs (set 0, as every step computed it)
     step(0)
@@ -492,6 +527,7 @@ def run_ours(args):
         "verifier": {"kernels": 4, **vr, "achieved_gbs": v_achieved, "frac": v_achieved / peak,
                      "timing": "CUDA events around spec_verify's four kernels, launch by launch"},
         "acceptance": acceptance,
+        "truncation": trunc,
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,  # per step: statistics, decisions, pass 2, finishing
         "clocks": clk,

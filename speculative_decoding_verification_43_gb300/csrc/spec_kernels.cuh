@@ -197,6 +197,24 @@ __device__ __forceinline__ float vec_elem(const uint4 &w, int e) {
 // which turns every later sum, ratio and draw into those of the truncated, renormalised law.
 template <int DT>
 __device__ __forceinline__ void mask_cut(uint4 &w, int vi, uint32_t tau, int id) {
+    // a vector wholly below the cut's logit (the common case after top-k) becomes -inf at once;
+    // the largest element is taken with NaN propagating, so a NaN always takes the exact test
+    // below and stays (it makes the row invalid)
+    float vm, ct;
+    if (DT == SPEC_BF16) {
+        const uint32_t m = bf16x2_max_nan(bf16x2_max_nan(w.x, w.y), bf16x2_max_nan(w.z, w.w));
+        vm = fmax_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+        const uint32_t b = (tau & 0x8000u) ? (tau & 0x7FFFu) : (~tau & 0xFFFFu);
+        ct = __uint_as_float(b << 16);
+    } else {
+        vm = fmax_nan(fmax_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
+                      fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
+        ct = __uint_as_float((tau & 0x80000000u) ? (tau & 0x7FFFFFFFu) : ~tau);
+    }
+    if (vm < ct) {
+        w = kNegInfVec<DT>();
+        return;
+    }
     uint32_t x[4] = {w.x, w.y, w.z, w.w};
     if (DT == SPEC_BF16) {
         const int base = vi * 8;
@@ -423,7 +441,10 @@ __device__ __noinline__ float2 row_sum_exact(uint4 v0, uint4 v1, uint4 v2, uint4
 template <int DT>
 __device__ __forceinline__ float2 row_sum(const uint4 (&v)[kVPT], float s_hi, float s_lo) {
     const float2 shi2 = f2splat(s_hi), slo2 = f2splat(s_lo);
-    const float b = floorf(Elt<DT>::vmax(v[0]) * s_hi);
+    // an all -inf first vector (masked vocabulary, a truncated row) takes 0 as its reference,
+    // which keeps its -inf terms at 0 instead of sending the warp to the exact form
+    const float m0 = Elt<DT>::vmax(v[0]);
+    const float b = (m0 == -INFINITY) ? 0.0f : floorf(m0 * s_hi);
     float s = 0.0f;
 #pragma unroll
     for (int k = 0; k < kVPT; ++k) s += vec_sum<DT>(v[k], shi2, slo2, b);

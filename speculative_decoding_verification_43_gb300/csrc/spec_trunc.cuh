@@ -10,8 +10,13 @@
 // kernel reads the cut and treats every other token of the row as a -inf logit, which is the
 // truncated, renormalised law.
 //
-// One CTA per target row: a radix select over the key, eight bits per pass, on counts (top-k)
-// or on masses (top-p), then an ordered search among the tokens tied at the cut. Masses are
+// One CTA per target row. With top-k of at most kTruncThreads tokens, two passes: each thread's
+// largest key, whose k-th largest over the CTA bounds the row's top-k set from below (at least k
+// tokens reach it); then every token at or above that bound is gathered into shared memory and
+// sorted (bitonic, by key then id), which gives the top-k cut exactly and, for top-p, the masses
+// of the top-k set in rank order for a prefix scan. Otherwise (no top-k, a larger k, or more
+// candidates than fit): a radix select over the key, eight bits per pass, on counts (top-k) or
+// on masses (top-p), then an ordered search among the tokens tied at the cut. Masses are
 // 2^((z - z_max) s) in fixed point (2^-40 units, 64-bit integer sums): the sums, and so the cut,
 // do not depend on the order of the atomic additions. Rows are read as 16-byte vectors; a row
 // stays in L2 across its passes (bf16 V = 128256: about six passes over 256 KB).
@@ -83,8 +88,15 @@ __device__ __forceinline__ void for_each_key(const uint4 *row, int nv, int tid, 
     }
 }
 
+constexpr int kCandCap = 4096;  // candidates the two-pass top-k path holds (a power of two)
+
 // Shared state of one row's selection.
 struct TruncShared {
+    unsigned long long cand[kCandCap];  // (key << 32) | (0xFFFFFFFF - id): larger ranks first
+    uint32_t tmax[kTruncThreads];   // each warp's 32 thread maxima, sorted descending
+    uint32_t bound;
+    unsigned long long scan[kTruncWarps];
+    uint32_t ncand;
     uint32_t hist[256];
     unsigned long long hmass[256];
     uint32_t wsum[kTruncWarps];
@@ -280,6 +292,194 @@ struct FixedMass {
     }
 };
 
+// Sorts a[0 .. n) (n a power of two, at most kCandCap) into descending order, the whole CTA.
+template <class T>
+__device__ __forceinline__ void bitonic_desc(T *a, int n, int tid) {
+    for (int size = 2; size <= n; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < n / 2; i += kTruncThreads) {
+                // the pair (lo, lo + stride) of comparator i
+                const int lo = 2 * stride * (i / stride) + (i % stride);
+                const int hi = lo + stride;
+                const bool desc = ((lo & size) == 0);
+                const T x = a[lo], y = a[hi];
+                if (desc ? (x < y) : (x > y)) {
+                    a[lo] = y;
+                    a[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Block-wide inclusive scan of one value per thread (every thread gets its prefix and the total).
+__device__ __forceinline__ unsigned long long block_scan_u64(TruncShared &sh, unsigned long long v, int tid,
+                                                             unsigned long long &total) {
+    const int lane = tid & 31, wp = tid >> 5;
+    unsigned long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh.scan[wp] = x;
+    __syncthreads();
+    unsigned long long before = 0ull;
+    total = 0ull;
+    for (int w = 0; w < kTruncWarps; ++w) {
+        const unsigned long long t = sh.scan[w];
+        if (w < wp) before += t;
+        total += t;
+    }
+    __syncthreads();
+    return before + x;
+}
+
+// The two-pass cut for top-k with k <= kTruncThreads (then top-p over the top-k set when use_p).
+// Returns false, with nothing written, when the candidates at or above the bound exceed
+// kCandCap (many tokens tied near the k-th key); the radix path then takes the row.
+template <int DT>
+__device__ bool cut_small_k(TruncShared &sh, const uint4 *row, int nv, int k, bool use_p, float tp, float T,
+                            int tid, int2 &cut) {
+    constexpr int E = TruncElt<DT>::kPerVec;
+    const int lane = tid & 31;
+    // pass 1: each thread's largest key (the key of its largest logit, NaN ignored: a row holding
+    // a NaN is invalid whatever its cut); four loads in flight per thread
+    float mx = -INFINITY;
+    bool any = false;
+    for (int i0 = tid; i0 < nv; i0 += 4 * kTruncThreads) {
+        uint4 w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = i0 + q * kTruncThreads;
+            w[q] = i < nv ? __ldg(row + i) : kNegInfVec<DT>();
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mx = fmaxf(mx, Elt<DT>::vmax(w[q]));
+        any = true;
+    }
+    uint32_t mk = any ? (DT == SPEC_BF16 ? key_bf16(__float_as_uint(mx) >> 16) : key_f32(__float_as_uint(mx))) : 0u;
+    // each warp sorts its 32 maxima (descending, by shuffles); then the k-th largest of all 512
+    // is the value with fewer than k larger and at least k not smaller, found by binary searches
+    // in the 16 sorted lists
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xffffffffu, mk, stride);
+            const bool lower = (lane & stride) == 0;   // this lane holds the pair's first slot
+            const bool desc = (lane & size) == 0;      // this run sorts descending
+            const uint32_t hi = max(mk, o), lo = min(mk, o);
+            mk = (lower == desc) ? hi : lo;
+        }
+    }
+    const int wp = tid >> 5;
+    sh.tmax[wp * 32 + lane] = mk;
+    if (tid == 0) {
+        sh.ncand = 0u;
+        sh.bound = 0u;
+    }
+    __syncthreads();
+    {
+        uint32_t gt = 0u, ge = 0u;  // values > mk and >= mk over all lists
+        for (int l = 0; l < kTruncWarps; ++l) {
+            const uint32_t *a = sh.tmax + l * 32;
+            int lo = 0, hi = 32;  // count of a[j] > mk (a descending)
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (a[mid] > mk) lo = mid + 1; else hi = mid;
+            }
+            gt += static_cast<uint32_t>(lo);
+            hi = 32;              // count of a[j] >= mk
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (a[mid] >= mk) lo = mid + 1; else hi = mid;
+            }
+            ge += static_cast<uint32_t>(lo);
+        }
+        if (gt < static_cast<uint32_t>(k) && static_cast<uint32_t>(k) <= ge) sh.bound = mk;  // the same value
+    }
+    __syncthreads();
+    // at least k tokens (the k largest thread maxima) have a key >= L
+    const uint32_t L = sh.bound;
+    // pass 2: every token with key >= L, appended warp by warp; a vector whose largest logit lies
+    // below L's is skipped whole (a NaN never reaches L: NaN compares false)
+    const float Lz = TruncElt<DT>::logit(L);
+    for (int base = tid & ~31; base < nv; base += 2 * kTruncThreads) {  // warp-uniform
+        uint4 w2[2];
+        bool ok2[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = base + q * kTruncThreads + lane;
+            ok2[q] = i < nv;
+            w2[q] = ok2[q] ? __ldg(row + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = base + q * kTruncThreads + lane;
+            const uint4 w = w2[q];
+            const bool ok = ok2[q];
+            if (!__any_sync(0xffffffffu, ok && Elt<DT>::vmax(w) >= Lz)) continue;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const uint32_t key = TruncElt<DT>::key(w, e);
+                const bool in = ok && key >= L;
+                const unsigned m = __ballot_sync(0xffffffffu, in);
+                if (m == 0u) continue;
+                uint32_t at = 0u;
+                if (lane == __ffs(m) - 1) at = atomicAdd(&sh.ncand, static_cast<uint32_t>(__popc(m)));
+                at = __shfl_sync(0xffffffffu, at, __ffs(m) - 1) + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+                if (in && at < static_cast<uint32_t>(kCandCap)) {
+                    const uint32_t id = static_cast<uint32_t>(i * E + e);
+                    sh.cand[at] = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - id);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int n = static_cast<int>(sh.ncand);
+    if (n > kCandCap) return false;  // uniform across the CTA
+    if (n <= kTruncThreads) {
+        // rank by counting (the candidates are distinct): thread t places candidate t
+        const unsigned long long c = tid < n ? sh.cand[tid] : 0ull;
+        int rank = 0;
+        for (int j = 0; j < n; ++j) rank += sh.cand[j] > c ? 1 : 0;
+        __syncthreads();
+        if (tid < n) sh.cand[rank] = c;
+        __syncthreads();
+    } else {
+        int np = 1;
+        while (np < n) np <<= 1;
+        for (int j = n + tid; j < np; j += kTruncThreads) sh.cand[j] = 0ull;  // ranks below every token
+        __syncthreads();
+        bitonic_desc(sh.cand, np, tid);
+    }
+    // the top-k set is cand[0 .. k): key, then id, descending rank
+    const unsigned long long ck = sh.cand[k - 1];
+    cut = make_int2(static_cast<int>(ck >> 32), static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(ck)));
+    if (use_p) {
+        // masses 2^((z - z_max) s) in 2^-40 units over the top-k set, in rank order; the cut is
+        // the first token whose inclusive prefix reaches ceil(tp * total) (at least the top token)
+        const FixedMass<DT> fm = {TruncElt<DT>::logit(static_cast<uint32_t>(sh.cand[0] >> 32)), 1.4426950408889634f / T};
+        const unsigned long long m = tid < k ? fm(static_cast<uint32_t>(sh.cand[tid] >> 32)) : 0ull;
+        unsigned long long total;
+        const unsigned long long incl = block_scan_u64(sh, m, tid, total);
+        unsigned long long need = 1ull;
+        if (tp > 0.0f) {
+            const double t = ceil(static_cast<double>(tp) * static_cast<double>(total));
+            need = t < 1.0 ? 1ull : (t > static_cast<double>(total) ? total : static_cast<unsigned long long>(t));
+        }
+        if (tid == 0) sh.found = k - 1;
+        __syncthreads();
+        if (tid < k && incl >= need && incl - m < need) atomicMin(&sh.found, tid);
+        __syncthreads();
+        const unsigned long long cp = sh.cand[sh.found];
+        cut = make_int2(static_cast<int>(cp >> 32), static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(cp)));
+    }
+    return true;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kTruncThreads) spec_trunc_kernel(const TruncParams P) {
     __shared__ TruncShared sh;
@@ -310,6 +510,13 @@ __global__ void __launch_bounds__(kTruncThreads) spec_trunc_kernel(const TruncPa
     const int nv = V / TruncElt<DT>::kPerVec;  // rows are 16-byte multiples
     const uint4 *rowp = static_cast<const uint4 *>(P.target) + static_cast<size_t>(row) * nv;
 
+    if (use_k && k <= kTruncThreads) {
+        int2 cut;
+        if (cut_small_k<DT>(sh, rowp, nv, k, use_p, tp, T, tid, cut)) {
+            if (tid == 0) P.cut[row] = cut;
+            return;
+        }
+    }
     // top-k: the k-th key from the top, then the tokens tied there in id order
     KeepCut kc = {kCutAllTau, kCutAllId};
     if (use_k) {
