@@ -196,7 +196,7 @@ __device__ __forceinline__ float vec_elem(const uint4 &w, int e) {
 // Top-k / top-p: the logits of vector `vi` of a target row outside the row's cut become -inf,
 // which turns every later sum, ratio and draw into those of the truncated, renormalised law.
 template <int DT>
-__device__ __forceinline__ void mask_cut(uint4 &w, int vi, uint32_t tau, int id) {
+__device__ __forceinline__ bool mask_cut(uint4 &w, int vi, uint32_t tau, int id) {
     // a vector wholly below the cut's logit (the common case after top-k) becomes -inf at once;
     // the largest element is taken with NaN propagating, so a NaN always takes the exact test
     // below and stays (it makes the row invalid)
@@ -213,7 +213,7 @@ __device__ __forceinline__ void mask_cut(uint4 &w, int vi, uint32_t tau, int id)
     }
     if (vm < ct) {
         w = kNegInfVec<DT>();
-        return;
+        return true;
     }
     uint32_t x[4] = {w.x, w.y, w.z, w.w};
     if (DT == SPEC_BF16) {
@@ -232,6 +232,7 @@ __device__ __forceinline__ void mask_cut(uint4 &w, int vi, uint32_t tau, int id)
             if (!cut_keeps(key_f32(x[h]), base + h, tau, id)) x[h] = 0xFF800000u;
     }
     w = make_uint4(x[0], x[1], x[2], x[3]);
+    return false;
 }
 
 // 2^d - 1 for d in [-1/4, 0] (and a little beyond) by its series in d: the coefficients are
@@ -492,9 +493,12 @@ __device__ __forceinline__ void chunk_stats(const VerifyParams &P, const ItemDes
     const int lane = threadIdx.x % kWarp;
     const bool pair = d.kind == I_PAIR, greedy = d.greedy != 0;
     const int vbase = c * kChunkVecs + lane;
+    bool t_empty = false;  // the target row's chunk lies wholly outside its top-k / top-p cut
     if (d.trunc) {
+        bool all = true;
 #pragma unroll
-        for (int k = 0; k < kVPT; ++k) mask_cut<DT>(vt[k], vbase + k * kWarp, d.cut_tau, d.cut_id);
+        for (int k = 0; k < kVPT; ++k) all &= mask_cut<DT>(vt[k], vbase + k * kWarp, d.cut_tau, d.cut_id);
+        t_empty = __all_sync(0xffffffffu, all);
     }
     if (pair && !greedy && d.xchunk == c) {
         // x = E * (c*128 + 32k + l) + e for one lane l and one k
@@ -524,7 +528,8 @@ __device__ __forceinline__ void chunk_stats(const VerifyParams &P, const ItemDes
         arg_max<kWarp>(bd, id);
         w = make_float4(bt, __int_as_float(it), bd, __int_as_float(id));
     } else {
-        const float2 t = row_sum<DT>(vt, d.s_hi, d.s_lo);
+        // a chunk with no target mass adds nothing to the target's sum: its exponentials are skipped
+        const float2 t = t_empty ? make_float2(0.0f, 0.0f) : row_sum<DT>(vt, d.s_hi, d.s_lo);
         const float2 q = pair ? row_sum<DT>(vd, d.s_hi, d.s_lo) : make_float2(0.0f, 0.0f);
         const float2 rt = ref_sum<kWarp>(t.x, t.y);
         const float2 rd = pair ? ref_sum<kWarp>(q.x, q.y) : make_float2(-INFINITY, 0.0f);
@@ -784,8 +789,11 @@ __device__ __forceinline__ float2 chunk_pass2(const ItemDesc &d, const ItemDec &
     constexpr int H = Elt<DT>::kPerVec / 2;
     const int lane = threadIdx.x % kWarp;
     if (d.trunc) {
+        bool all = true;
 #pragma unroll
-        for (int k = 0; k < kVPT; ++k) mask_cut<DT>(vt[k], c * kChunkVecs + k * kWarp + lane, d.cut_tau, d.cut_id);
+        for (int k = 0; k < kVPT; ++k) all &= mask_cut<DT>(vt[k], c * kChunkVecs + k * kWarp + lane, d.cut_tau, d.cut_id);
+        // p is 0 on the whole chunk: min(p, q) and max(p - q, 0) are 0 there
+        if (__all_sync(0xffffffffu, all)) return make_float2(0.0f, 0.0f);
     }
     const float2 shi2 = f2splat(d.s_hi);
     const float2 nct = f2splat(-D.c_t), nctf = f2splat(-D.c_tf);
