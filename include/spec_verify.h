@@ -138,16 +138,18 @@ typedef struct {
 
 /* Bytes of device workspace spec_verify needs for a batch of total_rows target rows of V logits
  * of type dtype. The workspace must be 256-byte aligned; its contents need no preparation (the
- * first kernel of each call zeroes the counters the second uses), so one workspace may serve
+ * first kernel of each call zeroes the counters the later ones use), so one workspace may serve
  * calls of any shape that fits its size. Calls that share a workspace must not overlap on the
  * GPU. */
 size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t total_rows, spec_dtype dtype);
 
-/* Verify one round. Enqueues three kernels on `stream` (four with top-k / top-p, whose cut of each
+/* Verify one round. Enqueues four kernels on `stream` (five with top-k / top-p, whose cut of each
  * target row runs first) and returns without waiting: spec_stats_kernel reads every logit once
- * (a persistent grid), spec_decide_kernel decides every position, and spec_finish_kernel reads the
- * pairs' rows again for alpha and the frontier's residual, draws, and selects each request's
- * result; each is launched so that its CTAs may start as the one before drains. */
+ * (a persistent grid), spec_decide_kernel decides every position and marks each request's
+ * frontier, spec_pass2_kernel reads the pairs' rows again (mostly from L2) for alpha and the
+ * frontier's residual, and spec_finish_kernel draws the frontier tokens and selects each
+ * request's result; each kernel after the first is launched so that its CTAs may start as the one
+ * before drains. */
 spec_status spec_verify(const spec_verify_args *args, void *workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 

@@ -1,9 +1,10 @@
 """GPU: the verifier's kernel and its grid, and spec_verify_round against the three calls.
 
-spec_verify launches two kernels: spec_stats_kernel (pass 1, a persistent grid that fills every
-SM) and spec_finish_kernel (decisions, pass 2, draws, selection). These tests check the plan the
-library reports, that a workspace serves many calls of different shapes in a row (the statistics
-kernel zeroes the finishing kernel's counters), and that the fused round equals the three calls.
+spec_verify launches four kernels: spec_stats_kernel (pass 1, a persistent grid that fills every
+SM), spec_decide_kernel (decisions and each request's frontier), spec_pass2_kernel (pass 2) and
+spec_finish_kernel (draws, selection). These tests check the plan the library reports, that a
+workspace serves many calls of different shapes in a row (the statistics kernel zeroes the later
+kernels' counters), and that the fused round equals the three calls.
 """
 import numpy as np
 import pytest
