@@ -95,7 +95,8 @@ typedef struct {
                                     (may be NULL)                                              */
     int32_t *out_tokens;         /* [T] slot row_off[i]+j: emitted token j, -1 past n_emitted   */
     int32_t *req_status;         /* [B] SPEC_REQ_* bits                                        */
-    float *alpha_rows;           /* [T-B] sum_v min(p_j(v), q_j(v)) per draft row (may be NULL) */
+    float *alpha_rows;           /* [T-B] sum_v min(p_j(v), q_j(v)) per draft row; NaN on every draft
+                                    row of a request with status bits (may be NULL)             */
     double *alpha_sum;           /* device scalar: sum of alpha over draft rows of OK requests
                                     (may be NULL)                                              */
     int32_t *alpha_count;        /* device scalar: number of those rows (may be NULL)           */

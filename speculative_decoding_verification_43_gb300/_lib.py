@@ -71,12 +71,14 @@ EXPORTS = ("spec_verify_workspace_size", "spec_verify", "spec_verify_noalloc", "
            "spec_version")
 
 
-def _load():
-    if not os.path.exists(LIB_PATH):
+def load_library(path: str):
+    """The library at `path` (the release build, or the index-checked debug build) with the
+    argument and result types of every call the header declares."""
+    if not os.path.exists(path):
         raise ImportError(
-            f"{LIB_PATH} is missing: build the CUDA library first "
+            f"{path} is missing: build the CUDA library first "
             "(python -c 'import __graft_entry__ as g; g.build()')")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(path)
     lib.spec_verify_workspace_size.argtypes = [_i32, _i32, _i32, ctypes.c_int]
     lib.spec_verify_workspace_size.restype = ctypes.c_size_t
     lib.spec_verify.argtypes = [ctypes.POINTER(SpecVerifyArgs), _p, ctypes.c_size_t, _p]
@@ -101,10 +103,13 @@ def _load():
     lib.spec_depth_objective.restype = ctypes.c_double
     lib.spec_version.argtypes = []
     lib.spec_version.restype = ctypes.c_char_p
+    if hasattr(lib, "spec_debug_fetch"):  # the debug build (include/spec_debug.h)
+        lib.spec_debug_fetch.argtypes = [_p]
+        lib.spec_debug_fetch.restype = ctypes.c_int
     return lib
 
 
-lib = _load()
+lib = load_library(LIB_PATH)
 
 
 def check(rc: int, what: str) -> None:

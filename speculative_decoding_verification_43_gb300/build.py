@@ -1,8 +1,10 @@
-"""Builds libspecverify.so in-tree with nvcc for sm_103a (one -gencode, no cmake).
+"""Builds libspecverify.so in-tree with nvcc for sm_103a (one -gencode, no cmake), and beside it
+libspecverify_debug.so, the same sources with -DSPEC_DEBUG (index-checked kernels, see
+include/spec_debug.h).
 
-Each .cu file is compiled in parallel, then linked into one shared library next to this file.
-The CUDA runtime is linked statically, so the library loads on a machine without a GPU (the
-driver is only needed once a CUDA call is made).
+Every .cu file of both libraries is compiled in parallel, then each set is linked into one shared
+library next to this file. The CUDA runtime is linked statically, so the library loads on a
+machine without a GPU (the driver is only needed once a CUDA call is made).
 """
 from __future__ import annotations
 
@@ -19,6 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libspecverify.so")
+DEBUG_LIB_PATH = os.path.join(HERE, "libspecverify_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
@@ -44,37 +47,44 @@ def _deps():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+    t = min((os.path.getmtime(p) for p in (LIB_PATH, DEBUG_LIB_PATH) if os.path.exists(p)), default=None)
+    if t is None or not (os.path.exists(LIB_PATH) and os.path.exists(DEBUG_LIB_PATH)):
         return False
-    t = os.path.getmtime(LIB_PATH)
     return all(os.path.getmtime(d) <= t for d in _deps() + [__file__])
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Builds both libraries (when a source is newer than either); returns the release path."""
     if not force and up_to_date():
         return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
+    variants = (("release", LIB_PATH, []), ("debug", DEBUG_LIB_PATH, ["-DSPEC_DEBUG"]))
+    for name, _, _ in variants:
+        os.makedirs(os.path.join(BUILD_DIR, name), exist_ok=True)
 
-    def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-        cmd = [cc, *ARCH, *FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+    def compile_one(job):
+        name, src, extra = job
+        obj = os.path.join(BUILD_DIR, name, os.path.basename(src) + ".o")
+        cmd = [cc, *ARCH, *FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed for {src} ({name}):\n{r.stdout}\n{r.stderr}")
         if verbose and (r.stdout or r.stderr):
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
     srcs = _sources()
-    with ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-fPIC"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    jobs = [(name, src, extra) for name, _, extra in variants for src in srcs]
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        objs = list(ex.map(compile_one, jobs))
+    for k, (name, path, _) in enumerate(variants):
+        mine = objs[k * len(srcs):(k + 1) * len(srcs)]
+        tmp = path + f".tmp{os.getpid()}"
+        cmd = [cc, *ARCH, "-shared", "-o", tmp, *mine, "-Xcompiler", "-fPIC"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed ({name}):\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, path)
     return LIB_PATH
 
 

@@ -202,3 +202,10 @@ extern "C" spec_status spec_choose_gamma_depth(const int32_t *n_reached, const i
                ? SPEC_OK
                : SPEC_ERR_CUDA;
 }
+
+#ifdef SPEC_DEBUG
+namespace spec {
+// The debug words of this translation unit's kernels (the compaction and the gamma choice).
+cudaError_t debug_take_compact(unsigned int out[4]) { return spec_dbg_take(out); }
+}  // namespace spec
+#endif

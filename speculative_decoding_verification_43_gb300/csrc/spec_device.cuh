@@ -289,6 +289,45 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
     return r;
 }
 
+// ---- the debug build (-DSPEC_DEBUG): index checks that record instead of trapping
+// SPEC_IN(i, n, code) is true when 0 <= i < n. In the debug build a failed check records, in this
+// translation unit's words, the first failure's code (which array), source line and index, counts
+// every failure, and the caller skips the access; spec_debug_fetch() reads and clears the words.
+// In the release build it is the constant true and costs nothing.
+enum : int {
+    DBG_LOGITS = 1,     // a target or draft row, or a vector beyond a row
+    DBG_RECORDS = 2,    // per-chunk workspace (statistics records, alpha and residual shares)
+    DBG_ROWS = 3,       // per-row workspace (values, decisions, draft-token records, item results)
+    DBG_OUT_ROWS = 4,   // per-row outputs (out_tokens, alpha_rows, rho_rows, resid_rows)
+    DBG_OUT_REQS = 5,   // per-request outputs and counters
+    DBG_PACKED = 6,     // the compaction's packed outputs
+    DBG_CUT = 7,        // the truncation kernel's rows and cuts
+};
+#ifdef SPEC_DEBUG
+static __device__ unsigned int g_spec_dbg[4];  // first code, its line, its index, failures
+static __device__ __noinline__ bool spec_dbg_fail(int code, int line, long long idx) {
+    if (atomicCAS(&g_spec_dbg[0], 0u, static_cast<unsigned>(code)) == 0u) {
+        g_spec_dbg[1] = static_cast<unsigned>(line);
+        g_spec_dbg[2] = static_cast<unsigned>(idx);
+    }
+    atomicAdd(&g_spec_dbg[3], 1u);
+    return false;
+}
+#define SPEC_IN(i, n, code)                                                                          \
+    ((static_cast<long long>(i) >= 0 && static_cast<long long>(i) < static_cast<long long>(n))      \
+         ? true                                                                                      \
+         : ::spec::spec_dbg_fail((code), __LINE__, static_cast<long long>(i)))
+// reads and clears this translation unit's words (host)
+static inline cudaError_t spec_dbg_take(unsigned int out[4]) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_spec_dbg, sizeof(unsigned int) * 4);
+    if (e != cudaSuccess) return e;
+    const unsigned int zero[4] = {0u, 0u, 0u, 0u};
+    return cudaMemcpyToSymbol(g_spec_dbg, zero, sizeof(zero));
+}
+#else
+#define SPEC_IN(i, n, code) true
+#endif
+
 // base-2 exponential on the special-function unit (relative error about 2 ulp)
 __device__ __forceinline__ float ex2(float x) {
     float y;

@@ -478,10 +478,12 @@ __device__ __forceinline__ void stats_load(const VerifyParams &P, const ItemDesc
     const uint4 *trow = static_cast<const uint4 *>(P.target) + static_cast<size_t>(d.item) * P.nvec_row;
     const uint4 *drow = static_cast<const uint4 *>(P.draft) + static_cast<size_t>(d.drow) * P.nvec_row;
     const uint64_t pol = has_p2(d) ? keep : drop;  // a pair's rows are read again by the finishing kernel
+    const bool rows_ok = SPEC_IN(d.item, P.total_rows, DBG_LOGITS) &&
+                         (!pair || SPEC_IN(d.drow, P.total_rows - P.B, DBG_LOGITS));
 #pragma unroll
     for (int k = 0; k < kVPT; ++k) {
         const int vi = c * kChunkVecs + k * kWarp + lane;
-        const bool in = vi < P.nvec_row;
+        const bool in = rows_ok && vi < P.nvec_row;
         vt[k] = in ? ldg_hint(trow + vi, pol) : kNegInfVec<DT>();
         vd[k] = (in && pair) ? ldg_hint(drow + vi, pol) : kNegInfVec<DT>();
     }
@@ -515,7 +517,8 @@ __device__ __forceinline__ void chunk_stats(const VerifyParams &P, const ItemDes
             const float yt = vec_elem<DT>(wt, d.x % E), yd = vec_elem<DT>(wd, d.x % E);
             const F2 Ex = f2_mul(f2_add({yt, 0.0f}, {-yd, 0.0f}), {d.s_hi, d.s_lo});
             const int flags = (yd == -INFINITY ? XF_QZERO : 0) | (yt == -INFINITY ? XF_PZERO : 0);
-            P.xrec[d.item] = make_float4(Ex.hi, Ex.lo, __int_as_float(flags), 0.0f);
+            if (SPEC_IN(d.item, P.total_rows, DBG_ROWS))
+                P.xrec[d.item] = make_float4(Ex.hi, Ex.lo, __int_as_float(flags), 0.0f);
         }
     }
     float4 w;
@@ -535,7 +538,9 @@ __device__ __forceinline__ void chunk_stats(const VerifyParams &P, const ItemDes
         const float2 rd = pair ? ref_sum<kWarp>(q.x, q.y) : make_float2(-INFINITY, 0.0f);
         w = make_float4(rt.x, rt.y, rd.x, rd.y);
     }
-    if (lane == 0) P.rec[static_cast<size_t>(d.item) * P.nchunk + c] = chunk_record(w, greedy, pair);
+    if (lane == 0 && SPEC_IN(static_cast<long long>(d.item) * P.nchunk + c, static_cast<long long>(P.total_rows) * P.nchunk,
+                             DBG_RECORDS))
+        P.rec[static_cast<size_t>(d.item) * P.nchunk + c] = chunk_record(w, greedy, pair);
 }
 
 // Pass 1: every chunk of every item, each warp a contiguous run of (item, chunk) pieces. The
@@ -584,7 +589,8 @@ __global__ void __launch_bounds__(kStatsBlock) spec_stats_kernel(const __grid_co
             d = item_desc<DT>(P, item);
             cur = item;
         }
-        if (c == 0 && tid % kWarp == 0) P.desc[item] = d;  // the item's values, for the finishing kernel
+        if (c == 0 && tid % kWarp == 0 && SPEC_IN(item, P.total_rows, DBG_ROWS))
+            P.desc[item] = d;  // the item's values, for the finishing kernel
         if (d.kind == I_SKIP) continue;
         uint4 vt[kVPT], vd[kVPT];
         stats_load<DT>(P, d, c, keep, drop, vt, vd);
@@ -770,10 +776,11 @@ __device__ __forceinline__ void load_chunk(const VerifyParams &P, const ItemDesc
     const int lane = threadIdx.x % kWarp;
     const uint4 *trow = static_cast<const uint4 *>(P.target) + static_cast<size_t>(d.item) * P.nvec_row;
     const uint4 *drow = static_cast<const uint4 *>(P.draft) + static_cast<size_t>(d.drow) * P.nvec_row;
+    const bool rows_ok = SPEC_IN(d.item, P.total_rows, DBG_LOGITS) && SPEC_IN(d.drow, P.total_rows - P.B, DBG_LOGITS);
 #pragma unroll
     for (int k = 0; k < kVPT; ++k) {
         const int vi = c * kChunkVecs + k * kWarp + lane;
-        const bool in = vi < P.nvec_row;
+        const bool in = rows_ok && vi < P.nvec_row;
         vt[k] = in ? ldg_hint(trow + vi, drop) : kNegInfVec<DT>();
         vd[k] = in ? ldg_hint(drow + vi, drop) : kNegInfVec<DT>();
     }
@@ -983,9 +990,9 @@ __device__ __noinline__ void draw_item(const VerifyParams &P, const ItemDesc &d,
         const int vi = csel * kChunkVecs + k * kWarp + lane;
         wt = kNegInfVec<DT>();
         wd = kNegInfVec<DT>();
-        if (vi < P.nvec_row) {
+        if (vi < P.nvec_row && SPEC_IN(d.item, P.total_rows, DBG_LOGITS)) {
             wt = __ldcg(trow + vi);
-            if (kind == SAMPLE_RESIDUAL) wd = __ldcg(drow + vi);
+            if (kind == SAMPLE_RESIDUAL && SPEC_IN(d.drow, P.total_rows - P.B, DBG_LOGITS)) wd = __ldcg(drow + vi);
         }
     };
     float c = 0.0f;  // mass before vector (k, lane) within the chunk
@@ -1117,9 +1124,18 @@ __device__ __noinline__ void select_request(const VerifyParams &P, int i) {
     }
     status |= st_items;
     if (status) {
+        // a request with any status bit emits nothing, and none of its draft rows has a result
         if (K >= 0)
-            for (int j = lane; j <= K; j += kWarp) P.out_tokens[r0 + j] = -1;
-        if (lane == 0) {
+            for (int j = lane; j <= K; j += kWarp) {
+                if (SPEC_IN(r0 + j, P.total_rows, DBG_OUT_ROWS)) P.out_tokens[r0 + j] = -1;
+                const int dr = r0 - i + j;
+                if (j < K && SPEC_IN(dr, P.total_rows - P.B, DBG_OUT_ROWS)) {
+                    if (P.alpha_rows) P.alpha_rows[dr] = NAN;
+                    if (P.rho_rows) P.rho_rows[dr] = NAN;
+                    if (P.resid_rows) P.resid_rows[dr] = -1.0f;
+                }
+            }
+        if (lane == 0 && SPEC_IN(i, P.B, DBG_OUT_REQS)) {
             P.req_status[i] = status;
             P.accept_len[i] = 0;
             if (P.n_emitted) P.n_emitted[i] = 0;
@@ -1147,11 +1163,13 @@ __device__ __noinline__ void select_request(const VerifyParams &P, int i) {
         else if (h1)
             n = kWarp + __ffs(h1);
     }
-    if (lane <= K) P.out_tokens[r0 + lane] = lane < n ? out0 : -1;
-    if (lane + kWarp <= K) P.out_tokens[r0 + lane + kWarp] = lane + kWarp < n ? out1 : -1;
-    if (lane == 0 && K == 2 * kWarp) P.out_tokens[r0 + K] = (A == K && n > K) ? frontier : -1;
+    if (lane <= K && SPEC_IN(r0 + lane, P.total_rows, DBG_OUT_ROWS)) P.out_tokens[r0 + lane] = lane < n ? out0 : -1;
+    if (lane + kWarp <= K && SPEC_IN(r0 + lane + kWarp, P.total_rows, DBG_OUT_ROWS))
+        P.out_tokens[r0 + lane + kWarp] = lane + kWarp < n ? out1 : -1;
+    if (lane == 0 && K == 2 * kWarp && SPEC_IN(r0 + K, P.total_rows, DBG_OUT_ROWS))
+        P.out_tokens[r0 + K] = (A == K && n > K) ? frontier : -1;
     const F2 asum = warp_sum_f2(f2_add({al0, 0.0f}, {al1, 0.0f}));
-    if (lane == 0) {
+    if (lane == 0 && SPEC_IN(i, P.B, DBG_OUT_REQS)) {
         P.req_status[i] = 0;
         P.accept_len[i] = A;
         if (P.n_emitted) P.n_emitted[i] = n;
@@ -1197,14 +1215,19 @@ __device__ __noinline__ bool finalize_item(const VerifyParams &P, const ItemDesc
         tok = D.argmax_t;  // Rule 1: the correction (or the extra token) is argmax p
         prob = 1.0f;
     }
-    if (lane == 0) {
+    // a draft position: a pair, or a position of a request rejected before any work (its per-draft
+    // outputs still get their no-result values)
+    const bool drow_item =
+        pair || (d.kind == I_SKIP && d.pos < d.K && d.drow >= 0 && d.drow < P.total_rows - P.B);
+    if (lane == 0 && SPEC_IN(d.item, P.total_rows, DBG_ROWS) &&
+        (!drow_item || SPEC_IN(d.drow, P.total_rows - P.B, DBG_OUT_ROWS))) {
         const int item = d.item;
         P.item_status[item] = st;
         P.item_fb[item] = fb;
         P.item_tok[item] = tok;
         P.item_prob[item] = prob;
         P.item_margin[item] = margin;
-        if (pair) {
+        if (drow_item) {
             const float a = d.greedy ? D.alpha_g : alpha;
             P.item_flag[item] = (st == 0) ? D.accept : 0;
             P.alpha_ws[d.drow] = (st == 0) ? a : 0.0f;
@@ -1219,7 +1242,7 @@ __device__ __noinline__ bool finalize_item(const VerifyParams &P, const ItemDesc
     }
     __syncwarp();
     uint32_t old = 0;
-    if (lane == 0) old = atomicAdd(P.req_cnt + d.req, 1u);
+    if (lane == 0 && SPEC_IN(d.req, P.B, DBG_OUT_REQS)) old = atomicAdd(P.req_cnt + d.req, 1u);
     old = __shfl_sync(0xffffffffu, old, 0);
     if (static_cast<int>(old) == d.K) {
         fence_gpu();
@@ -1303,6 +1326,7 @@ __global__ void __launch_bounds__(kDecWarps * kWarp) spec_decide_kernel(const __
     if (threadIdx.x == 0) s_first = INT_MAX;
     __syncthreads();
     for (int j = warp; j < n; j += kDecWarps) {
+        if (!SPEC_IN(r0 + j, P.total_rows, DBG_ROWS)) continue;
         const ItemDesc d = P.desc[r0 + j];
         const ItemDec D = (d.kind == I_SKIP) ? skip_decision(d) : decide_chunks(P, d);
         if (lane == 0) {
@@ -1312,7 +1336,8 @@ __global__ void __launch_bounds__(kDecWarps * kWarp) spec_decide_kernel(const __
     }
     __syncthreads();
     // the frontier: the first rejection, else the bonus row
-    if (threadIdx.x == 0) P.dec[r0 + min(s_first, n - 1)].frontier = 1;
+    if (threadIdx.x == 0 && SPEC_IN(r0 + min(s_first, n - 1), P.total_rows, DBG_ROWS))
+        P.dec[r0 + min(s_first, n - 1)].frontier = 1;
 }
 
 // Pass 2: every chunk of every pair under Rule 2, each warp a contiguous run of (item, chunk)
@@ -1356,7 +1381,8 @@ __global__ void __launch_bounds__(kFinBlock, 4) spec_pass2_kernel(const __grid_c
         uint4 vt[kVPT], vd[kVPT];
         load_chunk<DT>(P, d, c, drop, vt, vd);
         const float2 r = chunk_pass2<DT>(d, D, c, vt, vd);
-        if (lane == 0) {
+        if (lane == 0 && SPEC_IN(static_cast<long long>(item) * P.nchunk + c,
+                                 static_cast<long long>(P.total_rows) * P.nchunk, DBG_RECORDS)) {
             P.alpha_c[static_cast<size_t>(item) * P.nchunk + c] = r.x;
             if (frontier) P.zc[static_cast<size_t>(item) * P.nchunk + c] = r.y;
         }

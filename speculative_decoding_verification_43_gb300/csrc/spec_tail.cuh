@@ -138,14 +138,18 @@ __device__ __forceinline__ void compact_body(const CompactParams &P, bool wait, 
             const CopyJob jb = job[q];
             const int req = base + q, d0 = jb.r0 - req;
             for (int j = lane; j < jb.n; j += kWarp) {
-                P.packed_tokens[jb.off_n + j] = P.out_tokens[jb.r0 + j];
-                P.packed_pos[jb.off_n + j] = jb.Pi + j;
+                if (SPEC_IN(jb.off_n + j, P.total_rows, DBG_PACKED) && SPEC_IN(jb.r0 + j, P.total_rows, DBG_OUT_ROWS)) {
+                    P.packed_tokens[jb.off_n + j] = P.out_tokens[jb.r0 + j];
+                    P.packed_pos[jb.off_n + j] = jb.Pi + j;
+                }
             }
             for (int j = lane; j < jb.E; j += kWarp) {
                 const int pos = jb.Pi + j;
                 const int blk = P.block_table[static_cast<int64_t>(req) * P.max_blocks + pos / P.page_size];
-                P.kv_src[jb.off_e + j] = P.cand_kv_rows[d0 + j];
-                P.kv_dst[jb.off_e + j] = blk * P.page_size + pos % P.page_size;
+                if (SPEC_IN(jb.off_e + j, P.total_rows - P.B, DBG_PACKED) && SPEC_IN(d0 + j, P.total_rows - P.B, DBG_PACKED)) {
+                    P.kv_src[jb.off_e + j] = P.cand_kv_rows[d0 + j];
+                    P.kv_dst[jb.off_e + j] = blk * P.page_size + pos % P.page_size;
+                }
             }
         }
         __syncthreads();  // job[] is rewritten by the next chunk

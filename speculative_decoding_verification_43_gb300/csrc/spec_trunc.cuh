@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kTruncThreads) spec_trunc_kernel(const TruncPa
     const bool use_k = k > 0 && k < V;
     const bool use_p = tp < 1.0f;  // false for NaN (the request is then invalid)
     if ((!use_k && !use_p) || !(T > 0.0f) || isinf(T)) {  // the greedy rule ignores truncation
-        if (tid == 0) P.cut[row] = make_int2(static_cast<int>(kCutAllTau), kCutAllId);
+        if (tid == 0 && SPEC_IN(row, P.total_rows, DBG_CUT)) P.cut[row] = make_int2(static_cast<int>(kCutAllTau), kCutAllId);
         return;
     }
     const int nv = V / TruncElt<DT>::kPerVec;  // rows are 16-byte multiples
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kTruncThreads) spec_trunc_kernel(const TruncPa
     if (use_k && k <= kTruncThreads) {
         int2 cut;
         if (cut_small_k<DT>(sh, rowp, nv, k, use_p, tp, T, tid, cut)) {
-            if (tid == 0) P.cut[row] = cut;
+            if (tid == 0 && SPEC_IN(row, P.total_rows, DBG_CUT)) P.cut[row] = cut;
             return;
         }
     }
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kTruncThreads) spec_trunc_kernel(const TruncPa
         const int id = nth_tied<DT>(sh, rowp, nv, tau, n, kc, tid);
         fc = {tau, id};
     }
-    if (tid == 0) P.cut[row] = make_int2(static_cast<int>(fc.tau), fc.id);
+    if (tid == 0 && SPEC_IN(row, P.total_rows, DBG_CUT)) P.cut[row] = make_int2(static_cast<int>(fc.tau), fc.id);
 }
 
 }  // namespace spec

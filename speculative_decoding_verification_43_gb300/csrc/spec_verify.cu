@@ -263,7 +263,28 @@ extern "C" spec_status spec_verify_round(const spec_verify_args *a, void *worksp
     return verify_enqueue(a, workspace, workspace_bytes, stream, &C, &G);
 }
 
+#ifdef SPEC_DEBUG
+extern "C" const char *spec_version(void) { return "spec-verify-gb300 0.1 (sm_103a, index-checked debug build)"; }
+
+namespace spec {
+cudaError_t debug_take_compact(unsigned int out[4]);
+}
+
+extern "C" spec_status spec_debug_fetch(unsigned int *out) {
+    if (!out) return SPEC_ERR_INVALID_ARG;
+    unsigned int a[4] = {0u, 0u, 0u, 0u}, b[4] = {0u, 0u, 0u, 0u};
+    if (cudaDeviceSynchronize() != cudaSuccess) return SPEC_ERR_CUDA;
+    if (spec::spec_dbg_take(a) != cudaSuccess || spec::debug_take_compact(b) != cudaSuccess) return SPEC_ERR_CUDA;
+    const unsigned int *first = a[0] ? a : b;
+    out[0] = first[0];
+    out[1] = first[1];
+    out[2] = first[2];
+    out[3] = a[3] + b[3];
+    return SPEC_OK;
+}
+#else
 extern "C" const char *spec_version(void) { return "spec-verify-gb300 0.1 (sm_103a)"; }
+#endif
 
 // ------------------------------------------------------------------------------------------
 // spec_verify_noalloc: spec_verify for callers that cannot allocate device memory.

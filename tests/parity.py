@@ -185,6 +185,9 @@ def compare(gpu, orc, sb, reqs, full_row_off) -> Report:
             rep.compared += 1
             if not (gpu["out_tokens"][g_r0:g_r0 + K + 1] == -1).all() or gpu["n_emitted"][i] != 0:
                 rep.mismatches.append((i, "bad request emitted", gpu["out_tokens"][g_r0:g_r0 + K + 1]))
+            # its draft rows carry no result either (NaN, as the oracle's)
+            if K > 0 and not np.isnan(gpu["alpha_rows"][g_d0:g_d0 + K]).all():
+                rep.mismatches.append((i, "bad request alpha", gpu["alpha_rows"][g_d0:g_d0 + K]))
             continue
         greedy = float(sb["temperature"][k]) == 0.0
         tm = orc["trunc_margin"][r0:r1]

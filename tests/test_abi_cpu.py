@@ -20,8 +20,8 @@ def lib():
     return _lib
 
 
-def declared_functions():
-    src = open(os.path.join(ROOT, "include", "spec_verify.h")).read()
+def declared_functions(header="spec_verify.h"):
+    src = open(os.path.join(ROOT, "include", header)).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     src = re.sub(r"//[^\n]*", "", src)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
@@ -34,6 +34,23 @@ def test_every_declared_symbol_is_exported(lib):
     raw = ctypes.CDLL(lib.LIB_PATH if hasattr(lib, "LIB_PATH") else lib.lib._name)
     for n in names:
         assert hasattr(raw, n), n
+
+
+def test_debug_library_exports_everything_plus_its_fetch(lib):
+    """libspecverify_debug.so (the -DSPEC_DEBUG build) exports every symbol of spec_verify.h and
+    the one spec_debug.h adds; the release library does not export the debug call."""
+    from speculative_decoding_verification_43_gb300 import build
+    dbg = ctypes.CDLL(build.DEBUG_LIB_PATH)
+    extra = declared_functions("spec_debug.h")
+    assert extra == ["spec_debug_fetch"], extra
+    for n in declared_functions() + extra:
+        assert hasattr(dbg, n), n
+    assert not hasattr(ctypes.CDLL(build.LIB_PATH), "spec_debug_fetch")
+    dbg.spec_version.restype = ctypes.c_char_p
+    assert b"debug" in dbg.spec_version()
+    dbg.spec_debug_fetch.argtypes = [ctypes.c_void_p]
+    dbg.spec_debug_fetch.restype = ctypes.c_int
+    assert dbg.spec_debug_fetch(None) == lib.SPEC_ERR_INVALID_ARG
 
 
 def test_version_string(lib):
