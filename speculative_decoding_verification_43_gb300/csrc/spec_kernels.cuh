@@ -251,6 +251,16 @@ __device__ __forceinline__ float2 exp2m1_series(float2 d) {
     return __fmul2_rn(d, p);
 }
 
+// The fraction term of -log2 of a row's normaliser, c_f, less y_top s_lo: in log2 p = y s_hi - c -
+// c_f + y s_lo the term y s_lo is taken as y_top s_lo, one constant per row with y_top = (c + c_f)
+// / s_hi (the log-normaliser over s, within log2(V) / s of the row's largest logit). It differs
+// from y s_lo by (y - y_top) s_lo: at most about log2(V) 2^-24 relative on the terms that carry a
+// sum, where dropping it would cost y s_lo (3e-5 at T = 0.01). Pass 2 and the residual draw use it
+// alike, so a draw's weights are those pass 2 summed.
+__device__ __forceinline__ float neg_frac_lo(float c, float cf, float s_hi, float s_lo) {
+    return -cf + (c + cf) * (s_lo / s_hi);
+}
+
 // The residual weights max(p - q, 0) and min(p, q) of one pair of logits pairs, normalised: p =
 // 2^(y_t s - c_t) and q / p = 2^d with d = (y_d - y_t) s - (c_d - c_t), the logit difference
 // exact and its product with s a float pair, so that d is accurate even where p and q nearly
@@ -803,7 +813,7 @@ __device__ __forceinline__ float2 chunk_pass2(const ItemDesc &d, const ItemDec &
         if (__all_sync(0xffffffffu, all)) return make_float2(0.0f, 0.0f);
     }
     const float2 shi2 = f2splat(d.s_hi);
-    const float2 nct = f2splat(-D.c_t), nctf = f2splat(-D.c_tf);
+    const float2 nct = f2splat(-D.c_t), nctf = f2splat(neg_frac_lo(D.c_t, D.c_tf, d.s_hi, d.s_lo));
     float a, z = 0.0f;
     if (D.kind == SAMPLE_RESIDUAL) {
         const float2 slo2 = f2splat(d.s_lo);
@@ -824,8 +834,8 @@ __device__ __forceinline__ float2 chunk_pass2(const ItemDesc &d, const ItemDec &
         z = racc.x + racc.y;
     } else {
         // y s - c with c split: the product less the integral part rounds once (to a small result
-        // near the top of the row), then the fraction
-        const float2 ncd = f2splat(-D.c_d), ncdf = f2splat(-D.c_df);
+        // near the top of the row), then the fraction with the row's s_lo term (neg_frac_lo)
+        const float2 ncd = f2splat(-D.c_d), ncdf = f2splat(neg_frac_lo(D.c_d, D.c_df, d.s_hi, d.s_lo));
         float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int k = 0; k < kVPT; ++k) {
@@ -849,7 +859,7 @@ __device__ __forceinline__ void draw_weights(int kind, const uint4 &wt, const ui
     constexpr int H = Elt<DT>::kPerVec / 2;
     const float2 shi2 = f2splat(d.s_hi), slo2 = f2splat(d.s_lo);
     if (kind == SAMPLE_RESIDUAL) {
-        const float2 nct = f2splat(-D.c_t), nctf = f2splat(-D.c_tf);
+        const float2 nct = f2splat(-D.c_t), nctf = f2splat(neg_frac_lo(D.c_t, D.c_tf, d.s_hi, d.s_lo));
         const float2 ndch = f2splat(-D.dc.hi), ndcl = f2splat(-D.dc.lo);
 #pragma unroll
         for (int h = 0; h < H; ++h) {

@@ -20,6 +20,7 @@ from parity import Report, check_round, compare, run_gpu, run_oracle
 pytestmark = pytest.mark.gpu
 
 
+
 def record(name, rep):
     """Append the report's counts as one JSON line to the file named by SPEC_PARITY_COUNTS (when
     set): the per-configuration table of requests, compared and band counts."""
@@ -455,3 +456,19 @@ def test_all_64_drafts_accepted():
     assert (gpu["accept_len"] == 64).all() and (gpu["n_emitted"] == 65).all()
     assert (gpu["out_tokens"].reshape(rd.B, 65) >= 0).all()
     assert_report(check_round(rd), max_near=1, name="all_64_drafts_accepted")
+
+
+@pytest.mark.parametrize("dtype,V", [(torch.bfloat16, 32000), (torch.float32, 12348)])
+def test_extreme_temperatures(dtype, V):
+    """Temperatures near the greedy limit (s = log2(e)/T up to 144: exponent arguments far beyond
+    the float range, so the statistics take their exact form) and a very flat law (T = 50), mixed
+    in one batch."""
+    base = W.Workload("t", B=20, V=V, dtype=dtype, temperature=1.0, logits="normal", sigma=2.0,
+                      draft_sigma=0.3, K="uniform:0:4")
+    temps = np.array([0.01, 0.02, 0.05, 0.1, 50.0] * 4, np.float32)
+    tot = Report()
+    for rnd in range(2):
+        rd = W.make_round(base, seed=14, rnd=rnd, device="cuda", temperature=temps)
+        tot.add(check_round(rd))
+    # the oracle's band count on these rounds: 0 (both configurations)
+    assert_report(tot, max_near=1, name=f"extreme temperatures {str(dtype)[6:]} V={V} (2 rounds)")
