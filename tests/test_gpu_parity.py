@@ -21,6 +21,7 @@ pytestmark = pytest.mark.gpu
 
 
 
+
 def record(name, rep):
     """Append the report's counts as one JSON line to the file named by SPEC_PARITY_COUNTS (when
     set): the per-configuration table of requests, compared and band counts."""
@@ -472,3 +473,20 @@ def test_extreme_temperatures(dtype, V):
         tot.add(check_round(rd))
     # the oracle's band count on these rounds: 0 (both configurations)
     assert_report(tot, max_near=1, name=f"extreme temperatures {str(dtype)[6:]} V={V} (2 rounds)")
+
+
+@pytest.mark.parametrize("dtype,V,shift", [(torch.bfloat16, 32000, 1000.0), (torch.bfloat16, 32000, -3000.0),
+                                           (torch.float32, 12348, 30000.0)])
+def test_large_logit_offsets(dtype, V, shift):
+    """Every logit of the batch shifted by one large constant (the law is unchanged; the products
+    y s reach ~4e4, so every exponent argument depends on the reference being subtracted before
+    rounding, and the low part of s on the row's top logit). Temperatures 0.7 and 1.3."""
+    base = W.Workload("t", B=16, V=V, dtype=dtype, temperature=1.0, logits="normal", sigma=2.0,
+                      draft_sigma=0.6, K="uniform:0:5")
+    temps = np.array([0.7, 1.3] * 8, np.float32)
+    rd = W.make_round(base, seed=15, device="cuda", temperature=temps)
+    rd.target = (rd.target.float() + shift).to(dtype).contiguous()
+    rd.draft = (rd.draft.float() + shift).to(dtype).contiguous()
+    _resample_drafts(rd, 19)
+    # the oracle's band count on each of these rounds: 0
+    assert_report(check_round(rd), max_near=1, name=f"logits shifted by {shift:g} {str(dtype)[6:]} V={V}")
