@@ -22,6 +22,7 @@ pytestmark = pytest.mark.gpu
 
 
 
+
 def record(name, rep):
     """Append the report's counts as one JSON line to the file named by SPEC_PARITY_COUNTS (when
     set): the per-configuration table of requests, compared and band counts."""
@@ -490,3 +491,48 @@ def test_large_logit_offsets(dtype, V, shift):
     _resample_drafts(rd, 19)
     # the oracle's band count on each of these rounds: 0
     assert_report(check_round(rd), max_near=1, name=f"logits shifted by {shift:g} {str(dtype)[6:]} V={V}")
+
+
+def test_degenerate_laws():
+    """Laws at the edges of the rule, in one batch (SOTA-227 "What to do", steps 3-4):
+    - constant rows: p = q uniform, every draft accepted, the extra token drawn over equal weights;
+    - one-hot drafts (every draft logit -inf but the proposed token's): q(x) = 1, rho = p(x), and
+      the residual is p with x removed;
+    - sparse targets (all but 16 logits -inf) against dense drafts: p(x) = 0 rejects, and the
+      residual lives on p's 16 tokens."""
+    V = 4096
+    base = W.Workload("t", B=24, V=V, dtype=torch.float32, temperature=1.0, logits="normal", sigma=2.0,
+                      draft_sigma=0.5, K="uniform:1:4")
+    rd = W.make_round(base, seed=16, device="cuda")
+    tz, dz = rd.target.clone(), rd.draft.clone()
+    row_req = np.repeat(np.arange(rd.B), np.asarray(rd.K) + 1)
+    drow_req = np.repeat(np.arange(rd.B), np.asarray(rd.K))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(9)
+    keep = torch.zeros(rd.B, V, dtype=torch.bool, device="cuda")
+    for i in range(rd.B):
+        keep[i, torch.randperm(V, generator=gen, device="cuda")[:16]] = True
+    for i in range(rd.B):
+        rr = torch.as_tensor(np.nonzero(row_req == i)[0], device="cuda")
+        dr = torch.as_tensor(np.nonzero(drow_req == i)[0], device="cuda")
+        if i % 3 == 0:      # constant rows
+            tz[rr] = 0.5
+            dz[dr] = 0.5
+        elif i % 3 == 2:    # sparse targets
+            tz[rr] = tz[rr].masked_fill(~keep[i], float("-inf"))
+    rd.target = tz.contiguous()
+    rd.draft = dz.contiguous()
+    _resample_drafts(rd, 23)
+    # one-hot drafts on the second kind, around the proposed token
+    dz = rd.draft.clone()
+    toks = rd.draft_tokens.cpu().numpy()
+    for i in range(rd.B):
+        if i % 3 == 1:
+            for j in np.nonzero(drow_req == i)[0]:
+                row = torch.full((V,), float("-inf"), device="cuda")
+                row[int(toks[j])] = 1.0
+                dz[int(j)] = row
+    rd.draft = dz.contiguous()
+    rep = check_round(rd)
+    # the oracle's band count on this round: 0
+    assert_report(rep, max_near=1, name="degenerate laws")
