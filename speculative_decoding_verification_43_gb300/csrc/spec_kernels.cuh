@@ -1350,8 +1350,9 @@ __global__ void __launch_bounds__(kDecWarps * kWarp) spec_decide_kernel(const __
         P.dec[r0 + min(s_first, n - 1)].frontier = 1;
 }
 
-// Pass 2: every chunk of every pair under Rule 2, each warp a contiguous run of (item, chunk)
-// pieces (the item's values and decision read once per item). A chunk's alpha share goes to
+// Pass 2: every chunk of every pair under Rule 2, each warp a contiguous run of (pair, chunk)
+// pieces, the bonus rows left out of the enumeration (the item's values and decision read once
+// per item). A chunk's alpha share goes to
 // alpha_c; at the request's frontier (its first rejection) its residual mass goes to zc.
 template <int DT>
 __global__ void __launch_bounds__(kFinBlock, 4) spec_pass2_kernel(const __grid_constant__ VerifyParams P) {
@@ -1362,7 +1363,10 @@ __global__ void __launch_bounds__(kFinBlock, 4) spec_pass2_kernel(const __grid_c
     const uint64_t drop = policy_evict_first();
     const long long warps = static_cast<long long>(gridDim.x) * kFinWarps;
     const long long gw = static_cast<long long>(blockIdx.x) * kFinWarps + threadIdx.x / kWarp;
-    const long long total = static_cast<long long>(P.total_rows) * P.nchunk;
+    // units over the pairs only: unit u is chunk u % nchunk of draft row p = u / nchunk, whose
+    // target row is p + i for the request i holding it (the bonus rows of requests before it
+    // lie in between)
+    const long long total = static_cast<long long>(P.total_rows - P.B) * P.nchunk;
     const long long per = (total + warps - 1) / warps;
     const long long u1 = min(total, (gw + 1) * per);
     int cur = -1;
@@ -1371,13 +1375,31 @@ __global__ void __launch_bounds__(kFinBlock, 4) spec_pass2_kernel(const __grid_c
     ItemDec D = {};
     const long long ub = gw * per;
     if (ub >= u1) return;
-    // (item, chunk) stepped without divisions
-    int item = static_cast<int>(ub / P.nchunk), c = static_cast<int>(ub % P.nchunk) - 1;
+    int p = static_cast<int>(ub / P.nchunk), c = static_cast<int>(ub % P.nchunk) - 1;
+    int i = 0;
+    {
+        int lo = 0, hi = P.B - 1;  // the last request whose first draft row is at most p
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(P.row_off + mid) - mid <= p) lo = mid; else hi = mid - 1;
+        }
+        i = lo;
+    }
+    int next_first = __ldg(P.row_off + i + 1) - (i + 1);  // the first draft row past request i
+    while (p >= next_first && i + 1 < P.B) {
+        ++i;
+        next_first = __ldg(P.row_off + i + 1) - (i + 1);
+    }
     for (long long u = ub; u < u1; ++u) {
         if (++c == P.nchunk) {
             c = 0;
-            ++item;
+            ++p;
+            while (p >= next_first && i + 1 < P.B) {
+                ++i;
+                next_first = __ldg(P.row_off + i + 1) - (i + 1);
+            }
         }
+        const int item = p + i;
         if (item != cur) {
             cur = item;
             d = P.desc[item];
