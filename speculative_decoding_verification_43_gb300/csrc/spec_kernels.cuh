@@ -61,7 +61,7 @@ namespace vk {
 constexpr int kVPT = 4;                          // 16-byte vectors of a chunk per lane and row
 constexpr int kChunkVecs = kWarp * kVPT;         // 128 vectors: a chunk (2 KB)
 constexpr int kStatsBlock = 256;                 // statistics kernel: threads per CTA
-constexpr int kFinBlock = 256;                   // finishing kernel: threads per CTA
+constexpr int kFinBlock = 256;                   // pass-2 and finishing kernels: threads per CTA
 constexpr int kFinWarps = kFinBlock / kWarp;
 constexpr int kDecWarps = 8;                     // decision kernel: warps per CTA (one request)
 constexpr int kDrawRun = 16;                     // a draw's chunk masses per lane held at once
@@ -487,7 +487,7 @@ __device__ __forceinline__ void stats_load(const VerifyParams &P, const ItemDesc
     const bool pair = d.kind == I_PAIR;
     const uint4 *trow = static_cast<const uint4 *>(P.target) + static_cast<size_t>(d.item) * P.nvec_row;
     const uint4 *drow = static_cast<const uint4 *>(P.draft) + static_cast<size_t>(d.drow) * P.nvec_row;
-    const uint64_t pol = has_p2(d) ? keep : drop;  // a pair's rows are read again by the finishing kernel
+    const uint64_t pol = has_p2(d) ? keep : drop;  // a pair's rows are read again by pass 2
     const bool rows_ok = SPEC_IN(d.item, P.total_rows, DBG_LOGITS) &&
                          (!pair || SPEC_IN(d.drow, P.total_rows - P.B, DBG_LOGITS));
 #pragma unroll
@@ -554,7 +554,7 @@ __device__ __forceinline__ void chunk_stats(const VerifyParams &P, const ItemDes
 }
 
 // Pass 1: every chunk of every item, each warp a contiguous run of (item, chunk) pieces. The
-// kernel also zeroes the finishing kernel's counters, and CTA 0 checks the row offsets (start at 0,
+// kernel also zeroes the later kernels' counters, and CTA 0 checks the row offsets (start at 0,
 // end at total_rows, grow by at least one row).
 template <int DT>
 __global__ void __launch_bounds__(kStatsBlock) spec_stats_kernel(const __grid_constant__ VerifyParams P) {
@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(kStatsBlock) spec_stats_kernel(const __grid_co
             P.ctl[CTL_BAD_OFFSETS] = bad ? 1u : 0u;
         }
     }
-    // the finishing kernel may start its CTAs now; they wait for this grid before reading its output
+    // the decision kernel may start its CTAs now; they wait for this grid before reading its output
     griddep_launch_dependents();
     const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
     const long long warps = static_cast<long long>(gridDim.x) * (kStatsBlock / kWarp);
@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(kStatsBlock) spec_stats_kernel(const __grid_co
             cur = item;
         }
         if (c == 0 && tid % kWarp == 0 && SPEC_IN(item, P.total_rows, DBG_ROWS))
-            P.desc[item] = d;  // the item's values, for the finishing kernel
+            P.desc[item] = d;  // the item's values, for the later kernels
         if (d.kind == I_SKIP) continue;
         uint4 vt[kVPT], vd[kVPT];
         stats_load<DT>(P, d, c, keep, drop, vt, vd);
@@ -779,7 +779,7 @@ __device__ __forceinline__ ItemDec skip_decision(const ItemDesc &d) {
     return D;
 }
 
-// A lane's vectors of chunk c of a pair's two rows (the finishing kernel's loads, from L2).
+// A lane's vectors of chunk c of a pair's two rows (pass 2's loads, mostly from L2).
 template <int DT>
 __device__ __forceinline__ void load_chunk(const VerifyParams &P, const ItemDesc &d, int c, uint64_t drop,
                                            uint4 (&vt)[kVPT], uint4 (&vd)[kVPT]) {

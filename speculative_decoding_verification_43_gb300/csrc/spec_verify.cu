@@ -4,12 +4,13 @@
 // ("What to do", steps 3-4) and SDCP Rules 1 and 2 ("Acceptance Rules"); the C ABI and its
 // conventions are documented in include/spec_verify.h.
 //
-// Two kernels per call (three with top-k / top-p, whose cut of each target row comes first), both in
+// Four kernels per call (five with top-k / top-p, whose cut of each target row comes first), all in
 // spec_kernels.cuh: the statistics kernel reads every logit once (pass 1) on a persistent grid; the
-// finishing kernel, launched to start as the first drains, decides every (request, position), runs
-// pass 2 of the pairs from L2, draws the tokens, selects each request's result (first rejection,
-// emitted tokens, stopping), reduces alpha for the gamma controller and, for spec_verify_round,
-// compacts the round and chooses gamma.
+// decision kernel decides every (request, position) and marks each request's frontier; pass 2
+// reads the pairs again (mostly from L2) for alpha and the frontier's residual; the finishing
+// kernel draws the tokens, selects each request's result (first rejection, emitted tokens,
+// stopping), reduces alpha for the gamma controller and, for spec_verify_round, compacts the round
+// and chooses gamma. Each kernel after the first is launched to start as the one before drains.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -32,7 +33,7 @@ namespace spec {
 // Host side
 
 // Workspace of one call. It needs no preparation: the statistics kernel zeroes the counters the
-// finishing kernel uses, and every record is written before it is read within the call.
+// later kernels use, and every record is written before it is read within the call.
 struct WsLayout {
     size_t rec, xrec, desc, dec, alpha_c, zc, req_cnt, ctl, agg, flag, tok, status, fb, prob, margin, alpha, cut, req_alpha,
         total;
@@ -135,8 +136,8 @@ extern "C" size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t total
 }
 
 // spec_verify's checks and launches (the truncation kernel when top-k / top-p is given, then the
-// statistics and the finishing kernel); with C and G the finishing kernel also runs the round's
-// compaction and gamma choice.
+// statistics, decision, pass-2 and finishing kernels); with C and G the finishing kernel also runs
+// the round's compaction and gamma choice.
 // Nothing is enqueued when a check fails.
 static spec_status verify_enqueue(const spec_verify_args *a, void *workspace, size_t workspace_bytes,
                                   cudaStream_t stream, const CompactParams *C, const GammaParams *G) {
