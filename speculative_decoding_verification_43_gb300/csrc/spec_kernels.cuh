@@ -23,18 +23,20 @@
 //
 // spec_decide_kernel has one CTA per request and a warp per position: the warp combines the item's
 // chunk statistics (references by exact powers of two) and decides the accept test; the CTA then
-// marks the request's frontier, its first rejection or, with every draft accepted, its bonus row.
+// records the request's first rejection A and status bits, marks its frontier (position A: the
+// first rejection or, with every draft accepted, the bonus row), writes a bad request's outputs
+// and adds the request to the batch's counts.
 //
 // spec_pass2_kernel walks the pairs' chunks again like the statistics kernel (contiguous runs per
 // warp, from L2 where the rows stayed there): per chunk alpha = sum min(p, q) and, at the frontier,
 // the residual mass sum max(p - q, 0). Rejections after the first need no residual: nothing after
 // the first rejection is emitted.
 //
-// spec_finish_kernel has one warp per item: it sums the item's chunk shares, draws the frontier's
-// token (the chunk that holds u*Z by a scan over the chunk masses, then the token within it),
-// writes the item's results and counts the item for its request; the request's last item runs the
-// request's selection (first rejection, emitted tokens, stopping, its alpha into the batch's
-// fixed-point sums), and the CTA holding the batch's last item runs the batch's tail.
+// spec_finish_kernel has one warp per item: it sums the item's chunk shares, writes the item's
+// per-draft outputs and adds its alpha to the batch's fixed-point sum; the frontier's warp draws
+// the token (the chunk that holds u*Z by a scan over the chunk masses, then the token within it)
+// and writes the request's outputs (accepted drafts, frontier token, stopping); the CTA holding
+// the batch's last item runs the batch's tail.
 //
 // Each kernel after the first is launched with programmatic stream serialisation: its CTAs may
 // start while the one before drains, and wait for it (griddepcontrol.wait) before reading anything
@@ -126,13 +128,10 @@ struct VerifyParams {
     ItemDec *dec;            // [T] each item's decision, from the decision kernel
     float *alpha_c;          // [T][nchunk] each chunk's alpha share (a pair under Rule 2)
     float *zc;               // [T][nchunk] each chunk's residual mass (a frontier rejection)
-    uint32_t *req_cnt;       // [B] items of the request finalised
+    int32_t *req_first;      // [B] the request's first rejected position (K: none)
+    int32_t *req_st;         // [B] the request's status bits
     uint32_t *ctl;           // [kCtlWords] items finalised; row offsets invalid
     uint32_t *agg;           // [kAggWords] the batch's sums
-    int32_t *item_flag, *item_tok, *item_status, *item_fb;
-    float *item_prob, *item_margin;
-    float *alpha_ws;               // [T-B]
-    float2 *req_alpha;             // [B] alpha summed over the request's draft rows (float pair)
     // outputs
     int32_t *accept_len, *n_emitted, *out_tokens, *req_status, *fallback, *alpha_count;
     int32_t *depth_reached, *depth_accepted;
@@ -560,7 +559,6 @@ template <int DT>
 __global__ void __launch_bounds__(kStatsBlock) spec_stats_kernel(const __grid_constant__ VerifyParams P) {
     const int tid = threadIdx.x;
     const int nthreads = gridDim.x * kStatsBlock;
-    for (int i = blockIdx.x * kStatsBlock + tid; i < P.B; i += nthreads) P.req_cnt[i] = 0u;
     for (int i = blockIdx.x * kStatsBlock + tid; i < kAggWords; i += nthreads) P.agg[i] = 0u;
     if (blockIdx.x == 0) {
         int bad = 0;
@@ -1081,87 +1079,18 @@ __device__ __noinline__ void draw_item(const VerifyParams &P, const ItemDesc &d,
     }
 }
 
-// A request's selection (whole warp; every item of the request is finalised): the first rejection
-// A, the emitted tokens (x_1 .. x_A, then the frontier), stop-token and max_new truncation, and
-// the request's alpha sum. Lane j takes positions j and j + 32 (K_max <= 64: position 64 on lane 0).
-__device__ __noinline__ void select_request(const VerifyParams &P, int i) {
+// A request's outputs once its frontier token is known (whole warp, the frontier item's warp):
+// the accepted drafts x_1 .. x_A, then the frontier token, cut by the stop token and the
+// budget (SDCP "Verification and Commit" step 7), -1 past the emitted tokens. Lane j writes
+// positions j and j + 32 (K_max <= 64: position 64 on lane 0).
+__device__ __noinline__ void finish_request(const VerifyParams &P, int i, int r0, int K, int A, int frontier,
+                                            float fprob, float fmarg, int ffb) {
     const int lane = threadIdx.x % kWarp;
-    const int r0 = __ldg(P.row_off + i), r1 = __ldg(P.row_off + i + 1);
-    const int K = r1 - r0 - 1, d0 = r0 - i;
+    const int d0 = r0 - i;
     const int n_cap = P.max_new ? __ldg(P.max_new + i) : INT_MAX;
     const int stop = P.stop_token ? __ldg(P.stop_token + i) : -1;
-    int status = 0;
-    if (K < 0 || K > P.K_max) status |= SPEC_REQ_BAD_SHAPE;
-    int st_items = 0;
-    unsigned rej_lo = 0u, rej_hi = 0u;
-    int tok0 = -1, tok1 = -1, fb0 = 0, fb1 = 0, x0 = -1, x1 = -1, tok2 = -1, fb2 = 0;
-    float pr0 = NAN, pr1 = NAN, mg0 = NAN, mg1 = NAN, al0 = 0.0f, al1 = 0.0f, pr2 = NAN, mg2 = NAN;
-    if (!status) {
-        const int j0 = lane, j1 = lane + kWarp;
-        if (j0 <= K) {
-            st_items |= __ldcg(P.item_status + r0 + j0);
-            tok0 = __ldcg(P.item_tok + r0 + j0);
-            pr0 = __ldcg(P.item_prob + r0 + j0);
-            mg0 = __ldcg(P.item_margin + r0 + j0);
-            fb0 = __ldcg(P.item_fb + r0 + j0);
-            if (j0 < K) {
-                x0 = __ldg(P.draft_tokens + d0 + j0);
-                al0 = __ldcg(P.alpha_ws + d0 + j0);
-            }
-        }
-        if (j1 <= K) {
-            st_items |= __ldcg(P.item_status + r0 + j1);
-            tok1 = __ldcg(P.item_tok + r0 + j1);
-            pr1 = __ldcg(P.item_prob + r0 + j1);
-            mg1 = __ldcg(P.item_margin + r0 + j1);
-            fb1 = __ldcg(P.item_fb + r0 + j1);
-            if (j1 < K) {
-                x1 = __ldg(P.draft_tokens + d0 + j1);
-                al1 = __ldcg(P.alpha_ws + d0 + j1);
-            }
-        }
-        if (K == 2 * kWarp && lane == 0) {
-            st_items |= __ldcg(P.item_status + r0 + K);
-            tok2 = __ldcg(P.item_tok + r0 + K);
-            pr2 = __ldcg(P.item_prob + r0 + K);
-            mg2 = __ldcg(P.item_margin + r0 + K);
-            fb2 = __ldcg(P.item_fb + r0 + K);
-        }
-        rej_lo = __ballot_sync(0xffffffffu, j0 < K && __ldcg(P.item_flag + r0 + min(j0, K)) == 0);
-        rej_hi = __ballot_sync(0xffffffffu, j1 < K && __ldcg(P.item_flag + r0 + min(j1, K)) == 0);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) st_items |= __shfl_xor_sync(0xffffffffu, st_items, o);
-    }
-    status |= st_items;
-    if (status) {
-        // a request with any status bit emits nothing, and none of its draft rows has a result
-        if (K >= 0)
-            for (int j = lane; j <= K; j += kWarp) {
-                if (SPEC_IN(r0 + j, P.total_rows, DBG_OUT_ROWS)) P.out_tokens[r0 + j] = -1;
-                const int dr = r0 - i + j;
-                if (j < K && SPEC_IN(dr, P.total_rows - P.B, DBG_OUT_ROWS)) {
-                    if (P.alpha_rows) P.alpha_rows[dr] = NAN;
-                    if (P.rho_rows) P.rho_rows[dr] = NAN;
-                    if (P.resid_rows) P.resid_rows[dr] = -1.0f;
-                }
-            }
-        if (lane == 0 && SPEC_IN(i, P.B, DBG_OUT_REQS)) {
-            P.req_status[i] = status;
-            P.accept_len[i] = 0;
-            if (P.n_emitted) P.n_emitted[i] = 0;
-            if (P.frontier_prob) P.frontier_prob[i] = NAN;
-            if (P.frontier_margin) P.frontier_margin[i] = NAN;
-            if (P.fallback) P.fallback[i] = 0;
-            P.req_alpha[i] = make_float2(0.0f, 0.0f);
-        }
-        return;
-    }
-    const int A = rej_lo ? __ffs(rej_lo) - 1 : (rej_hi ? kWarp + __ffs(rej_hi) - 1 : K);
-    const int la = A & (kWarp - 1), half = A >> 5;
-    const int frontier = __shfl_sync(0xffffffffu, half == 0 ? tok0 : half == 1 ? tok1 : tok2, la);
-    const float fprob = __shfl_sync(0xffffffffu, half == 0 ? pr0 : half == 1 ? pr1 : pr2, la);
-    const float fmarg = __shfl_sync(0xffffffffu, half == 0 ? mg0 : half == 1 ? mg1 : mg2, la);
-    const int ffb = __shfl_sync(0xffffffffu, half == 0 ? fb0 : half == 1 ? fb1 : fb2, la);
+    const int x0 = lane < A ? __ldg(P.draft_tokens + d0 + lane) : -1;
+    const int x1 = lane + kWarp < A ? __ldg(P.draft_tokens + d0 + lane + kWarp) : -1;
     const int out0 = (lane < A) ? x0 : (lane == A ? frontier : -1);
     const int out1 = (lane + kWarp < A) ? x1 : (lane + kWarp == A ? frontier : -1);
     int n = min(A + 1, max(n_cap, 0));
@@ -1178,7 +1107,6 @@ __device__ __noinline__ void select_request(const VerifyParams &P, int i) {
         P.out_tokens[r0 + lane + kWarp] = lane + kWarp < n ? out1 : -1;
     if (lane == 0 && K == 2 * kWarp && SPEC_IN(r0 + K, P.total_rows, DBG_OUT_ROWS))
         P.out_tokens[r0 + K] = (A == K && n > K) ? frontier : -1;
-    const F2 asum = warp_sum_f2(f2_add({al0, 0.0f}, {al1, 0.0f}));
     if (lane == 0 && SPEC_IN(i, P.B, DBG_OUT_REQS)) {
         P.req_status[i] = 0;
         P.accept_len[i] = A;
@@ -1186,32 +1114,21 @@ __device__ __noinline__ void select_request(const VerifyParams &P, int i) {
         if (P.frontier_prob) P.frontier_prob[i] = fprob;
         if (P.frontier_margin) P.frontier_margin[i] = fmarg;
         if (P.fallback) P.fallback[i] = ffb;
-        P.req_alpha[i] = make_float2(asum.hi, asum.lo);
-        // the batch's alpha (fixed point: integer sums give the same result in any order) and count
-        const long long fx = __float2ll_rn(asum.hi * static_cast<float>(kAlphaFix)) +
-                             __float2ll_rn(asum.lo * static_cast<float>(kAlphaFix));
-        atomicAdd(reinterpret_cast<unsigned long long *>(P.agg + AGG_ALPHA), static_cast<unsigned long long>(fx));
-        atomicAdd(P.agg + AGG_COUNT, static_cast<uint32_t>(K));
-    }
-    // depth j + 1 was reached when the first j drafts were accepted, accepted when j < A
-    for (int j = lane; j < K; j += kWarp) {
-        if (j <= A) atomicAdd(P.agg + AGG_REACHED + j, 1u);
-        if (j < A) atomicAdd(P.agg + AGG_ACCEPTED + j, 1u);
     }
 }
 
-// The item's results and, at the request's frontier, its draw (whole warp; alpha and the residual
-// mass Zres from pass 2), then the request's count: the last item of a request runs the request's
-// selection. Returns, in every lane, whether this was the batch's last item (its CTA then runs the
-// batch's tail).
+// The item's results (whole warp; alpha and the residual mass Zres from pass 2): its per-draft
+// outputs and its share of the batch's alpha; at its request's frontier the draw and the request's
+// outputs (finish_request). Then the batch's count: returns, in every lane, whether this was the
+// batch's last item (its CTA then runs the batch's tail).
 template <int DT>
-__device__ __noinline__ bool finalize_item(const VerifyParams &P, const ItemDesc &d, const ItemDec &D, bool frontier,
+__device__ __noinline__ bool finalize_item(const VerifyParams &P, const ItemDesc &d, const ItemDec &D, int rst, int A,
                                            float alpha, float Zres) {
     const int lane = threadIdx.x % kWarp;
     const bool pair = d.kind == I_PAIR;
-    const int st = D.status;
-    // only a request's frontier (its first rejection, or the bonus row after K acceptances) is drawn
-    int kind = (st == 0 && frontier) ? D.kind : SAMPLE_NONE;
+    // the request's frontier: its first rejection, or its bonus row with every draft accepted
+    const bool frontier = rst == 0 && d.pos == A;
+    int kind = frontier ? D.kind : SAMPLE_NONE;
     int fb = 0;
     if (kind == SAMPLE_RESIDUAL && !(Zres > 0.0f)) {
         kind = SAMPLE_P;  // zero residual mass: draw from p and say so
@@ -1221,47 +1138,33 @@ __device__ __noinline__ bool finalize_item(const VerifyParams &P, const ItemDesc
     float prob = NAN, margin = NAN;
     if (kind != SAMPLE_NONE) {
         draw_item<DT>(P, d, D, kind, tok, prob, margin);
-    } else if (st == 0 && d.greedy && !(pair && D.accept)) {
+    } else if (frontier && d.greedy) {
         tok = D.argmax_t;  // Rule 1: the correction (or the extra token) is argmax p
         prob = 1.0f;
     }
-    // a draft position: a pair, or a position of a request rejected before any work (its per-draft
-    // outputs still get their no-result values)
+    // a draft position: a pair, or a position of a request rejected before any work (every draft
+    // row of a request with status bits gets the no-result values)
     const bool drow_item =
         pair || (d.kind == I_SKIP && d.pos < d.K && d.drow >= 0 && d.drow < P.total_rows - P.B);
-    if (lane == 0 && SPEC_IN(d.item, P.total_rows, DBG_ROWS) &&
-        (!drow_item || SPEC_IN(d.drow, P.total_rows - P.B, DBG_OUT_ROWS))) {
-        const int item = d.item;
-        P.item_status[item] = st;
-        P.item_fb[item] = fb;
-        P.item_tok[item] = tok;
-        P.item_prob[item] = prob;
-        P.item_margin[item] = margin;
-        if (drow_item) {
-            const float a = d.greedy ? D.alpha_g : alpha;
-            P.item_flag[item] = (st == 0) ? D.accept : 0;
-            P.alpha_ws[d.drow] = (st == 0) ? a : 0.0f;
-            if (P.alpha_rows) P.alpha_rows[d.drow] = (st == 0) ? a : NAN;
-            if (P.rho_rows) P.rho_rows[d.drow] = (st == 0) ? D.rho : NAN;
-            if (P.resid_rows)
-                P.resid_rows[d.drow] = (st == 0 && frontier && D.kind == SAMPLE_RESIDUAL && !d.greedy) ? Zres : -1.0f;
-        } else {
-            P.item_flag[item] = 0;
+    if (lane == 0 && drow_item && SPEC_IN(d.drow, P.total_rows - P.B, DBG_OUT_ROWS)) {
+        const float a = d.greedy ? D.alpha_g : alpha;
+        if (P.alpha_rows) P.alpha_rows[d.drow] = (rst == 0) ? a : NAN;
+        if (P.rho_rows) P.rho_rows[d.drow] = (rst == 0) ? D.rho : NAN;
+        if (P.resid_rows)
+            P.resid_rows[d.drow] = (frontier && D.kind == SAMPLE_RESIDUAL && !d.greedy) ? Zres : -1.0f;
+        if (rst == 0) {
+            // the batch's alpha in fixed point: integer sums give the same result in any order
+            atomicAdd(reinterpret_cast<unsigned long long *>(P.agg + AGG_ALPHA),
+                      static_cast<unsigned long long>(__float2ll_rn(a * static_cast<float>(kAlphaFix))));
         }
-        fence_gpu();
     }
-    __syncwarp();
-    uint32_t old = 0;
-    if (lane == 0 && SPEC_IN(d.req, P.B, DBG_OUT_REQS)) old = atomicAdd(P.req_cnt + d.req, 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (static_cast<int>(old) == d.K) {
-        fence_gpu();
-        select_request(P, d.req);
-        fence_gpu();
-    }
+    if (frontier) finish_request(P, d.req, d.item - d.pos, d.K, A, tok, prob, margin, fb);
     __syncwarp();
     uint32_t done = 0;
-    if (lane == 0) done = atomicAdd(P.ctl + CTL_DONE, 1u);
+    if (lane == 0) {
+        fence_gpu();  // this item's writes before the batch's count
+        done = atomicAdd(P.ctl + CTL_DONE, 1u);
+    }
     done = __shfl_sync(0xffffffffu, done, 0);
     return done == static_cast<uint32_t>(P.total_rows - 1);
 }
@@ -1322,7 +1225,8 @@ __device__ __noinline__ void batch_tail(const VerifyParams &P, TailScratch &S) {
 // accepted (only the frontier is drawn).
 template <int DT>
 __global__ void __launch_bounds__(kDecWarps * kWarp) spec_decide_kernel(const __grid_constant__ VerifyParams Pk) {
-    __shared__ int s_first;  // the first rejected position (none: INT_MAX)
+    __shared__ int s_first;   // the first rejected position (none: INT_MAX)
+    __shared__ int s_status;  // the status bits of the request's positions
     __shared__ __align__(16) VerifyParams s_P;
     stage_params<kDecWarps * kWarp>(Pk, s_P);
     const VerifyParams &P = s_P;
@@ -1333,7 +1237,10 @@ __global__ void __launch_bounds__(kDecWarps * kWarp) spec_decide_kernel(const __
     if (__ldcg(P.ctl + CTL_BAD_OFFSETS) != 0) return;
     const int r0 = __ldg(P.row_off + i), r1 = __ldg(P.row_off + i + 1);
     const int n = r1 - r0;  // K + 1 positions (offsets checked)
-    if (threadIdx.x == 0) s_first = INT_MAX;
+    if (threadIdx.x == 0) {
+        s_first = INT_MAX;
+        s_status = 0;
+    }
     __syncthreads();
     for (int j = warp; j < n; j += kDecWarps) {
         if (!SPEC_IN(r0 + j, P.total_rows, DBG_ROWS)) continue;
@@ -1341,13 +1248,46 @@ __global__ void __launch_bounds__(kDecWarps * kWarp) spec_decide_kernel(const __
         const ItemDec D = (d.kind == I_SKIP) ? skip_decision(d) : decide_chunks(P, d);
         if (lane == 0) {
             if (d.kind == I_PAIR && D.status == 0 && !D.accept) atomicMin(&s_first, j);
+            if (D.status) atomicOr(&s_status, D.status);
             P.dec[r0 + j] = D;
         }
     }
     __syncthreads();
-    // the frontier: the first rejection, else the bonus row
-    if (threadIdx.x == 0 && SPEC_IN(r0 + min(s_first, n - 1), P.total_rows, DBG_ROWS))
-        P.dec[r0 + min(s_first, n - 1)].frontier = 1;
+    const int K = n - 1;
+    const int A = min(s_first, K);  // drafts accepted before the first rejection
+    const int status = s_status;
+    if (threadIdx.x == 0) {
+        // the frontier: the first rejection, else the bonus row
+        if (SPEC_IN(r0 + A, P.total_rows, DBG_ROWS)) P.dec[r0 + A].frontier = 1;
+        if (SPEC_IN(i, P.B, DBG_OUT_REQS)) {
+            P.req_first[i] = A;
+            P.req_st[i] = status;
+        }
+    }
+    if (warp != 0) return;
+    if (status) {
+        // a request with any status bit emits nothing (its draft rows get their no-result values
+        // from the finishing kernel)
+        for (int j = lane; j <= K; j += kWarp)
+            if (SPEC_IN(r0 + j, P.total_rows, DBG_OUT_ROWS)) P.out_tokens[r0 + j] = -1;
+        if (lane == 0 && SPEC_IN(i, P.B, DBG_OUT_REQS)) {
+            P.req_status[i] = status;
+            P.accept_len[i] = 0;
+            if (P.n_emitted) P.n_emitted[i] = 0;
+            if (P.frontier_prob) P.frontier_prob[i] = NAN;
+            if (P.frontier_margin) P.frontier_margin[i] = NAN;
+            if (P.fallback) P.fallback[i] = 0;
+        }
+        return;
+    }
+    // the batch's counts ("M7.8 - Speculative Serving", sections 0x02D and 0x07B): the draft rows
+    // in alpha's mean, and depth j + 1 reached when the first j drafts were accepted, accepted
+    // when j < A
+    if (lane == 0) atomicAdd(P.agg + AGG_COUNT, static_cast<uint32_t>(K));
+    for (int j = lane; j < K; j += kWarp) {
+        if (j <= A) atomicAdd(P.agg + AGG_REACHED + j, 1u);
+        if (j < A) atomicAdd(P.agg + AGG_ACCEPTED + j, 1u);
+    }
 }
 
 // Pass 2: every chunk of every pair under Rule 2, each warp a contiguous run of (pair, chunk)
@@ -1461,7 +1401,8 @@ __global__ void __launch_bounds__(kFinBlock) spec_finish_kernel(const __grid_con
     } else if (item < P.total_rows) {
         const ItemDesc d = P.desc[item];
         const ItemDec D = P.dec[item];
-        const bool frontier = D.frontier != 0 && D.status == 0;
+        const int rst = P.req_st[d.req], A = P.req_first[d.req];  // from the decision kernel
+        const bool frontier = rst == 0 && d.pos == A;
         float alpha = 0.0f, Zres = 0.0f;
         if (has_p2(d) && D.status == 0) {
             // sums over the chunks, lane-strided, then over the lanes (the same in every lane)
@@ -1473,7 +1414,7 @@ __global__ void __launch_bounds__(kFinBlock) spec_finish_kernel(const __grid_con
             alpha = warp_sum(a);
             Zres = warp_sum(z);
         }
-        const bool tail = finalize_item<DT>(P, d, D, frontier, alpha, Zres);
+        const bool tail = finalize_item<DT>(P, d, D, rst, A, alpha, Zres);
         if (lane == 0 && tail) s_tail = 1;
     }
     __syncthreads();

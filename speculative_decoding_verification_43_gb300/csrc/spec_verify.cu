@@ -35,8 +35,7 @@ namespace spec {
 // Workspace of one call. It needs no preparation: the statistics kernel zeroes the counters the
 // later kernels use, and every record is written before it is read within the call.
 struct WsLayout {
-    size_t rec, xrec, desc, dec, alpha_c, zc, req_cnt, ctl, agg, flag, tok, status, fb, prob, margin, alpha, cut, req_alpha,
-        total;
+    size_t rec, xrec, desc, dec, alpha_c, zc, req_first, req_st, ctl, agg, cut, total;
     int32_t nvec_row, nchunk;
 };
 
@@ -45,7 +44,6 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 static WsLayout ws_layout(int32_t B, int32_t V, int32_t total_rows, spec_dtype dtype) {
     WsLayout L = {};
     const size_t T = static_cast<size_t>(total_rows > 0 ? total_rows : 0);
-    const size_t nd = total_rows > B ? static_cast<size_t>(total_rows - B) : 0;
     const size_t nb = static_cast<size_t>(B > 0 ? B : 0);
     const size_t eb = (dtype == SPEC_BF16) ? 2 : 4;
     const size_t nvec = V > 0 ? (static_cast<size_t>(V) * eb) / 16 : 0;
@@ -60,22 +58,15 @@ static WsLayout ws_layout(int32_t B, int32_t V, int32_t total_rows, spec_dtype d
     };
     L.ctl = take(vk::kCtlWords * 4);
     L.agg = take(vk::kAggWords * 4);
-    L.req_cnt = take(nb * 4);
+    L.req_first = take(nb * 4);
+    L.req_st = take(nb * 4);
     L.rec = take(chunks * 16);
     L.alpha_c = take(chunks * 4);
     L.zc = take(chunks * 4);
     L.xrec = take(T * 16);
     L.desc = take(T * sizeof(vk::ItemDesc));
     L.dec = take(T * sizeof(vk::ItemDec));
-    L.flag = take(T * 4);
-    L.tok = take(T * 4);
-    L.status = take(T * 4);
-    L.fb = take(T * 4);
-    L.prob = take(T * 4);
-    L.margin = take(T * 4);
-    L.alpha = take((nd > 0 ? nd : 1) * 4);
     L.cut = take(T * 8);  // top-k / top-p cut per target row
-    L.req_alpha = take(nb * 8);
     L.total = off;
     return L;
 }
@@ -186,17 +177,10 @@ static spec_status verify_enqueue(const spec_verify_args *a, void *workspace, si
     P.dec = reinterpret_cast<vk::ItemDec *>(ws + L.dec);
     P.alpha_c = reinterpret_cast<float *>(ws + L.alpha_c);
     P.zc = reinterpret_cast<float *>(ws + L.zc);
-    P.req_cnt = reinterpret_cast<uint32_t *>(ws + L.req_cnt);
+    P.req_first = reinterpret_cast<int32_t *>(ws + L.req_first);
+    P.req_st = reinterpret_cast<int32_t *>(ws + L.req_st);
     P.ctl = reinterpret_cast<uint32_t *>(ws + L.ctl);
     P.agg = reinterpret_cast<uint32_t *>(ws + L.agg);
-    P.item_flag = reinterpret_cast<int32_t *>(ws + L.flag);
-    P.item_tok = reinterpret_cast<int32_t *>(ws + L.tok);
-    P.item_status = reinterpret_cast<int32_t *>(ws + L.status);
-    P.item_fb = reinterpret_cast<int32_t *>(ws + L.fb);
-    P.item_prob = reinterpret_cast<float *>(ws + L.prob);
-    P.item_margin = reinterpret_cast<float *>(ws + L.margin);
-    P.alpha_ws = reinterpret_cast<float *>(ws + L.alpha);
-    P.req_alpha = reinterpret_cast<float2 *>(ws + L.req_alpha);
     P.accept_len = a->accept_len;
     P.n_emitted = a->n_emitted;
     P.out_tokens = a->out_tokens;
